@@ -1,0 +1,214 @@
+/*
+ * gbper.h -- GPU-resident prioritized experience replay (PER) on one GB300 (sm_103a).
+ *
+ * A C ABI over plain pointers and sizes.  Every transition, priority and batch lives in device
+ * memory; the library owns the replay ring and the priority trees, the caller owns every input
+ * and output buffer it passes.  No call takes or returns a torch type.
+ *
+ * Sources (cited by page title and section):
+ *   "GPU-Resident Prioritized Experience Replay" (foxhunt design document): Architecture,
+ *     Sampling Kernels (Proportional, Rank-based), Priority update, Experience Insertion,
+ *     Error Handling & Fallback.
+ *   "Putting prioritized replay's segment tree on a GPU": The Tree Under Every Prioritized
+ *     Replay, Sampling Is a Descent, Second Port: Make the Update GPU-Shaped.
+ *   "True Single-Graph Implementation Plan": Task 2 (padded row gather, int64 indices),
+ *     Task 3 (gather straight into the trainer's buffers), Task 4 (device-side counters),
+ *     Task 5 (PER calls as stream work that a CUDA graph can capture).
+ *
+ * Conventions shared by every call
+ *   - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it; no call below synchronises the host unless its
+ *     comment says so (per_total, per_min, per_status_device, per_read_state).
+ *   - Device pointers.  Arguments named d_* are device addresses (cudaMalloc or the caching
+ *     allocator of a framework) on the device that was current at per_create.  They must stay
+ *     valid until the enqueued work has run.  Row arrays must be 4-byte aligned; 16-byte
+ *     alignment together with a row length that is a multiple of 4 floats enables the
+ *     vectorised copy paths.
+ *   - Errors.  Every call returns a per_status.  Invalid host-side arguments return
+ *     PER_ERR_INVALID_ARG before anything is enqueued.  A failed CUDA call returns
+ *     PER_ERR_CUDA; per_last_error() then describes it.  Conditions only the device can see
+ *     (an update index outside the filled slots, a bounded wait that ran out) never trap or
+ *     abort: the kernel skips the offending element and sets a bit in the device error word,
+ *     which per_status_device() reads and clears.  Nothing falls back to the CPU.
+ *   - Concurrency.  One handle is driven from one host thread at a time, and its calls are
+ *     ordered by the caller (one stream, or explicit events across streams).
+ */
+#ifndef GBPER_H
+#define GBPER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct per_buffer per_buffer; /* opaque; owned by the library */
+
+typedef enum {
+    PER_OK = 0,
+    PER_ERR_INVALID_ARG = 1, /* rejected on the host; nothing was enqueued */
+    PER_ERR_OOM = 2,         /* device allocation in per_create failed */
+    PER_ERR_CUDA = 3,        /* a CUDA runtime call failed; see per_last_error */
+    PER_ERR_EMPTY = 4,       /* per_sample / per_min on a buffer with no filled slot */
+    PER_ERR_DEVICE_FLAG = 5, /* per_status_device: the device error word was non-zero */
+    PER_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up (reported as a flag bit) */
+} per_status;
+
+/* Sampling modes ("GPU-Resident Prioritized Experience Replay", Sampling Kernels). */
+enum {
+    PER_MODE_PROPORTIONAL = 0, /* P(i) = p_i^alpha / sum_k p_k^alpha, sum tree + min tree */
+    PER_MODE_RANK = 1          /* P(i) proportional to 1 / rank(i)^alpha, rank by raw priority */
+};
+
+/* Bits of the device error word (per_status_device). */
+enum {
+    PER_DEVFLAG_BAD_INDEX = 1u, /* an update named an index outside [0, size); it was skipped */
+    PER_DEVFLAG_TIMEOUT = 2u    /* a bounded wait gave up; the call's results are not valid */
+};
+
+typedef struct {
+    double alpha;            /* priority exponent, >= 0 */
+    double eps;              /* added to |td| before the exponent; > 0 */
+    uint32_t mode;           /* PER_MODE_* */
+    uint32_t row_stride_out; /* floats per gathered state row, >= state_dim (0: state_dim);
+                                columns past state_dim are written as 0.0f */
+    uint64_t seed;           /* key of the Philox4x32-10 stream that draws the batches */
+    uint32_t flags;          /* reserved; must be 0 */
+    uint32_t reserved;
+} per_config;
+
+/*
+ * per_create -- allocate a replay buffer of `capacity` slots holding rows of `state_dim`
+ * floats ("GPU-Resident Prioritized Experience Replay", Architecture: a fixed-capacity ring
+ * of states, next_states, actions, rewards, dones and priorities; no allocation during
+ * training).  Proportional mode also allocates the sum tree (binary64 internal nodes over
+ * binary32 leaves p^alpha) and its twin min tree ("Putting prioritized replay's segment tree
+ * on a GPU", The Tree Under Every Prioritized Replay); the tree has the next power of two
+ * >= capacity leaves, and the extra leaves are never filled.  Rank mode allocates the raw
+ * priorities, the sort workspace and the rank CDF, which it computes here.
+ * Every later call reuses these allocations.  The device current at this call owns them.
+ *   capacity  1 .. 2^31 slots.
+ *   state_dim floats per state row, 0 .. 65536.
+ *   cfg       copied; NULL means alpha 0.6, eps 1e-6, proportional, stride = state_dim.
+ *   out       receives the handle (unchanged on error).
+ * Errors: PER_ERR_INVALID_ARG (bad sizes or config), PER_ERR_OOM, PER_ERR_CUDA.
+ */
+per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *cfg,
+                      per_buffer **out);
+
+/* per_destroy -- synchronise the device, release every allocation and the handle.
+ * NULL is accepted and ignored. */
+per_status per_destroy(per_buffer *h);
+
+/*
+ * per_add -- insert `count` transitions at the ring cursor ("GPU-Resident Prioritized
+ * Experience Replay", Experience Insertion): row k goes to slot (cursor + k) mod capacity, so
+ * when count > capacity only the last `capacity` rows stay; the cursor wraps and the filled
+ * size grows to at most capacity.  Each new slot's raw priority is d_raw_prio[k] or, when
+ * d_raw_prio is NULL, the running maximum raw priority ("new experiences get max_priority").
+ * Raw priorities pass the clamp of Error Handling & Fallback: NaN becomes eps, +Inf becomes
+ * the running maximum as it stood when the call began, values below eps become eps.  The
+ * running maximum then takes every new raw priority.  Proportional mode writes the leaves
+ * p^alpha (binary64 pow rounded to binary32) and rebuilds the dirty ancestors of both trees
+ * level by level ("Putting prioritized replay's segment tree on a GPU", Second Port).
+ *   d_states, d_next  [count x state_dim] float, row-major (may be NULL when state_dim = 0).
+ *   d_actions [count] uint32, d_rewards [count] float, d_dones [count] uint8.
+ *   d_raw_prio [count] float or NULL.
+ * count = 0 is a no-op.  No host synchronisation.
+ */
+per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const float *d_next,
+                   const uint32_t *d_actions, const float *d_rewards, const uint8_t *d_dones,
+                   const float *d_raw_prio, void *stream);
+
+/*
+ * per_sample -- draw a stratified batch of B transitions and gather it into caller buffers.
+ * Proportional mode ("GPU-Resident Prioritized Experience Replay", Sampling Kernels,
+ * Proportional; "Putting prioritized replay's segment tree on a GPU", Sampling Is a Descent):
+ * draw j takes u_j from Philox4x32-10 (counter = (j, call lo, call hi, 0), key = seed, 53-bit
+ * uniform from the first two words), mass_j = (j + u_j) * (T / B) with T the root sum, and
+ * walks from the root: left when the left child's sum exceeds the mass, otherwise subtract
+ * and go right.  A walk that ends past the filled slots is clamped to the last filled slot.
+ * The IS weight is w = (n P(i))^-beta / max_w with max_w from the min tree, which equals
+ * (p_i^alpha / p_min^alpha)^-beta.
+ * Rank mode ("Sampling Kernels", Rank-based): sorts the filled slots by raw priority
+ * descending (ties by slot ascending), draws mass_j = (j + u_j) * (c_size / B) with counter
+ * tag 1, takes the rank r whose CDF interval c_{r-1} <= mass < c_r holds it, with
+ * c_r = sum_{k<=r} k^-alpha, and weights w = (r / size)^(alpha * beta).
+ * Gather ("True Single-Graph Implementation Plan", Task 2/3): row j of d_states and d_next
+ * receives the chosen slot's row, padded with 0.0f to row_stride_out floats.
+ *   d_idx [B] int64 (required); d_w [B] float; d_states, d_next [B x row_stride_out] float;
+ *   d_actions [B] uint32; d_rewards [B] float; d_dones [B] uint8 -- each may be NULL to skip.
+ *   B in 1 .. 2^24.  beta >= 0.
+ * The call counter lives on the device, so each call, captured in a graph or not, draws a
+ * fresh batch.  PER_ERR_EMPTY when the buffer holds no transition (host-side count).
+ */
+per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, float *d_w,
+                      float *d_states, float *d_next, uint32_t *d_actions, float *d_rewards,
+                      uint8_t *d_dones, void *stream);
+
+/*
+ * per_update_priorities -- write new priorities for a batch from its TD errors
+ * ("GPU-Resident Prioritized Experience Replay", Priority update and Error Handling &
+ * Fallback): raw = fl32(|td| + eps), NaN -> eps, +-Inf -> the running maximum as it stood
+ * when the call began; the leaf becomes raw^alpha.  When an index repeats, the highest batch
+ * position wins.  Proportional mode then rebuilds the dirty ancestors of the sum and min
+ * trees level by level ("Putting prioritized replay's segment tree on a GPU", Second Port),
+ * restricted to the nodes above a changed leaf.  Rank mode stores raw.  The running maximum
+ * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
+ * PER_DEVFLAG_BAD_INDEX.
+ *   d_idx [B] int64, d_td [B] float.  B in 0 .. 2^24 (0 is a no-op).
+ */
+per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx,
+                                 const float *d_td, void *stream);
+
+/* per_total -- the root of the sum tree (proportional) or c_size (rank), copied to *host_out.
+ * Synchronises `stream`. */
+per_status per_total(per_buffer *h, double *host_out, void *stream);
+
+/* per_min -- the root of the min tree: the smallest p^alpha over filled slots (proportional
+ * mode only).  Synchronises `stream`.  PER_ERR_EMPTY when no slot is filled. */
+per_status per_min(per_buffer *h, float *host_out, void *stream);
+
+/* per_size -- the number of filled slots as the host has counted the per_add calls enqueued
+ * so far.  No device access. */
+per_status per_size(const per_buffer *h, uint64_t *out);
+
+/* per_status_device -- read and clear the device error word (PER_DEVFLAG_* bits) into
+ * *host_flags (may be NULL).  Synchronises `stream`.  Returns PER_ERR_DEVICE_FLAG when the
+ * word was non-zero, PER_OK otherwise. */
+per_status per_status_device(per_buffer *h, uint32_t *host_flags, void *stream);
+
+/* per_last_error -- a description of the last failure on this handle ("" if none).  The
+ * string stays valid until the next call on the handle.  NULL handle: the last per_create
+ * failure on this thread. */
+const char *per_last_error(const per_buffer *h);
+
+/* What per_read_state copies out. */
+enum {
+    PER_STATE_LEAVES = 0,   /* float [nleaves]: p^alpha, 0 for empty slots (proportional) */
+    PER_STATE_SUMS = 1,     /* double [nleaves]: internal sums, entry 0 unused */
+    PER_STATE_MINS = 2,     /* float [nleaves]: internal mins, entry 0 unused */
+    PER_STATE_RAW = 3,      /* float [capacity]: raw priorities (rank mode) */
+    PER_STATE_CDF = 4,      /* double [capacity + 1]: rank CDF, entry 0 = 0 (rank mode) */
+    PER_STATE_STATES = 5,   /* float [capacity x state_dim]: ring states */
+    PER_STATE_NEXT = 6,     /* float [capacity x state_dim]: ring next_states */
+    PER_STATE_ACTIONS = 7,  /* uint32 [capacity] */
+    PER_STATE_REWARDS = 8,  /* float [capacity] */
+    PER_STATE_DONES = 9,    /* uint8 [capacity] */
+    PER_STATE_COUNTERS = 10 /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
+};
+
+/* per_read_state -- copy `count` elements starting at element `first` of one of the arrays
+ * above into host memory at host_dst (inspection, checkpoints, tests).  Synchronises
+ * `stream`.  PER_ERR_INVALID_ARG if the array does not exist in this mode or the range is
+ * out of bounds. */
+per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_t count,
+                          void *host_dst, void *stream);
+
+/* per_nleaves -- the tree's leaf count (power of two >= capacity). */
+per_status per_nleaves(const per_buffer *h, uint64_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,386 @@
+// k_sample.cu -- stratified sampling, importance weights and the row gather, fused.
+//
+// Proportional mode ("GPU-Resident Prioritized Experience Replay", Sampling Kernels,
+// Proportional; "Putting prioritized replay's segment tree on a GPU", Sampling Is a Descent).
+// One warp serves one draw j:
+//   u_j     Philox4x32-10, counter (j, call, tag 0)
+//   mass_j  (j + u_j) * (T / B): one draw per stratum of [0, T)
+//   descent the same walk as the post's st_find_prefixsum_idx (left when the left child's sum
+//           exceeds the mass, otherwise subtract and go right), evaluated in an order that
+//           reaches the same decisions with fewer dependent memory round trips:
+//             - the top `top` levels are staged once per CTA in shared memory;
+//             - below them the warp loads the left children of a 5-level subtree in one
+//               round (31 nodes, one per lane) and walks those 5 levels with shuffles;
+//             - the last round loads the 32 leaves under the node as one 128-byte line.
+//           Every comparison and subtraction is the binary64 operation of the sequential
+//           walk, so the leaf and the leftover mass are bit-identical to it.
+//   weight  w = (n P(i))^-beta / max_w with max_w from the min tree, i.e. (L[i]/p_min)^-beta
+//   gather  the warp copies the chosen rows (zero-padded to the output stride, as the padded
+//           gather of "True Single-Graph Implementation Plan", Task 2) and the scalars.
+// The last CTA to finish advances the device-side call counter.
+#include "per_internal.cuh"
+
+#include <algorithm>
+#include <cstdlib>
+
+namespace gbper {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct SampleArgs {
+    TreeRefs t;
+    RingRefs r;
+    Ctl *ctl;
+    unsigned B;
+    float beta;
+    unsigned long long seed;
+    SampleOut o;
+    int top;   // levels staged in shared memory
+    int vec4;  // rows move as float4
+};
+
+__device__ __forceinline__ void gather_rows(const RingRefs &r, const SampleOut &o, unsigned j,
+                                            unsigned long long slot, int lane, int vec4)
+{
+    const unsigned d = r.d, dp = o.dp;
+    if (vec4) {
+        const unsigned d4 = d >> 2, dp4 = dp >> 2;
+        const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
+        const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
+        float4 *dstS = o.states ? reinterpret_cast<float4 *>(o.states + (unsigned long long)j * dp) : nullptr;
+        float4 *dstN = o.next ? reinterpret_cast<float4 *>(o.next + (unsigned long long)j * dp) : nullptr;
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (unsigned c = lane; c < 2 * dp4; c += 32) {
+            const bool second = c >= dp4;
+            const unsigned cc = second ? c - dp4 : c;
+            float4 *dst = second ? dstN : dstS;
+            if (!dst) continue;
+            dst[cc] = cc < d4 ? __ldg((second ? srcN : srcS) + cc) : zero;
+        }
+    } else {
+        for (unsigned c = lane; c < 2 * dp; c += 32) {
+            const bool second = c >= dp;
+            const unsigned cc = second ? c - dp : c;
+            float *dst = second ? o.next : o.states;
+            if (!dst) continue;
+            const float *src = second ? r.next : r.states;
+            dst[(unsigned long long)j * dp + cc] = cc < d ? __ldg(src + slot * d + cc) : 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ void write_scalars(const RingRefs &r, const SampleOut &o, unsigned j,
+                                              unsigned long long slot, int lane)
+{
+    if (lane == 1 && o.actions) o.actions[j] = __ldg(r.actions + slot);
+    if (lane == 2 && o.rewards) o.rewards[j] = __ldg(r.rewards + slot);
+    if (lane == 3 && o.dones) o.dones[j] = __ldg(r.dones + slot);
+}
+
+// Walk k levels below `node` whose left children are all internal nodes.
+__device__ __forceinline__ unsigned long long walk_internal(const double *__restrict__ S,
+                                                            unsigned long long node, int k,
+                                                            double &m, int lane)
+{
+    double mine = 0.0;
+    if (lane < (1 << k) - 1) {
+        const int lev = 32 - __clz(lane + 1);           // relative depth 1..k of this lane's node
+        const int pos = lane + 1 - (1 << (lev - 1));    // position among the left children
+        mine = S[(node << lev) + 2 * pos];
+    }
+    int q = 0;
+    for (int lev = 1; lev <= k; ++lev) {
+        const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
+        if (left > m) {
+            q = 2 * q;
+        } else {
+            m = __dsub_rn(m, left);
+            q = 2 * q + 1;
+        }
+    }
+    return (node << k) + q;
+}
+
+__global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
+{
+    extern __shared__ double s_top[];  // nodes 2 .. 2^(top+1)-1 at s_top[node - 2]
+    const int top = a.top;
+    const int nstage = (1 << (top + 1)) - 2;
+    if (nstage > 0) {
+        const double2 *src = reinterpret_cast<const double2 *>(a.t.S + 2);
+        for (int i = threadIdx.x; i < nstage / 2; i += blockDim.x) {
+            const double2 v = src[i];
+            s_top[2 * i] = v.x;
+            s_top[2 * i + 1] = v.y;
+        }
+    }
+    __syncthreads();
+    const unsigned long long n = a.t.n;
+    const int D = a.t.D;
+    const double total = D == 0 ? (double)a.t.L[0] : a.t.S[1];
+    const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
+    const unsigned long long call = a.ctl->sample_calls;
+    const unsigned long long size = a.ctl->size;
+    const double seg = __ddiv_rn(total, (double)a.B);
+    const double nbeta = -(double)a.beta;
+    const int lane = threadIdx.x & 31;
+    const unsigned wpb = blockDim.x >> 5;
+    const unsigned warps_total = gridDim.x * wpb;
+    const int R = D - top;                 // levels walked below the staged top (>= 1 if D >= 1)
+    const int kL = R < 5 ? R : 5;          // last round, ending on the leaves
+    const int first = (R - kL) % 5;        // odd-sized first round (0 = none)
+
+    for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
+        const double u = draw_uniform(a.seed, j, call, 0);
+        double m = __dmul_rn(__dadd_rn((double)j, u), seg);
+        unsigned long long leaf;
+        float lv;
+        if (D == 0) {
+            leaf = 0;
+            lv = a.t.L[0];
+        } else {
+            unsigned long long node = 1;
+            for (int l = 0; l < top; ++l) {
+                const double left = s_top[2 * node - 2];
+                if (left > m) {
+                    node = 2 * node;
+                } else {
+                    m = __dsub_rn(m, left);
+                    node = 2 * node + 1;
+                }
+            }
+            int remaining = R - kL;
+            int k = first ? first : 5;
+            while (remaining > 0) {
+                node = walk_internal(a.t.S, node, k, m, lane);
+                remaining -= k;
+                k = 5;
+            }
+            // last round: kL - 1 internal levels, then the leaf level as one contiguous block
+            double mine = 0.0;
+            float myleaf = 0.0f;
+            if (lane < (1 << (kL - 1)) - 1) {
+                const int lev = 32 - __clz(lane + 1);
+                const int pos = lane + 1 - (1 << (lev - 1));
+                mine = a.t.S[(node << lev) + 2 * pos];
+            }
+            if (lane < (1 << kL)) myleaf = a.t.L[(node << kL) - n + lane];
+            int q = 0;
+            for (int lev = 1; lev < kL; ++lev) {
+                const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
+                if (left > m) {
+                    q = 2 * q;
+                } else {
+                    m = __dsub_rn(m, left);
+                    q = 2 * q + 1;
+                }
+            }
+            {
+                const double left = (double)__shfl_sync(kFull, myleaf, 2 * q);
+                if (left > m) {
+                    q = 2 * q;
+                } else {
+                    m = __dsub_rn(m, left);
+                    q = 2 * q + 1;
+                }
+            }
+            leaf = (node << kL) + q - n;
+            lv = __shfl_sync(kFull, myleaf, q);
+        }
+        if (leaf >= size) {  // ran past the filled slots: take the last filled slot
+            leaf = size - 1;
+            lv = a.t.L[leaf];
+        }
+        if (lane == 0) {
+            a.o.idx[j] = (long long)leaf;
+            if (a.o.w) a.o.w[j] = __double2float_rn(pow(__ddiv_rn((double)lv, (double)pmin), nbeta));
+        }
+        write_scalars(a.r, a.o, j, leaf, lane);
+        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, leaf, lane, a.vec4);
+    }
+
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&a.ctl->ticket_sample, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+        a.ctl->sample_calls = call + 1;
+        a.ctl->ticket_sample = 0;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Rank mode ("Sampling Kernels", Rank-based step 2): rank r is drawn with probability
+// r^-alpha / c_size by locating the stratified mass in the CDF c (a 32-way search per warp:
+// each round probes 32 evenly spaced entries and keeps the bracket that holds the first
+// entry above the mass).  The slot is sorted[r-1]; w = (r / size)^(alpha beta).
+// ------------------------------------------------------------------------------------------
+struct RankSampleArgs {
+    const double *cdf;
+    const unsigned *sorted;
+    RingRefs r;
+    Ctl *ctl;
+    unsigned B;
+    float beta;
+    double alpha;
+    unsigned long long seed;
+    SampleOut o;
+    int vec4;
+};
+
+__global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
+{
+    const unsigned long long size = a.ctl->size;
+    const unsigned long long call = a.ctl->sample_calls;
+    const double total = a.cdf[size];
+    const double seg = __ddiv_rn(total, (double)a.B);
+    const double ab = __dmul_rn(a.alpha, (double)a.beta);
+    const int lane = threadIdx.x & 31;
+    const unsigned wpb = blockDim.x >> 5;
+    const unsigned warps_total = gridDim.x * wpb;
+    for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
+        const double u = draw_uniform(a.seed, j, call, 1);
+        const double m = __dmul_rn(__dadd_rn((double)j, u), seg);
+        // first position p in [1, size] with cdf[p] > m; size + 1 when there is none
+        unsigned long long lo = 1, hi = size + 1, ans = size + 1;
+        while (true) {
+            const unsigned long long len = hi - lo;
+            if (len == 0) {
+                ans = hi;
+                break;
+            }
+            if (len <= 32) {
+                const unsigned long long p = lo + lane;
+                const bool pred = p < hi && a.cdf[p] > m;
+                const unsigned b = __ballot_sync(kFull, pred);
+                ans = b ? lo + (__ffs(b) - 1) : hi;
+                break;
+            }
+            const unsigned long long step = (len + 31) / 32;
+            unsigned long long p = lo + (unsigned long long)(lane + 1) * step - 1;
+            if (p > hi - 1) p = hi - 1;
+            const bool pred = a.cdf[p] > m;
+            const unsigned b = __ballot_sync(kFull, pred);
+            if (b == 0) {
+                ans = hi;
+                break;
+            }
+            const int f = __ffs(b) - 1;
+            unsigned long long pf = lo + (unsigned long long)(f + 1) * step - 1;
+            if (pf > hi - 1) pf = hi - 1;
+            unsigned long long pprev = lo;
+            if (f > 0) {
+                pprev = lo + (unsigned long long)f * step - 1;
+                if (pprev > hi - 1) pprev = hi - 1;
+                pprev += 1;
+            }
+            lo = pprev;
+            hi = pf;  // answer in [lo, pf]; pf itself satisfies the predicate
+        }
+        unsigned long long r = ans > size ? size : ans;
+        const unsigned long long slot = a.sorted[r - 1];
+        if (lane == 0) {
+            a.o.idx[j] = (long long)slot;
+            if (a.o.w) a.o.w[j] = __double2float_rn(pow(__ddiv_rn((double)r, (double)size), ab));
+        }
+        write_scalars(a.r, a.o, j, slot, lane);
+        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, slot, lane, a.vec4);
+    }
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&a.ctl->ticket_sample, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+        a.ctl->sample_calls = call + 1;
+        a.ctl->ticket_sample = 0;
+    }
+}
+
+int top_levels_for(int D)
+{
+    if (D <= 0) return 0;
+    int tmax = 11;
+    if (const char *e = std::getenv("GBPER_SAMPLE_TOP")) tmax = std::max(0, std::atoi(e));
+    tmax = std::min(tmax, 12);
+    // walk R = D - top levels from global memory in rounds of 5; prefer R a multiple of 5
+    int R = D - tmax;
+    if (R < 1) R = 1;
+    R = ((R + 4) / 5) * 5;
+    if (R > D) R = D;
+    return D - R;
+}
+
+int warps_per_cta()
+{
+    int w = 8;
+    if (const char *e = std::getenv("GBPER_SAMPLE_WARPS")) w = std::atoi(e);
+    if (w < 1) w = 1;
+    if (w > kThreads / 32) w = kThreads / 32;
+    return w;
+}
+
+bool rows_vec4(const RingRefs &r, const SampleOut &o)
+{
+    if (r.d % 4 != 0 || o.dp % 4 != 0) return false;
+    const uintptr_t bits = reinterpret_cast<uintptr_t>(o.states) | reinterpret_cast<uintptr_t>(o.next) |
+                           reinterpret_cast<uintptr_t>(r.states) | reinterpret_cast<uintptr_t>(r.next);
+    return bits % 16 == 0;
+}
+
+}  // namespace
+
+cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, unsigned B,
+                               float beta, unsigned long long seed, const SampleOut &o,
+                               int num_sms, cudaStream_t st)
+{
+    SampleArgs a;
+    a.t = t;
+    a.r = r;
+    a.ctl = ctl;
+    a.B = B;
+    a.beta = beta;
+    a.seed = seed;
+    a.o = o;
+    a.top = top_levels_for(t.D);
+    a.vec4 = rows_vec4(r, o) ? 1 : 0;
+    const int wpb = warps_per_cta();
+    const unsigned long long ctas = (B + wpb - 1) / wpb;
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    const size_t smem = a.top > 0 ? (size_t)((1 << (a.top + 1)) - 2) * sizeof(double) : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_sample_prop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    k_sample_prop<<<grid, wpb * 32, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,
+                               Ctl *ctl, unsigned B, float beta, double alpha,
+                               unsigned long long seed, const SampleOut &o, int num_sms,
+                               cudaStream_t st)
+{
+    RankSampleArgs a;
+    a.cdf = w.cdf;
+    a.sorted = sorted;
+    a.r = r;
+    a.ctl = ctl;
+    a.B = B;
+    a.beta = beta;
+    a.alpha = alpha;
+    a.seed = seed;
+    a.o = o;
+    a.vec4 = rows_vec4(r, o) ? 1 : 0;
+    const int wpb = warps_per_cta();
+    const unsigned long long ctas = (B + wpb - 1) / wpb;
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    k_sample_rank<<<grid, wpb * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace gbper

@@ -1,0 +1,400 @@
+// per_api.cu -- the C ABI of libgbper: argument checks, allocation, launches.  Every compute
+// step runs in the kernels of k_tree.cu, k_sample.cu and k_rank.cu; this file only validates,
+// allocates once at creation and enqueues work on the caller's stream.
+#include "gbper.h"
+#include "per_internal.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+using namespace gbper;
+
+struct per_buffer {
+    int device = 0;
+    int num_sms = 1;
+    uint64_t capacity = 0, n = 1;
+    int D = 0;
+    uint32_t d = 0, dp = 0;
+    double alpha = 0.6, eps = 1e-6;
+    uint32_t mode = PER_MODE_PROPORTIONAL;
+    uint64_t seed = 0;
+    // proportional
+    float *L = nullptr;
+    double *S = nullptr;
+    float *M = nullptr;
+    // rank
+    RankWork rank{};
+    // ring
+    float *states = nullptr, *next = nullptr;
+    uint32_t *actions = nullptr;
+    float *rewards = nullptr;
+    uint8_t *dones = nullptr;
+    Ctl *ctl = nullptr;
+    uint64_t host_size = 0, host_cursor = 0;
+    std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+per_status fail(per_buffer *h, per_status s, const std::string &msg)
+{
+    if (h) h->err = msg;
+    else g_create_err = msg;
+    return s;
+}
+
+per_status cuda_fail(per_buffer *h, cudaError_t e, const char *where)
+{
+    return fail(h, PER_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+TreeRefs tree_of(const per_buffer *h)
+{
+    TreeRefs t;
+    t.L = h->L;
+    t.S = h->S;
+    t.M = h->M;
+    t.n = h->n;
+    t.D = h->D;
+    return t;
+}
+
+RingRefs ring_of(const per_buffer *h)
+{
+    RingRefs r;
+    r.states = h->states;
+    r.next = h->next;
+    r.actions = h->actions;
+    r.rewards = h->rewards;
+    r.dones = h->dones;
+    r.capacity = h->capacity;
+    r.d = h->d;
+    return r;
+}
+
+void free_all(per_buffer *h)
+{
+    void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
+                    h->rank.vals[0], h->rank.vals[1], h->rank.tile_hist, h->rank.digit_hist,
+                    h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+}
+
+template <typename T>
+bool alloc(T **p, uint64_t count)
+{
+    if (count == 0) count = 1;
+    return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T)) == cudaSuccess;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *cfg, per_buffer **out)
+{
+    g_create_err.clear();
+    if (!out) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: out is NULL");
+    if (capacity == 0 || capacity > (1ull << 31))
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: capacity must be in 1 .. 2^31");
+    if (state_dim > 65536) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: state_dim > 65536");
+    per_config c;
+    if (cfg) {
+        c = *cfg;
+    } else {
+        std::memset(&c, 0, sizeof(c));
+        c.alpha = 0.6;
+        c.eps = 1e-6;
+    }
+    if (c.row_stride_out == 0) c.row_stride_out = state_dim;
+    if (c.row_stride_out < state_dim)
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: row_stride_out < state_dim");
+    if (c.row_stride_out > 65536) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: row_stride_out > 65536");
+    if (!(c.alpha >= 0.0) || !std::isfinite(c.alpha))
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: alpha must be finite and >= 0");
+    if (!(c.eps > 0.0) || !std::isfinite(c.eps))
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: eps must be finite and > 0");
+    if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK)
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown mode");
+    if (c.flags != 0) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: flags must be 0");
+    if (c.mode == PER_MODE_PROPORTIONAL && !((float)std::pow(c.eps, c.alpha) >= 1.17549435e-38f))
+        return fail(nullptr, PER_ERR_INVALID_ARG,
+                    "per_create: eps^alpha underflows binary32; a leaf of 0 would read as an empty slot");
+
+    per_buffer *h = new (std::nothrow) per_buffer();
+    if (!h) return fail(nullptr, PER_ERR_OOM, "per_create: host allocation failed");
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return fail(nullptr, PER_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    }
+    cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (h->num_sms < 1) h->num_sms = 1;
+    h->capacity = capacity;
+    while (h->n < capacity) {
+        h->n <<= 1;
+        h->D += 1;
+    }
+    h->d = state_dim;
+    h->dp = c.row_stride_out;
+    h->alpha = c.alpha;
+    h->eps = c.eps;
+    h->mode = c.mode;
+    h->seed = c.seed;
+
+    bool ok = alloc(&h->ctl, 1);
+    if (c.mode == PER_MODE_PROPORTIONAL) {
+        ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n);
+    } else {
+        const uint64_t tiles = rank_tile_count(capacity);
+        ok = ok && alloc(&h->rank.raw, capacity) && alloc(&h->rank.cdf, capacity + 1) &&
+             alloc(&h->rank.keys[0], capacity) && alloc(&h->rank.keys[1], capacity) &&
+             alloc(&h->rank.vals[0], capacity) && alloc(&h->rank.vals[1], capacity) &&
+             alloc(&h->rank.tile_hist, 256 * tiles) && alloc(&h->rank.digit_hist, 4 * 256);
+        h->rank.capacity = capacity;
+    }
+    ok = ok && alloc(&h->states, capacity * (uint64_t)state_dim) && alloc(&h->next, capacity * (uint64_t)state_dim) &&
+         alloc(&h->actions, capacity) && alloc(&h->rewards, capacity) && alloc(&h->dones, capacity);
+    if (!ok) {
+        cudaGetLastError();
+        free_all(h);
+        delete h;
+        return fail(nullptr, PER_ERR_OOM, "per_create: device allocation failed");
+    }
+    Ctl init;
+    std::memset(&init, 0, sizeof(init));
+    const float one = 1.0f;
+    std::memcpy(&init.max_raw_bits, &one, sizeof(one));
+    e = cudaMemcpy(h->ctl, &init, sizeof(init), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && h->L) e = cudaMemset(h->L, 0, h->n * sizeof(float));
+    if (e == cudaSuccess && h->S) e = cudaMemset(h->S, 0, h->n * sizeof(double));
+    if (e == cudaSuccess && h->M) e = launch_fill_mins(h->M, h->n, 0);
+    if (e == cudaSuccess && h->rank.raw) e = cudaMemset(h->rank.raw, 0, capacity * sizeof(float));
+    if (e == cudaSuccess && h->rank.cdf) e = launch_build_cdf(h->rank.cdf, capacity, h->alpha, 0);
+    if (e == cudaSuccess && state_dim) e = cudaMemset(h->states, 0, capacity * (uint64_t)state_dim * sizeof(float));
+    if (e == cudaSuccess && state_dim) e = cudaMemset(h->next, 0, capacity * (uint64_t)state_dim * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemset(h->actions, 0, capacity * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(h->rewards, 0, capacity * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemset(h->dones, 0, capacity);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_all(h);
+        delete h;
+        return fail(nullptr, PER_ERR_CUDA, std::string("per_create init: ") + cudaGetErrorString(e));
+    }
+    *out = h;
+    return PER_OK;
+}
+
+per_status per_destroy(per_buffer *h)
+{
+    if (!h) return PER_OK;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != h->device) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    free_all(h);
+    if (cur != h->device) cudaSetDevice(cur);
+    delete h;
+    return PER_OK;
+}
+
+per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const float *d_next,
+                   const uint32_t *d_actions, const float *d_rewards, const uint8_t *d_dones,
+                   const float *d_raw_prio, void *stream)
+{
+    if (!h) return PER_ERR_INVALID_ARG;
+    if (count == 0) return PER_OK;
+    if (!d_actions || !d_rewards || !d_dones)
+        return fail(h, PER_ERR_INVALID_ARG, "per_add: actions, rewards and dones are required");
+    if (h->d && (!d_states || !d_next))
+        return fail(h, PER_ERR_INVALID_ARG, "per_add: states and next_states are required");
+    if (h->d && ((reinterpret_cast<uintptr_t>(d_states) | reinterpret_cast<uintptr_t>(d_next)) % 4))
+        return fail(h, PER_ERR_INVALID_ARG, "per_add: row arrays must be 4-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(d_actions) | reinterpret_cast<uintptr_t>(d_rewards)) % 4 ||
+        (d_raw_prio && reinterpret_cast<uintptr_t>(d_raw_prio) % 4))
+        return fail(h, PER_ERR_INVALID_ARG, "per_add: scalar arrays must be 4-byte aligned");
+    if (count > (1ull << 40)) return fail(h, PER_ERR_INVALID_ARG, "per_add: count too large");
+    const cudaError_t e = launch_add(tree_of(h), ring_of(h), h->rank.raw, h->ctl, count, d_states, d_next,
+                                     d_actions, d_rewards, d_dones, d_raw_prio, h->alpha, h->eps,
+                                     h->mode == PER_MODE_PROPORTIONAL, h->host_cursor, h->num_sms,
+                                     as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "per_add launch");
+    h->host_cursor = (h->host_cursor + count) % h->capacity;
+    h->host_size = std::min<uint64_t>(h->host_size + count, h->capacity);
+    return PER_OK;
+}
+
+per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, float *d_w, float *d_states,
+                      float *d_next, uint32_t *d_actions, float *d_rewards, uint8_t *d_dones, void *stream)
+{
+    if (!h) return PER_ERR_INVALID_ARG;
+    if (B == 0 || B > (1u << 24)) return fail(h, PER_ERR_INVALID_ARG, "per_sample: B must be in 1 .. 2^24");
+    if (!d_idx) return fail(h, PER_ERR_INVALID_ARG, "per_sample: d_idx is required");
+    if (!(beta >= 0.0f) || !std::isfinite(beta))
+        return fail(h, PER_ERR_INVALID_ARG, "per_sample: beta must be finite and >= 0");
+    if (reinterpret_cast<uintptr_t>(d_idx) % 8 || reinterpret_cast<uintptr_t>(d_w) % 4 ||
+        reinterpret_cast<uintptr_t>(d_states) % 4 || reinterpret_cast<uintptr_t>(d_next) % 4 ||
+        reinterpret_cast<uintptr_t>(d_actions) % 4 || reinterpret_cast<uintptr_t>(d_rewards) % 4)
+        return fail(h, PER_ERR_INVALID_ARG, "per_sample: misaligned output pointer");
+    if (h->host_size == 0) return fail(h, PER_ERR_EMPTY, "per_sample: the buffer holds no transition");
+    SampleOut o;
+    o.idx = reinterpret_cast<long long *>(d_idx);
+    o.w = d_w;
+    o.states = d_states;
+    o.next = d_next;
+    o.actions = d_actions;
+    o.rewards = d_rewards;
+    o.dones = d_dones;
+    o.dp = h->dp;
+    cudaError_t e;
+    if (h->mode == PER_MODE_PROPORTIONAL) {
+        e = launch_sample_prop(tree_of(h), ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms, as_stream(stream));
+    } else {
+        unsigned *sorted = nullptr;
+        e = launch_rank_sort(h->rank, h->host_size, &sorted, as_stream(stream));
+        if (e == cudaSuccess)
+            e = launch_sample_rank(h->rank, sorted, ring_of(h), h->ctl, B, beta, h->alpha, h->seed, o,
+                                   h->num_sms, as_stream(stream));
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "per_sample launch");
+    return PER_OK;
+}
+
+per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx, const float *d_td,
+                                 void *stream)
+{
+    if (!h) return PER_ERR_INVALID_ARG;
+    if (B == 0) return PER_OK;
+    if (B > (1u << 24)) return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: B > 2^24");
+    if (!d_idx || !d_td) return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: NULL input");
+    if (reinterpret_cast<uintptr_t>(d_idx) % 8 || reinterpret_cast<uintptr_t>(d_td) % 4)
+        return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: misaligned input");
+    const cudaError_t e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, reinterpret_cast<const long long *>(d_idx),
+                                        d_td, h->alpha, h->eps, h->mode == PER_MODE_PROPORTIONAL, h->num_sms,
+                                        as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
+    return PER_OK;
+}
+
+per_status per_total(per_buffer *h, double *host_out, void *stream)
+{
+    if (!h || !host_out) return PER_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
+    if (h->mode == PER_MODE_RANK) {
+        e = cudaMemcpyAsync(host_out, h->rank.cdf + h->host_size, sizeof(double), cudaMemcpyDeviceToHost, st);
+    } else if (h->D == 0) {
+        float v = 0.0f;
+        e = cudaMemcpyAsync(&v, h->L, sizeof(float), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        *host_out = (double)v;
+        return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_total");
+    } else {
+        e = cudaMemcpyAsync(host_out, h->S + 1, sizeof(double), cudaMemcpyDeviceToHost, st);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_total");
+}
+
+per_status per_min(per_buffer *h, float *host_out, void *stream)
+{
+    if (!h || !host_out) return PER_ERR_INVALID_ARG;
+    if (h->mode != PER_MODE_PROPORTIONAL) return fail(h, PER_ERR_INVALID_ARG, "per_min: proportional mode only");
+    if (h->host_size == 0) return fail(h, PER_ERR_EMPTY, "per_min: the buffer holds no transition");
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
+    float v = 0.0f;
+    if (h->D == 0) {
+        e = cudaMemcpyAsync(&v, h->L, sizeof(float), cudaMemcpyDeviceToHost, st);
+    } else {
+        e = cudaMemcpyAsync(&v, h->M + 1, sizeof(float), cudaMemcpyDeviceToHost, st);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "per_min");
+    *host_out = v;
+    return PER_OK;
+}
+
+per_status per_size(const per_buffer *h, uint64_t *out)
+{
+    if (!h || !out) return PER_ERR_INVALID_ARG;
+    *out = h->host_size;
+    return PER_OK;
+}
+
+per_status per_nleaves(const per_buffer *h, uint64_t *out)
+{
+    if (!h || !out) return PER_ERR_INVALID_ARG;
+    *out = h->n;
+    return PER_OK;
+}
+
+per_status per_status_device(per_buffer *h, uint32_t *host_flags, void *stream)
+{
+    if (!h) return PER_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    uint32_t flags = 0;
+    cudaError_t e = cudaMemcpyAsync(&flags, &h->ctl->err_flags, sizeof(flags), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&h->ctl->err_flags, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(h, e, "per_status_device");
+    if (host_flags) *host_flags = flags;
+    return flags ? PER_ERR_DEVICE_FLAG : PER_OK;
+}
+
+const char *per_last_error(const per_buffer *h)
+{
+    return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_t count, void *host_dst,
+                          void *stream)
+{
+    if (!h || (!host_dst && count)) return PER_ERR_INVALID_ARG;
+    const void *src = nullptr;
+    uint64_t elems = 0, esz = 0;
+    switch (which) {
+    case PER_STATE_LEAVES: src = h->L; elems = h->n; esz = 4; break;
+    case PER_STATE_SUMS: src = h->S; elems = h->n; esz = 8; break;
+    case PER_STATE_MINS: src = h->M; elems = h->n; esz = 4; break;
+    case PER_STATE_RAW: src = h->rank.raw; elems = h->capacity; esz = 4; break;
+    case PER_STATE_CDF: src = h->rank.cdf; elems = h->capacity + 1; esz = 8; break;
+    case PER_STATE_STATES: src = h->states; elems = h->capacity * (uint64_t)h->d; esz = 4; break;
+    case PER_STATE_NEXT: src = h->next; elems = h->capacity * (uint64_t)h->d; esz = 4; break;
+    case PER_STATE_ACTIONS: src = h->actions; elems = h->capacity; esz = 4; break;
+    case PER_STATE_REWARDS: src = h->rewards; elems = h->capacity; esz = 4; break;
+    case PER_STATE_DONES: src = h->dones; elems = h->capacity; esz = 1; break;
+    case PER_STATE_COUNTERS: {
+        if (first + count > 4) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
+        Ctl c;
+        cudaStream_t st = as_stream(stream);
+        cudaError_t e = cudaMemcpyAsync(&c, h->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "per_read_state");
+        const uint64_t v[4] = {c.sample_calls, c.cursor, c.size, c.max_raw_bits};
+        std::memcpy(host_dst, v + first, count * sizeof(uint64_t));
+        return PER_OK;
+    }
+    default: return fail(h, PER_ERR_INVALID_ARG, "per_read_state: unknown array");
+    }
+    if (!src) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: array absent in this mode");
+    if (first > elems || count > elems - first) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
+    if (count == 0) return PER_OK;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = cudaMemcpyAsync(host_dst, static_cast<const char *>(src) + first * esz, count * esz,
+                                    cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_read_state");
+}
+
+}  // extern "C"

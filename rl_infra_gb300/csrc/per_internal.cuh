@@ -1,0 +1,162 @@
+// per_internal.cuh -- shared declarations of the CUDA side of libgbper (sm_103a).
+//
+// Device layout of one replay buffer (proportional mode), n = 2^D leaves >= capacity:
+//   L  float  [n]  leaves p^alpha; 0 marks an empty slot or a padding leaf
+//   S  double [n]  internal sums, node i in [1, n): children 2i, 2i+1; nodes >= n are leaves
+//   M  float  [n]  internal mins over filled leaves (+inf where none)
+// Levels are contiguous: depth l holds nodes [2^l, 2^(l+1)), so a level is one coalesced
+// stretch and every level from depth 4 down starts on a 128-byte line.
+// Rank mode keeps raw priorities [capacity] and the rank CDF [capacity + 1] instead.
+// The ring holds states / next_states [capacity x state_dim], actions, rewards, dones.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gbper {
+
+// Device-resident control block: counters that kernels advance themselves, so that a call
+// replayed from a CUDA graph still draws a fresh batch and inserts at the right slot
+// ("True Single-Graph Implementation Plan", Task 4: device-side counters).
+struct Ctl {
+    unsigned long long sample_calls;  // Philox call counter
+    unsigned long long cursor;        // next ring slot
+    unsigned long long size;          // filled slots
+    unsigned int max_raw_bits;        // running maximum raw priority (float bits, > 0)
+    unsigned int err_flags;           // PER_DEVFLAG_* bits
+    unsigned int ticket_sample;       // arrival tickets; the last CTA resets its own
+    unsigned int ticket_update;
+    unsigned int ticket_add;
+    unsigned int batch_max_bits;      // per-call maximum raw priority, folded in by the last CTA
+    unsigned int add_max_bits;
+    unsigned int pad[3];
+};
+
+constexpr unsigned kFlagBadIndex = 1u;
+constexpr unsigned kFlagTimeout = 2u;
+
+// ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) -----------------------------------
+// Round: (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0)) with
+// A = 0xD2511F53, B = 0xCD9E8D57; the key advances by (0x9E3779B9, 0xBB67AE85) per round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const unsigned a_lo = 0xD2511F53u * c.x, a_hi = __umulhi(0xD2511F53u, c.x);
+        const unsigned b_lo = 0xCD9E8D57u * c.z, b_hi = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(b_hi ^ c.y ^ k.x, b_lo, a_hi ^ c.w ^ k.y, a_lo);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// 53-bit uniform in [0, 1) of draw j in sample call `call`, stream tag `tag`.
+__device__ __forceinline__ double draw_uniform(unsigned long long seed, unsigned j,
+                                               unsigned long long call, unsigned tag)
+{
+    const uint4 x = philox4x32_10(make_uint4(j, (unsigned)call, (unsigned)(call >> 32), tag),
+                                  make_uint2((unsigned)seed, (unsigned)(seed >> 32)));
+    const unsigned long long bits = ((unsigned long long)x.x << 21) | (x.y >> 11);
+    return __dmul_rn((double)bits, 0x1.0p-53);
+}
+
+// ---- priority transforms ("GPU-Resident Prioritized Experience Replay": Priority update,
+// Error Handling & Fallback) -------------------------------------------------------------------
+__device__ __forceinline__ float td_to_raw(float td, double eps, float max_at_start)
+{
+    if (isnan(td)) return (float)eps;
+    const float a = fabsf(td);
+    if (isinf(a)) return max_at_start;
+    return __double2float_rn(__dadd_rn((double)a, eps));
+}
+
+__device__ __forceinline__ float prio_to_raw(float p, double eps, float max_at_start)
+{
+    if (isnan(p)) return (float)eps;
+    if (isinf(p) && p > 0.0f) return max_at_start;
+    if ((double)p < eps) return (float)eps;
+    return p;
+}
+
+__device__ __forceinline__ float raw_to_leaf(float raw, double alpha)
+{
+    return __double2float_rn(pow((double)raw, alpha));
+}
+
+__device__ __forceinline__ float leaf_min_value(float leaf)
+{
+    return leaf > 0.0f ? leaf : __int_as_float(0x7f800000);
+}
+
+// ---- launch arguments --------------------------------------------------------------------
+struct TreeRefs {
+    float *L;
+    double *S;
+    float *M;
+    unsigned long long n;
+    int D;
+};
+
+struct RingRefs {
+    float *states, *next;
+    unsigned *actions;
+    float *rewards;
+    unsigned char *dones;
+    unsigned long long capacity;
+    unsigned d;
+};
+
+// Host launchers (each returns the launch's cudaError_t).
+cudaError_t launch_fill_mins(float *M, unsigned long long n, cudaStream_t st);
+
+cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, Ctl *ctl,
+                       unsigned long long count, const float *states, const float *next,
+                       const unsigned *actions, const float *rewards, const unsigned char *dones,
+                       const float *prio, double alpha, double eps, bool proportional,
+                       unsigned long long host_cursor, int num_sms, cudaStream_t st);
+
+cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
+                          const long long *idx, const float *td, double alpha, double eps,
+                          bool proportional, int num_sms, cudaStream_t st);
+
+struct SampleOut {
+    long long *idx;
+    float *w;
+    float *states, *next;
+    unsigned *actions;
+    float *rewards;
+    unsigned char *dones;
+    unsigned dp;
+};
+
+cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, unsigned B,
+                               float beta, unsigned long long seed, const SampleOut &o,
+                               int num_sms, cudaStream_t st);
+
+struct RankWork {
+    float *raw;
+    double *cdf;
+    unsigned *keys[2];
+    unsigned *vals[2];
+    unsigned *digit_hist;  // [4][256]
+    unsigned *tile_hist;   // [256][ntiles]
+    unsigned long long capacity;
+};
+
+cudaError_t launch_build_cdf(double *cdf, unsigned long long capacity, double alpha,
+                             cudaStream_t st);
+
+// Sorts the `size` filled slots by raw priority descending, ties by slot ascending, leaving
+// the slot order in *sorted (a pointer into w.vals).
+cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned **sorted,
+                             cudaStream_t st);
+
+cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,
+                               Ctl *ctl, unsigned B, float beta, double alpha,
+                               unsigned long long seed, const SampleOut &o, int num_sms,
+                               cudaStream_t st);
+
+unsigned long long rank_tile_count(unsigned long long capacity);
+
+}  // namespace gbper

@@ -1,0 +1,321 @@
+"""GPU parity: libgbper (through the C ABI) against the oracle, element by element, on the
+same seeded inputs.  Indices bit-exact except oracle-marked boundary draws (< 0.01%), sums
+within 1e-6 relative (built to be bit-identical), IS weights within 1e-5 relative, gathered
+fields byte-exact."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines skip this module
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from rl_infra_gb300 import capi  # noqa: E402
+from rl_infra_gb300 import workloads as wl  # noqa: E402
+from tests import harness  # noqa: E402
+from tests.gpu_helpers import Pair, dev, prefill  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from rl_infra_gb300 import build
+    build.build()
+    capi.load()
+
+
+def _small(name, **kw):
+    w = wl.WORKLOADS[name]
+    return wl.Workload(**{**w.__dict__, **kw})
+
+
+# -- the small workload, end to end --------------------------------------------------------
+
+def test_tiny_workload_rounds():
+    w = wl.WORKLOADS["tiny"]
+    g = wl.rng(0)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, seed=0)
+    prefill(p, w, g)
+    p.check_tree()
+    p.check_counters()
+    for _ in range(w.rounds):
+        _, want = p.sample(w.batch, w.beta)
+        p.update(want["idx"], wl.td_errors(g, w.batch))
+        p.check_tree()
+        p.check_counters()
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
+@pytest.mark.parametrize("capacity,count", [(1, 1), (2, 2), (3, 3), (1000, 700), (4096, 4096),
+                                            (5000, 3000), (1 << 14, 1 << 14)])
+def test_partial_and_ragged_fills(capacity, count):
+    w = _small("tiny", capacity=capacity)
+    g = wl.rng(1, capacity)
+    p = Pair(capacity, 8, 8, 0.6, 1e-6, 0, seed=3)
+    prefill(p, w, g, count=count, chunk=max(1, count // 3))
+    p.check_tree()
+    p.check_counters()
+    for B in (1, 7, 32, 2 * count + 5):
+        _, want = p.sample(B, 0.4)
+        assert np.all(want["idx"] < count)
+        p.update(want["idx"], wl.td_errors(g, B))
+        p.check_tree()
+    p.check_counters()
+    p.close()
+
+
+def test_ring_wrap_and_oversized_insert():
+    cap = 3000
+    w = _small("tiny", capacity=cap, state_dim=5, row_stride=7)
+    g = wl.rng(2)
+    p = Pair(cap, 5, 7, 0.6, 1e-6, 0, seed=4)
+    for count, with_prio in ((1000, True), (1500, False), (1200, True), (7001, True), (1, False),
+                             (2999, False), (3000, True), (250, True)):
+        rows = wl.transitions(g, count, w)
+        prio = wl.raw_priorities(g, count, "lognormal") if with_prio else None
+        p.add(rows, prio)
+        p.check_tree()
+        p.check_counters()
+        _, want = p.sample(64, 0.5)
+        p.update(want["idx"], wl.td_errors(g, 64))
+    assert np.array_equal(p.gpu.read_state(capi.PER_STATE_STATES).reshape(cap, 5),
+                          p.orc.ring_states())
+    p.close()
+
+
+@pytest.mark.parametrize("d,dp", [(0, 0), (1, 1), (3, 8), (8, 8), (48, 64), (64, 64), (63, 65)])
+def test_gather_row_shapes(d, dp):
+    cap = 4096
+    w = _small("tiny", capacity=cap, state_dim=d, row_stride=dp)
+    g = wl.rng(3, d * 100 + dp)
+    p = Pair(cap, d, dp, 0.6, 1e-6, 0, seed=5)
+    prefill(p, w, g)
+    for B in (1, 33, 1000):
+        _, want = p.sample(B, 0.4)
+        p.update(want["idx"], wl.td_errors(g, B))
+    p.check_tree()
+    p.close()
+
+
+def test_update_duplicates_nan_inf_and_bad_indices():
+    cap = 1 << 12
+    w = _small("tiny", capacity=cap)
+    g = wl.rng(4)
+    p = Pair(cap, 8, 8, 0.7, 1e-6, 0, seed=6)
+    prefill(p, w, g, count=cap - 100)
+    for rnd in range(6):
+        _, want = p.sample(512, 0.5)
+        idx = wl.duplicate_positions(g, want["idx"], 0.25)
+        td = wl.td_errors(g, 512)
+        if rnd == 2:
+            td[:5] = [np.nan, np.inf, -np.inf, 0.0, -0.0]
+            td[7] = 1e30
+        if rnd == 3:
+            idx[10] = -5
+            idx[11] = cap - 50          # an unfilled slot: skipped
+            idx[12] = 1 << 40
+        p.update(idx, td)
+        p.check_tree()
+        p.check_counters()
+        flags = p.gpu.status_device()
+        assert flags == (capi.PER_DEVFLAG_BAD_INDEX if rnd == 3 else 0)
+    p.close()
+
+
+def test_update_all_in_one_subtree_overflow_path():
+    """More entries than one CTA sorts at once land in one subtree: the chunked path."""
+    cap = 1 << 16
+    w = _small("tiny", capacity=cap)
+    g = wl.rng(5)
+    p = Pair(cap, 8, 8, 0.6, 1e-6, 0, seed=7)
+    prefill(p, w, g)
+    for B in (4096, 20000):
+        idx = g.integers(0, 300, size=B).astype(np.int64)   # all inside the first subtree
+        p.update(idx, wl.td_errors(g, B))
+        p.check_tree()
+        p.check_counters()
+    _, want = p.sample(1024, 0.4)
+    p.close()
+
+
+def test_equal_priorities_and_beta_zero():
+    cap = 1 << 12
+    w = _small("tiny", capacity=cap)
+    g = wl.rng(6)
+    p = Pair(cap, 8, 8, 1.0, 1e-6, 0, seed=8)
+    rows = wl.transitions(g, cap, w)
+    p.add(rows, np.full(cap, 0.5, np.float32))
+    got, want = p.sample(cap, 0.0)
+    assert np.all(got["w"].cpu().numpy() == 1.0)
+    got, want = p.sample(cap, 0.7)
+    gi = got["idx"].cpu().numpy()
+    assert np.array_equal(np.sort(gi), np.arange(cap))  # one draw per leaf
+    p.close()
+
+
+def test_many_sizes_of_batch_and_tree():
+    for D in (1, 4, 5, 6, 9, 10, 11, 15, 16):
+        cap = 1 << D
+        w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
+        g = wl.rng(7, D)
+        p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=D)
+        prefill(p, w, g)
+        for B in (1, 31, 32, 33, 257, 2049):
+            _, want = p.sample(B, 0.4)
+            p.update(want["idx"], wl.td_errors(g, B))
+        p.check_tree()
+        p.check_counters()
+        p.close()
+
+
+# -- rank-based variant ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("cap,fill", [(1, 1), (100, 37), (4095, 4095), (4096, 4096), (4097, 4097),
+                                      (100000, 65536)])
+def test_rank_small(cap, fill):
+    w = _small("rank", capacity=cap, state_dim=6, row_stride=8)
+    g = wl.rng(8, cap)
+    p = Pair(cap, 6, 8, 0.7, 1e-6, 1, seed=9)
+    prefill(p, w, g, count=fill, chunk=max(1, fill // 2))
+    cdf = p.gpu.read_state(capi.PER_STATE_CDF)
+    harness.assert_sums_close(cdf[1:], p.orc.cdf()[1:], what="rank CDF")
+    for rnd in range(3):
+        _, want = p.sample(min(1024, 4 * fill + 1), 0.5)
+        idx = want["idx"].copy()
+        td = wl.td_errors(g, len(idx))
+        if rnd == 1:
+            idx[: len(idx) // 4] = idx[len(idx) // 4: 2 * (len(idx) // 4)]
+        p.update(idx, td)
+        p.check_tree()
+        p.check_counters()
+    p.close()
+
+
+def test_rank_ties_keep_slot_order():
+    cap = 9000
+    w = _small("rank", capacity=cap, state_dim=4, row_stride=4)
+    g = wl.rng(9)
+    p = Pair(cap, 4, 4, 0.7, 1e-6, 1, seed=10)
+    rows = wl.transitions(g, cap, w)
+    prio = np.repeat(np.array([0.5, 2.0, 1.0], np.float32), cap // 3)
+    p.add(rows, prio)
+    for _ in range(3):
+        p.sample(1024, 0.5)
+    p.close()
+
+
+# -- the full-size workloads (sampled checks) -------------------------------------------------
+
+@pytest.mark.slow
+def test_apex_full_size_rounds():
+    w = wl.WORKLOADS["apex"]
+    g = wl.rng(10)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, seed=0)
+    prefill(p, w, g)
+    p.check_tree()
+    staging = wl.transitions(wl.rng(10, 1), w.staging, w)
+    for r in range(12):
+        lo = (r * w.ingest) % w.staging
+        rows = {k: v[lo: lo + w.ingest] for k, v in staging.items()}
+        p.add(rows, None)
+        _, want = p.sample(w.batch, w.beta)
+        p.update(want["idx"], wl.td_errors(g, w.batch))
+        if r % 4 == 3:
+            p.check_tree()
+            p.check_counters()
+    p.check_tree()
+    p.check_counters()
+    assert p.stats["mismatch"] <= harness.IDX_MISMATCH_CAP * p.stats["draws"]
+    p.close()
+
+
+@pytest.mark.slow
+def test_dqn_full_size_steps():
+    w = wl.WORKLOADS["dqn"]
+    g = wl.rng(11)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, seed=0)
+    prefill(p, w, g)  # prio 'max': every row at the running maximum
+    for t in (0, 1, 2, 170, 339, 340):
+        _, want = p.sample(w.batch, w.beta_at(t))
+        p.update(want["idx"], wl.td_errors(g, w.batch))
+    p.check_tree()
+    p.check_counters()
+    p.close()
+
+
+@pytest.mark.slow
+def test_stress_full_size_sampled():
+    """2^24 slots x 256 floats: rows drawn on the device (32 GiB), priorities on the host; the
+    oracle keeps the priority trees only and rows are checked by re-drawing their chunk."""
+    w = wl.WORKLOADS["stress"]
+    g = wl.rng(12)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, seed=0,
+             with_ring=False)
+    chunk = 1 << 18
+    for c in range(w.capacity // chunk):
+        s, n = wl.device_rows(torch, 12, c, chunk, w.state_dim)
+        a, r, d = wl.device_scalars(torch, 12, c, chunk, w)
+        prio = wl.raw_priorities(g, chunk, w.prio)
+        p.gpu.add(s, n, a, r, d, dev(prio))
+        p.orc.add(raw_prio=prio, count=chunk)
+        del s, n
+    p.check_tree()
+    for rnd in range(3):
+        got, want = p.sample(w.batch, w.beta, check_rows=False)
+        idx = wl.duplicate_positions(g, want["idx"], w.dup_frac)
+        p.update(idx, wl.td_errors(g, w.batch))
+        # rows of a sample of draws against their re-drawn source chunk
+        gi = got["idx"].cpu().numpy()
+        for j in np.linspace(0, w.batch - 1, 16).astype(int):
+            slot = int(gi[j])
+            s, n = wl.device_rows(torch, 12, slot // chunk, chunk, w.state_dim)
+            assert torch.equal(got["states"][j], s[slot % chunk])
+            assert torch.equal(got["next_states"][j], n[slot % chunk])
+            a, r, d = wl.device_scalars(torch, 12, slot // chunk, chunk, w)
+            assert int(got["actions"][j]) == int(a[slot % chunk])
+            assert float(got["rewards"][j]) == float(r[slot % chunk])
+            assert int(got["dones"][j]) == int(d[slot % chunk])
+    p.check_tree()
+    p.check_counters()
+    p.close()
+
+
+@pytest.mark.slow
+def test_rank_full_size_steps():
+    w = wl.WORKLOADS["rank"]
+    g = wl.rng(13)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, seed=0)
+    prefill(p, w, g)
+    for _ in range(4):
+        _, want = p.sample(w.batch, w.beta)
+        p.update(want["idx"], wl.td_errors(g, w.batch))
+        p.check_tree()
+    p.check_counters()
+    p.close()
+
+
+# -- error paths (host-side rejection, no launch) ---------------------------------------------
+
+def test_invalid_arguments_rejected():
+    b = capi.ReplayBuffer(64, 4)
+    h = b._h
+    s = capi.per_sample(h, 8, 0.4, None, None, None, None, None, None, None, None)
+    assert s == capi.PER_ERR_INVALID_ARG
+    idx = torch.empty(8, dtype=torch.int64, device="cuda")
+    s = capi.per_sample(h, 8, 0.4, idx.data_ptr(), None, None, None, None, None, None, None)
+    assert s == capi.PER_ERR_EMPTY
+    s = capi.per_sample(h, 0, 0.4, idx.data_ptr(), None, None, None, None, None, None, None)
+    assert s == capi.PER_ERR_INVALID_ARG
+    s, _ = capi.per_min(h, None)
+    assert s == capi.PER_ERR_EMPTY
+    with pytest.raises(capi.PerError):
+        capi.ReplayBuffer(0, 4)
+    with pytest.raises(capi.PerError):
+        capi.ReplayBuffer(16, 8, row_stride_out=4)
+    with pytest.raises(capi.PerError):
+        capi.ReplayBuffer(16, 8, eps=0.0)
+    b.close()
