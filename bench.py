@@ -1,0 +1,480 @@
+"""Benchmark of the prioritized-replay hot path: PER steps/s on the 2^21-leaf, B=512 workload.
+
+One step = ingest 4096 rows at the ring cursor (priority = running maximum), draw a stratified
+batch of 512 (Philox + descent + IS weights + row gather), update the 512 priorities from TD
+errors.  Inputs (staging rows, TD errors) are resident in device memory before timing; L2 is
+flushed (a 512 MiB device write) between timed steps, outside the per-step CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica on its
+own GPU (the path has no cross-GPU exchange); the reported time is the maximum over ranks.
+--impl reference times the CPU oracle (test infrastructure, single thread) on the same
+workload, a bounded number of steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PER steps/s at 2^21 leaves, B=512 (sample+IS+gather+update); HBM GB/s"
+UNIT = "steps/s"
+WORKLOAD = "apex"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# -- algorithmic bytes (the byte model) -------------------------------------------------------
+
+def distinct_ancestors(leaves: np.ndarray, D: int, levels: range) -> int:
+    """Number of distinct nodes over the given heights above the given leaves."""
+    u = np.unique(np.asarray(leaves, dtype=np.int64))
+    return int(sum(len(np.unique(u >> h)) for h in levels))
+
+
+def bytes_ingest(count, d, D, cursor, C):
+    slots = (cursor + np.arange(count, dtype=np.int64)) % C
+    nodes = distinct_ancestors(slots, D, range(1, D + 1))
+    rows = count * 2 * (4 * d) * 2           # states + next: read source, write ring
+    scalars = count * (4 + 4 + 1) * 2        # actions, rewards, dones: read + write
+    return rows + scalars + 4 * count + 36 * nodes
+
+
+def bytes_sample(idx, d, dp, D):
+    # left child read at every visited internal node: distinct path nodes at depths 0..D-1
+    path_nodes = distinct_ancestors(idx, D, range(1, D + 1))
+    B = len(idx)
+    descent = 8 * path_nodes + 4 * B
+    weights = 8 * B
+    gather = B * (2 * (4 * d + 4 * dp) + (4 + 4 + 1) * 2 + 8)
+    return descent + weights + gather
+
+
+def bytes_update(idx, D):
+    B = len(idx)
+    nodes = distinct_ancestors(idx, D, range(1, D + 1))
+    return 12 * B + 4 * len(np.unique(idx)) + 36 * nodes
+
+
+def kernel_source_hash(name):
+    p = os.path.join(ROOT, "rl_infra_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_file):
+    """Per-launch DRAM bytes of a kernel, from the committed ncu summary, if the kernel's source
+    is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash(kernel_file)
+    for line in open(p):
+        parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if parts.get("file") == kernel_file and parts.get("src_sha") == want:
+            try:
+                return float(parts["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+# -- clocks during the timed region -------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# -- the GPU arm ---------------------------------------------------------------------------------
+
+def setup_gpu(torch, w, seed=0):
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, seed)
+    g = wl.rng(seed, 77)
+    chunk = 1 << 18
+    for c in range(w.capacity // chunk):
+        s, n = wl.device_rows(torch, seed, c, chunk, w.state_dim)
+        a, r, d = wl.device_scalars(torch, seed, c, chunk, w)
+        prio = torch.from_numpy(wl.raw_priorities(g, chunk, w.prio)).cuda()
+        buf.add(s, n, a, r, d, prio)
+    s, n = wl.device_rows(torch, seed + 1, 0, w.staging, w.state_dim)
+    a, r, d = wl.device_scalars(torch, seed + 1, 0, w.staging, w)
+    staging = {"states": s, "next_states": n, "actions": a, "rewards": r, "dones": d}
+    torch.cuda.synchronize()
+    return buf, staging, g
+
+
+def _check(L, h, status, what):
+    if status != 0:
+        raise RuntimeError(f"{what}: status {status}: {L.per_last_error(h).decode()}")
+
+
+def _ring_ptrs(t: dict, lo: int):
+    """Device addresses of row `lo` of each staging array (states, next, actions, rewards, dones)."""
+    out = []
+    for k in ("states", "next_states", "actions", "rewards", "dones"):
+        v = t[k]
+        row = v.element_size() * (v.shape[1] if v.dim() > 1 else 1)
+        out.append(v.data_ptr() + lo * row)
+    return out
+
+
+def _out_ptrs(out: dict):
+    return [out[k].data_ptr() for k in ("idx", "w", "states", "next_states", "actions", "rewards",
+                                         "dones")]
+
+
+def run_gpu(args, rank, world):
+    import ctypes
+    import torch
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", dev))
+    buf, staging, g = setup_gpu(torch, w)
+    L, h = capi.load(), buf._h
+    K, W = args.steps, args.warmup
+    B, I = w.batch, w.ingest
+    td = torch.from_numpy(wl.td_errors(g, (K + W) * B)).cuda()
+    out = buf.alloc_batch(B)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    st = ctypes.c_void_p(stream.cuda_stream)
+    beta = ctypes.c_float(w.beta)
+    # every pointer of the step, computed once: the timed loop only issues the three C calls
+    add_args = [(h, I, *_ring_ptrs(staging, o * I), None, st) for o in range(w.staging // I)]
+    sample_args = (h, B, beta, *_out_ptrs(out), st)
+    idx_ptr, td0 = out["idx"].data_ptr(), td.data_ptr()
+    n_ofs = len(add_args)
+
+    def step(t, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        _check(L, h, L.per_add(*add_args[t % n_ofs]), "per_add")
+        if ev is not None:
+            ev[1].record(stream)
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        if ev is not None:
+            ev[2].record(stream)
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * t, st), "per_update")
+        if ev is not None:
+            ev[3].record(stream)
+
+    for t in range(W):
+        step(t)
+        flush.zero_()
+    torch.cuda.synchronize()
+    cursor0 = int(buf.read_state(capi.PER_STATE_COUNTERS, 1, 1)[0])  # device cursor before timing
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(dev) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0 = time.perf_counter()
+    for t in range(K):
+        step(W + t, evs[t])
+        flush.zero_()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+
+    per = np.array([[evs[t][i].elapsed_time(evs[t][i + 1]) for i in range(3)] for t in range(K)])
+    step_ms = per.sum(axis=1)
+    total_s = float(step_ms.sum()) / 1e3
+    if dist:
+        tt = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    value = world * K / total_s
+    if buf.status_device() != 0:
+        raise RuntimeError("device error flag raised during the benchmark")
+
+    # byte model from this run's actual indices and ring range
+    idx = out["idx"].cpu().numpy()
+    D = int(np.log2(buf.nleaves))
+    b_add = bytes_ingest(I, w.state_dim, D, cursor0, w.capacity)
+    b_sam = bytes_sample(idx, w.state_dim, w.row_stride, D)
+    b_upd = bytes_update(idx, D)
+    ops = {
+        "k_add": (float(np.median(per[:, 0])), b_add, "k_tree.cu"),
+        "k_sample_prop": (float(np.median(per[:, 1])), b_sam, "k_sample.cu"),
+        "k_update": (float(np.median(per[:, 2])), b_upd, "k_tree.cu"),
+    }
+    peak, peak_src = load_peaks()
+    dom = max(ops, key=lambda k: ops[k][0])
+    ms, byt, src = ops[dom]
+    achieved = byt / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 5),
+                "traffic": traffic_from_profiles(src), "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": int(byt), "median_launch_us": round(ms * 1e3, 3)}
+    step_bytes = b_add + b_sam + b_upd
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; rows N(0,1) drawn on the device, lognormal(0,1) priorities)",
+        "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step, "
+                               "alpha 0.6, beta 0.4",
+                   "l2": "flushed between steps (512 MiB write, outside the step events)",
+                   "timing": "per-step CUDA events on the launching stream; value = steps / sum",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "wall_s_timed_loop": round(wall, 4)},
+        "hbm_gbs_algorithmic": round(step_bytes / (total_s / K) / 1e9 / world, 2),
+        "bytes_per_step": {"k_add": int(b_add), "k_sample_prop": int(b_sam), "k_update": int(b_upd)},
+        "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
+        "roofline": roofline,
+        "gpu_launches": 3 * K,
+    }
+    if clk:
+        res["clocks"] = clk
+    res["e2e"] = run_e2e(torch, buf, w, staging, g, min(K, 4000), dist)
+    buf.close()
+    if dist:
+        dist.destroy_process_group()
+    return res
+
+
+def run_e2e(torch, buf, w, staging, g, K, dist):
+    """Steps/s through the public C calls with the inputs in pinned host memory: each step copies
+    its ingest rows and TD errors host->device (one packed copy) and the sampled batch
+    device->host (one packed copy), inside the timing."""
+    import ctypes
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    L, h = capi.load(), buf._h
+    B, I, d = w.batch, w.ingest, w.state_dim
+    n_ofs = w.staging // I
+    # packed host arena per step: states | next | actions | rewards | dones | pad | td
+    sizes = [("states", I * d * 4), ("next_states", I * d * 4), ("actions", I * 4),
+             ("rewards", I * 4), ("dones", I), ("td", B * 4)]
+    offs, o = {}, 0
+    for k, n in sizes:
+        offs[k] = o
+        o = (o + n + 255) // 256 * 256
+    arena = o
+    host_in = torch.empty((n_ofs, arena), dtype=torch.uint8).pin_memory()
+    td_all = wl.td_errors(g, n_ofs * B).reshape(n_ofs, B)
+    for s_ in range(n_ofs):
+        lo = s_ * I
+        for k, n in sizes[:-1]:
+            v = staging[k][lo:lo + I].contiguous().view(torch.uint8).reshape(-1).cpu()
+            host_in[s_, offs[k]:offs[k] + n] = v
+        host_in[s_, offs["td"]:offs["td"] + B * 4] = torch.from_numpy(td_all[s_].view(np.uint8))
+    dev_in = torch.empty(arena, dtype=torch.uint8, device="cuda")
+    # packed device output arena: idx | w | states | next | actions | rewards | dones
+    osz = [("idx", B * 8), ("w", B * 4), ("states", B * w.row_stride * 4),
+           ("next_states", B * w.row_stride * 4), ("actions", B * 4), ("rewards", B * 4),
+           ("dones", B)]
+    ooffs, o = {}, 0
+    for k, n in osz:
+        ooffs[k] = o
+        o = (o + n + 255) // 256 * 256
+    dev_out = torch.empty(o, dtype=torch.uint8, device="cuda")
+    host_out = torch.empty(o, dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream()
+    st = ctypes.c_void_p(stream.cuda_stream)
+    base_in, base_out = dev_in.data_ptr(), dev_out.data_ptr()
+    add_args = (h, I, base_in + offs["states"], base_in + offs["next_states"],
+                base_in + offs["actions"], base_in + offs["rewards"], base_in + offs["dones"],
+                None, st)
+    sample_args = (h, B, ctypes.c_float(w.beta), *[base_out + ooffs[k] for k, _ in osz], st)
+    upd_args = (h, B, base_out + ooffs["idx"], base_in + offs["td"], st)
+
+    def step(t):
+        dev_in.copy_(host_in[t % n_ofs], non_blocking=True)
+        _check(L, h, L.per_add(*add_args), "per_add")
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        _check(L, h, L.per_update_priorities(*upd_args), "per_update")
+        host_out.copy_(dev_out, non_blocking=True)
+
+    for t in range(3):
+        step(t)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(K):
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3
+    world = 1
+    if dist:
+        tt = torch.tensor([secs], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        secs = float(tt.item())
+        world = dist.get_world_size()
+    return {"value": round(world * K / secs, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(sum(n for _, n in sizes)),
+            "d2h_bytes_per_step": int(sum(n for _, n in osz)), "steps": K,
+            "note": "pinned host rows + TD errors in, sampled batch out, inside the timing"}
+
+
+# -- the oracle on the host cores ------------------------------------------------------------------
+
+def oracle_steps_per_s(budget_s=12.0, max_steps=None):
+    import oracle
+    from rl_infra_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    g = wl.rng(0, 99)
+    o = oracle.Oracle(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, 0, True)
+    chunk = 1 << 18
+    for _ in range(w.capacity // chunk):
+        rows = wl.transitions(g, chunk, w)
+        o.add(rows["states"], rows["next_states"], rows["actions"], rows["rewards"],
+              rows["dones"], wl.raw_priorities(g, chunk, w.prio))
+    staging = wl.transitions(g, w.staging, w)
+    td = wl.td_errors(g, 64 * w.batch).reshape(64, w.batch)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        lo = (steps * w.ingest) % w.staging
+        o.add(*(staging[k][lo:lo + w.ingest] for k in
+                ("states", "next_states", "actions", "rewards", "dones")), None)
+        s = o.sample(w.batch, w.beta)
+        o.update(s["idx"], td[steps % 64])
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and steps >= max_steps):
+            break
+    o.close()
+    return steps / el, steps, el
+
+
+def cpu_info():
+    model = ""
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return model, os.cpu_count()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = min(args.cpu_budget * max(1, args.steps // 1000), 120.0)
+        sps, n, el = oracle_steps_per_s(budget_s=budget, max_steps=args.steps + args.warmup)
+        model, cores = cpu_info()
+        res = {"metric": METRIC, "value": round(sps, 3), "unit": UNIT, "n_gpus": world,
+               "steps": n, "warmup": 0, "ms_per_step": round(1e3 / sps, 4),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic (seeded)", "impl": "reference",
+               "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step"},
+               "cpu_baseline": {"value": round(sps, 3), "unit": UNIT, "cores": 1,
+                                "kind": "oracle", "sample": f"{n} apex steps in {el:.1f} s",
+                                "cpu": model, "host_cores": cores},
+               "e2e": {"value": round(sps, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(res))
+        return
+
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            sps, n, el = oracle_steps_per_s(budget_s=args.cpu_budget)
+            model, cores = cpu_info()
+            res["cpu_baseline"] = {"value": round(sps, 3), "unit": UNIT, "cores": 1,
+                                   "kind": "oracle", "sample": f"{n} apex steps in {el:.1f} s",
+                                   "cpu": model, "host_cores": cores}
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -276,6 +276,16 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
         const unsigned bm = block_max_u32(mymax);
         if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
     } else {
+        // rows that a later row of the same call overwrites still count toward the running
+        // maximum, as if they had been inserted one after another
+        unsigned mymax = 0;
+        if (a.prio) {
+            const unsigned long long t0 = (unsigned long long)(blockIdx.x - a.ntree) * kThreads + tid;
+            for (unsigned long long k = t0; k < a.k0; k += (unsigned long long)a.ncopy * kThreads)
+                mymax = max(mymax, __float_as_uint(prio_to_raw(__ldg(a.prio + k), a.eps, max_prev)));
+        }
+        const unsigned bm = block_max_u32(mymax);
+        if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
         // row copies: one warp per row, rows strided over the copy CTAs
         const unsigned long long cnt = a.count - a.k0;
         const int warp = tid >> 5, lane = tid & 31;
@@ -334,6 +344,11 @@ __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
     const unsigned long long wglob = (unsigned long long)blockIdx.x * (kThreads / 32) + warp;
     const unsigned long long wtotal = (unsigned long long)gridDim.x * (kThreads / 32);
     unsigned mymax = 0;
+    if (a.prio) {  // overwritten rows of this call still count toward the running maximum
+        const unsigned long long t0 = (unsigned long long)blockIdx.x * kThreads + threadIdx.x;
+        for (unsigned long long k = t0; k < a.k0; k += (unsigned long long)gridDim.x * kThreads)
+            mymax = max(mymax, __float_as_uint(prio_to_raw(__ldg(a.prio + k), a.eps, max_prev)));
+    }
     for (unsigned long long o = wglob; o < cnt; o += wtotal) {
         const unsigned long long k = a.k0 + o;
         const unsigned long long slot = (s0 + o) % C;
