@@ -208,6 +208,31 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
 /* per_nleaves -- the tree's leaf count (power of two >= capacity). */
 per_status per_nleaves(const per_buffer *h, uint64_t *out);
 
+/*
+ * per_rank_order_noalloc -- the slot order of the rank-based variant without a replay
+ * buffer and without allocating: d_order[r-1] receives the slot of rank r, where rank 1 holds
+ * the largest of d_raw[0, n) and equal priorities keep ascending slot order.  It runs the
+ * same radix-sort kernels that per_sample uses in rank mode.  The pages have no counterpart:
+ * this call exists for callers that may not allocate device memory -- code enqueuing work
+ * while a CUDA graph is being captured (cudaMalloc is not permitted then), real-time loops
+ * that forbid allocator latency, or hosts whose device memory belongs to another framework's
+ * pool.  The call itself makes no cudaMalloc, cudaFree or other allocating call.
+ *   d_raw   [n] float, device, > 0 and finite (caller-owned input).
+ *   d_order [n] uint32, device (caller-owned output).
+ *   n       1 .. 262144 (2^18); larger n returns PER_ERR_INVALID_ARG.
+ * Scratch: a fixed device array of 4 MiB + 64 KiB compiled into the library, which every GPU
+ * that loads the library holds until the process exits.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) and caches it; make that first call on
+ * each device before any stream capture begins.  All calls share the one array and it keeps
+ * the last call's contents (every call overwrites all it reads, so nothing has to start at
+ * zero); calls whose GPU work overlaps -- on different streams, or concurrently from several
+ * host threads -- race on it and must be serialised by the caller.
+ * Errors: PER_ERR_INVALID_ARG (NULL or misaligned pointer, n out of range), PER_ERR_CUDA.
+ * It records no message for per_last_error.
+ */
+per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uint32_t *d_order,
+                                  void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,7 +42,7 @@ _STATE_DTYPE = {
 # every symbol include/gbper.h declares
 EXPORTS = ("per_create", "per_destroy", "per_add", "per_sample", "per_update_priorities",
            "per_total", "per_min", "per_size", "per_status_device", "per_last_error",
-           "per_read_state", "per_nleaves")
+           "per_read_state", "per_nleaves", "per_rank_order_noalloc")
 
 
 class per_config(ctypes.Structure):
@@ -103,6 +103,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.per_last_error.restype = ctypes.c_char_p
         L.per_read_state.argtypes = [vp, u32, u64, u64, vp, vp]
         L.per_read_state.restype = st
+        L.per_rank_order_noalloc.argtypes = [vp, u32, vp, vp]
+        L.per_rank_order_noalloc.restype = st
         _lib = L
         return L
 
@@ -173,6 +175,11 @@ def per_last_error(h):
 
 def per_read_state(h, which, first, count, host_dst, stream):
     return load().per_read_state(h, which, first, count, host_dst, stream)
+
+
+def per_rank_order_noalloc(d_raw, n, d_order, stream):
+    """Slot order by raw priority, descending, without any device allocation (n <= 2^18)."""
+    return load().per_rank_order_noalloc(d_raw, n, d_order, stream)
 
 
 # -- torch-facing convenience ---------------------------------------------------------------

@@ -222,3 +222,77 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
 }
 
 }  // namespace gbper
+
+// ------------------------------------------------------------------------------------------
+// per_rank_order_noalloc: the same descending sort for callers that may not allocate device
+// memory.  Its scratch (key and value ping-pong buffers, tile histograms) is a file-scope
+// device array of fixed size, resolved to a device address once per device.
+// ------------------------------------------------------------------------------------------
+#include "gbper.h"
+
+#include <mutex>
+
+namespace gbper {
+namespace {
+
+constexpr unsigned long long kNoAllocMaxKeys = 1ull << 18;
+constexpr unsigned long long kNoAllocTiles = (kNoAllocMaxKeys + kTile - 1) / kTile;
+constexpr unsigned long long kNoAllocWords = 4 * kNoAllocMaxKeys + 256 * kNoAllocTiles;
+constexpr int kNoAllocMaxDevices = 64;
+
+// 4 MiB + 64 KiB per device, held by every device that loads the library until exit.
+__device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocWords];
+
+std::mutex g_noalloc_mu;
+unsigned *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (host code cannot use the symbol
+// itself: on the host it names a stand-in, not device memory).
+cudaError_t noalloc_scratch(unsigned **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace gbper
+
+extern "C" per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uint32_t *d_order,
+                                             void *stream)
+{
+    using namespace gbper;
+    if (!d_raw || !d_order || n == 0 || n > kNoAllocMaxKeys) return PER_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_raw) % 4 || reinterpret_cast<uintptr_t>(d_order) % 4)
+        return PER_ERR_INVALID_ARG;
+    unsigned *base = nullptr;
+    if (noalloc_scratch(&base) != cudaSuccess) {
+        cudaGetLastError();
+        return PER_ERR_CUDA;
+    }
+    RankWork w{};
+    w.raw = const_cast<float *>(d_raw);
+    w.keys[0] = base;
+    w.keys[1] = base + kNoAllocMaxKeys;
+    w.vals[0] = base + 2 * kNoAllocMaxKeys;
+    w.vals[1] = base + 3 * kNoAllocMaxKeys;
+    w.tile_hist = base + 4 * kNoAllocMaxKeys;
+    w.capacity = n;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned *sorted = nullptr;
+    cudaError_t e = launch_rank_sort(w, n, &sorted, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_order, sorted, (size_t)n * sizeof(unsigned), cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess ? PER_OK : PER_ERR_CUDA;
+}
