@@ -151,6 +151,50 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# -- raw CUDA runtime calls for the timed loop (a few microseconds of host time per step, so the
+#    host stays ahead of the device and the events time device work only) -------------------------
+
+class Cudart:
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        lib = None
+        for name in ("libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so.13", "libcudart.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise RuntimeError("libcudart not found")
+        vp = ctypes.c_void_p
+        lib.cudaEventCreate.argtypes = [ctypes.POINTER(vp)]
+        lib.cudaEventRecord.argtypes = [vp, vp]
+        lib.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), vp, vp]
+        lib.cudaEventDestroy.argtypes = [vp]
+        lib.cudaMemsetAsync.argtypes = [vp, ctypes.c_int, ctypes.c_size_t, vp]
+        self.lib = lib
+
+    def events(self, n):
+        out = []
+        for _ in range(n):
+            e = self.ct.c_void_p()
+            if self.lib.cudaEventCreate(self.ct.byref(e)) != 0:
+                raise RuntimeError("cudaEventCreate failed")
+            out.append(e)
+        return out
+
+    def elapsed_ms(self, a, b):
+        v = self.ct.c_float()
+        if self.lib.cudaEventElapsedTime(self.ct.byref(v), a, b) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return v.value
+
+    def destroy(self, evs):
+        for e in evs:
+            self.lib.cudaEventDestroy(e)
+
+
 # -- the GPU arm ---------------------------------------------------------------------------------
 
 def setup_gpu(torch, w, seed=0):
@@ -207,9 +251,12 @@ def run_gpu(args, rank, world):
     L, h = capi.load(), buf._h
     K, W = args.steps, args.warmup
     B, I = w.batch, w.ingest
-    td = torch.from_numpy(wl.td_errors(g, (K + W) * B)).cuda()
+    TD_SLOTS = 4096
+    td = torch.from_numpy(wl.td_errors(g, TD_SLOTS * B)).cuda()
     out = buf.alloc_batch(B)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    evict = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    evict_out = torch.empty((), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     st = ctypes.c_void_p(stream.cuda_stream)
     beta = ctypes.c_float(w.beta)
@@ -219,26 +266,38 @@ def run_gpu(args, rank, world):
     idx_ptr, td0 = out["idx"].data_ptr(), td.data_ptr()
     n_ofs = len(add_args)
 
+    flush_l2 = args.l2 == "flush"
+    cr = Cudart()
+    rec, memset = cr.lib.cudaEventRecord, cr.lib.cudaMemsetAsync
+    flush_ptr, flush_n = flush.data_ptr(), flush.numel()
+
     def step(t, ev=None):
         if ev is not None:
-            ev[0].record(stream)
+            rec(ev[0], st)
         _check(L, h, L.per_add(*add_args[t % n_ofs]), "per_add")
-        if ev is not None:
-            ev[1].record(stream)
+        if ev is not None and ev[1] is not None:
+            rec(ev[1], st)
         _check(L, h, L.per_sample(*sample_args), "per_sample")
+        if ev is not None and ev[2] is not None:
+            rec(ev[2], st)
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * (t % TD_SLOTS), st),
+               "per_update")
         if ev is not None:
-            ev[2].record(stream)
-        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * t, st), "per_update")
-        if ev is not None:
-            ev[3].record(stream)
+            rec(ev[3], st)
+        if flush_l2:
+            # evict L2 between steps, outside the step's events: write 512 MiB, then read 256 MiB
+            # so the next step starts on clean, unrelated lines rather than a write-back backlog
+            memset(flush_ptr, 0, flush_n, st)
+            torch.sum(evict, 0, out=evict_out)
 
     for t in range(W):
         step(t)
-        flush.zero_()
     torch.cuda.synchronize()
     cursor0 = int(buf.read_state(capi.PER_STATE_COUNTERS, 1, 1)[0])  # device cursor before timing
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # timed region: K steps, each bracketed by two events on the launching stream (no events
+    # between the three calls, so each kernel's launch overlaps its predecessor's tail)
+    sev = cr.events(2 * K)
     clocks = ClockSampler(dev) if rank == 0 else None
     if dist:
         dist.barrier()
@@ -248,16 +307,68 @@ def run_gpu(args, rank, world):
         time.sleep(0.3)
     t0 = time.perf_counter()
     for t in range(K):
-        step(W + t, evs[t])
-        flush.zero_()
+        step(W + t, (sev[2 * t], None, None, sev[2 * t + 1]))
+    host_s = time.perf_counter() - t0
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
+    step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
+    cr.destroy(sev)
 
-    per = np.array([[evs[t][i].elapsed_time(evs[t][i + 1]) for i in range(3)] for t in range(K)])
-    step_ms = per.sum(axis=1)
+    # per-kernel breakdown (for the roofline): a second pass with an event between the calls.
+    # Each event pair also carries a launch (about 4 us on this GPU for an empty kernel), so
+    # these durations are upper bounds.
+    Kop = min(K, 4000)
+    flat = cr.events(4 * Kop)
+    for t in range(Kop):
+        step(W + K + t, flat[4 * t: 4 * t + 4])
+    torch.cuda.synchronize()
+    per = np.array([[cr.elapsed_ms(flat[4 * t + i], flat[4 * t + i + 1]) for i in range(3)]
+                    for t in range(Kop)])
+    cr.destroy(flat)
+
+    # the same step captured once per staging offset as a CUDA graph and replayed: the kernels
+    # advance their own device counters, so every replay inserts at the cursor and draws anew
+    graph_res = None
+    if args.graph:
+        graphs = []
+        for o in range(n_ofs):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+                a_args = add_args[o][:-1] + (cs,)
+                _check(L, h, L.per_add(*a_args), "per_add")
+                _check(L, h, L.per_sample(*(sample_args[:-1] + (cs,))), "per_sample")
+                _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * o, cs), "per_update")
+            graphs.append(gr)
+        torch.cuda.synchronize()
+        gK = K
+        gev = cr.events(2 * gK)
+        for t in range(W):
+            graphs[t % n_ofs].replay()
+            if flush_l2:
+                memset(flush_ptr, 0, flush_n, st)
+                torch.sum(evict, 0, out=evict_out)
+        torch.cuda.synchronize()
+        for t in range(gK):
+            rec(gev[2 * t], st)
+            graphs[t % n_ofs].replay()
+            rec(gev[2 * t + 1], st)
+            if flush_l2:
+                memset(flush_ptr, 0, flush_n, st)
+                torch.sum(evict, 0, out=evict_out)
+        torch.cuda.synchronize()
+        gms = np.array([cr.elapsed_ms(gev[2 * t], gev[2 * t + 1]) for t in range(gK)])
+        cr.destroy(gev)
+        if buf.status_device() != 0:
+            raise RuntimeError("device error flag raised during the graph replays")
+        graph_res = {"value": round(gK / (gms.sum() / 1e3), 2), "unit": UNIT,
+                     "ms_per_step": round(float(gms.mean()), 5),
+                     "median_us_per_step": round(float(np.median(gms)) * 1e3, 3), "steps": gK,
+                     "note": "one CUDA graph launch per step (ingest + sample + update)"}
+        del graphs
     total_s = float(step_ms.sum()) / 1e3
     if dist:
         tt = torch.tensor([total_s], dtype=torch.float64, device="cuda")
@@ -295,18 +406,28 @@ def run_gpu(args, rank, world):
         "data": "synthetic (seeded; rows N(0,1) drawn on the device, lognormal(0,1) priorities)",
         "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step, "
                                "alpha 0.6, beta 0.4",
-                   "l2": "flushed between steps (512 MiB write, outside the step events)",
-                   "timing": "per-step CUDA events on the launching stream; value = steps / sum",
+                   "l2": ("flushed between steps (512 MiB write + 256 MiB read, outside the step "
+                          "events)" if flush_l2 else "not flushed; inputs larger than L2 (1 GiB ring, "
+                          "48 MiB trees, 32 MiB staging; 129 MB L2)"),
+                   "timing": ("two CUDA events per step on the launching stream; value = steps / sum "
+                              "of step times; per-kernel figures from a second pass"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "wall_s_timed_loop": round(wall, 4)},
+                   "wall_s_timed_loop": round(wall, 4), "host_enqueue_s": round(host_s, 4)},
         "hbm_gbs_algorithmic": round(step_bytes / (total_s / K) / 1e9 / world, 2),
         "bytes_per_step": {"k_add": int(b_add), "k_sample_prop": int(b_sam), "k_update": int(b_upd)},
         "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
+        "ops_p99_us": {k: round(float(np.percentile(per[:, i], 99)) * 1e3, 3)
+                       for i, k in enumerate(ops)},
+        "ops_max_us": {k: round(float(per[:, i].max()) * 1e3, 3) for i, k in enumerate(ops)},
         "roofline": roofline,
         "gpu_launches": 3 * K,
+        "step_us_median": round(float(np.median(step_ms)) * 1e3, 3),
+        "step_us_p99": round(float(np.percentile(step_ms, 99)) * 1e3, 3),
     }
     if clk:
         res["clocks"] = clk
+    if graph_res:
+        res["graph"] = graph_res
     res["e2e"] = run_e2e(torch, buf, w, staging, g, min(K, 4000), dist)
     buf.close()
     if dist:
@@ -441,6 +562,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured as one CUDA graph per staging offset")
+    ap.add_argument("--l2", default="flush", choices=["flush", "warm"],
+                    help="flush L2 between timed steps, or rely on inputs larger than L2")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))

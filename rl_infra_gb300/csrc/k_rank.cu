@@ -186,6 +186,18 @@ __global__ void __launch_bounds__(1024) k_build_cdf(double *cdf, unsigned long l
 
 }  // namespace
 
+cudaError_t init_rank_kernels(int carveout)
+{
+    if (carveout < 0) return cudaSuccess;
+    const void *fns[] = {(const void *)k_rs_tile_hist, (const void *)k_rs_scan, (const void *)k_rs_scatter,
+                         (const void *)k_build_cdf};
+    for (const void *f : fns) {
+        const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 unsigned long long rank_tile_count(unsigned long long capacity)
 {
     return (capacity + kTile - 1) / kTile;

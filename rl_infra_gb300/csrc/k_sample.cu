@@ -80,6 +80,13 @@ __device__ __forceinline__ void write_scalars(const RingRefs &r, const SampleOut
     if (lane == 3 && o.dones) o.dones[j] = __ldg(r.dones + slot);
 }
 
+// a > b for binary64 values >= +0: their bit patterns order like the values, so the compare
+// runs on the integer pipe (GB300's binary64 pipe retires far fewer lanes per cycle).
+__device__ __forceinline__ bool gt_nonneg(double a, double b)
+{
+    return __double_as_longlong(a) > __double_as_longlong(b);
+}
+
 // Walk k levels below `node` whose left children are all internal nodes.
 __device__ __forceinline__ unsigned long long walk_internal(const double *__restrict__ S,
                                                             unsigned long long node, int k,
@@ -94,7 +101,7 @@ __device__ __forceinline__ unsigned long long walk_internal(const double *__rest
     int q = 0;
     for (int lev = 1; lev <= k; ++lev) {
         const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
-        if (left > m) {
+        if (gt_nonneg(left, m)) {
             q = 2 * q;
         } else {
             m = __dsub_rn(m, left);
@@ -107,8 +114,15 @@ __device__ __forceinline__ unsigned long long walk_internal(const double *__rest
 __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
 {
     extern __shared__ double s_top[];  // nodes 2 .. 2^(top+1)-1 at s_top[node - 2]
+    __shared__ double s_seg;
+    pdl_wait();
+    pdl_release();
     const int top = a.top;
     const int nstage = (1 << (top + 1)) - 2;
+    if (threadIdx.x == 0) {  // the stratum width T / B, once per CTA
+        const double tot = a.t.D == 0 ? (double)a.t.L[0] : a.t.S[1];
+        s_seg = __ddiv_rn(tot, (double)a.B);
+    }
     if (nstage > 0) {
         const double2 *src = reinterpret_cast<const double2 *>(a.t.S + 2);
         for (int i = threadIdx.x; i < nstage / 2; i += blockDim.x) {
@@ -120,12 +134,11 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
     __syncthreads();
     const unsigned long long n = a.t.n;
     const int D = a.t.D;
-    const double total = D == 0 ? (double)a.t.L[0] : a.t.S[1];
     const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
     const unsigned long long call = a.ctl->sample_calls;
     const unsigned long long size = a.ctl->size;
-    const double seg = __ddiv_rn(total, (double)a.B);
-    const double nbeta = -(double)a.beta;
+    const double seg = s_seg;
+    const float nbeta = -a.beta;
     const int lane = threadIdx.x & 31;
     const unsigned wpb = blockDim.x >> 5;
     const unsigned warps_total = gridDim.x * wpb;
@@ -135,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
 
     for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
         const double u = draw_uniform(a.seed, j, call, 0);
-        double m = __dmul_rn(__dadd_rn((double)j, u), seg);
+        double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         unsigned long long leaf;
         float lv;
         if (D == 0) {
@@ -145,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             unsigned long long node = 1;
             for (int l = 0; l < top; ++l) {
                 const double left = s_top[2 * node - 2];
-                if (left > m) {
+                if (gt_nonneg(left, m)) {
                     node = 2 * node;
                 } else {
                     m = __dsub_rn(m, left);
@@ -171,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             int q = 0;
             for (int lev = 1; lev < kL; ++lev) {
                 const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
-                if (left > m) {
+                if (gt_nonneg(left, m)) {
                     q = 2 * q;
                 } else {
                     m = __dsub_rn(m, left);
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             }
             {
                 const double left = (double)__shfl_sync(kFull, myleaf, 2 * q);
-                if (left > m) {
+                if (gt_nonneg(left, m)) {
                     q = 2 * q;
                 } else {
                     m = __dsub_rn(m, left);
@@ -194,12 +207,13 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             leaf = size - 1;
             lv = a.t.L[leaf];
         }
+        // rows first, so their loads are in flight while the weight is computed
+        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, leaf, lane, a.vec4);
+        write_scalars(a.r, a.o, j, leaf, lane);
         if (lane == 0) {
             a.o.idx[j] = (long long)leaf;
-            if (a.o.w) a.o.w[j] = __double2float_rn(pow(__ddiv_rn((double)lv, (double)pmin), nbeta));
+            if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
         }
-        write_scalars(a.r, a.o, j, leaf, lane);
-        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, leaf, lane, a.vec4);
     }
 
     __shared__ int s_last;
@@ -225,8 +239,7 @@ struct RankSampleArgs {
     RingRefs r;
     Ctl *ctl;
     unsigned B;
-    float beta;
-    double alpha;
+    float ab;  // alpha * beta, the exponent of the closed-form weight
     unsigned long long seed;
     SampleOut o;
     int vec4;
@@ -234,17 +247,21 @@ struct RankSampleArgs {
 
 __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
 {
+    __shared__ double s_seg;
+    pdl_wait();
+    pdl_release();
     const unsigned long long size = a.ctl->size;
     const unsigned long long call = a.ctl->sample_calls;
-    const double total = a.cdf[size];
-    const double seg = __ddiv_rn(total, (double)a.B);
-    const double ab = __dmul_rn(a.alpha, (double)a.beta);
+    if (threadIdx.x == 0) s_seg = __ddiv_rn(a.cdf[size], (double)a.B);
+    __syncthreads();
+    const double seg = s_seg;
+    const float fsize = (float)size;
     const int lane = threadIdx.x & 31;
     const unsigned wpb = blockDim.x >> 5;
     const unsigned warps_total = gridDim.x * wpb;
     for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
         const double u = draw_uniform(a.seed, j, call, 1);
-        const double m = __dmul_rn(__dadd_rn((double)j, u), seg);
+        const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         // first position p in [1, size] with cdf[p] > m; size + 1 when there is none
         unsigned long long lo = 1, hi = size + 1, ans = size + 1;
         while (true) {
@@ -255,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
             }
             if (len <= 32) {
                 const unsigned long long p = lo + lane;
-                const bool pred = p < hi && a.cdf[p] > m;
+                const bool pred = p < hi && gt_nonneg(a.cdf[p], m);
                 const unsigned b = __ballot_sync(kFull, pred);
                 ans = b ? lo + (__ffs(b) - 1) : hi;
                 break;
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
             const unsigned long long step = (len + 31) / 32;
             unsigned long long p = lo + (unsigned long long)(lane + 1) * step - 1;
             if (p > hi - 1) p = hi - 1;
-            const bool pred = a.cdf[p] > m;
+            const bool pred = gt_nonneg(a.cdf[p], m);
             const unsigned b = __ballot_sync(kFull, pred);
             if (b == 0) {
                 ans = hi;
@@ -285,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
         const unsigned long long slot = a.sorted[r - 1];
         if (lane == 0) {
             a.o.idx[j] = (long long)slot;
-            if (a.o.w) a.o.w[j] = __double2float_rn(pow(__ddiv_rn((double)r, (double)size), ab));
+            if (a.o.w) a.o.w[j] = powf(__fdiv_rn((float)r, fsize), a.ab);
         }
         write_scalars(a.r, a.o, j, slot, lane);
         if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, slot, lane, a.vec4);
@@ -334,6 +351,19 @@ bool rows_vec4(const RingRefs &r, const SampleOut &o)
 
 }  // namespace
 
+cudaError_t init_sample_kernels(int carveout)
+{
+    // the staged top levels need up to 2^13 - 2 doubles (64 KiB) when 12 levels are staged
+    cudaError_t e = cudaFuncSetAttribute(k_sample_prop, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    if (e != cudaSuccess || carveout < 0) return e;
+    const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank};
+    for (const void *f : fns) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, unsigned B,
                                float beta, unsigned long long seed, const SampleOut &o,
                                int num_sms, cudaStream_t st)
@@ -352,12 +382,7 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     const size_t smem = a.top > 0 ? (size_t)((1 << (a.top + 1)) - 2) * sizeof(double) : 0;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_sample_prop, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    k_sample_prop<<<grid, wpb * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_sample_prop, grid, wpb * 32, smem, st, a);
 }
 
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,
@@ -371,16 +396,14 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
     a.r = r;
     a.ctl = ctl;
     a.B = B;
-    a.beta = beta;
-    a.alpha = alpha;
+    a.ab = (float)(alpha * (double)beta);
     a.seed = seed;
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta();
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
-    k_sample_rank<<<grid, wpb * 32, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_sample_rank, grid, wpb * 32, 0, st, a);
 }
 
 }  // namespace gbper

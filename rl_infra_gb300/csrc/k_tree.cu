@@ -23,7 +23,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kAddBlockLog = 8;      // leaves per tree CTA in the insertion kernel: 256
 constexpr int kTopSpan = 1040;       // widest dirty span the last CTA handles on insertion
-constexpr int kUpdCap = 1024;        // batch entries one update CTA sorts in shared memory
 constexpr int kMaxTopLog = 10;       // update grid <= 2^10 CTAs
 
 __device__ __forceinline__ float fmin_tree(float a, float b) { return a < b ? a : b; }
@@ -88,24 +87,27 @@ __device__ void top_range_upsweep(const TreeRefs &t, int L0, unsigned long long 
                                   unsigned long long hi, double *spS0, float *spM0,
                                   double *spS1, float *spM1, double *exS, float *exM)
 {
-    if (L0 <= 0) return;
+    // run by warp 0 alone: every level is a handful of nodes, and a warp barrier is far cheaper
+    // than a CTA barrier per level
+    const int lane = threadIdx.x;
+    if (L0 <= 0 || lane >= 32) return;
     const unsigned long long lvl0 = 1ull << L0;
     // span at depth L0: [2(lo>>1), 2(hi>>1)+1]
     unsigned long long sp_lo = (lo >> 1) << 1;
     unsigned long long sp_hi = ((hi >> 1) << 1) + 1;
     const int w0 = (int)(sp_hi - sp_lo + 1);
-    for (int i = threadIdx.x; i < w0; i += blockDim.x) {
+    for (int i = lane; i < w0; i += 32) {
         spS0[i] = ld_sum_cg(t, lvl0 + sp_lo + i);
         spM0[i] = ld_min_cg(t, lvl0 + sp_lo + i);
     }
     // clean edge siblings of depths L0-1 .. 1: slot 2l (left) and 2l+1 (right)
-    for (int l = 1 + (int)threadIdx.x; l < L0; l += blockDim.x) {
+    for (int l = 1 + lane; l < L0; l += 32) {
         const unsigned long long a = lo >> (L0 - l), b = hi >> (L0 - l);
         const unsigned long long base = 1ull << l;
         if (a & 1ull) { exS[2 * l] = ld_sum_cg(t, base + a - 1); exM[2 * l] = ld_min_cg(t, base + a - 1); }
         if (!(b & 1ull)) { exS[2 * l + 1] = ld_sum_cg(t, base + b + 1); exM[2 * l + 1] = ld_min_cg(t, base + b + 1); }
     }
-    __syncthreads();
+    __syncwarp();
     double *curS = spS0, *nxtS = spS1;
     float *curM = spM0, *nxtM = spM1;
     unsigned long long a = lo, b = hi;  // dirty range at the current depth
@@ -115,7 +117,7 @@ __device__ void top_range_upsweep(const TreeRefs &t, int L0, unsigned long long 
         // next span at depth l-1 (only needed when l-1 >= 1)
         const unsigned long long nsp_lo = (pa >> 1) << 1;
         const unsigned long long pbase = 1ull << (l - 1);
-        for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        for (int i = lane; i < np; i += 32) {
             const unsigned long long p = pa + i;
             const int c = (int)(2 * p - sp_lo);
             const double s = curS[c] + curS[c + 1];
@@ -125,7 +127,7 @@ __device__ void top_range_upsweep(const TreeRefs &t, int L0, unsigned long long 
             nxtS[p - nsp_lo] = s;
             nxtM[p - nsp_lo] = m;
         }
-        if (threadIdx.x == 0 && l - 1 >= 1) {
+        if (lane == 0 && l - 1 >= 1) {
             if (pa & 1ull) { nxtS[0] = exS[2 * (l - 1)]; nxtM[0] = exM[2 * (l - 1)]; }
             if (!(pb & 1ull)) {
                 const int r = (int)(pb + 1 - nsp_lo);
@@ -133,7 +135,7 @@ __device__ void top_range_upsweep(const TreeRefs &t, int L0, unsigned long long 
                 nxtM[r] = exM[2 * (l - 1) + 1];
             }
         }
-        __syncthreads();
+        __syncwarp();
         double *ts = curS; curS = nxtS; nxtS = ts;
         float *tm = curM; curM = nxtM; nxtM = tm;
         sp_lo = nsp_lo;
@@ -209,12 +211,61 @@ __device__ __forceinline__ void copy_row(const AddArgs &a, unsigned long long k,
     }
 }
 
+// The inserted rows land on at most two contiguous slot ranges, [s0, endA) and [0, lenB), so
+// each array is copied as one or two flat streams: thread t moves elements t, t + stride, ...,
+// four of them in flight per pass (float4 for the state rows when their layout allows).
+template <typename V>
+__device__ __forceinline__ void copy_flat(V *dst, const V *src, unsigned long long lenA,
+                                          unsigned long long total, unsigned long long dstA,
+                                          unsigned long long t0, unsigned long long stride)
+{
+    for (unsigned long long e0 = t0; e0 < total; e0 += 4 * stride) {
+        V v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned long long e = e0 + u * stride;
+            if (e < total) v[u] = __ldg(src + e);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned long long e = e0 + u * stride;
+            if (e < total) dst[e < lenA ? dstA + e : e - lenA] = v[u];
+        }
+    }
+}
+
+__device__ __forceinline__ void copy_rows_flat(const AddArgs &a, const AddGeom &g,
+                                               unsigned long long t0, unsigned long long stride)
+{
+    const unsigned long long cnt = a.count - a.k0;
+    const unsigned long long lenA = g.endA - g.s0;
+    const unsigned d = a.r.d;
+    if (d) {
+        if (a.vec4) {
+            const unsigned d4 = d >> 2;
+            copy_flat(reinterpret_cast<float4 *>(a.r.states), reinterpret_cast<const float4 *>(a.states) + a.k0 * d4,
+                      lenA * d4, cnt * d4, g.s0 * d4, t0, stride);
+            copy_flat(reinterpret_cast<float4 *>(a.r.next), reinterpret_cast<const float4 *>(a.next) + a.k0 * d4,
+                      lenA * d4, cnt * d4, g.s0 * d4, t0, stride);
+        } else {
+            copy_flat(a.r.states, a.states + a.k0 * d, lenA * d, cnt * d, g.s0 * d, t0, stride);
+            copy_flat(a.r.next, a.next + a.k0 * d, lenA * d, cnt * d, g.s0 * d, t0, stride);
+        }
+    }
+    copy_flat(a.r.actions, a.actions + a.k0, lenA, cnt, g.s0, t0, stride);
+    copy_flat(a.r.rewards, a.rewards + a.k0, lenA, cnt, g.s0, t0, stride);
+    copy_flat(a.r.dones, a.dones + a.k0, lenA, cnt, g.s0, t0, stride);
+}
+
 __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
 {
     __shared__ double s_vs[1 << kAddBlockLog];
     __shared__ float s_vm[1 << kAddBlockLog];
+    pdl_wait();
+    pdl_release();
     const unsigned long long cursor = a.ctl->cursor;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    const float max_leaf = __uint_as_float(a.ctl->max_leaf_bits);
     const unsigned long long C = a.r.capacity;
     const AddGeom g = add_geometry(a, cursor);
     const int tid = threadIdx.x;
@@ -238,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                     const float raw = a.prio ? prio_to_raw(__ldg(a.prio + k), a.eps, max_prev) : max_prev;
                     mymax = __float_as_uint(raw);
                     if (a.proportional) {
-                        leaf = raw_to_leaf(raw, a.alpha);
+                        leaf = a.prio ? raw_to_leaf(raw, a.alpha) : max_leaf;
                         a.t.L[s] = leaf;
                     } else {
                         a.raw_store[s] = raw;
@@ -286,21 +337,8 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
         }
         const unsigned bm = block_max_u32(mymax);
         if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
-        // row copies: one warp per row, rows strided over the copy CTAs
-        const unsigned long long cnt = a.count - a.k0;
-        const int warp = tid >> 5, lane = tid & 31;
-        const unsigned long long wglob = (unsigned long long)(blockIdx.x - a.ntree) * (kThreads / 32) + warp;
-        const unsigned long long wtotal = (unsigned long long)a.ncopy * (kThreads / 32);
-        for (unsigned long long o = wglob; o < cnt; o += wtotal) {
-            const unsigned long long k = a.k0 + o;
-            const unsigned long long slot = (g.s0 + o) % C;
-            if (a.r.d) copy_row(a, k, slot, lane, 32);
-            if (lane == 0) {
-                a.r.actions[slot] = __ldg(a.actions + k);
-                a.r.rewards[slot] = __ldg(a.rewards + k);
-                a.r.dones[slot] = __ldg(a.dones + k);
-            }
-        }
+        copy_rows_flat(a, g, (unsigned long long)(blockIdx.x - a.ntree) * kThreads + tid,
+                       (unsigned long long)a.ncopy * kThreads);
     }
 
     if (last_to_arrive(&a.ctl->ticket_add)) {
@@ -313,15 +351,14 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
             top_range_upsweep(a.t, L0, g.blkA0, g.blkA0 + g.nA - 1, s_spS0, s_spM0, s_spS1,
                               s_spM1, s_exS, s_exM);
             if (g.nB) {
-                __syncthreads();
+                __syncwarp();
                 top_range_upsweep(a.t, L0, 0, g.nB - 1, s_spS0, s_spM0, s_spS1, s_spM1, s_exS,
                                   s_exM);
             }
         }
         if (tid == 0) {
             Ctl *c = a.ctl;
-            const unsigned am = __ldcg(&c->add_max_bits);
-            if (am > c->max_raw_bits) c->max_raw_bits = am;
+            fold_running_max(c, __ldcg(&c->add_max_bits), a.alpha);
             c->add_max_bits = 0;
             c->cursor = (cursor + a.count) % C;
             const unsigned long long sz = c->size + a.count;
@@ -335,6 +372,8 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
 
 __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
 {
+    pdl_wait();
+    pdl_release();
     const unsigned long long cursor = a.ctl->cursor;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
     const unsigned long long C = a.r.capacity;
@@ -359,7 +398,8 @@ __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
             a.r.dones[slot] = __ldg(a.dones + k);
             const float raw = a.prio ? prio_to_raw(__ldg(a.prio + k), a.eps, max_prev) : max_prev;
             mymax = max(mymax, __float_as_uint(raw));
-            if (a.proportional) a.t.L[slot] = raw_to_leaf(raw, a.alpha);
+            if (a.proportional)
+                a.t.L[slot] = a.prio ? raw_to_leaf(raw, a.alpha) : __uint_as_float(a.ctl->max_leaf_bits);
             else a.raw_store[slot] = raw;
         }
     }
@@ -402,11 +442,10 @@ __global__ void __launch_bounds__(kThreads) k_rebuild_levels(TreeRefs t, int cd,
     }
 }
 
-__global__ void k_add_finish(Ctl *c, unsigned long long count, unsigned long long C)
+__global__ void k_add_finish(Ctl *c, unsigned long long count, unsigned long long C, double alpha)
 {
     if (threadIdx.x == 0 && blockIdx.x == 0) {
-        const unsigned am = c->add_max_bits;
-        if (am > c->max_raw_bits) c->max_raw_bits = am;
+        fold_running_max(c, c->add_max_bits, alpha);
         c->add_max_bits = 0;
         c->cursor = (c->cursor + count) % C;
         const unsigned long long sz = c->size + count;
@@ -423,16 +462,35 @@ __global__ void k_fill(float *p, unsigned long long n, float v)
 
 // ------------------------------------------------------------------------------------------
 // Priority update: last-writer-wins scatter + dirty-ancestor upsweep, one launch.
-// CTA c owns the subtree at depth P whose leaves are [c << shift, (c+1) << shift).  It reads
-// the whole batch, keeps the entries in its subtree, sorts them by (leaf, batch position) in
-// shared memory, keeps the last position of each leaf, writes those leaves, and climbs its
-// subtree level by level.  On each level the first entry of every run of entries below the
-// same node owns that node; the owner of a left child reaches the owner of a dirty right
-// sibling through a run-end pointer (pointer jumping), and clean siblings come from global
-// memory, loaded for a window of levels before the window is combined.  The last CTA to
-// arrive rebuilds the 2^P - 1 nodes above the subtree roots and folds the batch maximum into
-// the running maximum.
+// The tree below depth P is cut into 2^P subtrees and each subtree belongs to one warp (a CTA
+// holds kUpdWarps of them), so nothing below depth P needs more than warp synchronisation:
+//   1. the CTA reads the batch once, coalesced, and files each entry under its subtree's warp;
+//   2. each warp sorts its entries by (leaf, batch position) in shared memory, keeps the last
+//      position of every leaf, writes those leaves and climbs its subtree level by level.  On
+//      a level the first entry of each run of entries under one node owns the node; the owner
+//      of a left child reaches the owner of a dirty right sibling through a run-end pointer
+//      (pointer jumping); clean siblings are loaded from global memory, a window of levels at
+//      a time, before the window is combined;
+//   3. the last CTA to arrive rebuilds the 2^P - 1 nodes above the subtree roots and folds the
+//      batch maximum into the running maximum.
+// A warp whose subtree receives more entries than its shared-memory list holds applies the
+// batch in position order 32 entries at a time (later chunks overwrite earlier ones, so the
+// last writer wins) and then rebuilds its whole subtree.
 // ------------------------------------------------------------------------------------------
+#ifndef GBPER_UPD_WARPS
+#define GBPER_UPD_WARPS 4
+#endif
+#ifndef GBPER_WARP_CAP
+#define GBPER_WARP_CAP 512
+#endif
+#ifndef GBPER_UPD_WINDOW
+#define GBPER_UPD_WINDOW 8
+#endif
+constexpr int kUpdWarps = GBPER_UPD_WARPS;   // subtrees (warps) per CTA
+constexpr int kUpdThreads = 32 * kUpdWarps;
+constexpr int kWarpCap = GBPER_WARP_CAP;     // entries one warp sorts in shared memory
+constexpr int kUpdWindow = GBPER_UPD_WINDOW; // tree levels whose clean siblings load in one round
+
 struct UpdArgs {
     TreeRefs t;
     float *raw_store;
@@ -440,55 +498,32 @@ struct UpdArgs {
     const long long *idx;
     const float *td;
     unsigned B;
-    int P;      // log2 grid size
+    int P;      // log2 number of subtrees
     int pb;     // bits for a batch position
     double alpha, eps;
     int proportional;
 };
 
-struct UpdSmem {
-    unsigned long long *keys;  // [cap] (leaf offset << pb) | position
-    unsigned *pay;             // [cap] entry slot carried through the sort
-    float *rawv;               // [cap] raw priority by entry slot
-    unsigned *ulist;           // [cap] sorted distinct leaves (absolute)
-    float *uleaf;              // [cap] new leaf value (sum/min seed)
-    double *vs;                // [cap]
-    float *vm;                 // [cap]
-    int *rend;                 // [cap]
-    int *flag;                 // [cap + 1] winner flags -> exclusive scan
-    double *heapS;             // [2^(kMaxTopLog+1)]
-    float *heapM;
+struct WarpLists {
+    unsigned long long keys[kWarpCap];  // (leaf offset << pb) | position
+    double vs[kWarpCap];
+    unsigned pay[kWarpCap];             // entry slot carried through the sort
+    float rawv[kWarpCap];               // raw priority by entry slot
+    unsigned ulist[kWarpCap];           // distinct leaves, ascending (absolute)
+    float vm[kWarpCap];
+    int rend[kWarpCap];
 };
 
-__device__ __forceinline__ UpdSmem upd_smem_layout(unsigned char *base)
-{
-    UpdSmem s;
-    s.keys = reinterpret_cast<unsigned long long *>(base);
-    s.vs = reinterpret_cast<double *>(s.keys + kUpdCap);
-    s.heapS = s.vs + kUpdCap;
-    unsigned char *p = reinterpret_cast<unsigned char *>(s.heapS + (2 << kMaxTopLog));
-    s.pay = reinterpret_cast<unsigned *>(p);
-    s.rawv = reinterpret_cast<float *>(s.pay + kUpdCap);
-    s.ulist = reinterpret_cast<unsigned *>(s.rawv + kUpdCap);
-    s.uleaf = reinterpret_cast<float *>(s.ulist + kUpdCap);
-    s.vm = s.uleaf + kUpdCap;
-    s.rend = reinterpret_cast<int *>(s.vm + kUpdCap);
-    s.flag = s.rend + kUpdCap;
-    s.heapM = reinterpret_cast<float *>(s.flag + kUpdCap + 32);
-    return s;
-}
+constexpr size_t kTopHeapBytes = (size_t)(2 << kMaxTopLog) * 12;  // the last CTA's top levels
+constexpr size_t kUpdSmemBytes = sizeof(WarpLists) * kUpdWarps > kTopHeapBytes
+                                     ? sizeof(WarpLists) * kUpdWarps : kTopHeapBytes;
 
-constexpr size_t kUpdSmemBytes =
-    (size_t)kUpdCap * 8 * 2 + (size_t)(2 << kMaxTopLog) * 8 +
-    (size_t)kUpdCap * 4 * 7 + 32 * 4 + (size_t)(2 << kMaxTopLog) * 4;
-
-// Bitonic sort of keys[0, m2) (m2 a power of two) carrying pay[]; ascending.
-__device__ void bitonic_sort_kv(unsigned long long *keys, unsigned *pay, int m2)
+__device__ __forceinline__ void warp_bitonic_kv(unsigned long long *keys, unsigned *pay, int m2, int lane)
 {
     for (int k = 2; k <= m2; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int t = threadIdx.x; t < (m2 >> 1); t += blockDim.x) {
-                const int i = (t / j) * 2 * j + (t % j);
+            for (int t = lane; t < (m2 >> 1); t += 32) {
+                const int i = ((t & ~(j - 1)) << 1) | (t & (j - 1));
                 const int l = i + j;
                 const bool up = (i & k) == 0;
                 const unsigned long long ki = keys[i], kl = keys[l];
@@ -500,309 +535,324 @@ __device__ void bitonic_sort_kv(unsigned long long *keys, unsigned *pay, int m2)
                     pay[l] = pi;
                 }
             }
-            __syncthreads();
+            __syncwarp();
         }
     }
 }
 
-// Exclusive scan of flag[0, m) in place; returns the total (valid in all threads).
-__device__ int block_exclusive_scan(int *flag, int m)
+// Bitonic sort of one key per lane (ascending across lanes 0..31), carrying a payload.
+__device__ __forceinline__ void warp_sort32(unsigned long long &key, unsigned &pay, int lane)
 {
-    __shared__ int s_warp[kThreads / 32];
-    __shared__ int s_total;
-    const int per = (m + blockDim.x - 1) / blockDim.x;
-    const int beg = threadIdx.x * per;
-    int sum = 0;
-    for (int i = 0; i < per; ++i)
-        if (beg + i < m) sum += flag[beg + i];
-    // warp inclusive scan of per-thread sums
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = sum;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            const int v = s_warp[w];
-            s_warp[w] = run;
-            run += v;
-        }
-        s_total = run;
-    }
-    __syncthreads();
-    int run = s_warp[warp] + incl - sum;
-    for (int i = 0; i < per; ++i)
-        if (beg + i < m) {
-            const int v = flag[beg + i];
-            flag[beg + i] = run;
-            run += v;
-        }
-    __syncthreads();
-    return s_total;
-}
-
-template <int W>
-__global__ void __launch_bounds__(kThreads) k_update(UpdArgs a)
-{
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const UpdSmem sm = upd_smem_layout(smem_raw);
-    __shared__ int s_count;
-    __shared__ unsigned s_max;
-    const int tid = threadIdx.x;
-    const int D = a.t.D;
-    const int shift = D - a.P;
-    const unsigned long long c = blockIdx.x;
-    const unsigned long long base = c << shift;
-    const unsigned long long n = a.t.n;
-    const unsigned long long size = a.ctl->size;
-    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
-    if (tid == 0) {
-        s_count = 0;
-        s_max = 0;
-    }
-    __syncthreads();
-
-    // 1. keep this subtree's entries
-    for (unsigned j = tid; j < a.B; j += blockDim.x) {
-        const long long i = __ldg(a.idx + j);
-        if (i < 0 || (unsigned long long)i >= size) {
-            if (c == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
-            continue;
-        }
-        if (((unsigned long long)i >> shift) != c) continue;
-        const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
-        atomicMax(&s_max, __float_as_uint(raw));
-        const int slot = atomicAdd(&s_count, 1);
-        if (slot < kUpdCap) {
-            sm.keys[slot] = (((unsigned long long)i - base) << a.pb) | j;
-            sm.pay[slot] = (unsigned)slot;
-            sm.rawv[slot] = raw;
-        }
-    }
-    __syncthreads();
-    const int m = s_count;
-    if (tid == 0 && s_max) atomicMax(&a.ctl->batch_max_bits, s_max);
-
-    if (m > kUpdCap) {
-        // Rare: more entries than one CTA sorts at once.  Apply the batch in position order,
-        // chunk by chunk (a later chunk overwrites an earlier one: last writer wins), then
-        // rebuild this whole subtree level by level.
-        for (unsigned p0 = 0; p0 < a.B; p0 += blockDim.x) {
-            if (tid == 0) s_count = 0;
-            __syncthreads();
-            const unsigned j = p0 + tid;
-            if (j < a.B) {
-                const long long i = __ldg(a.idx + j);
-                if (i >= 0 && (unsigned long long)i < size && ((unsigned long long)i >> shift) == c) {
-                    const int slot = atomicAdd(&s_count, 1);
-                    sm.keys[slot] = (((unsigned long long)i - base) << a.pb) | j;
-                    sm.pay[slot] = (unsigned)slot;
-                    sm.rawv[slot] = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
-                }
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const unsigned op = __shfl_xor_sync(0xffffffffu, pay, stride);
+            const bool up = (lane & size) == 0;
+            const bool lower = (lane & stride) == 0;
+            const bool take = lower ? (up ? ok < key : ok > key) : (up ? ok > key : ok < key);
+            if (take) {
+                key = ok;
+                pay = op;
             }
-            __syncthreads();
-            const int mc = s_count;
-            if (mc > 0) {
-                int m2 = 1;
-                while (m2 < mc) m2 <<= 1;
-                for (int i = mc + tid; i < m2; i += blockDim.x) sm.keys[i] = ~0ull;
-                __syncthreads();
-                bitonic_sort_kv(sm.keys, sm.pay, m2);
-                for (int k = tid; k < mc; k += blockDim.x) {
-                    const unsigned long long lk = sm.keys[k] >> a.pb;
-                    if (k == mc - 1 || (sm.keys[k + 1] >> a.pb) != lk) {
-                        const unsigned long long leaf = base + lk;
-                        const float raw = sm.rawv[sm.pay[k]];
-                        if (a.proportional) a.t.L[leaf] = raw_to_leaf(raw, a.alpha);
-                        else a.raw_store[leaf] = raw;
+        }
+    }
+}
+
+// Climb one warp's subtree from its U distinct leaves (ulist ascending, vs/vm seeded with the
+// new leaf values, rend[k] = k + 1) up to the subtree root at depth D - shift.
+template <int W>
+__device__ void warp_upsweep(const TreeRefs &t, WarpLists &wl, int U, int shift, int lane)
+{
+    const unsigned long long n = t.n;
+    if (U <= 32) {
+        const int k = lane;
+        const bool have = k < U;
+        const unsigned long long myleaf = have ? (unsigned long long)wl.ulist[k] + n : 0;
+        const unsigned long long prevleaf = (have && k > 0) ? (unsigned long long)wl.ulist[k - 1] + n : 0;
+        for (int h0 = 0; h0 < shift; h0 += W) {
+            double ps[W];
+            float pmn[W];
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const int h = h0 + w;
+                ps[w] = 0.0;
+                pmn[w] = 0.0f;
+                if (have && h < shift) {
+                    const unsigned long long v = myleaf >> h;
+                    if (k == 0 || (prevleaf >> h) != v) {
+                        ps[w] = ld_sum(t, v ^ 1ull);
+                        pmn[w] = ld_min(t, v ^ 1ull);
                     }
                 }
             }
-            __syncthreads();
-        }
-        if (a.proportional) {
-            for (int h = 1; h <= shift; ++h) {
-                const unsigned long long cnt = 1ull << (shift - h);
-                const unsigned long long first = (n + base) >> h;
-                for (unsigned long long q = tid; q < cnt; q += blockDim.x) {
-                    const unsigned long long node = first + q;
-                    a.t.S[node] = ld_sum(a.t, 2 * node) + ld_sum(a.t, 2 * node + 1);
-                    a.t.M[node] = fmin_tree(ld_min(a.t, 2 * node), ld_min(a.t, 2 * node + 1));
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const int h = h0 + w;
+                if (h >= shift) break;
+                if (have) {
+                    const unsigned long long v = myleaf >> h;
+                    if (k == 0 || (prevleaf >> h) != v) {
+                        const double ms = wl.vs[k];
+                        const float mm = wl.vm[k];
+                        int ne = wl.rend[k];
+                        bool compute = true;
+                        double sum;
+                        float mn;
+                        if ((v & 1ull) == 0) {
+                            const int e = ne;
+                            if (e < U && ((((unsigned long long)wl.ulist[e] + n) >> h) == v + 1)) {
+                                sum = ms + wl.vs[e];
+                                mn = fmin_tree(mm, wl.vm[e]);
+                                ne = wl.rend[e];
+                            } else {
+                                sum = ms + ps[w];
+                                mn = fmin_tree(mm, pmn[w]);
+                            }
+                        } else if (k > 0 && (prevleaf >> h) == v - 1) {
+                            compute = false;  // the left sibling's owner combines this pair
+                        } else {
+                            sum = ps[w] + ms;
+                            mn = fmin_tree(pmn[w], mm);
+                        }
+                        if (compute) {
+                            wl.vs[k] = sum;
+                            wl.vm[k] = mn;
+                            wl.rend[k] = ne;
+                            t.S[v >> 1] = sum;
+                            t.M[v >> 1] = mn;
+                        }
+                    }
                 }
-                __syncthreads();
+                __syncwarp();
             }
         }
-    } else if (m > 0) {
-        int m2 = 2;
-        while (m2 < m) m2 <<= 1;
-        for (int i = m + tid; i < m2; i += blockDim.x) sm.keys[i] = ~0ull;
-        __syncthreads();
-        bitonic_sort_kv(sm.keys, sm.pay, m2);
-        // 2. winners: the last position of each leaf
-        for (int k = tid; k < m; k += blockDim.x)
-            sm.flag[k] = (k == m - 1 || (sm.keys[k + 1] >> a.pb) != (sm.keys[k] >> a.pb)) ? 1 : 0;
-        __syncthreads();
-        const int U = block_exclusive_scan(sm.flag, m);
-        for (int k = tid; k < m; k += blockDim.x) {
-            const bool win = (k == m - 1) || (sm.flag[k + 1] != sm.flag[k]);
+        return;
+    }
+    for (int h = 0; h < shift; ++h) {
+        for (int k = lane; k < U; k += 32) {
+            const unsigned long long v = ((unsigned long long)wl.ulist[k] + n) >> h;
+            const unsigned long long pv = k > 0 ? ((unsigned long long)wl.ulist[k - 1] + n) >> h : 0;
+            if (k > 0 && pv == v) continue;  // not the first entry under this node
+            const double ms = wl.vs[k];
+            const float mm = wl.vm[k];
+            int ne = wl.rend[k];
+            double sum;
+            float mn;
+            if ((v & 1ull) == 0) {
+                const int e = ne;
+                if (e < U && ((((unsigned long long)wl.ulist[e] + n) >> h) == v + 1)) {
+                    sum = ms + wl.vs[e];
+                    mn = fmin_tree(mm, wl.vm[e]);
+                    ne = wl.rend[e];
+                } else {
+                    sum = ms + ld_sum(t, v + 1);
+                    mn = fmin_tree(mm, ld_min(t, v + 1));
+                }
+            } else {
+                if (k > 0 && pv == v - 1) continue;
+                sum = ld_sum(t, v - 1) + ms;
+                mn = fmin_tree(ld_min(t, v - 1), mm);
+            }
+            wl.vs[k] = sum;
+            wl.vm[k] = mn;
+            wl.rend[k] = ne;
+            t.S[v >> 1] = sum;
+            t.M[v >> 1] = mn;
+        }
+        __syncwarp();
+    }
+}
+
+template <int W>
+__global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    WarpLists *lists = reinterpret_cast<WarpLists *>(smem_raw);
+    __shared__ int s_cnt[kUpdWarps];
+    __shared__ unsigned s_max;
+    pdl_wait();
+    pdl_release();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int D = a.t.D;
+    const int shift = D - a.P;
+    const unsigned long long nsub = 1ull << a.P;
+    const unsigned long long first_sub = (unsigned long long)blockIdx.x * kUpdWarps;
+    const unsigned long long n = a.t.n;
+    const unsigned long long size = a.ctl->size;
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    if (tid < kUpdWarps) s_cnt[tid] = 0;
+    if (tid == 0) s_max = 0;
+    __syncthreads();
+
+    // 1. file this CTA's entries under their subtree's warp (indices and TD errors are read
+    //    together, four per thread in flight)
+    unsigned mymax = 0;
+    for (unsigned j0 = tid; j0 < a.B; j0 += 4 * blockDim.x) {
+        long long iv[4];
+        float tv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned j = j0 + u * blockDim.x;
+            iv[u] = j < a.B ? __ldg(a.idx + j) : -2;
+            tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned j = j0 + u * blockDim.x;
+            const long long i = iv[u];
+            if (i == -2) continue;
+            if (i < 0 || (unsigned long long)i >= size) {
+                if (blockIdx.x == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
+                continue;
+            }
+            const unsigned long long sub = (unsigned long long)i >> shift;
+            if (sub < first_sub || sub >= first_sub + kUpdWarps) continue;
+            const int w = (int)(sub - first_sub);
+            const float raw = td_to_raw(tv[u], a.eps, max_prev);
+            mymax = max(mymax, __float_as_uint(raw));
+            const int slot = atomicAdd(&s_cnt[w], 1);
+            if (slot < kWarpCap) {
+                WarpLists &wl = lists[w];
+                wl.keys[slot] = (((unsigned long long)i - (sub << shift)) << a.pb) | j;
+                wl.pay[slot] = (unsigned)slot;
+                wl.rawv[slot] = raw;
+            }
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
+    if (lane == 0 && mymax) atomicMax(&s_max, mymax);
+    __syncthreads();
+    if (tid == 0 && s_max) atomicMax(&a.ctl->batch_max_bits, s_max);
+
+    // 2. one warp per subtree
+    const unsigned long long sub = first_sub + warp;
+    const int m = s_cnt[warp];
+    if (sub < nsub && m > 0) {
+        WarpLists &wl = lists[warp];
+        const unsigned long long base = sub << shift;
+        if (m > kWarpCap) {
+            for (unsigned p0 = 0; p0 < a.B; p0 += 32) {
+                const unsigned j = p0 + lane;
+                long long i = -1;
+                if (j < a.B) i = __ldg(a.idx + j);
+                const bool mine = i >= 0 && (unsigned long long)i < size && ((unsigned long long)i >> shift) == sub;
+                const unsigned long long key = mine ? (unsigned long long)i : ~0ull;
+                const unsigned peers = __match_any_sync(0xffffffffu, key);
+                if (mine && (31 - __clz(peers)) == lane) {  // the last lane of this chunk for the leaf
+                    const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
+                    if (a.proportional) a.t.L[i] = raw_to_leaf(raw, a.alpha);
+                    else a.raw_store[i] = raw;
+                }
+                __syncwarp();
+            }
+            if (a.proportional) {
+                for (int h = 1; h <= shift; ++h) {
+                    const unsigned long long cnt = 1ull << (shift - h);
+                    const unsigned long long first = (n + base) >> h;
+                    for (unsigned long long q = lane; q < cnt; q += 32) {
+                        const unsigned long long node = first + q;
+                        a.t.S[node] = ld_sum(a.t, 2 * node) + ld_sum(a.t, 2 * node + 1);
+                        a.t.M[node] = fmin_tree(ld_min(a.t, 2 * node), ld_min(a.t, 2 * node + 1));
+                    }
+                    __syncwarp();
+                }
+            }
+        } else if (m <= 32) {
+            // one entry per lane: sort in registers, keep the last position of each leaf
+            unsigned long long key = lane < m ? wl.keys[lane] : ~0ull;
+            unsigned pay = lane < m ? wl.pay[lane] : 0u;
+            warp_sort32(key, pay, lane);
+            const unsigned long long nxt = __shfl_down_sync(0xffffffffu, key, 1);
+            const bool win = lane < m && (lane == m - 1 || (nxt >> a.pb) != (key >> a.pb));
+            const unsigned bal = __ballot_sync(0xffffffffu, win);
+            const int u = __popc(bal & ((1u << lane) - 1u));
+            const int U = __popc(bal);
             if (win) {
-                const int u = sm.flag[k];
-                const unsigned long long leaf = base + (sm.keys[k] >> a.pb);
-                const float raw = sm.rawv[sm.pay[k]];
-                sm.ulist[u] = (unsigned)leaf;
+                const unsigned long long leaf = base + (key >> a.pb);
+                const float raw = wl.rawv[pay];
+                wl.ulist[u] = (unsigned)leaf;
                 if (a.proportional) {
                     const float lv = raw_to_leaf(raw, a.alpha);
                     a.t.L[leaf] = lv;
-                    sm.vs[u] = (double)lv;
-                    sm.vm[u] = leaf_min_value(lv);
-                    sm.rend[u] = u + 1;
+                    wl.vs[u] = (double)lv;
+                    wl.vm[u] = leaf_min_value(lv);
+                    wl.rend[u] = u + 1;
                 } else {
                     a.raw_store[leaf] = raw;
                 }
             }
-        }
-        __syncthreads();
-
-        // 3. climb from the leaves (h = 0) to the subtree root at depth P
-        if (a.proportional) {
-            const int R = (U + blockDim.x - 1) / blockDim.x;
-            if (R == 1) {
-                // one entry per thread: clean siblings of W levels are loaded up front
-                const int k = tid;
-                const bool have = k < U;
-                const unsigned long long myleaf = have ? (unsigned long long)sm.ulist[k] + n : 0;
-                const unsigned long long prevleaf = (have && k > 0) ? (unsigned long long)sm.ulist[k - 1] + n : 0;
-                for (int h0 = 0; h0 < shift; h0 += W) {
-                    double ps[W];
-                    float pmn[W];
-#pragma unroll
-                    for (int w = 0; w < W; ++w) {
-                        const int h = h0 + w;
-                        ps[w] = 0.0;
-                        pmn[w] = 0.0f;
-                        if (have && h < shift) {
-                            const unsigned long long v = myleaf >> h;
-                            const bool owner = (k == 0) || ((prevleaf >> h) != v);
-                            if (owner) {
-                                ps[w] = ld_sum(a.t, v ^ 1ull);
-                                pmn[w] = ld_min(a.t, v ^ 1ull);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int w = 0; w < W; ++w) {
-                        const int h = h0 + w;
-                        if (h < shift) {
-                            if (have) {
-                                const unsigned long long v = myleaf >> h;
-                                const bool owner = (k == 0) || ((prevleaf >> h) != v);
-                                if (owner) {
-                                    const double ms = sm.vs[k];
-                                    const float mm = sm.vm[k];
-                                    bool compute = true;
-                                    double s;
-                                    float mn;
-                                    int ne = sm.rend[k];
-                                    if ((v & 1ull) == 0) {
-                                        const int e = ne;
-                                        if (e < U && ((((unsigned long long)sm.ulist[e] + n) >> h) == v + 1)) {
-                                            s = ms + sm.vs[e];
-                                            mn = fmin_tree(mm, sm.vm[e]);
-                                            ne = sm.rend[e];
-                                        } else {
-                                            s = ms + ps[w];
-                                            mn = fmin_tree(mm, pmn[w]);
-                                        }
-                                    } else {
-                                        if (k > 0 && ((prevleaf >> h) == v - 1)) {
-                                            compute = false;
-                                        } else {
-                                            s = ps[w] + ms;
-                                            mn = fmin_tree(pmn[w], mm);
-                                        }
-                                    }
-                                    if (compute) {
-                                        sm.vs[k] = s;
-                                        sm.vm[k] = mn;
-                                        sm.rend[k] = ne;
-                                        a.t.S[v >> 1] = s;
-                                        a.t.M[v >> 1] = mn;
-                                    }
-                                }
-                            }
-                            __syncthreads();
-                        }
+            __syncwarp();
+            if (a.proportional) warp_upsweep<W>(a.t, wl, U, shift, lane);
+        } else {
+            int m2 = 2;
+            while (m2 < m) m2 <<= 1;
+            for (int i = m + lane; i < m2; i += 32) wl.keys[i] = ~0ull;
+            __syncwarp();
+            warp_bitonic_kv(wl.keys, wl.pay, m2, lane);
+            // distinct leaves, keeping the last batch position of each; compacted in order
+            int U = 0;
+            for (int k0 = 0; k0 < m; k0 += 32) {
+                const int k = k0 + lane;
+                bool win = false;
+                if (k < m) win = (k == m - 1) || ((wl.keys[k + 1] >> a.pb) != (wl.keys[k] >> a.pb));
+                const unsigned bal = __ballot_sync(0xffffffffu, win);
+                const int u = U + __popc(bal & ((1u << lane) - 1u));
+                unsigned long long leaf = 0;
+                float raw = 0.0f;
+                if (win) {
+                    leaf = base + (wl.keys[k] >> a.pb);
+                    raw = wl.rawv[wl.pay[k]];
+                }
+                __syncwarp();
+                if (win) {
+                    wl.ulist[u] = (unsigned)leaf;
+                    if (a.proportional) {
+                        const float lv = raw_to_leaf(raw, a.alpha);
+                        a.t.L[leaf] = lv;
+                        wl.vs[u] = (double)lv;
+                        wl.vm[u] = leaf_min_value(lv);
+                        wl.rend[u] = u + 1;
+                    } else {
+                        a.raw_store[leaf] = raw;
                     }
                 }
-            } else {
-                for (int h = 0; h < shift; ++h) {
-                    for (int k = tid; k < U; k += blockDim.x) {
-                        const unsigned long long v = ((unsigned long long)sm.ulist[k] + n) >> h;
-                        const bool owner = (k == 0) || (((((unsigned long long)sm.ulist[k - 1]) + n) >> h) != v);
-                        if (!owner) continue;
-                        const double ms = sm.vs[k];
-                        const float mm = sm.vm[k];
-                        int ne = sm.rend[k];
-                        double s;
-                        float mn;
-                        if ((v & 1ull) == 0) {
-                            const int e = ne;
-                            if (e < U && ((((unsigned long long)sm.ulist[e] + n) >> h) == v + 1)) {
-                                s = ms + sm.vs[e];
-                                mn = fmin_tree(mm, sm.vm[e]);
-                                ne = sm.rend[e];
-                            } else {
-                                s = ms + ld_sum(a.t, v + 1);
-                                mn = fmin_tree(mm, ld_min(a.t, v + 1));
-                            }
-                        } else {
-                            if (k > 0 && ((((unsigned long long)sm.ulist[k - 1] + n) >> h) == v - 1)) continue;
-                            s = ld_sum(a.t, v - 1) + ms;
-                            mn = fmin_tree(ld_min(a.t, v - 1), mm);
-                        }
-                        sm.vs[k] = s;
-                        sm.vm[k] = mn;
-                        sm.rend[k] = ne;
-                        a.t.S[v >> 1] = s;
-                        a.t.M[v >> 1] = mn;
-                    }
-                    __syncthreads();
-                }
+                U += __popc(bal);
             }
+            __syncwarp();
+            if (a.proportional) warp_upsweep<W>(a.t, wl, U, shift, lane);
         }
     }
 
-    // 4. the last CTA rebuilds the top P levels and folds in the batch maximum
+    // 3. the last CTA rebuilds the top P levels and folds in the batch maximum
     if (last_to_arrive(&a.ctl->ticket_update)) {
         if (a.proportional && a.P > 0) {
+            double *heapS = reinterpret_cast<double *>(smem_raw);
+            float *heapM = reinterpret_cast<float *>(heapS + (2 << kMaxTopLog));
             const int P = a.P;
             const int width = 1 << P;
             for (int i = tid; i < width; i += blockDim.x) {
-                sm.heapS[width + i] = ld_sum_cg(a.t, (unsigned long long)width + i);
-                sm.heapM[width + i] = ld_min_cg(a.t, (unsigned long long)width + i);
+                heapS[width + i] = ld_sum_cg(a.t, (unsigned long long)width + i);
+                heapM[width + i] = ld_min_cg(a.t, (unsigned long long)width + i);
             }
             for (int l = P - 1; l >= 0; --l) {
                 __syncthreads();
                 const int lw = 1 << l;
                 for (int i = tid; i < lw; i += blockDim.x) {
                     const int node = lw + i;
-                    const double s = sm.heapS[2 * node] + sm.heapS[2 * node + 1];
-                    const float mn = fmin_tree(sm.heapM[2 * node], sm.heapM[2 * node + 1]);
-                    sm.heapS[node] = s;
-                    sm.heapM[node] = mn;
-                    a.t.S[node] = s;
+                    const double sum = heapS[2 * node] + heapS[2 * node + 1];
+                    const float mn = fmin_tree(heapM[2 * node], heapM[2 * node + 1]);
+                    heapS[node] = sum;
+                    heapM[node] = mn;
+                    a.t.S[node] = sum;
                     a.t.M[node] = mn;
                 }
             }
         }
         if (tid == 0) {
             Ctl *cc = a.ctl;
-            const unsigned bm = __ldcg(&cc->batch_max_bits);
-            if (bm > cc->max_raw_bits) cc->max_raw_bits = bm;
+            fold_running_max(cc, __ldcg(&cc->batch_max_bits), a.alpha);
             cc->batch_max_bits = 0;
             cc->ticket_update = 0;
         }
@@ -817,6 +867,20 @@ int ilog2_ceil(unsigned long long v)
 }
 
 }  // namespace
+
+cudaError_t init_tree_kernels(int carveout)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kUpdSmemBytes);
+    if (e != cudaSuccess || carveout < 0) return e;
+    const void *fns[] = {(const void *)k_update<kUpdWindow>, (const void *)k_add, (const void *)k_add_bulk_rows,
+                         (const void *)k_rebuild_levels, (const void *)k_add_finish, (const void *)k_fill};
+    for (const void *f : fns) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t launch_fill_mins(float *M, unsigned long long n, cudaStream_t st)
 {
@@ -855,22 +919,21 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.vec4 = (r.d % 4 == 0) && ((reinterpret_cast<uintptr_t>(states) | reinterpret_cast<uintptr_t>(next)) % 16 == 0);
     if (r.d == 0) a.vec4 = 0;
 
-    // rows: aim for ~8 rows per warp, at most 4 CTAs per SM
-    const unsigned long long warps = (cnt + 7) / 8;
-    unsigned ncopy = (unsigned)std::min<unsigned long long>((warps + 7) / 8, (unsigned long long)num_sms * 4);
+    // rows: about four elements in flight per copy thread, at most 4 CTAs per SM
+    const unsigned long long elems = a.vec4 ? cnt * (r.d / 4) : cnt * (unsigned long long)std::max(r.d, 1u);
+    unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + 4ull * kThreads - 1) / (4ull * kThreads),
+                                                            (unsigned long long)num_sms * 4);
     if (ncopy == 0) ncopy = 1;
 
     const bool incremental = cnt + bsz <= C && cnt * 8 <= t.n && cnt <= (1ull << 18);
     if (incremental) {
         a.ntree = (unsigned)(cnt / bsz + 3);
         a.ncopy = ncopy;
-        k_add<<<a.ntree + a.ncopy, kThreads, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(k_add, a.ntree + a.ncopy, kThreads, 0, st, a);
     }
     a.ntree = 0;
     a.ncopy = ncopy;
-    k_add_bulk_rows<<<ncopy, kThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_add_bulk_rows, ncopy, kThreads, 0, st, a);
     if (e != cudaSuccess) return e;
     if (proportional) {
         for (int cd = t.D; cd > 0; cd -= 8) {
@@ -882,7 +945,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
             if (e != cudaSuccess) return e;
         }
     }
-    k_add_finish<<<1, 32, 0, st>>>(ctl, count, C);
+    k_add_finish<<<1, 32, 0, st>>>(ctl, count, C, alpha);
     return cudaGetLastError();
 }
 
@@ -902,18 +965,15 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.alpha = alpha;
     a.eps = eps;
     a.proportional = proportional ? 1 : 0;
-    // ~32 batch entries per CTA; the grid never exceeds 2^10 CTAs or half the leaves
-    int P = ilog2_ceil((B + 31) / 32);
+    // about 8 batch entries per subtree (a warp's list holds up to kWarpCap, so a batch
+    // concentrated on a stretch of recent slots still fits); at most 2^10 subtrees, and no
+    // more than half the leaves
+    int P = ilog2_ceil((B + 7) / 8);
     P = std::min(P, kMaxTopLog);
     P = std::min(P, std::max(t.D - 1, 0));
     a.P = P;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(k_update<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kUpdSmemBytes);
-        attr_set = true;
-    }
-    k_update<8><<<1u << P, kThreads, kUpdSmemBytes, st>>>(a);
-    return cudaGetLastError();
+    const unsigned grid = (unsigned)(((1ull << P) + kUpdWarps - 1) / kUpdWarps);
+    return launch_pdl(k_update<kUpdWindow>, grid, kUpdThreads, kUpdSmemBytes, st, a);
 }
 
 }  // namespace gbper

@@ -7,7 +7,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -96,7 +98,38 @@ bool alloc(T **p, uint64_t count)
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Kernel attributes are per device: set them the first time a buffer is created on a device.
+// The carveout (percent of the unified L1/shared array given to shared memory) is the same for
+// every kernel of the library when GBPER_CARVEOUT is set (measured: no effect on this path, so
+// by default the driver chooses).
+cudaError_t init_kernels_once(int device)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (done[device]) return cudaSuccess;
+    int carveout = -1;
+    if (const char *env = std::getenv("GBPER_CARVEOUT")) carveout = std::atoi(env);
+    cudaError_t e = init_tree_kernels(carveout);
+    if (e == cudaSuccess) e = init_sample_kernels(carveout);
+    if (e == cudaSuccess) e = init_rank_kernels(carveout);
+    if (e == cudaSuccess) done[device] = true;
+    return e;
+}
+
 }  // namespace
+
+namespace gbper {
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char *env = std::getenv("GBPER_PDL");
+        return !(env && env[0] == '0');
+    }();
+    return on;
+}
+}  // namespace gbper
 
 extern "C" {
 
@@ -138,6 +171,11 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         return fail(nullptr, PER_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     }
     cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    e = init_kernels_once(h->device);
+    if (e != cudaSuccess) {
+        delete h;
+        return fail(nullptr, PER_ERR_CUDA, std::string("kernel attributes: ") + cudaGetErrorString(e));
+    }
     if (h->num_sms < 1) h->num_sms = 1;
     h->capacity = capacity;
     while (h->n < capacity) {
@@ -174,6 +212,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     std::memset(&init, 0, sizeof(init));
     const float one = 1.0f;
     std::memcpy(&init.max_raw_bits, &one, sizeof(one));
+    std::memcpy(&init.max_leaf_bits, &one, sizeof(one));  // pow(1, alpha) = 1
     e = cudaMemcpy(h->ctl, &init, sizeof(init), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && h->L) e = cudaMemset(h->L, 0, h->n * sizeof(float));
     if (e == cudaSuccess && h->S) e = cudaMemset(h->S, 0, h->n * sizeof(double));

@@ -29,8 +29,19 @@ struct Ctl {
     unsigned int ticket_add;
     unsigned int batch_max_bits;      // per-call maximum raw priority, folded in by the last CTA
     unsigned int add_max_bits;
-    unsigned int pad[3];
+    unsigned int max_leaf_bits;       // fl32(pow(running maximum, alpha)): the leaf of a new row
+    unsigned int pad[2];
 };
+
+// Fold a call's maximum raw priority into the running maximum and keep the cached leaf value
+// of the maximum in step (one binary64 pow, only when the maximum rises).  Last CTA only.
+__device__ __forceinline__ void fold_running_max(Ctl *c, unsigned call_max_bits, double alpha)
+{
+    if (call_max_bits > c->max_raw_bits) {
+        c->max_raw_bits = call_max_bits;
+        c->max_leaf_bits = __float_as_uint(__double2float_rn(pow((double)__uint_as_float(call_max_bits), alpha)));
+    }
+}
 
 constexpr unsigned kFlagBadIndex = 1u;
 constexpr unsigned kFlagTimeout = 2u;
@@ -51,6 +62,18 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k)
     return c;
 }
 
+// v * 2^scale for an integer 0 <= v < 2^53, assembled from bits on the integer pipe (the
+// value is exact, as the binary64 conversion and scaling would give, without using GB300's
+// narrow binary64 pipe).
+__device__ __forceinline__ double exact_double(unsigned long long v, int scale)
+{
+    if (v == 0) return 0.0;
+    const int p = 63 - __clzll((long long)v);
+    const unsigned long long mant = (v << (52 - p)) & 0xFFFFFFFFFFFFFull;
+    const unsigned long long ex = (unsigned long long)(p + scale + 1023);
+    return __longlong_as_double((long long)((ex << 52) | mant));
+}
+
 // 53-bit uniform in [0, 1) of draw j in sample call `call`, stream tag `tag`.
 __device__ __forceinline__ double draw_uniform(unsigned long long seed, unsigned j,
                                                unsigned long long call, unsigned tag)
@@ -58,7 +81,7 @@ __device__ __forceinline__ double draw_uniform(unsigned long long seed, unsigned
     const uint4 x = philox4x32_10(make_uint4(j, (unsigned)call, (unsigned)(call >> 32), tag),
                                   make_uint2((unsigned)seed, (unsigned)(seed >> 32)));
     const unsigned long long bits = ((unsigned long long)x.x << 21) | (x.y >> 11);
-    return __dmul_rn((double)bits, 0x1.0p-53);
+    return exact_double(bits, -53);
 }
 
 // ---- priority transforms ("GPU-Resident Prioritized Experience Replay": Priority update,
@@ -158,5 +181,39 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
                                cudaStream_t st);
 
 unsigned long long rank_tile_count(unsigned long long capacity);
+
+// ---- programmatic dependent launch -----------------------------------------------------------
+// Every hot kernel is launched with programmatic stream serialization: its CTAs may be scheduled
+// while the previous kernel in the stream is still finishing, and they wait in pdl_wait() --
+// before reading any state a predecessor may write -- until that kernel has completed and its
+// memory is visible.  pdl_release() lets the next kernel begin launching early.  Launched
+// without the attribute (GBPER_PDL=0), both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Kernel attributes set once per device before the first launch (dynamic shared-memory limits
+// and one common L1/shared carveout, so consecutive kernels never make an SM reconfigure).
+cudaError_t init_tree_kernels(int carveout);
+cudaError_t init_sample_kernels(int carveout);
+cudaError_t init_rank_kernels(int carveout);
 
 }  // namespace gbper
