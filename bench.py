@@ -317,6 +317,25 @@ def run_gpu(args, rank, world):
     step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
     cr.destroy(sev)
 
+    # continuous: the same K steps back to back between one pair of events (the canonical form:
+    # K steps bracketed by synchronisation; no flush, the 1 GiB ring exceeds L2)
+    ca, cb = cr.events(2)
+    torch.cuda.synchronize()
+    rec(ca, st)
+    for t in range(K):
+        _check(L, h, L.per_add(*add_args[(W + t) % n_ofs]), "per_add")
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * ((W + t) % TD_SLOTS), st),
+               "per_update")
+    rec(cb, st)
+    torch.cuda.synchronize()
+    cont_s = cr.elapsed_ms(ca, cb) / 1e3
+    cr.destroy([ca, cb])
+    if dist:
+        tt = torch.tensor([cont_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        cont_s = float(tt.item())
+
     # per-kernel breakdown (for the roofline): a second pass with an event between the calls.
     # Each event pair also carries a launch (about 4 us on this GPU for an empty kernel), so
     # these durations are upper bounds.
@@ -374,7 +393,7 @@ def run_gpu(args, rank, world):
         tt = torch.tensor([total_s], dtype=torch.float64, device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_s = float(tt.item())
-    value = world * K / total_s
+    value_flushed = world * K / total_s
     if buf.status_device() != 0:
         raise RuntimeError("device error flag raised during the benchmark")
 
@@ -400,20 +419,21 @@ def run_gpu(args, rank, world):
     step_bytes = b_add + b_sam + b_upd
 
     res = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 5), "higher_is_better": True,
+        "metric": METRIC, "value": round(world * K / cont_s, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(cont_s * 1e3 / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; rows N(0,1) drawn on the device, lognormal(0,1) priorities)",
         "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step, "
                                "alpha 0.6, beta 0.4",
-                   "l2": ("flushed between steps (512 MiB write + 256 MiB read, outside the step "
-                          "events)" if flush_l2 else "not flushed; inputs larger than L2 (1 GiB ring, "
-                          "48 MiB trees, 32 MiB staging; 129 MB L2)"),
-                   "timing": ("two CUDA events per step on the launching stream; value = steps / sum "
-                              "of step times; per-kernel figures from a second pass"),
+                   "l2": ("value: not flushed, inputs larger than L2 (1 GiB ring + 48 MiB trees + "
+                          "32 MiB staging vs 129 MB L2; each step ingests new rows and gathers random "
+                          "ones); per_step_l2_flushed: 512 MiB write + 256 MiB read between steps"),
+                   "timing": ("value: K steps back to back on one stream between two CUDA events, "
+                              "synchronised on both sides; per-kernel figures from a separate pass "
+                              "with an event between the calls"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "wall_s_timed_loop": round(wall, 4), "host_enqueue_s": round(host_s, 4)},
-        "hbm_gbs_algorithmic": round(step_bytes / (total_s / K) / 1e9 / world, 2),
+        "hbm_gbs_algorithmic": round(step_bytes / (cont_s / K) / 1e9 / world, 2),
         "bytes_per_step": {"k_add": int(b_add), "k_sample_prop": int(b_sam), "k_update": int(b_upd)},
         "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
         "ops_p99_us": {k: round(float(np.percentile(per[:, i], 99)) * 1e3, 3)
@@ -421,8 +441,11 @@ def run_gpu(args, rank, world):
         "ops_max_us": {k: round(float(per[:, i].max()) * 1e3, 3) for i, k in enumerate(ops)},
         "roofline": roofline,
         "gpu_launches": 3 * K,
-        "step_us_median": round(float(np.median(step_ms)) * 1e3, 3),
-        "step_us_p99": round(float(np.percentile(step_ms, 99)) * 1e3, 3),
+        "per_step_l2_flushed": {"value": round(value_flushed, 2), "unit": UNIT,
+                                "us_per_step_median": round(float(np.median(step_ms)) * 1e3, 3),
+                                "us_per_step_p99": round(float(np.percentile(step_ms, 99)) * 1e3, 3),
+                                "timing": "two events per step, L2 flushed between steps"
+                                          if flush_l2 else "two events per step, no flush"},
     }
     if clk:
         res["clocks"] = clk
@@ -512,6 +535,132 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
             "note": "pinned host rows + TD errors in, sampled batch out, inside the timing"}
 
 
+# -- the other workloads (sample + update steps; rank adds the sort) -------------------------------
+
+OTHER = {
+    "tiny": "tiny: 2^10 leaves, state_dim 8, B=32, alpha 0.6, beta 0.4",
+    "dqn": "dqn: 2^20 leaves, state_dim 48 gathered into 64-float rows, B=1024, beta 0.4->1.0 over 341 steps",
+    "stress": "stress: 2^24 leaves, state_dim 256, B=8192, 25% duplicate update indices, alpha 0.7, beta 0.5",
+    "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, radix sort + rank sample, alpha 0.7, beta 0.5",
+}
+
+
+def run_other(args, name):
+    """Steps/s of one sample (+IS +gather) and one update per step on another workload; the rank
+    workload's sample call includes the sort.  Same timing rules as the apex step."""
+    import ctypes
+    import torch
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    torch.cuda.set_device(0)
+    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0)
+    g = wl.rng(0, 55)
+    chunk = min(w.capacity, 1 << 18)
+    for c in range(w.capacity // chunk):
+        sd, nd = wl.device_rows(torch, 0, c, chunk, w.state_dim)
+        a, r, d = wl.device_scalars(torch, 0, c, chunk, w)
+        prio = wl.raw_priorities(g, chunk, w.prio)
+        buf.add(sd, nd, a, r, d, None if prio is None else torch.from_numpy(prio).cuda())
+        del sd, nd
+    torch.cuda.synchronize()
+    L, h = capi.load(), buf._h
+    K, W, B = args.steps, args.warmup, w.batch
+    out = buf.alloc_batch(B)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # update batches: the sampled indices, or (stress) a copy with 25% duplicated positions
+    NS = 64
+    idx_sets = torch.empty((NS, B), dtype=torch.int64, device="cuda")
+    td = torch.from_numpy(wl.td_errors(g, NS * B)).cuda().view(NS, B)
+    for k in range(NS):
+        buf.sample(B, w.beta_at(0), out=out)
+        ix = out["idx"].cpu().numpy()
+        if w.dup_frac:
+            ix = wl.duplicate_positions(g, ix, w.dup_frac)
+        idx_sets[k] = torch.from_numpy(ix).cuda()
+    torch.cuda.synchronize()
+    ptrs = [out[k].data_ptr() for k in ("idx", "w", "states", "next_states", "actions", "rewards", "dones")]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    evict = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    evict_out = torch.empty((), dtype=torch.float32, device="cuda")
+    cr = Cudart()
+    rec, memset = cr.lib.cudaEventRecord, cr.lib.cudaMemsetAsync
+    flush_l2 = args.l2 == "flush"
+
+    def step(t, ev):
+        beta = ctypes.c_float(w.beta_at(t % max(w.rounds, 1)))
+        k = t % NS
+        rec(ev[0], st)
+        _check(L, h, L.per_sample(h, B, beta, *ptrs, st), "per_sample")
+        if ev[1] is not None:
+            rec(ev[1], st)
+        _check(L, h, L.per_update_priorities(h, B, idx_sets[k].data_ptr(), td[k].data_ptr(), st),
+               "per_update")
+        rec(ev[2], st)
+        if flush_l2:
+            memset(flush.data_ptr(), 0, flush.numel(), st)
+            torch.sum(evict, 0, out=evict_out)
+
+    warm = cr.events(3)
+    for t in range(W):
+        step(t, warm)
+    torch.cuda.synchronize()
+    sev = cr.events(2 * K)
+    t0 = time.perf_counter()
+    for t in range(K):
+        step(W + t, (sev[2 * t], None, sev[2 * t + 1]))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
+    cr.destroy(sev)
+    Kop = min(K, 1000)
+    fl = cr.events(3 * Kop)
+    for t in range(Kop):
+        step(W + K + t, fl[3 * t: 3 * t + 3])
+    torch.cuda.synchronize()
+    per = np.array([[cr.elapsed_ms(fl[3 * t + i], fl[3 * t + i + 1]) for i in range(2)] for t in range(Kop)])
+    cr.destroy(fl + warm)
+    if buf.status_device() != 0:
+        raise RuntimeError("device error flag raised during the benchmark")
+    idx = out["idx"].cpu().numpy()
+    D = int(np.log2(buf.nleaves))
+    upd_idx = idx_sets[(W + K + Kop - 1) % NS].cpu().numpy()
+    if w.mode == wl.RANK:
+        n = w.capacity
+        b_sam = 4 * 16 * n + 4 * n + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
+        b_upd = 12 * B + 4 * len(np.unique(upd_idx))
+        names = ("rank sort + k_sample_rank", "k_update")
+    else:
+        b_sam = bytes_sample(idx, w.state_dim, w.row_stride, D)
+        b_upd = bytes_update(upd_idx, D)
+        names = ("k_sample_prop", "k_update")
+    ops = {names[0]: (float(np.median(per[:, 0])), b_sam), names[1]: (float(np.median(per[:, 1])), b_upd)}
+    peak, peak_src = load_peaks()
+    dom = max(ops, key=lambda k: ops[k][0])
+    ms, byt = ops[dom]
+    achieved = byt / (ms * 1e-3) / 1e9
+    total_s = float(step_ms.sum()) / 1e3
+    res = {
+        "metric": f"PER steps/s ({OTHER[name].split(':')[0]} workload)", "value": round(K / total_s, 2),
+        "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": OTHER[name], "l2": "flushed between steps" if flush_l2 else "not flushed",
+                   "wall_s_timed_loop": round(wall, 4)},
+        "step_us_median": round(float(np.median(step_ms)) * 1e3, 3),
+        "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
+        "bytes_per_step": {k: int(v[1]) for k, v in ops.items()},
+        "hbm_gbs_algorithmic": round((b_sam + b_upd) / (total_s / K) / 1e9, 2),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 5), "traffic": None,
+                     "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
+                     "median_launch_us": round(ms * 1e3, 3)},
+        "gpu_launches": (14 if w.mode == wl.RANK else 2) * K,
+    }
+    buf.close()
+    return res
+
+
 # -- the oracle on the host cores ------------------------------------------------------------------
 
 def oracle_steps_per_s(budget_s=12.0, max_steps=None):
@@ -562,6 +711,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="apex", choices=["apex", "tiny", "dqn", "stress", "rank"],
+                    help="apex is the headline workload; the others are measured with --workload")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured as one CUDA graph per staging offset")
     ap.add_argument("--l2", default="flush", choices=["flush", "warm"],
@@ -590,6 +741,10 @@ def main():
         print(json.dumps(res))
         return
 
+    if args.workload != "apex":
+        if rank == 0:
+            print(json.dumps(run_other(args, args.workload)))
+        return
     res = run_gpu(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

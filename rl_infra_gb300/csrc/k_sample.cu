@@ -7,17 +7,18 @@
 //   mass_j  (j + u_j) * (T / B): one draw per stratum of [0, T)
 //   descent the same walk as the post's st_find_prefixsum_idx (left when the left child's sum
 //           exceeds the mass, otherwise subtract and go right), evaluated in an order that
-//           reaches the same decisions with fewer dependent memory round trips:
-//             - the top `top` levels are staged once per CTA in shared memory;
-//             - below them the warp loads the left children of a 5-level subtree in one
-//               round (31 nodes, one per lane) and walks those 5 levels with shuffles;
-//             - the last round loads the 32 leaves under the node as one 128-byte line.
-//           Every comparison and subtraction is the binary64 operation of the sequential
-//           walk, so the leaf and the leftover mass are bit-identical to it.
+//           reaches the same decisions with few dependent memory round trips: the warp loads
+//           the 2^k - 1 left children of a k-level subtree (k <= 7) in one round, four per
+//           lane, and walks those k levels with shuffles; the last round loads the leaves under
+//           its node as one contiguous stretch.  A 2^21-leaf tree takes three rounds.  Every
+//           comparison and subtraction is the binary64 operation of the sequential walk (the
+//           compare on the integer pipe, since the operands are non-negative), so the leaf and
+//           the leftover mass are bit-identical to it.
 //   weight  w = (n P(i))^-beta / max_w with max_w from the min tree, i.e. (L[i]/p_min)^-beta
 //   gather  the warp copies the chosen rows (zero-padded to the output stride, as the padded
 //           gather of "True Single-Graph Implementation Plan", Task 2) and the scalars.
-// The last CTA to finish advances the device-side call counter.
+// Each CTA takes the call number from the device-side counter when it starts; the last to
+// start advances it.
 #include "per_internal.cuh"
 
 #include <algorithm>
@@ -38,7 +39,6 @@ struct SampleArgs {
     float beta;
     unsigned long long seed;
     SampleOut o;
-    int top;   // levels staged in shared memory
     int vec4;  // rows move as float4
 };
 
@@ -87,20 +87,37 @@ __device__ __forceinline__ bool gt_nonneg(double a, double b)
     return __double_as_longlong(a) > __double_as_longlong(b);
 }
 
-// Walk k levels below `node` whose left children are all internal nodes.
-__device__ __forceinline__ unsigned long long walk_internal(const double *__restrict__ S,
-                                                            unsigned long long node, int k,
-                                                            double &m, int lane)
+// One round of the walk: k <= 7 levels below `node`.  The 2^k - 1 left children the walk may
+// read are loaded at once, four per lane (child i of the round sits in lane i % 32, slot i / 32),
+// and the k decisions then run on registers and shuffles.  When `last`, the deepest level is
+// the leaves: the 2^k leaves under `node` are one contiguous stretch, four per lane, and *lv
+// receives the chosen leaf's value.
+__device__ __forceinline__ unsigned long long walk_round(const TreeRefs &t, unsigned long long node,
+                                                         int k, bool last, double &m, int lane,
+                                                         float *lv)
 {
-    double mine = 0.0;
-    if (lane < (1 << k) - 1) {
-        const int lev = 32 - __clz(lane + 1);           // relative depth 1..k of this lane's node
-        const int pos = lane + 1 - (1 << (lev - 1));    // position among the left children
-        mine = S[(node << lev) + 2 * pos];
+    const int ninternal = (1 << (last ? k - 1 : k)) - 1;  // left children that are internal nodes
+    double v[4];
+    float lf[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = lane + 32 * r;
+        v[r] = 0.0;
+        if (i < ninternal) {
+            const int lev = 32 - __clz(i + 1);
+            const int pos = i + 1 - (1 << (lev - 1));
+            v[r] = t.S[(node << lev) + 2 * pos];
+        }
+        lf[r] = 0.0f;
+        if (last && i < (1 << k)) lf[r] = t.L[(node << k) - t.n + i];
     }
     int q = 0;
-    for (int lev = 1; lev <= k; ++lev) {
-        const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
+    const int kint = last ? k - 1 : k;
+    for (int lev = 1; lev <= kint; ++lev) {
+        const int i = (1 << (lev - 1)) - 1 + q;
+        const int r = i >> 5;
+        const double mine = r == 0 ? v[0] : r == 1 ? v[1] : r == 2 ? v[2] : v[3];
+        const double left = __shfl_sync(kFull, mine, i & 31);
         if (gt_nonneg(left, m)) {
             q = 2 * q;
         } else {
@@ -108,100 +125,63 @@ __device__ __forceinline__ unsigned long long walk_internal(const double *__rest
             q = 2 * q + 1;
         }
     }
+    if (last) {
+        const int i = 2 * q;  // the left leaf of the final pair
+        const int r = i >> 5;
+        const float mine = r == 0 ? lf[0] : r == 1 ? lf[1] : r == 2 ? lf[2] : lf[3];
+        const double left = (double)__shfl_sync(kFull, mine, i & 31);
+        if (gt_nonneg(left, m)) {
+            q = 2 * q;
+        } else {
+            m = __dsub_rn(m, left);
+            q = 2 * q + 1;
+        }
+        const int rr = q >> 5;
+        const float pick = rr == 0 ? lf[0] : rr == 1 ? lf[1] : rr == 2 ? lf[2] : lf[3];
+        *lv = __shfl_sync(kFull, pick, q & 31);
+    }
     return (node << k) + q;
 }
 
 __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
 {
-    extern __shared__ double s_top[];  // nodes 2 .. 2^(top+1)-1 at s_top[node - 2]
+    __shared__ unsigned long long s_call;
     __shared__ double s_seg;
     pdl_wait();
     pdl_release();
-    const int top = a.top;
-    const int nstage = (1 << (top + 1)) - 2;
-    if (threadIdx.x == 0) {  // the stratum width T / B, once per CTA
-        const double tot = a.t.D == 0 ? (double)a.t.L[0] : a.t.S[1];
-        s_seg = __ddiv_rn(tot, (double)a.B);
-    }
-    if (nstage > 0) {
-        const double2 *src = reinterpret_cast<const double2 *>(a.t.S + 2);
-        for (int i = threadIdx.x; i < nstage / 2; i += blockDim.x) {
-            const double2 v = src[i];
-            s_top[2 * i] = v.x;
-            s_top[2 * i + 1] = v.y;
-        }
-    }
-    __syncthreads();
     const unsigned long long n = a.t.n;
     const int D = a.t.D;
+    if (threadIdx.x == 0) {
+        s_call = take_call_number(a.ctl);
+        s_seg = __ddiv_rn(D == 0 ? (double)a.t.L[0] : a.t.S[1], (double)a.B);  // stratum width T / B
+    }
     const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
-    const unsigned long long call = a.ctl->sample_calls;
     const unsigned long long size = a.ctl->size;
+    __syncthreads();
+    const unsigned long long call = s_call;
     const double seg = s_seg;
     const float nbeta = -a.beta;
     const int lane = threadIdx.x & 31;
     const unsigned wpb = blockDim.x >> 5;
     const unsigned warps_total = gridDim.x * wpb;
-    const int R = D - top;                 // levels walked below the staged top (>= 1 if D >= 1)
-    const int kL = R < 5 ? R : 5;          // last round, ending on the leaves
-    const int first = (R - kL) % 5;        // odd-sized first round (0 = none)
+    const int rounds = (D + 6) / 7;                 // 7 levels per round; the first takes the rest
+    const int first = D - 7 * (rounds - 1);
 
     for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
         const double u = draw_uniform(a.seed, j, call, 0);
         double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         unsigned long long leaf;
-        float lv;
+        float lv = 0.0f;
         if (D == 0) {
             leaf = 0;
             lv = a.t.L[0];
         } else {
             unsigned long long node = 1;
-            for (int l = 0; l < top; ++l) {
-                const double left = s_top[2 * node - 2];
-                if (gt_nonneg(left, m)) {
-                    node = 2 * node;
-                } else {
-                    m = __dsub_rn(m, left);
-                    node = 2 * node + 1;
-                }
+            for (int rd = 0; rd < rounds; ++rd) {
+                const int k = rd == 0 ? first : 7;
+                node = walk_round(a.t, node, k, rd == rounds - 1, m, lane, &lv);
             }
-            int remaining = R - kL;
-            int k = first ? first : 5;
-            while (remaining > 0) {
-                node = walk_internal(a.t.S, node, k, m, lane);
-                remaining -= k;
-                k = 5;
-            }
-            // last round: kL - 1 internal levels, then the leaf level as one contiguous block
-            double mine = 0.0;
-            float myleaf = 0.0f;
-            if (lane < (1 << (kL - 1)) - 1) {
-                const int lev = 32 - __clz(lane + 1);
-                const int pos = lane + 1 - (1 << (lev - 1));
-                mine = a.t.S[(node << lev) + 2 * pos];
-            }
-            if (lane < (1 << kL)) myleaf = a.t.L[(node << kL) - n + lane];
-            int q = 0;
-            for (int lev = 1; lev < kL; ++lev) {
-                const double left = __shfl_sync(kFull, mine, (1 << (lev - 1)) - 1 + q);
-                if (gt_nonneg(left, m)) {
-                    q = 2 * q;
-                } else {
-                    m = __dsub_rn(m, left);
-                    q = 2 * q + 1;
-                }
-            }
-            {
-                const double left = (double)__shfl_sync(kFull, myleaf, 2 * q);
-                if (gt_nonneg(left, m)) {
-                    q = 2 * q;
-                } else {
-                    m = __dsub_rn(m, left);
-                    q = 2 * q + 1;
-                }
-            }
-            leaf = (node << kL) + q - n;
-            lv = __shfl_sync(kFull, myleaf, q);
+            leaf = node - n;
         }
         if (leaf >= size) {  // ran past the filled slots: take the last filled slot
             leaf = size - 1;
@@ -214,16 +194,6 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             a.o.idx[j] = (long long)leaf;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
         }
-    }
-
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&a.ctl->ticket_sample, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (s_last && threadIdx.x == 0) {
-        a.ctl->sample_calls = call + 1;
-        a.ctl->ticket_sample = 0;
     }
 }
 
@@ -248,12 +218,16 @@ struct RankSampleArgs {
 __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
 {
     __shared__ double s_seg;
+    __shared__ unsigned long long s_call;
     pdl_wait();
     pdl_release();
     const unsigned long long size = a.ctl->size;
-    const unsigned long long call = a.ctl->sample_calls;
-    if (threadIdx.x == 0) s_seg = __ddiv_rn(a.cdf[size], (double)a.B);
+    if (threadIdx.x == 0) {
+        s_call = take_call_number(a.ctl);
+        s_seg = __ddiv_rn(a.cdf[size], (double)a.B);
+    }
     __syncthreads();
+    const unsigned long long call = s_call;
     const double seg = s_seg;
     const float fsize = (float)size;
     const int lane = threadIdx.x & 31;
@@ -307,29 +281,6 @@ __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
         write_scalars(a.r, a.o, j, slot, lane);
         if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, slot, lane, a.vec4);
     }
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&a.ctl->ticket_sample, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (s_last && threadIdx.x == 0) {
-        a.ctl->sample_calls = call + 1;
-        a.ctl->ticket_sample = 0;
-    }
-}
-
-int top_levels_for(int D)
-{
-    if (D <= 0) return 0;
-    int tmax = 11;
-    if (const char *e = std::getenv("GBPER_SAMPLE_TOP")) tmax = std::max(0, std::atoi(e));
-    tmax = std::min(tmax, 12);
-    // walk R = D - top levels from global memory in rounds of 5; prefer R a multiple of 5
-    int R = D - tmax;
-    if (R < 1) R = 1;
-    R = ((R + 4) / 5) * 5;
-    if (R > D) R = D;
-    return D - R;
 }
 
 int warps_per_cta()
@@ -353,9 +304,8 @@ bool rows_vec4(const RingRefs &r, const SampleOut &o)
 
 cudaError_t init_sample_kernels(int carveout)
 {
-    // the staged top levels need up to 2^13 - 2 doubles (64 KiB) when 12 levels are staged
-    cudaError_t e = cudaFuncSetAttribute(k_sample_prop, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    if (e != cudaSuccess || carveout < 0) return e;
+    if (carveout < 0) return cudaSuccess;
+    cudaError_t e;
     const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
@@ -376,13 +326,11 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     a.beta = beta;
     a.seed = seed;
     a.o = o;
-    a.top = top_levels_for(t.D);
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta();
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
-    const size_t smem = a.top > 0 ? (size_t)((1 << (a.top + 1)) - 2) * sizeof(double) : 0;
-    return launch_pdl(k_sample_prop, grid, wpb * 32, smem, st, a);
+    return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
 }
 
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,

@@ -13,12 +13,25 @@
 // an update a scattered set.  Values are recomputed as S[i] = S[2i] + S[2i+1] (binary64) and
 // M[i] = min(M[2i], M[2i+1]) (binary32), so any order of recomputation yields the same bits.
 #include "per_internal.cuh"
+#include "leaf_pow.cuh"
 
 #include <algorithm>
 
 namespace gbper {
 
 namespace {
+
+// Tables of the binary32 power (leaf_pow.cuh), uploaded once per device.
+__device__ LeafPowTables g_leafpow;
+
+// fl32(pow(raw, alpha)): the double-float evaluation when it decides, else the binary64 pow.
+__device__ __forceinline__ float leaf_of(float raw, const LeafPowAlpha &al,
+                                         const LeafPowTables &tb = g_leafpow)
+{
+    float out;
+    if (leaf_pow_fast(raw, al, tb, &out)) return out;
+    return __double2float_rn(pow((double)raw, al.alpha));
+}
 
 constexpr int kThreads = 256;
 constexpr int kAddBlockLog = 8;      // leaves per tree CTA in the insertion kernel: 256
@@ -83,10 +96,104 @@ __device__ __forceinline__ unsigned block_max_u32(unsigned v)
 // the clean edge siblings of every level) are issued before the first level is combined, so
 // the whole climb costs one round trip to L2 plus one barrier per level.
 // ------------------------------------------------------------------------------------------
+// The same climb for a span of at most 32 nodes, on registers: lane i holds span node i, lane
+// l holds the clean edge siblings of depth l, and each level pulls its children by shuffles.
+__device__ void top_range_climb_regs(const TreeRefs &t, int L0, unsigned long long lo,
+                                     unsigned long long hi, int lane)
+{
+    const unsigned long long lvl0 = 1ull << L0;
+    unsigned long long sp_lo = (lo >> 1) << 1;
+    const int w0 = (int)(((hi >> 1) << 1) + 1 - sp_lo + 1);
+    double cs = 0.0;
+    float cm = 0.0f;
+    if (lane < w0) {
+        cs = ld_sum_cg(t, lvl0 + sp_lo + lane);
+        cm = ld_min_cg(t, lvl0 + sp_lo + lane);
+    }
+    double exLs = 0.0, exRs = 0.0;
+    float exLm = 0.0f, exRm = 0.0f;
+    if (lane >= 1 && lane < L0) {  // clean edge siblings of depth `lane`
+        const unsigned long long a = lo >> (L0 - lane), b = hi >> (L0 - lane);
+        const unsigned long long base = 1ull << lane;
+        if (a & 1ull) { exLs = ld_sum_cg(t, base + a - 1); exLm = ld_min_cg(t, base + a - 1); }
+        if (!(b & 1ull)) { exRs = ld_sum_cg(t, base + b + 1); exRm = ld_min_cg(t, base + b + 1); }
+    }
+    // where the range has narrowed to one node, its sibling at depth `lane` is an edge sibling
+    double sib1s = 0.0;
+    float sib1m = 0.0f;
+    if (lane >= 1 && lane < L0) {
+        const unsigned long long a_d = lo >> (L0 - lane);
+        sib1s = (a_d & 1ull) ? exLs : exRs;
+        sib1m = (a_d & 1ull) ? exLm : exRm;
+    }
+    unsigned long long a = lo, b = hi;
+    for (int l = L0; l >= 1; --l) {
+        if (a == b) {
+            // a single dirty node at depth l: the rest is one path to the root, summed on lane 0
+            // from siblings that lane d holds for depth d
+            double cur = __shfl_sync(0xffffffffu, cs, (int)(a - sp_lo));
+            float curm = __shfl_sync(0xffffffffu, cm, (int)(a - sp_lo));
+            unsigned long long node = a;
+            for (int d = l; d >= 1; --d) {
+                // at depth l the sibling is in the current span; above it, an edge sibling
+                const int sl = d == l ? (int)((a ^ 1ull) - sp_lo) : d;
+                const double sd = __shfl_sync(0xffffffffu, d == l ? cs : sib1s, sl);
+                const float sm = __shfl_sync(0xffffffffu, d == l ? cm : sib1m, sl);
+                if (lane == 0) {
+                    if (node & 1ull) {
+                        cur = sd + cur;
+                        curm = fmin_tree(sm, curm);
+                    } else {
+                        cur = cur + sd;
+                        curm = fmin_tree(curm, sm);
+                    }
+                    node >>= 1;
+                    t.S[(1ull << (d - 1)) + node] = cur;
+                    t.M[(1ull << (d - 1)) + node] = curm;
+                }
+            }
+            return;
+        }
+        const unsigned long long pa = a >> 1, pb = b >> 1;   // dirty parents at depth l-1
+        const unsigned long long nsp_lo = (pa >> 1) << 1;
+        const unsigned long long p = nsp_lo + lane;          // this lane's node at depth l-1
+        const int c = (int)(2 * p - sp_lo);
+        const int c0 = c >= 0 && c < 32 ? c : 0, c1 = c + 1 >= 0 && c + 1 < 32 ? c + 1 : 0;
+        const double l0s = __shfl_sync(0xffffffffu, cs, c0), l1s = __shfl_sync(0xffffffffu, cs, c1);
+        const float l0m = __shfl_sync(0xffffffffu, cm, c0), l1m = __shfl_sync(0xffffffffu, cm, c1);
+        const int xl = l - 1 >= 1 ? l - 1 : 0;
+        const double xLs = __shfl_sync(0xffffffffu, exLs, xl), xRs = __shfl_sync(0xffffffffu, exRs, xl);
+        const float xLm = __shfl_sync(0xffffffffu, exLm, xl), xRm = __shfl_sync(0xffffffffu, exRm, xl);
+        double ns = 0.0;
+        float nm = 0.0f;
+        if (p >= pa && p <= pb) {
+            ns = l0s + l1s;
+            nm = fmin_tree(l0m, l1m);
+            t.S[(1ull << (l - 1)) + p] = ns;
+            t.M[(1ull << (l - 1)) + p] = nm;
+        } else if (l - 1 >= 1 && p == pa - 1 && (pa & 1ull)) {
+            ns = xLs;
+            nm = xLm;
+        } else if (l - 1 >= 1 && p == pb + 1 && !(pb & 1ull)) {
+            ns = xRs;
+            nm = xRm;
+        }
+        cs = ns;
+        cm = nm;
+        sp_lo = nsp_lo;
+        a = pa;
+        b = pb;
+    }
+}
+
 __device__ void top_range_upsweep(const TreeRefs &t, int L0, unsigned long long lo,
                                   unsigned long long hi, double *spS0, float *spM0,
                                   double *spS1, float *spM1, double *exS, float *exM)
 {
+    if (L0 > 0 && L0 <= 32 && ((hi >> 1) << 1) + 2 - ((lo >> 1) << 1) <= 32) {
+        if (threadIdx.x < 32) top_range_climb_regs(t, L0, lo, hi, threadIdx.x);
+        return;
+    }
     // run by warp 0 alone: every level is a handful of nodes, and a warp barrier is far cheaper
     // than a CTA barrier per level
     const int lane = threadIdx.x;
@@ -163,6 +270,7 @@ struct AddArgs {
     const unsigned char *dones;
     const float *prio;
     double alpha, eps;
+    LeafPowAlpha lp;
     int proportional;
     int bl;            // log2 leaves per tree block
     unsigned ntree;    // tree CTAs (upper bound over cursor positions)
@@ -289,7 +397,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                     const float raw = a.prio ? prio_to_raw(__ldg(a.prio + k), a.eps, max_prev) : max_prev;
                     mymax = __float_as_uint(raw);
                     if (a.proportional) {
-                        leaf = a.prio ? raw_to_leaf(raw, a.alpha) : max_leaf;
+                        leaf = a.prio ? leaf_of(raw, a.lp) : max_leaf;
                         a.t.L[s] = leaf;
                     } else {
                         a.raw_store[s] = raw;
@@ -399,7 +507,7 @@ __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
             const float raw = a.prio ? prio_to_raw(__ldg(a.prio + k), a.eps, max_prev) : max_prev;
             mymax = max(mymax, __float_as_uint(raw));
             if (a.proportional)
-                a.t.L[slot] = a.prio ? raw_to_leaf(raw, a.alpha) : __uint_as_float(a.ctl->max_leaf_bits);
+                a.t.L[slot] = a.prio ? leaf_of(raw, a.lp) : __uint_as_float(a.ctl->max_leaf_bits);
             else a.raw_store[slot] = raw;
         }
     }
@@ -501,6 +609,7 @@ struct UpdArgs {
     int P;      // log2 number of subtrees
     int pb;     // bits for a batch position
     double alpha, eps;
+    LeafPowAlpha lp;
     int proportional;
 };
 
@@ -555,6 +664,176 @@ __device__ __forceinline__ void warp_sort32(unsigned long long &key, unsigned &p
             if (take) {
                 key = ok;
                 pay = op;
+            }
+        }
+    }
+}
+
+// Climb one warp's subtree when it has U <= 32 distinct leaves, one per lane, ascending
+// (lane u holds leaf node `node0` = leaf index + n and its raw priority).  Two phases:
+//   private  below the height where its path meets a neighbour's, a lane's node always has a
+//            clean sibling, so the lane runs those levels alone as a chain of binary64 adds
+//            over siblings loaded up front (all levels requested before the leaf value, a
+//            binary64 pow, is computed, so the two latencies overlap);
+//   shared   from the lowest meeting height up, the owner of a left child reads a dirty right
+//            sibling's value and run end from that sibling's owner lane by shuffles.
+// No level needs shared memory or a warp barrier.
+constexpr int kMaxClimb = 16;  // levels whose siblings are loaded in the single prefetch round
+
+template <int W>
+__device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
+                                unsigned long long node0, float raw, const LeafPowAlpha &alpha,
+                                const LeafPowTables &tb)
+{
+    const bool have = lane < U;
+    const unsigned long long prev0 = __shfl_up_sync(0xffffffffu, node0, 1);
+    const unsigned long long next0 = __shfl_down_sync(0xffffffffu, node0, 1);
+    // heights at which this path meets the previous / next lane's path
+    const int meet_prev = (have && lane > 0) ? 64 - __clzll((long long)(prev0 ^ node0)) : 64;
+    const int meet_next = (have && lane + 1 < U) ? 64 - __clzll((long long)(next0 ^ node0)) : 64;
+    const int hpre = min(shift, kMaxClimb);  // heights covered by the prefetch round
+    int priv = min(min(meet_prev, meet_next) - 1, hpre);  // levels this lane climbs alone
+    if (priv < 0) priv = 0;
+    int h_shared = priv;
+    for (int o = 16; o > 0; o >>= 1) h_shared = min(h_shared, __shfl_xor_sync(0xffffffffu, h_shared, o));
+
+    // one round of loads: the clean sibling at every height this lane owns (height 0 is a leaf,
+    // every height above it an internal node)
+    double ps[kMaxClimb];
+    float pmn[kMaxClimb];
+#pragma unroll
+    for (int h = 0; h < kMaxClimb; ++h) {
+        ps[h] = 0.0;
+        pmn[h] = 0.0f;
+        if (have && h < hpre) {
+            const unsigned long long v = node0 >> h;
+            if (lane == 0 || (prev0 >> h) != v) {
+                if (h == 0) {
+                    const float lf = t.L[(v ^ 1ull) - t.n];
+                    ps[0] = (double)lf;
+                    pmn[0] = leaf_min_value(lf);
+                } else {
+                    ps[h] = t.S[v ^ 1ull];
+                    pmn[h] = t.M[v ^ 1ull];
+                }
+            }
+        }
+    }
+    double vs = 0.0;
+    float vm = 0.0f;
+    if (have) {
+        const float lv = leaf_of(raw, alpha, tb);
+        t.L[node0 - t.n] = lv;
+        vs = (double)lv;
+        vm = leaf_min_value(lv);
+    }
+    // private phase: a chain of binary64 adds over the prefetched siblings
+#pragma unroll
+    for (int h = 0; h < kMaxClimb; ++h) {
+        if (have && h < priv) {
+            const unsigned long long v = node0 >> h;
+            if ((v & 1ull) == 0) {
+                vs = vs + ps[h];
+                vm = fmin_tree(vm, pmn[h]);
+            } else {
+                vs = ps[h] + vs;
+                vm = fmin_tree(pmn[h], vm);
+            }
+            t.S[v >> 1] = vs;
+            t.M[v >> 1] = vm;
+        }
+    }
+    // shared phase: heights h_shared .. shift-1, one shuffle step per level
+    int rend = lane + 1;
+#pragma unroll
+    for (int h = 0; h < kMaxClimb; ++h) {
+        if (h >= h_shared && h < hpre) {
+            const int src = rend < 32 ? rend : 31;
+            const unsigned long long e_node = __shfl_sync(0xffffffffu, node0, src);
+            const double e_vs = __shfl_sync(0xffffffffu, vs, src);
+            const float e_vm = __shfl_sync(0xffffffffu, vm, src);
+            const int e_rend = __shfl_sync(0xffffffffu, rend, src);
+            const unsigned long long v = node0 >> h;
+            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
+                bool compute = true;
+                double sum = 0.0;
+                float mn = 0.0f;
+                if ((v & 1ull) == 0) {
+                    if (rend < U && (e_node >> h) == v + 1) {
+                        sum = vs + e_vs;
+                        mn = fmin_tree(vm, e_vm);
+                        rend = e_rend;
+                    } else {
+                        sum = vs + ps[h];
+                        mn = fmin_tree(vm, pmn[h]);
+                    }
+                } else if (lane > 0 && (prev0 >> h) == v - 1) {
+                    compute = false;  // the left sibling's owner combines this pair
+                } else {
+                    sum = ps[h] + vs;
+                    mn = fmin_tree(pmn[h], vm);
+                }
+                if (compute) {
+                    vs = sum;
+                    vm = mn;
+                    t.S[v >> 1] = sum;
+                    t.M[v >> 1] = mn;
+                }
+            }
+        }
+    }
+    // heights beyond the prefetch round (subtrees deeper than kMaxClimb levels)
+    for (int h0 = hpre; h0 < shift; h0 += W) {
+        double qs[W];
+        float qm[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const int h = h0 + w;
+            qs[w] = 0.0;
+            qm[w] = 0.0f;
+            if (have && h < shift) {
+                const unsigned long long v = node0 >> h;
+                if (lane == 0 || (prev0 >> h) != v) {
+                    qs[w] = t.S[v ^ 1ull];
+                    qm[w] = t.M[v ^ 1ull];
+                }
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const int h = h0 + w;
+            if (h >= shift) break;
+            const int src = rend < 32 ? rend : 31;
+            const unsigned long long e_node = __shfl_sync(0xffffffffu, node0, src);
+            const double e_vs = __shfl_sync(0xffffffffu, vs, src);
+            const float e_vm = __shfl_sync(0xffffffffu, vm, src);
+            const int e_rend = __shfl_sync(0xffffffffu, rend, src);
+            const unsigned long long v = node0 >> h;
+            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
+                bool compute = true;
+                double sum = 0.0;
+                float mn = 0.0f;
+                if ((v & 1ull) == 0) {
+                    if (rend < U && (e_node >> h) == v + 1) {
+                        sum = vs + e_vs;
+                        mn = fmin_tree(vm, e_vm);
+                        rend = e_rend;
+                    } else {
+                        sum = vs + qs[w];
+                        mn = fmin_tree(vm, qm[w]);
+                    }
+                } else if (lane > 0 && (prev0 >> h) == v - 1) {
+                    compute = false;
+                } else {
+                    sum = qs[w] + vs;
+                    mn = fmin_tree(qm[w], vm);
+                }
+                if (compute) {
+                    vs = sum;
+                    vm = mn;
+                    t.S[v >> 1] = sum;
+                    t.M[v >> 1] = mn;
+                }
             }
         }
     }
@@ -672,6 +951,12 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     WarpLists *lists = reinterpret_cast<WarpLists *>(smem_raw);
     __shared__ int s_cnt[kUpdWarps];
     __shared__ unsigned s_max;
+    __shared__ LeafPowTables s_lp;
+    {   // the power's tables (constant since the library loaded), staged while the batch is read
+        const unsigned *src = reinterpret_cast<const unsigned *>(&g_leafpow);
+        unsigned *dst = reinterpret_cast<unsigned *>(&s_lp);
+        for (int i = threadIdx.x; i < (int)(sizeof(LeafPowTables) / 4); i += blockDim.x) dst[i] = src[i];
+    }
     pdl_wait();
     pdl_release();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -742,7 +1027,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                 const unsigned peers = __match_any_sync(0xffffffffu, key);
                 if (mine && (31 - __clz(peers)) == lane) {  // the last lane of this chunk for the leaf
                     const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
-                    if (a.proportional) a.t.L[i] = raw_to_leaf(raw, a.alpha);
+                    if (a.proportional) a.t.L[i] = leaf_of(raw, a.lp);
                     else a.raw_store[i] = raw;
                 }
                 __syncwarp();
@@ -760,31 +1045,25 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                 }
             }
         } else if (m <= 32) {
-            // one entry per lane: sort in registers, keep the last position of each leaf
+            // one entry per lane: sort in registers, keep the last position of each leaf, and
+            // move the u-th surviving leaf to lane u
             unsigned long long key = lane < m ? wl.keys[lane] : ~0ull;
             unsigned pay = lane < m ? wl.pay[lane] : 0u;
             warp_sort32(key, pay, lane);
             const unsigned long long nxt = __shfl_down_sync(0xffffffffu, key, 1);
             const bool win = lane < m && (lane == m - 1 || (nxt >> a.pb) != (key >> a.pb));
             const unsigned bal = __ballot_sync(0xffffffffu, win);
-            const int u = __popc(bal & ((1u << lane) - 1u));
             const int U = __popc(bal);
-            if (win) {
-                const unsigned long long leaf = base + (key >> a.pb);
-                const float raw = wl.rawv[pay];
-                wl.ulist[u] = (unsigned)leaf;
-                if (a.proportional) {
-                    const float lv = raw_to_leaf(raw, a.alpha);
-                    a.t.L[leaf] = lv;
-                    wl.vs[u] = (double)lv;
-                    wl.vm[u] = leaf_min_value(lv);
-                    wl.rend[u] = u + 1;
-                } else {
-                    a.raw_store[leaf] = raw;
-                }
+            const float myraw = lane < m ? wl.rawv[pay] : 0.0f;
+            const int from = lane < U ? (int)__fns(bal, 0, lane + 1) : 0;
+            const unsigned long long k_from = __shfl_sync(0xffffffffu, key, from);
+            const float raw = __shfl_sync(0xffffffffu, myraw, from);
+            const unsigned long long leaf = base + (k_from >> a.pb);
+            if (a.proportional) {
+                warp_climb_regs<W>(a.t, U, shift, lane, lane < U ? leaf + n : 0ull, raw, a.lp, s_lp);
+            } else if (lane < U) {
+                a.raw_store[leaf] = raw;
             }
-            __syncwarp();
-            if (a.proportional) warp_upsweep<W>(a.t, wl, U, shift, lane);
         } else {
             int m2 = 2;
             while (m2 < m) m2 <<= 1;
@@ -809,7 +1088,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                 if (win) {
                     wl.ulist[u] = (unsigned)leaf;
                     if (a.proportional) {
-                        const float lv = raw_to_leaf(raw, a.alpha);
+                        const float lv = leaf_of(raw, a.lp);
                         a.t.L[leaf] = lv;
                         wl.vs[u] = (double)lv;
                         wl.vm[u] = leaf_min_value(lv);
@@ -870,7 +1149,10 @@ int ilog2_ceil(unsigned long long v)
 
 cudaError_t init_tree_kernels(int carveout)
 {
-    cudaError_t e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const LeafPowTables tables = make_leaf_pow_tables();
+    cudaError_t e = cudaMemcpyToSymbol(g_leafpow, &tables, sizeof(tables));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kUpdSmemBytes);
     if (e != cudaSuccess || carveout < 0) return e;
     const void *fns[] = {(const void *)k_update<kUpdWindow>, (const void *)k_add, (const void *)k_add_bulk_rows,
@@ -913,6 +1195,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.prio = prio;
     a.alpha = alpha;
     a.eps = eps;
+    a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
     a.bl = std::min(kAddBlockLog, t.D);
     const unsigned long long bsz = 1ull << a.bl;
@@ -964,6 +1247,7 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.pb = std::max(1, ilog2_ceil(B));
     a.alpha = alpha;
     a.eps = eps;
+    a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
     // about 8 batch entries per subtree (a warp's list holds up to kWarpCap, so a batch
     // concentrated on a stretch of recent slots still fits); at most 2^10 subtrees, and no

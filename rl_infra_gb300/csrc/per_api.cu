@@ -420,7 +420,7 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
         cudaError_t e = cudaMemcpyAsync(&c, h->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return cuda_fail(h, e, "per_read_state");
-        const uint64_t v[4] = {c.sample_calls, c.cursor, c.size, c.max_raw_bits};
+        const uint64_t v[4] = {c.call_tix >> kCallShift, c.cursor, c.size, c.max_raw_bits};
         std::memcpy(host_dst, v + first, count * sizeof(uint64_t));
         return PER_OK;
     }

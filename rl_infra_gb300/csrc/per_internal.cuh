@@ -19,12 +19,12 @@ namespace gbper {
 // replayed from a CUDA graph still draws a fresh batch and inserts at the right slot
 // ("True Single-Graph Implementation Plan", Task 4: device-side counters).
 struct Ctl {
-    unsigned long long sample_calls;  // Philox call counter
+    unsigned long long call_tix;      // sample calls << 24 | CTAs of the current call that started
     unsigned long long cursor;        // next ring slot
     unsigned long long size;          // filled slots
     unsigned int max_raw_bits;        // running maximum raw priority (float bits, > 0)
     unsigned int err_flags;           // PER_DEVFLAG_* bits
-    unsigned int ticket_sample;       // arrival tickets; the last CTA resets its own
+    unsigned int ticket_sample;       // (unused)
     unsigned int ticket_update;
     unsigned int ticket_add;
     unsigned int batch_max_bits;      // per-call maximum raw priority, folded in by the last CTA
@@ -41,6 +41,18 @@ __device__ __forceinline__ void fold_running_max(Ctl *c, unsigned call_max_bits,
         c->max_raw_bits = call_max_bits;
         c->max_leaf_bits = __float_as_uint(__double2float_rn(pow((double)__uint_as_float(call_max_bits), alpha)));
     }
+}
+
+// The Philox call number of a sample launch, taken by each CTA at its start: one 64-bit atomic
+// returns the call count (high 40 bits) and this CTA's arrival index (low 24 bits); the last CTA
+// to arrive rolls the count over, so no CTA waits and none needs a fence at its end.
+constexpr int kCallShift = 24;
+__device__ __forceinline__ unsigned long long take_call_number(Ctl *c)
+{
+    const unsigned long long old = atomicAdd(&c->call_tix, 1ull);
+    if ((unsigned)(old & ((1ull << kCallShift) - 1)) == gridDim.x - 1)
+        atomicAdd(&c->call_tix, (1ull << kCallShift) - gridDim.x);
+    return old >> kCallShift;
 }
 
 constexpr unsigned kFlagBadIndex = 1u;

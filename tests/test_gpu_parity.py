@@ -172,6 +172,28 @@ def test_many_sizes_of_batch_and_tree():
         p.close()
 
 
+@pytest.mark.parametrize("alpha", [0.6, 0.5, 1.5, 0.123456789])
+def test_leaf_values_over_a_wide_range(alpha):
+    """Leaves p^alpha for priorities spread over 2^-30 .. 2^30 (and exact powers of two),
+    through the insert path and the update path, bit-identical to the oracle's."""
+    cap = 1 << 20
+    g = wl.rng(14, int(alpha * 1000))
+    p = Pair(cap, 0, 0, alpha, 1e-9, 0, seed=1, with_ring=True)
+    raw = np.exp2(g.uniform(-30, 30, cap)).astype(np.float32)
+    raw[::97] = np.float32(2.0) ** g.integers(-20, 20, len(raw[::97])).astype(np.float32)
+    z = np.zeros(cap, np.uint32)
+    rows = {"states": np.zeros((cap, 0), np.float32), "next_states": np.zeros((cap, 0), np.float32),
+            "actions": z, "rewards": z.view(np.float32), "dones": z.astype(np.uint8)}
+    for lo in range(0, cap, 1 << 18):
+        p.add({k: v[lo: lo + (1 << 18)] for k, v in rows.items()}, raw[lo: lo + (1 << 18)])
+    p.check_tree()
+    idx = g.integers(0, cap, 8192).astype(np.int64)
+    td = (np.exp2(g.uniform(-20, 20, 8192)) * g.choice([-1, 1], 8192)).astype(np.float32)
+    p.update(idx, td)
+    p.check_tree()
+    p.close()
+
+
 # -- rank-based variant ---------------------------------------------------------------------
 
 @pytest.mark.parametrize("cap,fill", [(1, 1), (100, 37), (4095, 4095), (4096, 4096), (4097, 4097),
