@@ -83,7 +83,7 @@ RingRefs ring_of(const per_buffer *h)
 void free_all(per_buffer *h)
 {
     void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
-                    h->rank.vals[0], h->rank.vals[1], h->rank.tile_hist, h->rank.digit_hist,
+                    h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -193,11 +193,11 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (c.mode == PER_MODE_PROPORTIONAL) {
         ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n);
     } else {
-        const uint64_t tiles = rank_tile_count(capacity);
         ok = ok && alloc(&h->rank.raw, capacity) && alloc(&h->rank.cdf, capacity + 1) &&
              alloc(&h->rank.keys[0], capacity) && alloc(&h->rank.keys[1], capacity) &&
              alloc(&h->rank.vals[0], capacity) && alloc(&h->rank.vals[1], capacity) &&
-             alloc(&h->rank.tile_hist, 256 * tiles) && alloc(&h->rank.digit_hist, 4 * 256);
+             alloc(&h->rank.status, rank_status_words(capacity)) && alloc(&h->rank.digit_hist, 4 * 256 + 16);
+        h->rank.sort_ctl = h->rank.digit_hist + 4 * 256;
         h->rank.capacity = capacity;
     }
     ok = ok && alloc(&h->states, capacity * (uint64_t)state_dim) && alloc(&h->next, capacity * (uint64_t)state_dim) &&
@@ -218,6 +218,10 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (e == cudaSuccess && h->S) e = cudaMemset(h->S, 0, h->n * sizeof(double));
     if (e == cudaSuccess && h->M) e = launch_fill_mins(h->M, h->n, 0);
     if (e == cudaSuccess && h->rank.raw) e = cudaMemset(h->rank.raw, 0, capacity * sizeof(float));
+    if (e == cudaSuccess && h->rank.status)
+        e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
+    if (e == cudaSuccess && h->rank.digit_hist) e = cudaMemset(h->rank.digit_hist, 0, (4 * 256 + 16) * sizeof(unsigned));
+    if (h->rank.raw) h->rank.err = &h->ctl->err_flags;
     if (e == cudaSuccess && h->rank.cdf) e = launch_build_cdf(h->rank.cdf, capacity, h->alpha, 0);
     if (e == cudaSuccess && state_dim) e = cudaMemset(h->states, 0, capacity * (uint64_t)state_dim * sizeof(float));
     if (e == cudaSuccess && state_dim) e = cudaMemset(h->next, 0, capacity * (uint64_t)state_dim * sizeof(float));

@@ -174,10 +174,15 @@ struct RankWork {
     double *cdf;
     unsigned *keys[2];
     unsigned *vals[2];
-    unsigned *digit_hist;  // [4][256]
-    unsigned *tile_hist;   // [256][ntiles]
+    unsigned *digit_hist;          // [4][256] digit counts of the sort in progress (zero between sorts)
+    unsigned long long *status;    // [4][ntiles][256] look-back words: epoch | flag | count
+    unsigned *sort_ctl;            // [8]: tile counters of the four passes, [4] the sort epoch
+    unsigned *err;                 // device error word (PER_DEVFLAG_TIMEOUT)
     unsigned long long capacity;
 };
+
+// Words of RankWork scratch the sort needs for `capacity` keys (beyond keys and values).
+unsigned long long rank_status_words(unsigned long long capacity);
 
 cudaError_t launch_build_cdf(double *cdf, unsigned long long capacity, double alpha,
                              cudaStream_t st);

@@ -217,6 +217,22 @@ def test_rank_small(cap, fill):
     p.close()
 
 
+@pytest.mark.slow
+def test_rank_more_than_a_million_slots():
+    """3M slots: more than 256 sort tiles, so the look-back reads group totals in rounds."""
+    cap = 3_000_000
+    w = _small("rank", capacity=cap, state_dim=2, row_stride=4)
+    g = wl.rng(15)
+    p = Pair(cap, 2, 4, 0.7, 1e-6, 1, seed=11)
+    prefill(p, w, g, chunk=1 << 20)
+    for _ in range(2):
+        _, want = p.sample(2048, 0.5)
+        p.update(want["idx"], wl.td_errors(g, 2048))
+    p.check_tree()
+    p.check_counters()
+    p.close()
+
+
 def test_rank_ties_keep_slot_order():
     cap = 9000
     w = _small("rank", capacity=cap, state_dim=4, row_stride=4)
