@@ -14,55 +14,71 @@
 #include "per_internal.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace gbper {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 16;                       // keys per thread per tile
-constexpr int kTile = kThreads * kItems;          // 4096
+constexpr int kItems = 7;                        // keys per thread per tile
+constexpr int kTile = kThreads * kItems;          // 7168: 2^20 keys are 147 tiles, one per SM
 constexpr int kGroup = 16;                        // tiles per look-back group
 constexpr int kMaxGroups = 16;                    // group totals read per round
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ unsigned key_of_raw(float raw) { return ~__float_as_uint(raw); }
 
-// All four digit histograms at once: they depend on the key set, not on its order.  Block 0
-// also opens a new sort epoch, which tags this sort's look-back words.
-__global__ void __launch_bounds__(kThreads) k_rs_hist4(const float *raw, unsigned long long size,
-                                                        unsigned *digit_hist, unsigned *sort_ctl)
+// All four digit histograms at once: they depend on the key set, not on its order.  Every lane
+// counts into its own copy of the 4 x 256 bins, laid out with a stride of 257 words, so lanes
+// that meet the same digit (the high digits of floats of similar magnitude) hit distinct banks.
+// Block 0 also opens a new sort epoch, which tags this sort's look-back words.
+constexpr int kHistThreads = 1024;
+constexpr int kHistStride = 257;
+constexpr int kHistCopy = 32 * kHistStride;
+constexpr size_t kHistSmem = 4ull * kHistCopy * sizeof(unsigned);   // 131,584 bytes
+
+__global__ void __launch_bounds__(kHistThreads) k_rs_hist4(const float *raw, unsigned long long size,
+                                                            unsigned *digit_hist, unsigned *sort_ctl)
 {
-    __shared__ unsigned s_h[4 * 256];
-    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) s_h[i] = 0;
+    extern __shared__ unsigned s_h[];   // [4 digits][32 lanes][257]
+    for (int i = threadIdx.x; i < 4 * kHistCopy; i += blockDim.x) s_h[i] = 0;
     pdl_wait();
     pdl_release();
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&sort_ctl[4], 1u);
     __syncthreads();
-    // keys of similar magnitude share their high digits, so lanes with equal digits add once
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-    const unsigned long long p0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const unsigned long long rounds = (size + stride - 1) / stride;
     const int lane = threadIdx.x & 31;
-    for (unsigned long long r = 0; r < rounds; ++r) {
-        const unsigned long long p = p0 + r * stride;
-        const bool ok = p < size;
-        const unsigned k = ok ? key_of_raw(raw[p]) : 0u;
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    unsigned *mine = s_h + lane * kHistStride;
+    constexpr int kU = 8;   // loads in flight per thread
+    for (unsigned long long p0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; p0 < size;
+         p0 += kU * stride) {
+        unsigned k[kU];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const unsigned dg = ok ? (k >> (8 * b)) & 255u : 256u;
-            const unsigned peers = __match_any_sync(kFull, dg);
-            if (ok && (__ffs(peers) - 1) == lane) atomicAdd(&s_h[256 * b + dg], (unsigned)__popc(peers));
+        for (int u = 0; u < kU; ++u) {
+            const unsigned long long p = p0 + u * stride;
+            k[u] = p < size ? key_of_raw(__ldg(raw + p)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (p0 + u * stride >= size) break;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) atomicAdd(&mine[b * kHistCopy + ((k[u] >> (8 * b)) & 255u)], 1u);
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x)
-        if (s_h[i]) atomicAdd(&digit_hist[i], s_h[i]);
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) {
+        const unsigned *c = s_h + (i >> 8) * kHistCopy + (i & 255);
+        unsigned sum = 0;
+#pragma unroll 8
+        for (int l = 0; l < 32; ++l) sum += c[l * kHistStride];
+        if (sum) atomicAdd(&digit_hist[i], sum);
+    }
 }
 
-constexpr unsigned long long kFlagAgg = 1ull, kFlagInc = 2ull;
-constexpr int kSpinLimit = 1 << 20;  // look-back polls before the wait is declared lost
+constexpr unsigned long long kFlagAgg = 1ull;
+constexpr int kSpinLimit = 1 << 20;  // look-back poll rounds before the wait is declared lost
 
 __device__ __forceinline__ unsigned long long status_word(unsigned epoch, unsigned long long flag,
                                                           unsigned count)
@@ -70,14 +86,83 @@ __device__ __forceinline__ unsigned long long status_word(unsigned epoch, unsign
     return ((unsigned long long)(epoch & 0x3FFFFFFFu) << 34) | (flag << 32) | count;
 }
 
-// One pass of the sort (8 bits at `shift`), one kernel.  Tiles take their index in start
-// order, so every predecessor of a tile is already running.  A tile ranks its keys stably
-// (per-warp running counts; lanes with equal digits found by bit ballots), publishes its digit
-// counts, and learns how many keys of each digit precede it from two levels of published
-// words: the totals of the earlier groups of 16 tiles (each published by the group's last tile)
-// and the counts of the earlier tiles of its own group -- one round of loads, no chain.  The
-// digit's global start comes from the pass histogram.  The tile is then staged in digit order
-// in shared memory and every digit's run is written contiguously.
+__device__ __forceinline__ bool word_ready(unsigned long long w, unsigned want)
+{
+    return (unsigned)(w >> 34) == want && ((w >> 32) & 3ull) != 0;
+}
+
+// Adds the counts of the published words p[q * stride], q < count <= N, to *sum.  Every round
+// re-reads all words still pending at once, so the wait costs one memory round trip beyond the
+// last word's arrival.  Returns false when the rounds ran out (the sum is then incomplete).
+template <int N>
+__device__ __forceinline__ bool sum_published(const volatile unsigned long long *p, unsigned long long stride,
+                                              unsigned count, unsigned want, unsigned *sum)
+{
+    unsigned pending = count >= 32 ? 0xffffffffu : ((1u << count) - 1u);
+    unsigned long long w[N];
+    for (int it = 0; pending && it < kSpinLimit; ++it) {
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            if ((pending >> q) & 1u) w[q] = p[(unsigned long long)q * stride];
+#pragma unroll
+        for (int q = 0; q < N; ++q)
+            if (((pending >> q) & 1u) && word_ready(w[q], want)) {
+                *sum += (unsigned)w[q];
+                pending &= ~(1u << q);
+            }
+    }
+    return pending == 0;
+}
+
+// The digit's global start (exclusive scan of this pass's histogram row, into s_base), the sort
+// epoch and the tile index.  Tiles take their index in start order, so every predecessor of a
+// tile is already running.  The tile that takes the last index clears the histogram row and the
+// counter for the next sort: every tile read the row before taking its index.
+__device__ __forceinline__ void onesweep_prologue(int pass, unsigned ntiles, unsigned *digit_hist,
+                                                  unsigned *sort_ctl, unsigned *s_base, unsigned *s_warp_tot,
+                                                  unsigned *s_tile, unsigned *s_epoch)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;   // digit tid: threads 0..255
+    unsigned c = 0, incl = 0;
+    if (tid < 256) {
+        c = digit_hist[pass * 256 + tid];
+        incl = c;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp_tot[warp] = incl;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        unsigned before = 0;
+        for (int w = 0; w < warp; ++w) before += s_warp_tot[w];
+        s_base[tid] = before + incl - c;
+    }
+    if (tid == 0) {
+        *s_epoch = *(volatile unsigned *)&sort_ctl[4];
+        *s_tile = atomicAdd(&sort_ctl[pass], 1u);
+    }
+    __syncthreads();
+    if (*s_tile == ntiles - 1 && tid < 256) {
+        digit_hist[pass * 256 + tid] = 0;
+        if (tid == 0) sort_ctl[pass] = 0;
+    }
+}
+
+// One pass of the sort (8 bits at `shift`), one kernel, one tile of 7168 keys per CTA.  A tile
+// ranks its keys stably (per-warp running counts; lanes with equal digits found by bit ballots),
+// publishes its digit counts, and learns how many keys of each digit precede it from two levels
+// of published words: the totals of the earlier groups of 16 tiles (each published by the
+// group's last tile) and the counts of the earlier tiles of its own group.  The digit's global
+// start comes from the pass histogram.  The tile is staged in digit order in shared memory and
+// every digit's run is written contiguously.
+//
+// Passes 1-3 run their prologue before waiting on the previous pass: the histogram row, the
+// epoch and the tile counter were last written two or more kernels earlier (the histogram
+// kernel, and the previous sort), and a kernel starts only once the kernel two places before it
+// in the stream has completed.  Pass 0 reads the histogram its predecessor wrote, so it waits
+// first.
 __global__ void __launch_bounds__(kThreads) k_rs_onesweep(const float *raw, const unsigned *keys_in,
                                                            const unsigned *vals_in, unsigned *keys_out,
                                                            unsigned *vals_out, unsigned long long size,
@@ -86,176 +171,165 @@ __global__ void __launch_bounds__(kThreads) k_rs_onesweep(const float *raw, cons
                                                            unsigned *err)
 {
     __shared__ unsigned s_base[256];
-    __shared__ unsigned s_toff[256], s_gstart[256];
+    __shared__ unsigned s_toff[256], s_part[4][256], s_delta[256];
     __shared__ unsigned s_wcnt[kWarps][256];
-    __shared__ unsigned s_keys[kTile], s_vals[kTile];
+    extern __shared__ unsigned s_stage[];   // the tile in digit order: keys [kTile], values [kTile]
+    unsigned *s_keys = s_stage, *s_vals = s_stage + kTile;
     __shared__ unsigned s_tile, s_epoch;
     __shared__ unsigned s_warp_tot[kWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int shift = 8 * pass;
     const unsigned ngroups = (ntiles + kGroup - 1) / kGroup;
-    for (int w = 0; w < kWarps; ++w) s_wcnt[w][tid] = 0;
-    pdl_wait();
+    for (int i = tid; i < kWarps * 256; i += kThreads) (&s_wcnt[0][0])[i] = 0;
+    if (pass > 0) {
+        onesweep_prologue(pass, ntiles, digit_hist, sort_ctl, s_base, s_warp_tot, &s_tile, &s_epoch);
+        pdl_wait();
+    } else {
+        pdl_wait();
+        onesweep_prologue(pass, ntiles, digit_hist, sort_ctl, s_base, s_warp_tot, &s_tile, &s_epoch);
+    }
     pdl_release();
-    // the digit's global start: exclusive scan of this pass's histogram
-    const unsigned c = digit_hist[pass * 256 + tid];
-    unsigned incl = c;
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned v = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_warp_tot[warp] = incl;
-    __syncthreads();
-    unsigned before = 0;
-    for (int w = 0; w < warp; ++w) before += s_warp_tot[w];
-    s_base[tid] = before + incl - c;
-    if (tid == 0) {
-        s_epoch = sort_ctl[4];
-        s_tile = atomicAdd(&sort_ctl[pass], 1u);
-    }
-    __syncthreads();
     const unsigned tile = s_tile, epoch = s_epoch;
-    if (tile == ntiles - 1) {
-        // every tile index has been handed out, so every tile has read the histogram row
-        digit_hist[pass * 256 + tid] = 0;
-        if (tid == 0) sort_ctl[pass] = 0;
-    }
 
-    // local stable ranking: warp w takes keys [tile*4096 + w*512, +512) in 16 rounds of 32
-    const unsigned long long base = (unsigned long long)tile * kTile + (unsigned long long)warp * (kTile / kWarps);
+    // local stable ranking: warp w takes keys [w * 224, +224) of the tile in 7 rounds of 32
+    const unsigned long long tbase = (unsigned long long)tile * kTile;
+    const int nvalid = size - tbase < (unsigned long long)kTile ? (int)(size - tbase) : kTile;
+    const int wofs = warp * (kTile / kWarps);
+    const int wvalid = nvalid - wofs;       // keys of this warp: rounds i with i*32+lane < wvalid
     unsigned k[kItems], v[kItems], rk[kItems];
     const unsigned lt = (1u << lane) - 1u;
     // every key and value of the thread first, in one round of loads (the ranking loop below
     // synchronises the warp, which loads may not cross)
+    {
+        const unsigned long long w0 = tbase + wofs + lane;
+        const unsigned *kp = keys_in ? keys_in + w0 : nullptr, *vp = vals_in ? vals_in + w0 : nullptr;
+        const float *rp = raw ? raw + w0 : nullptr;
 #pragma unroll
-    for (int i = 0; i < kItems; ++i) {
-        const unsigned long long p = base + (unsigned long long)i * 32 + lane;
-        const bool ok = p < size;
-        k[i] = ok ? (raw ? key_of_raw(__ldg(raw + p)) : __ldg(keys_in + p)) : 0u;
-        v[i] = ok ? (raw ? (unsigned)p : __ldg(vals_in + p)) : 0u;
+        for (int i = 0; i < kItems; ++i) {
+            const bool ok = i * 32 + lane < wvalid;
+            k[i] = ok ? (rp ? key_of_raw(__ldg(rp + i * 32)) : __ldg(kp + i * 32)) : 0u;
+            v[i] = ok ? (rp ? (unsigned)(w0 + i * 32) : __ldg(vp + i * 32)) : 0u;
+        }
     }
+    // lanes with each key's digit: one ballot per digit bit and one for validity, for all rounds
+    // first (independent of one another), then one shared-memory atomic per digit and round by
+    // the digit's lowest lane, whose result (the warp's count of that digit so far) is broadcast
+    unsigned pm[kItems];
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
-        const unsigned long long p = base + (unsigned long long)i * 32 + lane;
-        const bool ok = p < size;
-        const unsigned dg = ok ? (k[i] >> shift) & 255u : 256u;
-        // lanes with this lane's digit: one ballot per digit bit (and one for validity)
+        const bool ok = i * 32 + lane < wvalid;
+        const unsigned dg = (k[i] >> shift) & 255u;
         unsigned peers = __ballot_sync(kFull, ok);
         if (!ok) peers = ~peers;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            const unsigned bit = (dg >> b) & 1u;
-            const unsigned bb = __ballot_sync(kFull, bit);
-            peers &= bit ? bb : ~bb;
+            const unsigned ones = 0u - ((dg >> b) & 1u);    // all ones where the bit is set
+            const unsigned bb = __ballot_sync(kFull, ones);
+            peers &= ~(bb ^ ones);
         }
-        const unsigned bef = __popc(peers & lt);
-        rk[i] = ok ? s_wcnt[warp][dg] + bef : 0;
-        __syncwarp();
-        if (ok && bef == 0) s_wcnt[warp][dg] += __popc(peers);
+        pm[i] = peers;
+    }
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const bool ok = i * 32 + lane < wvalid;
+        const unsigned dg = (k[i] >> shift) & 255u;
+        const int leader = __ffs(pm[i]) - 1;
+        unsigned old = 0;
+        if (ok && lane == leader) old = atomicAdd(&s_wcnt[warp][dg], (unsigned)__popc(pm[i]));
+        old = __shfl_sync(kFull, old, leader);
+        rk[i] = old + __popc(pm[i] & lt);
         __syncwarp();
     }
     __syncthreads();
-    // this tile's count of digit tid, the start of its run within the tile, and the tile
-    // staged in digit order in shared memory (which frees the key registers for the look-back)
-    unsigned cnt = 0;
-    for (int w = 0; w < kWarps; ++w) cnt += s_wcnt[w][tid];
+    // this tile's count of each digit, published at once (four threads per digit add eight
+    // warps' counts each); then the start of each digit's run within the tile and of each
+    // warp's share of it, and the tile staged in digit order in shared memory
+    unsigned long long *row = status + ((unsigned long long)pass * ntiles) * 256;
+    unsigned long long *grow = status + 4ull * ntiles * 256 + (unsigned long long)pass * ngroups * 256;
+    volatile unsigned long long *vrow = row, *vgrow = grow;
+    const unsigned want = epoch & 0x3FFFFFFFu;
+    const int d = tid & 255, quarter = tid >> 8;
     {
-        unsigned inc = cnt;
+        unsigned c = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps / 4; ++w) c += s_wcnt[quarter * (kWarps / 4) + w][d];
+        s_part[quarter][d] = c;
+    }
+    __syncthreads();
+    unsigned cnt = 0, inc = 0;
+    if (tid < 256) {
+        cnt = s_part[0][d] + s_part[1][d] + s_part[2][d] + s_part[3][d];
+        vrow[(unsigned long long)tile * 256 + d] = status_word(epoch, kFlagAgg, cnt);
+        inc = cnt;
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned x = __shfl_up_sync(kFull, inc, o);
             if (lane >= o) inc += x;
         }
         if (lane == 31) s_warp_tot[warp] = inc;
-        __syncthreads();
+    }
+    __syncthreads();
+    {
+        // exclusive start of digit d within the tile (each quarter redoes the warp scan of its
+        // 32 digits), then of the first of this quarter's eight warps within the digit's run
         unsigned bef = 0;
-        for (int w = 0; w < warp; ++w) bef += s_warp_tot[w];
-        s_toff[tid] = bef + inc - cnt;
-        unsigned run = bef + inc - cnt;   // per warp, within the tile
-        for (int w = 0; w < kWarps; ++w) {
-            const unsigned cw = s_wcnt[w][tid];
-            s_wcnt[w][tid] = run;
+        for (int w = 0; w < (d >> 5); ++w) bef += s_warp_tot[w];
+        const unsigned cd = s_part[0][d] + s_part[1][d] + s_part[2][d] + s_part[3][d];
+        unsigned in = cd;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned x = __shfl_up_sync(kFull, in, o);
+            if (lane >= o) in += x;
+        }
+        const unsigned dx = bef + in - cd;
+        unsigned run = dx;
+        for (int q = 0; q < quarter; ++q) run += s_part[q][d];
+#pragma unroll
+        for (int w = 0; w < kWarps / 4; ++w) {
+            const int ww = quarter * (kWarps / 4) + w;
+            const unsigned cw = s_wcnt[ww][d];
+            s_wcnt[ww][d] = run;
             run += cw;
         }
+        if (tid < 256) s_toff[d] = dx;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
-        const unsigned long long p = base + (unsigned long long)i * 32 + lane;
-        if (p < size) {
+        if (i * 32 + lane < wvalid) {
             const unsigned dg = (k[i] >> shift) & 255u;
             const unsigned tpos = s_wcnt[warp][dg] + rk[i];
             s_keys[tpos] = k[i];
             s_vals[tpos] = v[i];
         }
     }
-    // keys of digit tid in earlier tiles: the totals of the earlier complete groups of
-    // kGroup tiles plus the counts of the earlier tiles of this tile's group
-    unsigned long long *row = status + ((unsigned long long)pass * ntiles) * 256;
-    unsigned long long *grow = status + 4ull * ntiles * 256 + (unsigned long long)pass * ngroups * 256;
-    volatile unsigned long long *vrow = row, *vgrow = grow;
-    const unsigned want = epoch & 0x3FFFFFFFu;
-    vrow[(unsigned long long)tile * 256 + tid] = status_word(epoch, kFlagAgg, cnt);
+    // keys of digit d in earlier tiles: the counts of the earlier tiles of this tile's group
+    // (quarter 0) plus the totals of the earlier complete groups of kGroup tiles (quarter 1)
     const unsigned grp = tile / kGroup, first = grp * kGroup;
-    bool lost = false;
-    if (tile % kGroup == kGroup - 1) {  // the last tile of a group publishes the group total
-        unsigned gsum = cnt;
-        unsigned long long wv[kGroup - 1];
-#pragma unroll
-        for (int q = 0; q < kGroup - 1; ++q) wv[q] = vrow[(unsigned long long)(first + q) * 256 + tid];
-#pragma unroll
-        for (int q = 0; q < kGroup - 1; ++q) {
-            unsigned long long w = wv[q];
-            int it = 0;
-            while (!lost && ((unsigned)(w >> 34) != want || ((w >> 32) & 3ull) == 0) && ++it < kSpinLimit)
-                w = vrow[(unsigned long long)(first + q) * 256 + tid];
-            if (it >= kSpinLimit) lost = true;
-            gsum += (unsigned)w;
+    bool ok = true;
+    unsigned part = 0;
+    if (quarter == 0) {
+        if (tile % kGroup == kGroup - 1) {  // the last tile of a group publishes the group total
+            unsigned gsum = cnt;
+            ok &= sum_published<kGroup - 1>(vrow + (unsigned long long)first * 256 + d, 256, kGroup - 1, want, &gsum);
+            vgrow[(unsigned long long)grp * 256 + d] = status_word(epoch, kFlagAgg, gsum);
+            part = gsum - cnt;
+        } else {
+            ok &= sum_published<kGroup - 1>(vrow + (unsigned long long)first * 256 + d, 256, tile - first, want, &part);
         }
-        vgrow[(unsigned long long)grp * 256 + tid] = status_word(epoch, kFlagAgg, gsum);
-    }
-    unsigned excl = 0;
-    {
-        unsigned long long tv[kGroup - 1];
-#pragma unroll
-        for (int q = 0; q < kGroup - 1; ++q)
-            tv[q] = first + q < tile ? vrow[(unsigned long long)(first + q) * 256 + tid] : 0ull;
-        // group totals, kMaxGroups per round (one round up to 2^20 keys)
+    } else if (quarter == 1) {
         for (unsigned q0 = 0; q0 < grp; q0 += kMaxGroups) {
-            unsigned long long gv[kMaxGroups];
-#pragma unroll
-            for (int q = 0; q < kMaxGroups; ++q)
-                gv[q] = q0 + q < grp ? vgrow[(unsigned long long)(q0 + q) * 256 + tid] : 0ull;
-#pragma unroll
-            for (int q = 0; q < kMaxGroups; ++q) {
-                if (q0 + q >= grp) continue;
-                unsigned long long w = gv[q];
-                int it = 0;
-                while (!lost && ((unsigned)(w >> 34) != want || ((w >> 32) & 3ull) == 0) && ++it < kSpinLimit)
-                    w = vgrow[(unsigned long long)(q0 + q) * 256 + tid];
-                if (it >= kSpinLimit) lost = true;
-                excl += (unsigned)w;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kGroup - 1; ++q) {
-            if (first + q >= tile) continue;
-            unsigned long long w = tv[q];
-            int it = 0;
-            while (!lost && ((unsigned)(w >> 34) != want || ((w >> 32) & 3ull) == 0) && ++it < kSpinLimit)
-                w = vrow[(unsigned long long)(first + q) * 256 + tid];
-            if (it >= kSpinLimit) lost = true;
-            excl += (unsigned)w;
+            const unsigned m = grp - q0 < kMaxGroups ? grp - q0 : kMaxGroups;
+            ok &= sum_published<kMaxGroups>(vgrow + (unsigned long long)q0 * 256 + d, 256, m, want, &part);
         }
     }
-    if (lost) atomicOr(err, kFlagTimeout);  // a wait gave up: this sort's output is not valid
-    s_gstart[tid] = s_base[tid] + excl;
+    if (!ok) atomicOr(err, kFlagTimeout);  // a wait gave up: this sort's output is not valid
+    if (quarter == 1) s_part[1][d] = part;   // s_part was last read before the staging barrier
     __syncthreads();
-    const unsigned long long tbase = (unsigned long long)tile * kTile;
-    const int nvalid = size - tbase < (unsigned long long)kTile ? (int)(size - tbase) : kTile;
-    for (int t = tid; t < nvalid; t += blockDim.x) {
+    // output position of staged key t of digit d: s_delta[d] + t
+    if (quarter == 0) s_delta[d] = s_base[d] + s_part[1][d] + part - s_toff[d];
+    __syncthreads();
+    for (int t = tid; t < nvalid; t += kThreads) {
         const unsigned key = s_keys[t];
-        const unsigned dg = (key >> shift) & 255u;
-        const unsigned pos = s_gstart[dg] + (unsigned)t - s_toff[dg];
+        const unsigned pos = s_delta[(key >> shift) & 255u] + (unsigned)t;
         if (keys_out) keys_out[pos] = key;
         vals_out[pos] = s_vals[t];
     }
@@ -302,14 +376,37 @@ __global__ void __launch_bounds__(1024) k_build_cdf(double *cdf, unsigned long l
     }
 }
 
+constexpr size_t kStageSmem = 2ull * kTile * sizeof(unsigned);
+
+// Dynamic shared-memory limits of the sort kernels, set once per device (the sort is also
+// reached without a buffer, through per_rank_order_noalloc).
+std::mutex g_attr_mu;
+bool g_attr_done[64] = {};
+
+cudaError_t ensure_sort_attributes()
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (g_attr_done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_rs_hist4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHistSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_rs_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageSmem);
+    if (e == cudaSuccess) g_attr_done[dev] = true;
+    return e;
+}
+
 }  // namespace
 
 cudaError_t init_rank_kernels(int carveout)
 {
-    if (carveout < 0) return cudaSuccess;
+    cudaError_t e = ensure_sort_attributes();
+    if (e != cudaSuccess || carveout < 0) return e;
     const void *fns[] = {(const void *)k_rs_hist4, (const void *)k_rs_onesweep, (const void *)k_build_cdf};
     for (const void *f : fns) {
-        const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+        e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -336,9 +433,12 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
 {
     const unsigned long long size = host_size;
     const unsigned ntiles = (unsigned)std::max<unsigned long long>(rank_tile_count(size), 1);
-    const unsigned hgrid = (unsigned)std::min<unsigned long long>((size + kThreads * 16ull - 1) / (kThreads * 16ull), 512);
-    cudaError_t e = launch_pdl(k_rs_hist4, std::max(hgrid, 1u), kThreads, 0, st, (const float *)w.raw, size,
-                               w.digit_hist, w.sort_ctl);
+    cudaError_t e = ensure_sort_attributes();
+    if (e != cudaSuccess) return e;
+    const unsigned hgrid = (unsigned)std::min<unsigned long long>((size + kHistThreads - 1) / kHistThreads,
+                                                                  (unsigned long long)std::max(w.num_sms, 1));
+    e = launch_pdl(k_rs_hist4, std::max(hgrid, 1u), kHistThreads, kHistSmem, st, (const float *)w.raw, size,
+                   w.digit_hist, w.sort_ctl);
     if (e != cudaSuccess) return e;
     const unsigned *kin = nullptr, *vin = nullptr;
     int cur = 0;
@@ -346,7 +446,7 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
         const float *raw = pass == 0 ? w.raw : nullptr;
         unsigned *kout = pass == 3 ? nullptr : w.keys[cur];
         unsigned *vout = w.vals[cur];
-        e = launch_pdl(k_rs_onesweep, ntiles, kThreads, 0, st, raw, kin, vin, kout, vout, size, pass, ntiles,
+        e = launch_pdl(k_rs_onesweep, ntiles, kThreads, kStageSmem, st, raw, kin, vin, kout, vout, size, pass, ntiles,
                        w.digit_hist, (unsigned long long *)w.status, w.sort_ctl, w.err);
         if (e != cudaSuccess) return e;
         kin = w.keys[cur];
@@ -432,6 +532,12 @@ extern "C" per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uin
     w.err = w.sort_ctl + 8;
     w.status = reinterpret_cast<unsigned long long *>(w.sort_ctl + 16);  // 8-byte aligned
     w.capacity = n;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&w.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PER_ERR_CUDA;
+    }
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     unsigned *sorted = nullptr;
     cudaError_t e = launch_rank_sort(w, n, &sorted, st);

@@ -199,6 +199,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
              alloc(&h->rank.status, rank_status_words(capacity)) && alloc(&h->rank.digit_hist, 4 * 256 + 16);
         h->rank.sort_ctl = h->rank.digit_hist + 4 * 256;
         h->rank.capacity = capacity;
+        h->rank.num_sms = h->num_sms;
     }
     ok = ok && alloc(&h->states, capacity * (uint64_t)state_dim) && alloc(&h->next, capacity * (uint64_t)state_dim) &&
          alloc(&h->actions, capacity) && alloc(&h->rewards, capacity) && alloc(&h->dones, capacity);

@@ -179,6 +179,7 @@ struct RankWork {
     unsigned *sort_ctl;            // [8]: tile counters of the four passes, [4] the sort epoch
     unsigned *err;                 // device error word (PER_DEVFLAG_TIMEOUT)
     unsigned long long capacity;
+    int num_sms;                   // grid of the histogram kernel
 };
 
 // Words of RankWork scratch the sort needs for `capacity` keys (beyond keys and values).
