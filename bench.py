@@ -79,16 +79,17 @@ def kernel_source_hash(name):
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel_file):
-    """Per-launch DRAM bytes of a kernel, from the committed ncu summary, if the kernel's source
-    is unchanged since the capture (else None)."""
+def traffic_from_profiles(kernel, kernel_file):
+    """Per-launch DRAM bytes (read + write) of a kernel, from the committed ncu summary
+    profiles/traffic.txt (lines of key=value: kernel, file, src_sha, dram_bytes_per_launch), if
+    the kernel's source file is unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     want = kernel_source_hash(kernel_file)
     for line in open(p):
         parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if parts.get("file") == kernel_file and parts.get("src_sha") == want:
+        if parts.get("kernel") == kernel and parts.get("file") == kernel_file and parts.get("src_sha") == want:
             try:
                 return float(parts["dram_bytes_per_launch"])
             except (KeyError, ValueError):
@@ -313,7 +314,6 @@ def run_gpu(args, rank, world):
     wall = time.perf_counter() - t0
     if dist:
         dist.barrier()
-    clk = clocks.stop() if clocks else None
     step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
     cr.destroy(sev)
 
@@ -329,6 +329,7 @@ def run_gpu(args, rank, world):
                "per_update")
     rec(cb, st)
     torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None   # the sampler spans both timed loops
     cont_s = cr.elapsed_ms(ca, cb) / 1e3
     cr.destroy([ca, cb])
     if dist:
@@ -414,7 +415,7 @@ def run_gpu(args, rank, world):
     achieved = byt / (ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 5),
-                "traffic": traffic_from_profiles(src), "peak_source": peak_src,
+                "traffic": traffic_from_profiles(dom, src), "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": int(byt), "median_launch_us": round(ms * 1e3, 3)}
     step_bytes = b_add + b_sam + b_upd
 
