@@ -36,31 +36,64 @@ struct SampleArgs {
     RingRefs r;
     Ctl *ctl;
     unsigned B;
+    double inv_b;   // 1/B when B is a power of two (exact), else 0
     float beta;
     unsigned long long seed;
     SampleOut o;
     int vec4;  // rows move as float4
 };
 
-__device__ __forceinline__ void gather_rows(const RingRefs &r, const SampleOut &o, unsigned j,
-                                            unsigned long long slot, int lane, int vec4)
+// The sampled row: every load of the warp's share (states, next_states, and the action, reward
+// and done fields on lanes 1-3) is issued before the first store, so the gather costs one memory
+// round trip.  Rows shorter than the output stride are padded with zeros.
+__device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o, unsigned j,
+                                           unsigned long long slot, int lane, int vec4)
 {
     const unsigned d = r.d, dp = o.dp;
-    if (vec4) {
+    unsigned act = 0;
+    float rew = 0.0f;
+    unsigned char done = 0;
+    if (lane == 1 && o.actions) act = __ldg(r.actions + slot);
+    if (lane == 2 && o.rewards) rew = __ldg(r.rewards + slot);
+    if (lane == 3 && o.dones) done = __ldg(r.dones + slot);
+    const bool rows = d && (o.states || o.next);
+    if (rows && vec4 && 2 * (dp >> 2) <= 64) {
+        // up to 64 float4 per row pair: two per lane, loaded together
         const unsigned d4 = d >> 2, dp4 = dp >> 2;
         const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
         const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
-        float4 *dstS = o.states ? reinterpret_cast<float4 *>(o.states + (unsigned long long)j * dp) : nullptr;
-        float4 *dstN = o.next ? reinterpret_cast<float4 *>(o.next + (unsigned long long)j * dp) : nullptr;
+        float4 v[2];
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const unsigned c = lane + 32 * q;
+            const bool second = c >= dp4;
+            const unsigned cc = second ? c - dp4 : c;
+            v[q] = zero;
+            if (c < 2 * dp4 && cc < d4 && (second ? o.next : o.states)) v[q] = __ldg((second ? srcN : srcS) + cc);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const unsigned c = lane + 32 * q;
+            const bool second = c >= dp4;
+            const unsigned cc = second ? c - dp4 : c;
+            float *base = second ? o.next : o.states;
+            if (c < 2 * dp4 && base) reinterpret_cast<float4 *>(base + (unsigned long long)j * dp)[cc] = v[q];
+        }
+    } else if (rows && vec4) {
+        const unsigned d4 = d >> 2, dp4 = dp >> 2;
+        const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
+        const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
         for (unsigned c = lane; c < 2 * dp4; c += 32) {
             const bool second = c >= dp4;
             const unsigned cc = second ? c - dp4 : c;
-            float4 *dst = second ? dstN : dstS;
-            if (!dst) continue;
-            dst[cc] = cc < d4 ? __ldg((second ? srcN : srcS) + cc) : zero;
+            float *base = second ? o.next : o.states;
+            if (!base) continue;
+            reinterpret_cast<float4 *>(base + (unsigned long long)j * dp)[cc] =
+                cc < d4 ? __ldg((second ? srcN : srcS) + cc) : zero;
         }
-    } else {
+    } else if (rows) {
         for (unsigned c = lane; c < 2 * dp; c += 32) {
             const bool second = c >= dp;
             const unsigned cc = second ? c - dp : c;
@@ -70,14 +103,9 @@ __device__ __forceinline__ void gather_rows(const RingRefs &r, const SampleOut &
             dst[(unsigned long long)j * dp + cc] = cc < d ? __ldg(src + slot * d + cc) : 0.0f;
         }
     }
-}
-
-__device__ __forceinline__ void write_scalars(const RingRefs &r, const SampleOut &o, unsigned j,
-                                              unsigned long long slot, int lane)
-{
-    if (lane == 1 && o.actions) o.actions[j] = __ldg(r.actions + slot);
-    if (lane == 2 && o.rewards) o.rewards[j] = __ldg(r.rewards + slot);
-    if (lane == 3 && o.dones) o.dones[j] = __ldg(r.dones + slot);
+    if (lane == 1 && o.actions) o.actions[j] = act;
+    if (lane == 2 && o.rewards) o.rewards[j] = rew;
+    if (lane == 3 && o.dones) o.dones[j] = done;
 }
 
 // a > b for binary64 values >= +0: their bit patterns order like the values, so the compare
@@ -91,32 +119,42 @@ __device__ __forceinline__ bool gt_nonneg(double a, double b)
 // read are loaded at once, four per lane (child i of the round sits in lane i % 32, slot i / 32),
 // and the k decisions then run on registers and shuffles.  When `last`, the deepest level is
 // the leaves: the 2^k leaves under `node` are one contiguous stretch, four per lane, and *lv
-// receives the chosen leaf's value.
-__device__ __forceinline__ unsigned long long walk_round(const TreeRefs &t, unsigned long long node,
-                                                         int k, bool last, double &m, int lane,
-                                                         float *lv)
-{
-    const int ninternal = (1 << (last ? k - 1 : k)) - 1;  // left children that are internal nodes
+// receives the chosen leaf's value.  The loads (walk_load) and the decisions (walk_decide) are
+// separate so that the first round's loads, which do not depend on the draw, can be issued
+// before the call number is known.
+struct WalkRegs {
     double v[4];
     float lf[4];
+};
+
+__device__ __forceinline__ void walk_load(const TreeRefs &t, unsigned long long node, int k, bool last,
+                                          int lane, WalkRegs &w)
+{
+    const int ninternal = (1 << (last ? k - 1 : k)) - 1;  // left children that are internal nodes
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = lane + 32 * r;
-        v[r] = 0.0;
+        w.v[r] = 0.0;
         if (i < ninternal) {
             const int lev = 32 - __clz(i + 1);
             const int pos = i + 1 - (1 << (lev - 1));
-            v[r] = t.S[(node << lev) + 2 * pos];
+            w.v[r] = t.S[(node << lev) + 2 * pos];
         }
-        lf[r] = 0.0f;
-        if (last && i < (1 << k)) lf[r] = t.L[(node << k) - t.n + i];
+        w.lf[r] = 0.0f;
+        if (last && i < (1 << k)) w.lf[r] = t.L[(node << k) - t.n + i];
     }
+}
+
+__device__ __forceinline__ unsigned long long walk_decide(unsigned long long node, int k, bool last,
+                                                          double &m, int lane, const WalkRegs &w,
+                                                          float *lv)
+{
     int q = 0;
     const int kint = last ? k - 1 : k;
     for (int lev = 1; lev <= kint; ++lev) {
         const int i = (1 << (lev - 1)) - 1 + q;
         const int r = i >> 5;
-        const double mine = r == 0 ? v[0] : r == 1 ? v[1] : r == 2 ? v[2] : v[3];
+        const double mine = r == 0 ? w.v[0] : r == 1 ? w.v[1] : r == 2 ? w.v[2] : w.v[3];
         const double left = __shfl_sync(kFull, mine, i & 31);
         if (gt_nonneg(left, m)) {
             q = 2 * q;
@@ -128,7 +166,7 @@ __device__ __forceinline__ unsigned long long walk_round(const TreeRefs &t, unsi
     if (last) {
         const int i = 2 * q;  // the left leaf of the final pair
         const int r = i >> 5;
-        const float mine = r == 0 ? lf[0] : r == 1 ? lf[1] : r == 2 ? lf[2] : lf[3];
+        const float mine = r == 0 ? w.lf[0] : r == 1 ? w.lf[1] : r == 2 ? w.lf[2] : w.lf[3];
         const double left = (double)__shfl_sync(kFull, mine, i & 31);
         if (gt_nonneg(left, m)) {
             q = 2 * q;
@@ -137,35 +175,37 @@ __device__ __forceinline__ unsigned long long walk_round(const TreeRefs &t, unsi
             q = 2 * q + 1;
         }
         const int rr = q >> 5;
-        const float pick = rr == 0 ? lf[0] : rr == 1 ? lf[1] : rr == 2 ? lf[2] : lf[3];
+        const float pick = rr == 0 ? w.lf[0] : rr == 1 ? w.lf[1] : rr == 2 ? w.lf[2] : w.lf[3];
         *lv = __shfl_sync(kFull, pick, q & 31);
     }
     return (node << k) + q;
 }
 
-__global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
+__global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
 {
     __shared__ unsigned long long s_call;
-    __shared__ double s_seg;
     pdl_wait();
     pdl_release();
     const unsigned long long n = a.t.n;
     const int D = a.t.D;
-    if (threadIdx.x == 0) {
-        s_call = take_call_number(a.ctl);
-        s_seg = __ddiv_rn(D == 0 ? (double)a.t.L[0] : a.t.S[1], (double)a.B);  // stratum width T / B
-    }
+    if (threadIdx.x == 0) s_call = take_call_number(a.ctl);
+    // while the call number is on its way: the total, the minimum, the size and the first
+    // round's nodes (the same for every draw)
+    const double total = D == 0 ? (double)a.t.L[0] : a.t.S[1];
     const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
     const unsigned long long size = a.ctl->size;
-    __syncthreads();
-    const unsigned long long call = s_call;
-    const double seg = s_seg;
-    const float nbeta = -a.beta;
-    const int lane = threadIdx.x & 31;
-    const unsigned wpb = blockDim.x >> 5;
-    const unsigned warps_total = gridDim.x * wpb;
     const int rounds = (D + 6) / 7;                 // 7 levels per round; the first takes the rest
     const int first = D - 7 * (rounds - 1);
+    const int lane = threadIdx.x & 31;
+    WalkRegs w0;
+    if (D > 0) walk_load(a.t, 1, first, rounds == 1, lane, w0);
+    // stratum width T / B: one exact scaling when B is a power of two
+    const double seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
+    __syncthreads();
+    const unsigned long long call = s_call;
+    const float nbeta = -a.beta;
+    const unsigned wpb = blockDim.x >> 5;
+    const unsigned warps_total = gridDim.x * wpb;
 
     for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
         const double u = draw_uniform(a.seed, j, call, 0);
@@ -176,10 +216,11 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             leaf = 0;
             lv = a.t.L[0];
         } else {
-            unsigned long long node = 1;
-            for (int rd = 0; rd < rounds; ++rd) {
-                const int k = rd == 0 ? first : 7;
-                node = walk_round(a.t, node, k, rd == rounds - 1, m, lane, &lv);
+            unsigned long long node = walk_decide(1, first, rounds == 1, m, lane, w0, &lv);
+            for (int rd = 1; rd < rounds; ++rd) {
+                WalkRegs w;
+                walk_load(a.t, node, 7, rd == rounds - 1, lane, w);
+                node = walk_decide(node, 7, rd == rounds - 1, m, lane, w, &lv);
             }
             leaf = node - n;
         }
@@ -187,13 +228,11 @@ __global__ void __launch_bounds__(kThreads) k_sample_prop(SampleArgs a)
             leaf = size - 1;
             lv = a.t.L[leaf];
         }
-        // rows first, so their loads are in flight while the weight is computed
-        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, leaf, lane, a.vec4);
-        write_scalars(a.r, a.o, j, leaf, lane);
         if (lane == 0) {
             a.o.idx[j] = (long long)leaf;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
         }
+        gather_row(a.r, a.o, j, leaf, lane, a.vec4);
     }
 }
 
@@ -278,8 +317,7 @@ __global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
             a.o.idx[j] = (long long)slot;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn((float)r, fsize), a.ab);
         }
-        write_scalars(a.r, a.o, j, slot, lane);
-        if (a.r.d && (a.o.states || a.o.next)) gather_rows(a.r, a.o, j, slot, lane, a.vec4);
+        gather_row(a.r, a.o, j, slot, lane, a.vec4);
     }
 }
 
@@ -323,6 +361,7 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     a.r = r;
     a.ctl = ctl;
     a.B = B;
+    a.inv_b = (B & (B - 1)) == 0 ? 1.0 / (double)B : 0.0;
     a.beta = beta;
     a.seed = seed;
     a.o = o;

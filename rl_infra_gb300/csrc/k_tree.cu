@@ -16,6 +16,7 @@
 #include "leaf_pow.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace gbper {
 
@@ -342,38 +343,85 @@ __device__ __forceinline__ void copy_flat(V *dst, const V *src, unsigned long lo
     }
 }
 
+// One pass over the inserted rows: a thread issues the loads of its whole share (states and
+// next_states elements and the scalar fields, kCopyU of each) before its first store, so the
+// copy costs one memory round trip per kCopyU x stride elements.  Range A of the ring starts at
+// slot s0 and holds lenA rows; the rest wraps to slot 0.
+constexpr int kCopyU = 4;
+
+template <typename V>
+__device__ __forceinline__ void copy_rows_pass(const AddArgs &a, const V *srcS, const V *srcN, V *dstS,
+                                               V *dstN, unsigned per_row, unsigned long long s0,
+                                               unsigned long long lenA, unsigned long long cnt,
+                                               unsigned long long t0, unsigned long long stride)
+{
+    const unsigned long long nv = cnt * per_row;   // elements of states (and of next_states)
+    const unsigned long long lenAv = lenA * per_row, s0v = s0 * per_row;
+    const unsigned long long total = nv > cnt ? nv : cnt;
+    const unsigned *srcA = a.actions + a.k0;
+    const float *srcR = a.rewards + a.k0;
+    const unsigned char *srcD = a.dones + a.k0;
+    for (unsigned long long e0 = t0; e0 < total; e0 += kCopyU * stride) {
+        V vs[kCopyU], vn[kCopyU];
+        unsigned va[kCopyU];
+        float vr[kCopyU];
+        unsigned char vd[kCopyU];
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const unsigned long long e = e0 + u * stride;
+            if (e < nv) {
+                vs[u] = __ldg(srcS + e);
+                vn[u] = __ldg(srcN + e);
+            }
+            if (e < cnt) {
+                va[u] = __ldg(srcA + e);
+                vr[u] = __ldg(srcR + e);
+                vd[u] = __ldg(srcD + e);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyU; ++u) {
+            const unsigned long long e = e0 + u * stride;
+            if (e < nv) {
+                const unsigned long long o = e < lenAv ? s0v + e : e - lenAv;
+                dstS[o] = vs[u];
+                dstN[o] = vn[u];
+            }
+            if (e < cnt) {
+                const unsigned long long o = e < lenA ? s0 + e : e - lenA;
+                a.r.actions[o] = va[u];
+                a.r.rewards[o] = vr[u];
+                a.r.dones[o] = vd[u];
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void copy_rows_flat(const AddArgs &a, const AddGeom &g,
                                                unsigned long long t0, unsigned long long stride)
 {
     const unsigned long long cnt = a.count - a.k0;
     const unsigned long long lenA = g.endA - g.s0;
     const unsigned d = a.r.d;
-    if (d) {
-        if (a.vec4) {
-            const unsigned d4 = d >> 2;
-            copy_flat(reinterpret_cast<float4 *>(a.r.states), reinterpret_cast<const float4 *>(a.states) + a.k0 * d4,
-                      lenA * d4, cnt * d4, g.s0 * d4, t0, stride);
-            copy_flat(reinterpret_cast<float4 *>(a.r.next), reinterpret_cast<const float4 *>(a.next) + a.k0 * d4,
-                      lenA * d4, cnt * d4, g.s0 * d4, t0, stride);
-        } else {
-            copy_flat(a.r.states, a.states + a.k0 * d, lenA * d, cnt * d, g.s0 * d, t0, stride);
-            copy_flat(a.r.next, a.next + a.k0 * d, lenA * d, cnt * d, g.s0 * d, t0, stride);
-        }
+    if (d && a.vec4) {
+        const unsigned d4 = d >> 2;
+        copy_rows_pass(a, reinterpret_cast<const float4 *>(a.states) + a.k0 * d4,
+                       reinterpret_cast<const float4 *>(a.next) + a.k0 * d4, reinterpret_cast<float4 *>(a.r.states),
+                       reinterpret_cast<float4 *>(a.r.next), d4, g.s0, lenA, cnt, t0, stride);
+    } else {
+        copy_rows_pass(a, d ? a.states + a.k0 * d : nullptr, d ? a.next + a.k0 * d : nullptr, a.r.states, a.r.next,
+                       d, g.s0, lenA, cnt, t0, stride);
     }
-    copy_flat(a.r.actions, a.actions + a.k0, lenA, cnt, g.s0, t0, stride);
-    copy_flat(a.r.rewards, a.rewards + a.k0, lenA, cnt, g.s0, t0, stride);
-    copy_flat(a.r.dones, a.dones + a.k0, lenA, cnt, g.s0, t0, stride);
 }
 
 __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
 {
-    __shared__ double s_vs[1 << kAddBlockLog];
-    __shared__ float s_vm[1 << kAddBlockLog];
     pdl_wait();
     pdl_release();
     const unsigned long long cursor = a.ctl->cursor;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
     const float max_leaf = __uint_as_float(a.ctl->max_leaf_bits);
+    const unsigned long long size0 = a.ctl->size;
     const unsigned long long C = a.r.capacity;
     const AddGeom g = add_geometry(a, cursor);
     const int tid = threadIdx.x;
@@ -405,29 +453,49 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                 } else if (a.proportional) {
                     leaf = a.t.L[s];
                 }
-                if (a.proportional) {
-                    s_vs[tid] = (double)leaf;
-                    s_vm[tid] = leaf_min_value(leaf);
-                }
             }
             if (a.proportional) {
+                // the block's subtree: five levels inside each warp by shuffles, the rest on
+                // warp 0 from the warps' sums
                 const unsigned long long first = a.t.n + ((unsigned long long)blk << a.bl);
-                for (int h = 1; h <= a.bl; ++h) {
-                    const int cnt = bsz >> h;
-                    double sv = 0.0;
-                    float mv = 0.0f;
-                    __syncthreads();
-                    if (tid < cnt) {
-                        sv = s_vs[2 * tid] + s_vs[2 * tid + 1];
-                        mv = fmin_tree(s_vm[2 * tid], s_vm[2 * tid + 1]);
-                    }
-                    __syncthreads();
-                    if (tid < cnt) {
-                        s_vs[tid] = sv;
-                        s_vm[tid] = mv;
-                        const unsigned long long node = (first >> h) + tid;
+                const int lane = tid & 31, warp = tid >> 5;
+                double sv = tid < bsz ? (double)leaf : 0.0;
+                float mv = tid < bsz ? leaf_min_value(leaf) : __int_as_float(0x7f800000);
+                const int hw = a.bl < 5 ? a.bl : 5;
+                for (int h = 1; h <= hw; ++h) {
+                    const double os = __shfl_down_sync(0xffffffffu, sv, 1 << (h - 1));
+                    const float om = __shfl_down_sync(0xffffffffu, mv, 1 << (h - 1));
+                    sv = sv + os;
+                    mv = fmin_tree(mv, om);
+                    if ((tid & ((1 << h) - 1)) == 0 && tid < bsz) {
+                        const unsigned long long node = (first >> h) + (tid >> h);
                         a.t.S[node] = sv;
                         a.t.M[node] = mv;
+                    }
+                }
+                if (a.bl > 5) {
+                    __shared__ double s_ws[kThreads / 32];
+                    __shared__ float s_wm[kThreads / 32];
+                    if (lane == 0) {
+                        s_ws[warp] = sv;
+                        s_wm[warp] = mv;
+                    }
+                    __syncthreads();
+                    if (warp == 0) {
+                        const int nw = bsz >> 5;
+                        sv = lane < nw ? s_ws[lane] : 0.0;
+                        mv = lane < nw ? s_wm[lane] : __int_as_float(0x7f800000);
+                        for (int h = 6; h <= a.bl; ++h) {
+                            const double os = __shfl_down_sync(0xffffffffu, sv, 1 << (h - 6));
+                            const float om = __shfl_down_sync(0xffffffffu, mv, 1 << (h - 6));
+                            sv = sv + os;
+                            mv = fmin_tree(mv, om);
+                            if ((lane & ((1 << (h - 5)) - 1)) == 0 && lane < nw) {
+                                const unsigned long long node = (first >> h) + (lane >> (h - 5));
+                                a.t.S[node] = sv;
+                                a.t.M[node] = mv;
+                            }
+                        }
                     }
                 }
             }
@@ -450,6 +518,8 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
     }
 
     if (last_to_arrive(&a.ctl->ticket_add)) {
+        unsigned call_max = 0;
+        if (tid == 0) call_max = __ldcg(&a.ctl->add_max_bits);   // in flight during the climb
         if (a.proportional) {
             __shared__ double s_spS0[kTopSpan], s_spS1[kTopSpan];
             __shared__ float s_spM0[kTopSpan], s_spM1[kTopSpan];
@@ -466,10 +536,10 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
         }
         if (tid == 0) {
             Ctl *c = a.ctl;
-            fold_running_max(c, __ldcg(&c->add_max_bits), a.alpha);
+            fold_running_max(c, call_max, a.alpha);
             c->add_max_bits = 0;
             c->cursor = (cursor + a.count) % C;
-            const unsigned long long sz = c->size + a.count;
+            const unsigned long long sz = size0 + a.count;
             c->size = sz < C ? sz : C;
             c->ticket_add = 0;
         }
@@ -607,6 +677,7 @@ struct UpdArgs {
     const float *td;
     unsigned B;
     int P;      // log2 number of subtrees
+    int subs;   // subtrees per CTA (warps 0 .. subs-1 climb; all warps file the batch)
     int pb;     // bits for a batch position
     double alpha, eps;
     LeafPowAlpha lp;
@@ -650,10 +721,13 @@ __device__ __forceinline__ void warp_bitonic_kv(unsigned long long *keys, unsign
 }
 
 // Bitonic sort of one key per lane (ascending across lanes 0..31), carrying a payload.
-__device__ __forceinline__ void warp_sort32(unsigned long long &key, unsigned &pay, int lane)
+// Bitonic sort of the keys of lanes [0, N) in each aligned group of N lanes (ascending), with a
+// payload; lanes beyond the entries hold the largest key.
+template <int N>
+__device__ __forceinline__ void warp_sort_n(unsigned long long &key, unsigned &pay, int lane)
 {
 #pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
+    for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             const unsigned long long ok = __shfl_xor_sync(0xffffffffu, key, stride);
@@ -696,11 +770,16 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
     if (priv < 0) priv = 0;
     int h_shared = priv;
     for (int o = 16; o > 0; o >>= 1) h_shared = min(h_shared, __shfl_xor_sync(0xffffffffu, h_shared, o));
+    // heights at which two paths join (a left owner takes its right neighbour's value there);
+    // at every other height each owner adds its own prefetched sibling, without shuffles
+    unsigned merge_mask = (have && lane + 1 < U && meet_next - 1 < 32) ? (1u << (meet_next - 1)) : 0u;
+    for (int o = 16; o > 0; o >>= 1) merge_mask |= __shfl_xor_sync(0xffffffffu, merge_mask, o);
 
     // one round of loads: the clean sibling at every height this lane owns (height 0 is a leaf,
     // every height above it an internal node)
     double ps[kMaxClimb];
     float pmn[kMaxClimb];
+    float sib_leaf = 0.0f;   // the leaf's sibling, converted only after the power below
 #pragma unroll
     for (int h = 0; h < kMaxClimb; ++h) {
         ps[h] = 0.0;
@@ -709,9 +788,7 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
             const unsigned long long v = node0 >> h;
             if (lane == 0 || (prev0 >> h) != v) {
                 if (h == 0) {
-                    const float lf = t.L[(v ^ 1ull) - t.n];
-                    ps[0] = (double)lf;
-                    pmn[0] = leaf_min_value(lf);
+                    sib_leaf = t.L[(v ^ 1ull) - t.n];
                 } else {
                     ps[h] = t.S[v ^ 1ull];
                     pmn[h] = t.M[v ^ 1ull];
@@ -727,6 +804,8 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
         vs = (double)lv;
         vm = leaf_min_value(lv);
     }
+    ps[0] = (double)sib_leaf;
+    pmn[0] = leaf_min_value(sib_leaf);
     // private phase: a chain of binary64 adds over the prefetched siblings
 #pragma unroll
     for (int h = 0; h < kMaxClimb; ++h) {
@@ -743,11 +822,24 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
             t.M[v >> 1] = vm;
         }
     }
-    // shared phase: heights h_shared .. shift-1, one shuffle step per level
+    // shared phase: heights h_shared .. shift-1, one shuffle step per joining height
     int rend = lane + 1;
 #pragma unroll
     for (int h = 0; h < kMaxClimb; ++h) {
-        if (h >= h_shared && h < hpre) {
+        if (h >= h_shared && h < hpre && !((merge_mask >> h) & 1u)) {
+            const unsigned long long v = node0 >> h;
+            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
+                if ((v & 1ull) == 0) {
+                    vs = vs + ps[h];
+                    vm = fmin_tree(vm, pmn[h]);
+                } else {
+                    vs = ps[h] + vs;
+                    vm = fmin_tree(pmn[h], vm);
+                }
+                t.S[v >> 1] = vs;
+                t.M[v >> 1] = vm;
+            }
+        } else if (h >= h_shared && h < hpre) {
             const int src = rend < 32 ? rend : 31;
             const unsigned long long e_node = __shfl_sync(0xffffffffu, node0, src);
             const double e_vs = __shfl_sync(0xffffffffu, vs, src);
@@ -963,7 +1055,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     const int D = a.t.D;
     const int shift = D - a.P;
     const unsigned long long nsub = 1ull << a.P;
-    const unsigned long long first_sub = (unsigned long long)blockIdx.x * kUpdWarps;
+    const unsigned long long first_sub = (unsigned long long)blockIdx.x * a.subs;
     const unsigned long long n = a.t.n;
     const unsigned long long size = a.ctl->size;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
@@ -993,7 +1085,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                 continue;
             }
             const unsigned long long sub = (unsigned long long)i >> shift;
-            if (sub < first_sub || sub >= first_sub + kUpdWarps) continue;
+            if (sub < first_sub || sub >= first_sub + a.subs) continue;
             const int w = (int)(sub - first_sub);
             const float raw = td_to_raw(tv[u], a.eps, max_prev);
             mymax = max(mymax, __float_as_uint(raw));
@@ -1014,7 +1106,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     // 2. one warp per subtree
     const unsigned long long sub = first_sub + warp;
     const int m = s_cnt[warp];
-    if (sub < nsub && m > 0) {
+    if (warp < a.subs && sub < nsub && m > 0) {
         WarpLists &wl = lists[warp];
         const unsigned long long base = sub << shift;
         if (m > kWarpCap) {
@@ -1049,7 +1141,9 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
             // move the u-th surviving leaf to lane u
             unsigned long long key = lane < m ? wl.keys[lane] : ~0ull;
             unsigned pay = lane < m ? wl.pay[lane] : 0u;
-            warp_sort32(key, pay, lane);
+            if (m <= 8) warp_sort_n<8>(key, pay, lane);
+            else if (m <= 16) warp_sort_n<16>(key, pay, lane);
+            else warp_sort_n<32>(key, pay, lane);
             const unsigned long long nxt = __shfl_down_sync(0xffffffffu, key, 1);
             const bool win = lane < m && (lane == m - 1 || (nxt >> a.pb) != (key >> a.pb));
             const unsigned bal = __ballot_sync(0xffffffffu, win);
@@ -1106,7 +1200,66 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
 
     // 3. the last CTA rebuilds the top P levels and folds in the batch maximum
     if (last_to_arrive(&a.ctl->ticket_update)) {
-        if (a.proportional && a.P > 0) {
+        if (a.proportional && a.P > 0 && a.P <= 8) {
+            // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
+            // node of depth 5 in registers, or starts from depth-P node l (P < 5); every level
+            // above is one shuffle and one add
+            if (warp == 0) {
+                const int P = a.P;
+                double sv = 0.0;
+                float mv = __int_as_float(0x7f800000);
+                int w;   // nodes of the current depth, held by lanes 0, st, 2 st, ...
+                if (P >= 5) {
+                    const int g = 1 << (P - 5);
+                    double gs[8];
+                    float gm[8];
+                    const unsigned long long c0 = (1ull << P) + (unsigned long long)lane * g;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        gs[i] = i < g ? ld_sum_cg(a.t, c0 + i) : 0.0;
+                        gm[i] = i < g ? ld_min_cg(a.t, c0 + i) : 0.0f;
+                    }
+#pragma unroll
+                    for (int half = 4; half >= 1; half >>= 1) {
+                        if (2 * half <= g) {
+#pragma unroll
+                            for (int i = 0; i < half; ++i) {
+                                gs[i] = gs[2 * i] + gs[2 * i + 1];
+                                gm[i] = fmin_tree(gm[2 * i], gm[2 * i + 1]);
+                            }
+                            // the sums are this lane's nodes of depth 5 + log2(half)
+                            const int dlev = 5 + (31 - __clz(half));
+#pragma unroll
+                            for (int i = 0; i < half; ++i) {
+                                const unsigned long long node = (1ull << dlev) + (unsigned long long)lane * half + i;
+                                a.t.S[node] = gs[i];
+                                a.t.M[node] = gm[i];
+                            }
+                        }
+                    }
+                    sv = gs[0];   // depth-5 node 32 + lane
+                    mv = gm[0];
+                    w = 32;
+                } else {
+                    w = 1 << P;
+                    if (lane < w) {
+                        sv = ld_sum_cg(a.t, (unsigned long long)w + lane);
+                        mv = ld_min_cg(a.t, (unsigned long long)w + lane);
+                    }
+                }
+                for (int st = 1; w > 1; st <<= 1, w >>= 1) {
+                    const double os = __shfl_down_sync(0xffffffffu, sv, st);
+                    const float om = __shfl_down_sync(0xffffffffu, mv, st);
+                    if ((lane & (2 * st - 1)) == 0 && lane < w * st) {
+                        sv = sv + os;
+                        mv = fmin_tree(mv, om);
+                        const int node = (w >> 1) + lane / (2 * st);
+                        a.t.S[node] = sv;
+                        a.t.M[node] = mv;
+                    }
+                }
+            }
+        } else if (a.proportional && a.P > 0) {
             double *heapS = reinterpret_cast<double *>(smem_raw);
             float *heapM = reinterpret_cast<float *>(heapS + (2 << kMaxTopLog));
             const int P = a.P;
@@ -1136,6 +1289,29 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
             cc->ticket_update = 0;
         }
     }
+}
+
+// Subtrees per CTA of the update kernel: fewer per CTA spreads the climbs' sibling loads over
+// more SMs (GBPER_UPD_SUBS, 1..kUpdWarps).
+int update_subtrees_per_cta()
+{
+    static const int v = [] {
+        int s = kUpdWarps;
+        if (const char *e = std::getenv("GBPER_UPD_SUBS")) s = std::atoi(e);
+        return s < 1 ? 1 : (s > kUpdWarps ? kUpdWarps : s);
+    }();
+    return v;
+}
+
+// Target batch entries per subtree of the update kernel (GBPER_UPD_PER, 1..64; default 8).
+int update_entries_per_subtree()
+{
+    static const int v = [] {
+        int s = 8;
+        if (const char *e = std::getenv("GBPER_UPD_PER")) s = std::atoi(e);
+        return s < 1 ? 1 : (s > 64 ? 64 : s);
+    }();
+    return v;
 }
 
 int ilog2_ceil(unsigned long long v)
@@ -1202,9 +1378,9 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.vec4 = (r.d % 4 == 0) && ((reinterpret_cast<uintptr_t>(states) | reinterpret_cast<uintptr_t>(next)) % 16 == 0);
     if (r.d == 0) a.vec4 = 0;
 
-    // rows: about four elements in flight per copy thread, at most 4 CTAs per SM
+    // rows: about two elements of each array per copy thread, at most 4 CTAs per SM
     const unsigned long long elems = a.vec4 ? cnt * (r.d / 4) : cnt * (unsigned long long)std::max(r.d, 1u);
-    unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + 4ull * kThreads - 1) / (4ull * kThreads),
+    unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + 2ull * kThreads - 1) / (2ull * kThreads),
                                                             (unsigned long long)num_sms * 4);
     if (ncopy == 0) ncopy = 1;
 
@@ -1252,11 +1428,13 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     // about 8 batch entries per subtree (a warp's list holds up to kWarpCap, so a batch
     // concentrated on a stretch of recent slots still fits); at most 2^10 subtrees, and no
     // more than half the leaves
-    int P = ilog2_ceil((B + 7) / 8);
+    const int per = update_entries_per_subtree();
+    int P = ilog2_ceil((B + per - 1) / per);
     P = std::min(P, kMaxTopLog);
     P = std::min(P, std::max(t.D - 1, 0));
     a.P = P;
-    const unsigned grid = (unsigned)(((1ull << P) + kUpdWarps - 1) / kUpdWarps);
+    a.subs = update_subtrees_per_cta();
+    const unsigned grid = (unsigned)(((1ull << P) + a.subs - 1) / a.subs);
     return launch_pdl(k_update<kUpdWindow>, grid, kUpdThreads, kUpdSmemBytes, st, a);
 }
 
