@@ -743,138 +743,161 @@ __device__ __forceinline__ void warp_sort_n(unsigned long long &key, unsigned &p
     }
 }
 
-// Climb one warp's subtree when it has U <= 32 distinct leaves, one per lane, ascending
-// (lane u holds leaf node `node0` = leaf index + n and its raw priority).  Two phases:
-//   private  below the height where its path meets a neighbour's, a lane's node always has a
-//            clean sibling, so the lane runs those levels alone as a chain of binary64 adds
-//            over siblings loaded up front (all levels requested before the leaf value, a
-//            binary64 pow, is computed, so the two latencies overlap);
-//   shared   from the lowest meeting height up, the owner of a left child reads a dirty right
-//            sibling's value and run end from that sibling's owner lane by shuffles.
-// No level needs shared memory or a warp barrier.
+// Climb one warp's subtree when it has U <= 32 distinct leaves, one per lane, ascending: lane u
+// holds local leaf li (leaf - base, base = the subtree's first leaf) and its raw priority.
+//
+// Let J be the height at which a lane's path joins the previous lane's (the bit length of the
+// two local leaves' xor; lane 0 has none).  At height h the lane owns its node when h < J (or it
+// is lane 0), and the owners of one height are in leaf order, so the next owner after a lane is
+// the next set bit of the height's owner ballot.  The owner of a left child whose right sibling
+// is owned too (that owner has J = h + 1) adds the sibling owner's value, taken by a shuffle; the
+// owner of a right child whose left sibling is owned stops; every other owner adds its clean
+// sibling, loaded up front with all the others in one round.
+//
+// Everything but the values is known before the first add: the owner ballots of all heights,
+// which lanes add at each height and where a dirty sibling's value comes from.  So the chain of
+// binary64 adds carries nothing else: a lane that does not add at a height adds +0 (every value
+// is >= +0, and x + 0 = x), a shuffle and a select sit on it only at heights where two paths
+// join, and the nodes are stored after the chain.  (Binary64 addition is commutative, so one
+// operand order serves left and right children alike.)  Node indices inside the subtree are
+// 32-bit; no level needs shared memory or a warp barrier.
 constexpr int kMaxClimb = 16;  // levels whose siblings are loaded in the single prefetch round
 
-template <int W>
-__device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
-                                unsigned long long node0, float raw, const LeafPowAlpha &alpha,
-                                const LeafPowTables &tb)
-{
-    const bool have = lane < U;
-    const unsigned long long prev0 = __shfl_up_sync(0xffffffffu, node0, 1);
-    const unsigned long long next0 = __shfl_down_sync(0xffffffffu, node0, 1);
-    // heights at which this path meets the previous / next lane's path
-    const int meet_prev = (have && lane > 0) ? 64 - __clzll((long long)(prev0 ^ node0)) : 64;
-    const int meet_next = (have && lane + 1 < U) ? 64 - __clzll((long long)(next0 ^ node0)) : 64;
-    const int hpre = min(shift, kMaxClimb);  // heights covered by the prefetch round
-    int priv = min(min(meet_prev, meet_next) - 1, hpre);  // levels this lane climbs alone
-    if (priv < 0) priv = 0;
-    int h_shared = priv;
-    for (int o = 16; o > 0; o >>= 1) h_shared = min(h_shared, __shfl_xor_sync(0xffffffffu, h_shared, o));
-    // heights at which two paths join (a left owner takes its right neighbour's value there);
-    // at every other height each owner adds its own prefetched sibling, without shuffles
-    unsigned merge_mask = (have && lane + 1 < U && meet_next - 1 < 32) ? (1u << (meet_next - 1)) : 0u;
-    for (int o = 16; o > 0; o >>= 1) merge_mask |= __shfl_xor_sync(0xffffffffu, merge_mask, o);
+struct ClimbLane {
+    unsigned li;      // local leaf index
+    int J;            // joining height with the previous lane (64: none)
+    bool have;
+    double vs;        // value of the lane's current node
+    float vm;
+};
 
-    // one round of loads: the clean sibling at every height this lane owns (height 0 is a leaf,
-    // every height above it an internal node)
+// One level of the climb for heights beyond the prefetch round: children at height h, parent at
+// h + 1.  `merge` is warp-uniform.
+__device__ __forceinline__ void climb_level(const TreeRefs &t, unsigned long long top, int h, bool merge,
+                                            int lane, ClimbLane &c, double sib_s, float sib_m)
+{
+    const bool own = c.have && (lane == 0 || c.J > h);
+    const unsigned v = c.li >> h;
+    bool compute = own;
+    double ss = sib_s;
+    float sm = sib_m;
+    if (merge) {
+        const unsigned own_h = __ballot_sync(0xffffffffu, own);
+        const unsigned own_h1 = __ballot_sync(0xffffffffu, c.have && (lane == 0 || c.J > h + 1));
+        const int R = __ffs(own_h & ~((2u << lane) - 1u)) - 1;   // next owner of height h
+        const int src = R < 0 ? lane : R;
+        const double e_s = __shfl_sync(0xffffffffu, c.vs, src);
+        const float e_m = __shfl_sync(0xffffffffu, c.vm, src);
+        if (v & 1u) {
+            compute = own && (lane == 0 || c.J > h + 1);   // else the left sibling's owner adds
+        } else if (R >= 0 && !((own_h1 >> R) & 1u)) {
+            ss = e_s;                                       // the right sibling is dirty
+            sm = e_m;
+        }
+    }
+    if (compute) {
+        c.vs = c.vs + ss;
+        c.vm = fmin_tree(c.vm, sm);
+        const unsigned long long node = (top >> (h + 1)) + (v >> 1);
+        t.S[node] = c.vs;
+        t.M[node] = c.vm;
+    }
+}
+
+template <int W>
+__device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane, unsigned long long base,
+                                unsigned li, float raw, const LeafPowAlpha &alpha, const LeafPowTables &tb)
+{
+    ClimbLane c;
+    c.li = li;
+    c.have = lane < U;
+    const unsigned prev = __shfl_up_sync(0xffffffffu, li, 1);
+    c.J = (c.have && lane > 0) ? 32 - __clz(prev ^ li) : 64;
+    const unsigned long long top = t.n + base;   // node index of the subtree's first leaf
+    const int hpre = min(shift, kMaxClimb);
+
+    // one round of loads: the sibling at every height this lane owns
     double ps[kMaxClimb];
     float pmn[kMaxClimb];
-    float sib_leaf = 0.0f;   // the leaf's sibling, converted only after the power below
+    float sib_leaf = 0.0f;
 #pragma unroll
     for (int h = 0; h < kMaxClimb; ++h) {
         ps[h] = 0.0;
         pmn[h] = 0.0f;
-        if (have && h < hpre) {
-            const unsigned long long v = node0 >> h;
-            if (lane == 0 || (prev0 >> h) != v) {
-                if (h == 0) {
-                    sib_leaf = t.L[(v ^ 1ull) - t.n];
-                } else {
-                    ps[h] = t.S[v ^ 1ull];
-                    pmn[h] = t.M[v ^ 1ull];
-                }
+        if (c.have && h < hpre && (lane == 0 || c.J > h)) {
+            const unsigned long long sib = (top >> h) + ((li >> h) ^ 1u);
+            if (h == 0) {
+                sib_leaf = t.L[sib - t.n];
+            } else {
+                ps[h] = t.S[sib];
+                pmn[h] = t.M[sib];
             }
         }
     }
-    double vs = 0.0;
-    float vm = 0.0f;
-    if (have) {
+    c.vs = 0.0;
+    c.vm = 0.0f;
+    if (c.have) {
         const float lv = leaf_of(raw, alpha, tb);
-        t.L[node0 - t.n] = lv;
-        vs = (double)lv;
-        vm = leaf_min_value(lv);
+        t.L[base + li] = lv;
+        c.vs = (double)lv;
+        c.vm = leaf_min_value(lv);
     }
+    // the plan, while the loads are in flight: owner ballots of every height, then per height
+    // whether this lane adds (add) and whether it takes a shuffled value (dty) from lane src
+    unsigned om[kMaxClimb + 1];
+#pragma unroll
+    for (int h = 0; h <= kMaxClimb; ++h) om[h] = __ballot_sync(0xffffffffu, c.have && (lane == 0 || c.J > h));
+    const unsigned above = ~((2u << lane) - 1u);
+    unsigned add = 0, dty = 0, join = 0;
+    int src[kMaxClimb];
+#pragma unroll
+    for (int h = 0; h < kMaxClimb; ++h) {
+        const bool own = (om[h] >> lane) & 1u;
+        const bool odd = (li >> h) & 1u;
+        const int R = __ffs(om[h] & above) - 1;
+        const bool d = own && !odd && R >= 0 && !((om[h + 1] >> R) & 1u);
+        src[h] = d ? R : lane;
+        if (h < hpre && own && (!odd || ((om[h + 1] >> lane) & 1u))) add |= 1u << h;
+        if (h < hpre && d) dty |= 1u << h;
+        if (om[h] != om[h + 1] && (om[h] & ~om[h + 1] & ~1u)) join |= 1u << h;   // some lane has J = h + 1
+    }
+    // every prefetched sibling is complete here, in one wait after the power and the plan: the
+    // compiler may otherwise sink each load to its first use and pay one round trip per level
+#pragma unroll
+    for (int h = 0; h < kMaxClimb; ++h) asm volatile("" ::"d"(ps[h]), "f"(pmn[h]));
+    asm volatile("" ::"f"(sib_leaf));
     ps[0] = (double)sib_leaf;
     pmn[0] = leaf_min_value(sib_leaf);
-    // private phase: a chain of binary64 adds over the prefetched siblings
+    const float kInf = __int_as_float(0x7f800000);
+    // the chain; ps[h] / pmn[h] then hold the parent's value at height h + 1 for the store
 #pragma unroll
     for (int h = 0; h < kMaxClimb; ++h) {
-        if (have && h < priv) {
-            const unsigned long long v = node0 >> h;
-            if ((v & 1ull) == 0) {
-                vs = vs + ps[h];
-                vm = fmin_tree(vm, pmn[h]);
-            } else {
-                vs = ps[h] + vs;
-                vm = fmin_tree(pmn[h], vm);
+        if (h < hpre) {
+            const bool a = (add >> h) & 1u;
+            double as = a ? ps[h] : 0.0;
+            float am = a ? pmn[h] : kInf;
+            if ((join >> h) & 1u) {
+                const double e = __shfl_sync(0xffffffffu, c.vs, src[h]);
+                const float em = __shfl_sync(0xffffffffu, c.vm, src[h]);
+                if ((dty >> h) & 1u) {
+                    as = e;
+                    am = em;
+                }
             }
-            t.S[v >> 1] = vs;
-            t.M[v >> 1] = vm;
+            c.vs = c.vs + as;
+            c.vm = fmin_tree(c.vm, am);
+            ps[h] = c.vs;
+            pmn[h] = c.vm;
         }
     }
-    // shared phase: heights h_shared .. shift-1, one shuffle step per joining height
-    int rend = lane + 1;
 #pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h) {
-        if (h >= h_shared && h < hpre && !((merge_mask >> h) & 1u)) {
-            const unsigned long long v = node0 >> h;
-            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
-                if ((v & 1ull) == 0) {
-                    vs = vs + ps[h];
-                    vm = fmin_tree(vm, pmn[h]);
-                } else {
-                    vs = ps[h] + vs;
-                    vm = fmin_tree(pmn[h], vm);
-                }
-                t.S[v >> 1] = vs;
-                t.M[v >> 1] = vm;
-            }
-        } else if (h >= h_shared && h < hpre) {
-            const int src = rend < 32 ? rend : 31;
-            const unsigned long long e_node = __shfl_sync(0xffffffffu, node0, src);
-            const double e_vs = __shfl_sync(0xffffffffu, vs, src);
-            const float e_vm = __shfl_sync(0xffffffffu, vm, src);
-            const int e_rend = __shfl_sync(0xffffffffu, rend, src);
-            const unsigned long long v = node0 >> h;
-            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
-                bool compute = true;
-                double sum = 0.0;
-                float mn = 0.0f;
-                if ((v & 1ull) == 0) {
-                    if (rend < U && (e_node >> h) == v + 1) {
-                        sum = vs + e_vs;
-                        mn = fmin_tree(vm, e_vm);
-                        rend = e_rend;
-                    } else {
-                        sum = vs + ps[h];
-                        mn = fmin_tree(vm, pmn[h]);
-                    }
-                } else if (lane > 0 && (prev0 >> h) == v - 1) {
-                    compute = false;  // the left sibling's owner combines this pair
-                } else {
-                    sum = ps[h] + vs;
-                    mn = fmin_tree(pmn[h], vm);
-                }
-                if (compute) {
-                    vs = sum;
-                    vm = mn;
-                    t.S[v >> 1] = sum;
-                    t.M[v >> 1] = mn;
-                }
-            }
+    for (int h = 0; h < kMaxClimb; ++h)
+        if (h < hpre && ((add >> h) & 1u)) {
+            const unsigned long long node = (top >> (h + 1)) + ((li >> h) >> 1);
+            t.S[node] = ps[h];
+            t.M[node] = pmn[h];
         }
-    }
-    // heights beyond the prefetch round (subtrees deeper than kMaxClimb levels)
+    // heights beyond the prefetch round (subtrees deeper than kMaxClimb levels), W per round
     for (int h0 = hpre; h0 < shift; h0 += W) {
         double qs[W];
         float qm[W];
@@ -883,50 +906,17 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane,
             const int h = h0 + w;
             qs[w] = 0.0;
             qm[w] = 0.0f;
-            if (have && h < shift) {
-                const unsigned long long v = node0 >> h;
-                if (lane == 0 || (prev0 >> h) != v) {
-                    qs[w] = t.S[v ^ 1ull];
-                    qm[w] = t.M[v ^ 1ull];
-                }
+            if (c.have && h < shift && (lane == 0 || c.J > h)) {
+                const unsigned long long sib = (top >> h) + ((li >> h) ^ 1u);
+                qs[w] = t.S[sib];
+                qm[w] = t.M[sib];
             }
         }
 #pragma unroll
         for (int w = 0; w < W; ++w) {
             const int h = h0 + w;
-            if (h >= shift) break;
-            const int src = rend < 32 ? rend : 31;
-            const unsigned long long e_node = __shfl_sync(0xffffffffu, node0, src);
-            const double e_vs = __shfl_sync(0xffffffffu, vs, src);
-            const float e_vm = __shfl_sync(0xffffffffu, vm, src);
-            const int e_rend = __shfl_sync(0xffffffffu, rend, src);
-            const unsigned long long v = node0 >> h;
-            if (have && h >= priv && (lane == 0 || (prev0 >> h) != v)) {
-                bool compute = true;
-                double sum = 0.0;
-                float mn = 0.0f;
-                if ((v & 1ull) == 0) {
-                    if (rend < U && (e_node >> h) == v + 1) {
-                        sum = vs + e_vs;
-                        mn = fmin_tree(vm, e_vm);
-                        rend = e_rend;
-                    } else {
-                        sum = vs + qs[w];
-                        mn = fmin_tree(vm, qm[w]);
-                    }
-                } else if (lane > 0 && (prev0 >> h) == v - 1) {
-                    compute = false;
-                } else {
-                    sum = qs[w] + vs;
-                    mn = fmin_tree(qm[w], vm);
-                }
-                if (compute) {
-                    vs = sum;
-                    vm = mn;
-                    t.S[v >> 1] = sum;
-                    t.M[v >> 1] = mn;
-                }
-            }
+            const bool merge = __any_sync(0xffffffffu, c.have && lane > 0 && c.J == h + 1);
+            if (h < shift) climb_level(t, top, h, merge, lane, c, qs[w], qm[w]);
         }
     }
 }
@@ -1036,6 +1026,50 @@ __device__ void warp_upsweep(const TreeRefs &t, WarpLists &wl, int U, int shift,
     }
 }
 
+// Files the batch entries of this CTA's subtrees under their warp's list (slot order is the
+// order of arrival; the sort below restores batch order).  Returns this thread's largest raw
+// priority among the filed entries.
+template <int U>
+__device__ __forceinline__ unsigned file_batch(const UpdArgs &a, WarpLists *lists, int *s_cnt,
+                                               unsigned long long first_sub, int shift,
+                                               unsigned long long size, float max_prev)
+{
+    unsigned mymax = 0;
+    for (unsigned j0 = threadIdx.x; j0 < a.B; j0 += U * blockDim.x) {
+        long long iv[U];
+        float tv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned j = j0 + u * blockDim.x;
+            iv[u] = j < a.B ? __ldg(a.idx + j) : -2;
+            tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned j = j0 + u * blockDim.x;
+            const long long i = iv[u];
+            if (i == -2) continue;
+            if (i < 0 || (unsigned long long)i >= size) {
+                if (blockIdx.x == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
+                continue;
+            }
+            const unsigned long long sub = (unsigned long long)i >> shift;
+            if (sub < first_sub || sub >= first_sub + a.subs) continue;
+            const int w = (int)(sub - first_sub);
+            const float raw = td_to_raw(tv[u], a.eps, max_prev);
+            mymax = max(mymax, __float_as_uint(raw));
+            const int slot = atomicAdd(&s_cnt[w], 1);
+            if (slot < kWarpCap) {
+                WarpLists &wl = lists[w];
+                wl.keys[slot] = (((unsigned long long)i - (sub << shift)) << a.pb) | j;
+                wl.pay[slot] = (unsigned)slot;
+                wl.rawv[slot] = raw;
+            }
+        }
+    }
+    return mymax;
+}
+
 template <int W>
 __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
 {
@@ -1063,41 +1097,13 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     if (tid == 0) s_max = 0;
     __syncthreads();
 
-    // 1. file this CTA's entries under their subtree's warp (indices and TD errors are read
-    //    together, four per thread in flight)
+    // 1. file this CTA's entries under their subtree's warp (every CTA reads the whole batch:
+    //    indices and TD errors together, 4, 8 or 16 per thread in flight as the batch grows)
     unsigned mymax = 0;
-    for (unsigned j0 = tid; j0 < a.B; j0 += 4 * blockDim.x) {
-        long long iv[4];
-        float tv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const unsigned j = j0 + u * blockDim.x;
-            iv[u] = j < a.B ? __ldg(a.idx + j) : -2;
-            tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const unsigned j = j0 + u * blockDim.x;
-            const long long i = iv[u];
-            if (i == -2) continue;
-            if (i < 0 || (unsigned long long)i >= size) {
-                if (blockIdx.x == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
-                continue;
-            }
-            const unsigned long long sub = (unsigned long long)i >> shift;
-            if (sub < first_sub || sub >= first_sub + a.subs) continue;
-            const int w = (int)(sub - first_sub);
-            const float raw = td_to_raw(tv[u], a.eps, max_prev);
-            mymax = max(mymax, __float_as_uint(raw));
-            const int slot = atomicAdd(&s_cnt[w], 1);
-            if (slot < kWarpCap) {
-                WarpLists &wl = lists[w];
-                wl.keys[slot] = (((unsigned long long)i - (sub << shift)) << a.pb) | j;
-                wl.pay[slot] = (unsigned)slot;
-                wl.rawv[slot] = raw;
-            }
-        }
-    }
+    const unsigned per_round = (a.B + blockDim.x - 1) / blockDim.x;
+    if (per_round <= 4) mymax = file_batch<4>(a, lists, s_cnt, first_sub, shift, size, max_prev);
+    else if (per_round <= 8) mymax = file_batch<8>(a, lists, s_cnt, first_sub, shift, size, max_prev);
+    else mymax = file_batch<16>(a, lists, s_cnt, first_sub, shift, size, max_prev);
     for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
     if (lane == 0 && mymax) atomicMax(&s_max, mymax);
     __syncthreads();
@@ -1152,11 +1158,11 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
             const int from = lane < U ? (int)__fns(bal, 0, lane + 1) : 0;
             const unsigned long long k_from = __shfl_sync(0xffffffffu, key, from);
             const float raw = __shfl_sync(0xffffffffu, myraw, from);
-            const unsigned long long leaf = base + (k_from >> a.pb);
+            const unsigned li = (unsigned)(k_from >> a.pb);   // local leaf index
             if (a.proportional) {
-                warp_climb_regs<W>(a.t, U, shift, lane, lane < U ? leaf + n : 0ull, raw, a.lp, s_lp);
+                warp_climb_regs<W>(a.t, U, shift, lane, base, lane < U ? li : 0u, raw, a.lp, s_lp);
             } else if (lane < U) {
-                a.raw_store[leaf] = raw;
+                a.raw_store[base + li] = raw;
             }
         } else {
             int m2 = 2;
@@ -1256,6 +1262,73 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                         const int node = (w >> 1) + lane / (2 * st);
                         a.t.S[node] = sv;
                         a.t.M[node] = mv;
+                    }
+                }
+            }
+        } else if (a.proportional && a.P >= 7 && a.P <= 10 && kUpdWarps == 4) {
+            // four warps: warp w rebuilds the subtree of node 4 + w from its 2^(P-2) depth-P
+            // nodes (g = 2^(P-7) per lane combined in registers down to depth 7, then five
+            // shuffle levels down to depth 2); warp 0 then adds nodes 4..7 up to the root
+            __shared__ double s_q[4];
+            __shared__ float s_qm[4];
+            const int P = a.P;
+            const int g = 1 << (P - 7);
+            double gs[8];
+            float gm[8];
+            const unsigned long long c0 = (1ull << P) + ((unsigned long long)warp << (P - 2)) + (unsigned long long)lane * g;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                gs[i] = i < g ? ld_sum_cg(a.t, c0 + i) : 0.0;
+                gm[i] = i < g ? ld_min_cg(a.t, c0 + i) : 0.0f;
+            }
+#pragma unroll
+            for (int half = 4; half >= 1; half >>= 1) {
+                if (2 * half <= g) {
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        gs[i] = gs[2 * i] + gs[2 * i + 1];
+                        gm[i] = fmin_tree(gm[2 * i], gm[2 * i + 1]);
+                    }
+                    const int dlev = 7 + (31 - __clz(half));   // depth of these sums
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const unsigned long long node = (1ull << dlev) + ((unsigned long long)warp << (dlev - 2)) +
+                                                        (unsigned long long)lane * half + i;
+                        a.t.S[node] = gs[i];
+                        a.t.M[node] = gm[i];
+                    }
+                }
+            }
+            double sv = gs[0];   // depth-7 node 128 + 32 warp + lane
+            float mv = gm[0];
+            for (int st = 1, w = 32, dep = 7; w > 1; st <<= 1, w >>= 1, --dep) {
+                const double os = __shfl_down_sync(0xffffffffu, sv, st);
+                const float om = __shfl_down_sync(0xffffffffu, mv, st);
+                if ((lane & (2 * st - 1)) == 0) {
+                    sv = sv + os;
+                    mv = fmin_tree(mv, om);
+                    const int node = (1 << (dep - 1)) + (warp << (dep - 3)) + lane / (2 * st);
+                    a.t.S[node] = sv;
+                    a.t.M[node] = mv;
+                }
+            }
+            if (lane == 0) {
+                s_q[warp] = sv;
+                s_qm[warp] = mv;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                double qv = lane < 4 ? s_q[lane] : 0.0;   // nodes 4..7 on lanes 0..3
+                float qm = lane < 4 ? s_qm[lane] : __int_as_float(0x7f800000);
+                for (int st = 1, w = 4; w > 1; st <<= 1, w >>= 1) {
+                    const double os = __shfl_down_sync(0xffffffffu, qv, st);
+                    const float om = __shfl_down_sync(0xffffffffu, qm, st);
+                    if ((lane & (2 * st - 1)) == 0 && lane < w * st) {
+                        qv = qv + os;
+                        qm = fmin_tree(qm, om);
+                        const int node = (w >> 1) + lane / (2 * st);
+                        a.t.S[node] = qv;
+                        a.t.M[node] = qm;
                     }
                 }
             }
