@@ -220,7 +220,7 @@ per_status per_nleaves(const per_buffer *h, uint64_t *out);
  *   d_raw   [n] float, device, > 0 and finite (caller-owned input).
  *   d_order [n] uint32, device (caller-owned output).
  *   n       1 .. 262144 (2^18); larger n returns PER_ERR_INVALID_ARG.
- * Scratch: a fixed device array of about 4.6 MiB compiled into the library, which every GPU
+ * Scratch: a fixed device array of about 4.3 MiB compiled into the library, which every GPU
  * that loads the library holds until the process exits.  The first call on a device looks up
  * that array's device address (cudaGetSymbolAddress) and caches it; make that first call on
  * each device before any stream capture begins.  All calls share the one array and it keeps

@@ -479,7 +479,7 @@ constexpr unsigned long long kNoAllocWords =
     4 * kNoAllocMaxKeys + 1024 + 16 + 2 * (4 * (kNoAllocTiles + kNoAllocGroups) * 256);
 constexpr int kNoAllocMaxDevices = 64;
 
-// About 4.5 MiB per device, held by every device that loads the library until exit;
+// About 4.3 MiB per device, held by every device that loads the library until exit;
 // zero at load, which the sort's histograms, control words and epoch tags rely on.
 __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocWords];
 
