@@ -236,6 +236,27 @@ def _out_ptrs(out: dict):
                                          "dones")]
 
 
+# -- replicas: one process per GPU, each running the whole step on its own buffer --------------
+
+def max_over_ranks(value: float, dist=None) -> float:
+    """The slowest replica's time: MAX all-reduce of one float over every rank (a no-op on one
+    process).  NCCL reduces a CUDA tensor, gloo a CPU tensor."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(world: int, steps: int, max_secs: float) -> float:
+    """Whole-job steps/s: every rank ran `steps` steps; the job took the slowest rank's time."""
+    if max_secs <= 0:
+        raise ValueError("timed region must be positive")
+    return world * steps / max_secs
+
+
 def run_gpu(args, rank, world):
     import ctypes
     import torch
@@ -332,10 +353,7 @@ def run_gpu(args, rank, world):
     clk = clocks.stop() if clocks else None   # the sampler spans both timed loops
     cont_s = cr.elapsed_ms(ca, cb) / 1e3
     cr.destroy([ca, cb])
-    if dist:
-        tt = torch.tensor([cont_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        cont_s = float(tt.item())
+    cont_s = max_over_ranks(cont_s, dist)
 
     # per-kernel breakdown (for the roofline): a second pass with an event between the calls.
     # Each event pair also carries a launch (about 4 us on this GPU for an empty kernel), so
@@ -390,11 +408,8 @@ def run_gpu(args, rank, world):
                      "note": "one CUDA graph launch per step (ingest + sample + update)"}
         del graphs
     total_s = float(step_ms.sum()) / 1e3
-    if dist:
-        tt = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
-    value_flushed = world * K / total_s
+    total_s = max_over_ranks(total_s, dist)
+    value_flushed = aggregate_throughput(world, K, total_s)
     if buf.status_device() != 0:
         raise RuntimeError("device error flag raised during the benchmark")
 
@@ -420,7 +435,7 @@ def run_gpu(args, rank, world):
     step_bytes = b_add + b_sam + b_upd
 
     res = {
-        "metric": METRIC, "value": round(world * K / cont_s, 2), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(aggregate_throughput(world, K, cont_s), 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(cont_s * 1e3 / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; rows N(0,1) drawn on the device, lognormal(0,1) priorities)",
@@ -524,13 +539,9 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     secs = e0.elapsed_time(e1) / 1e3
-    world = 1
-    if dist:
-        tt = torch.tensor([secs], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        secs = float(tt.item())
-        world = dist.get_world_size()
-    return {"value": round(world * K / secs, 2), "unit": UNIT,
+    secs = max_over_ranks(secs, dist)
+    world = dist.get_world_size() if dist else 1
+    return {"value": round(aggregate_throughput(world, K, secs), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(sum(n for _, n in sizes)),
             "d2h_bytes_per_step": int(sum(n for _, n in osz)), "steps": K,
             "note": "pinned host rows + TD errors in, sampled batch out, inside the timing"}
