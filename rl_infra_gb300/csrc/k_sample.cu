@@ -43,6 +43,8 @@ struct SampleArgs {
     int vec4;  // rows move as float4
 };
 
+constexpr int kGatherV = 4;   // float4 per lane in the single-round gather: rows of up to 256 floats
+
 // The sampled row: every load of the warp's share (states, next_states, and the action, reward
 // and done fields on lanes 1-3) is issued before the first store, so the gather costs one memory
 // round trip.  Rows shorter than the output stride are padded with zeros.
@@ -57,15 +59,15 @@ __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o
     if (lane == 2 && o.rewards) rew = __ldg(r.rewards + slot);
     if (lane == 3 && o.dones) done = __ldg(r.dones + slot);
     const bool rows = d && (o.states || o.next);
-    if (rows && vec4 && 2 * (dp >> 2) <= 64) {
-        // up to 64 float4 per row pair: two per lane, loaded together
+    if (rows && vec4 && 2 * (dp >> 2) <= 32 * kGatherV) {
+        // up to 32 kGatherV float4 per row pair: kGatherV per lane, all loaded before any store
         const unsigned d4 = d >> 2, dp4 = dp >> 2;
         const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
         const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
-        float4 v[2];
+        float4 v[kGatherV];
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kGatherV; ++q) {
             const unsigned c = lane + 32 * q;
             const bool second = c >= dp4;
             const unsigned cc = second ? c - dp4 : c;
@@ -73,7 +75,7 @@ __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o
             if (c < 2 * dp4 && cc < d4 && (second ? o.next : o.states)) v[q] = __ldg((second ? srcN : srcS) + cc);
         }
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kGatherV; ++q) {
             const unsigned c = lane + 32 * q;
             const bool second = c >= dp4;
             const unsigned cc = second ? c - dp4 : c;
@@ -254,7 +256,7 @@ struct RankSampleArgs {
     int vec4;
 };
 
-__global__ void __launch_bounds__(kThreads) k_sample_rank(RankSampleArgs a)
+__global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
 {
     __shared__ double s_seg;
     __shared__ unsigned long long s_call;

@@ -641,7 +641,7 @@ __global__ void k_fill(float *p, unsigned long long n, float v)
 // ------------------------------------------------------------------------------------------
 // Priority update: last-writer-wins scatter + dirty-ancestor upsweep, one launch.
 // The tree below depth P is cut into 2^P subtrees and each subtree belongs to one warp (a CTA
-// holds kUpdWarps of them), so nothing below depth P needs more than warp synchronisation:
+// holds 4 or 16 of them), so nothing below depth P needs more than warp synchronisation:
 //   1. the CTA reads the batch once, coalesced, and files each entry under its subtree's warp;
 //   2. each warp sorts its entries by (leaf, batch position) in shared memory, keeps the last
 //      position of every leaf, writes those leaves and climbs its subtree level by level.  On
@@ -655,18 +655,17 @@ __global__ void k_fill(float *p, unsigned long long n, float v)
 // batch in position order 32 entries at a time (later chunks overwrite earlier ones, so the
 // last writer wins) and then rebuilds its whole subtree.
 // ------------------------------------------------------------------------------------------
-#ifndef GBPER_UPD_WARPS
-#define GBPER_UPD_WARPS 4
-#endif
-#ifndef GBPER_WARP_CAP
-#define GBPER_WARP_CAP 512
-#endif
 #ifndef GBPER_UPD_WINDOW
 #define GBPER_UPD_WINDOW 8
 #endif
-constexpr int kUpdWarps = GBPER_UPD_WARPS;   // subtrees (warps) per CTA
-constexpr int kUpdThreads = 32 * kUpdWarps;
-constexpr int kWarpCap = GBPER_WARP_CAP;     // entries one warp sorts in shared memory
+// Two CTA shapes: 4 warps with lists of 512 entries (batches below 4096 entries), or 16 warps
+// with lists of 128 (larger batches: a quarter as many CTAs read the whole batch, each in one
+// round).  Both take the same shared memory.
+constexpr int kUpdMaxWarps = 16;
+constexpr int kUpdMaxThreads = 32 * kUpdMaxWarps;
+constexpr int kUpdSmallWarps = 4, kUpdSmallCap = 512;
+constexpr int kUpdLargeWarps = 16, kUpdLargeCap = 128;
+constexpr unsigned kUpdLargeBatch = 4096;
 constexpr int kUpdWindow = GBPER_UPD_WINDOW; // tree levels whose clean siblings load in one round
 
 struct UpdArgs {
@@ -678,25 +677,49 @@ struct UpdArgs {
     unsigned B;
     int P;      // log2 number of subtrees
     int subs;   // subtrees per CTA (warps 0 .. subs-1 climb; all warps file the batch)
+    int cap;    // entries a warp's list holds (more take the chunked path)
     int pb;     // bits for a batch position
     double alpha, eps;
     LeafPowAlpha lp;
     int proportional;
 };
 
+// One warp's entry lists in shared memory, `cap` entries each (36 bytes per entry).
 struct WarpLists {
-    unsigned long long keys[kWarpCap];  // (leaf offset << pb) | position
-    double vs[kWarpCap];
-    unsigned pay[kWarpCap];             // entry slot carried through the sort
-    float rawv[kWarpCap];               // raw priority by entry slot
-    unsigned ulist[kWarpCap];           // distinct leaves, ascending (absolute)
-    float vm[kWarpCap];
-    int rend[kWarpCap];
+    unsigned long long *keys;  // (leaf offset << pb) | position
+    double *vs;
+    unsigned *pay;             // entry slot carried through the sort
+    float *rawv;               // raw priority by entry slot
+    unsigned *ulist;           // distinct leaves, ascending (absolute)
+    float *vm;
+    int *rend;
 };
+constexpr size_t kListBytesPerEntry = 36;
+
+__device__ __forceinline__ WarpLists warp_lists(unsigned char *smem, int w, int cap)
+{
+    unsigned char *b = smem + (size_t)w * kListBytesPerEntry * cap;
+    WarpLists l;
+    l.keys = reinterpret_cast<unsigned long long *>(b);
+    b += 8 * (size_t)cap;
+    l.vs = reinterpret_cast<double *>(b);
+    b += 8 * (size_t)cap;
+    l.pay = reinterpret_cast<unsigned *>(b);
+    b += 4 * (size_t)cap;
+    l.rawv = reinterpret_cast<float *>(b);
+    b += 4 * (size_t)cap;
+    l.ulist = reinterpret_cast<unsigned *>(b);
+    b += 4 * (size_t)cap;
+    l.vm = reinterpret_cast<float *>(b);
+    b += 4 * (size_t)cap;
+    l.rend = reinterpret_cast<int *>(b);
+    return l;
+}
 
 constexpr size_t kTopHeapBytes = (size_t)(2 << kMaxTopLog) * 12;  // the last CTA's top levels
-constexpr size_t kUpdSmemBytes = sizeof(WarpLists) * kUpdWarps > kTopHeapBytes
-                                     ? sizeof(WarpLists) * kUpdWarps : kTopHeapBytes;
+constexpr size_t kListsBytes = kListBytesPerEntry * (kUpdSmallWarps * kUpdSmallCap > kUpdLargeWarps * kUpdLargeCap
+                                                         ? kUpdSmallWarps * kUpdSmallCap : kUpdLargeWarps * kUpdLargeCap);
+constexpr size_t kUpdSmemBytes = kListsBytes > kTopHeapBytes ? kListsBytes : kTopHeapBytes;
 
 __device__ __forceinline__ void warp_bitonic_kv(unsigned long long *keys, unsigned *pay, int m2, int lane)
 {
@@ -924,7 +947,7 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane, u
 // Climb one warp's subtree from its U distinct leaves (ulist ascending, vs/vm seeded with the
 // new leaf values, rend[k] = k + 1) up to the subtree root at depth D - shift.
 template <int W>
-__device__ void warp_upsweep(const TreeRefs &t, WarpLists &wl, int U, int shift, int lane)
+__device__ void warp_upsweep(const TreeRefs &t, const WarpLists &wl, int U, int shift, int lane)
 {
     const unsigned long long n = t.n;
     if (U <= 32) {
@@ -1030,7 +1053,7 @@ __device__ void warp_upsweep(const TreeRefs &t, WarpLists &wl, int U, int shift,
 // order of arrival; the sort below restores batch order).  Returns this thread's largest raw
 // priority among the filed entries.
 template <int U>
-__device__ __forceinline__ unsigned file_batch(const UpdArgs &a, WarpLists *lists, int *s_cnt,
+__device__ __forceinline__ unsigned file_batch(const UpdArgs &a, unsigned char *lists, int *s_cnt,
                                                unsigned long long first_sub, int shift,
                                                unsigned long long size, float max_prev)
 {
@@ -1059,8 +1082,8 @@ __device__ __forceinline__ unsigned file_batch(const UpdArgs &a, WarpLists *list
             const float raw = td_to_raw(tv[u], a.eps, max_prev);
             mymax = max(mymax, __float_as_uint(raw));
             const int slot = atomicAdd(&s_cnt[w], 1);
-            if (slot < kWarpCap) {
-                WarpLists &wl = lists[w];
+            if (slot < a.cap) {
+                const WarpLists wl = warp_lists(lists, w, a.cap);
                 wl.keys[slot] = (((unsigned long long)i - (sub << shift)) << a.pb) | j;
                 wl.pay[slot] = (unsigned)slot;
                 wl.rawv[slot] = raw;
@@ -1071,11 +1094,11 @@ __device__ __forceinline__ unsigned file_batch(const UpdArgs &a, WarpLists *list
 }
 
 template <int W>
-__global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
+__global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    WarpLists *lists = reinterpret_cast<WarpLists *>(smem_raw);
-    __shared__ int s_cnt[kUpdWarps];
+    unsigned char *lists = smem_raw;
+    __shared__ int s_cnt[kUpdMaxWarps];
     __shared__ unsigned s_max;
     __shared__ LeafPowTables s_lp;
     {   // the power's tables (constant since the library loaded), staged while the batch is read
@@ -1093,7 +1116,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     const unsigned long long n = a.t.n;
     const unsigned long long size = a.ctl->size;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
-    if (tid < kUpdWarps) s_cnt[tid] = 0;
+    if (tid < kUpdMaxWarps) s_cnt[tid] = 0;
     if (tid == 0) s_max = 0;
     __syncthreads();
 
@@ -1113,9 +1136,9 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     const unsigned long long sub = first_sub + warp;
     const int m = s_cnt[warp];
     if (warp < a.subs && sub < nsub && m > 0) {
-        WarpLists &wl = lists[warp];
+        const WarpLists wl = warp_lists(lists, warp, a.cap);
         const unsigned long long base = sub << shift;
-        if (m > kWarpCap) {
+        if (m > a.cap) {
             for (unsigned p0 = 0; p0 < a.B; p0 += 32) {
                 const unsigned j = p0 + lane;
                 long long i = -1;
@@ -1265,7 +1288,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                     }
                 }
             }
-        } else if (a.proportional && a.P >= 7 && a.P <= 10 && kUpdWarps == 4) {
+        } else if (a.proportional && a.P >= 7 && a.P <= 10 && (blockDim.x >> 5) >= 4) {
             // four warps: warp w rebuilds the subtree of node 4 + w from its 2^(P-2) depth-P
             // nodes (g = 2^(P-7) per lane combined in registers down to depth 7, then five
             // shuffle levels down to depth 2); warp 0 then adds nodes 4..7 up to the root
@@ -1273,6 +1296,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
             __shared__ float s_qm[4];
             const int P = a.P;
             const int g = 1 << (P - 7);
+            if (warp < 4) {
             double gs[8];
             float gm[8];
             const unsigned long long c0 = (1ull << P) + ((unsigned long long)warp << (P - 2)) + (unsigned long long)lane * g;
@@ -1316,6 +1340,7 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
                 s_q[warp] = sv;
                 s_qm[warp] = mv;
             }
+            }   // warp < 4
             __syncthreads();
             if (warp == 0) {
                 double qv = lane < 4 ? s_q[lane] : 0.0;   // nodes 4..7 on lanes 0..3
@@ -1364,16 +1389,16 @@ __global__ void __launch_bounds__(kUpdThreads) k_update(UpdArgs a)
     }
 }
 
-// Subtrees per CTA of the update kernel: fewer per CTA spreads the climbs' sibling loads over
-// more SMs (GBPER_UPD_SUBS, 1..kUpdWarps).
-int update_subtrees_per_cta()
+// Subtrees per CTA of the update kernel, at most its warps: fewer per CTA spreads the climbs
+// over more SMs (GBPER_UPD_SUBS; default: one per warp).
+int update_subtrees_per_cta(int warps)
 {
     static const int v = [] {
-        int s = kUpdWarps;
+        int s = 0;
         if (const char *e = std::getenv("GBPER_UPD_SUBS")) s = std::atoi(e);
-        return s < 1 ? 1 : (s > kUpdWarps ? kUpdWarps : s);
+        return s;
     }();
-    return v;
+    return v < 1 ? warps : (v > warps ? warps : v);
 }
 
 // Target batch entries per subtree of the update kernel (GBPER_UPD_PER, 1..64; default 8).
@@ -1498,17 +1523,20 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.eps = eps;
     a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
-    // about 8 batch entries per subtree (a warp's list holds up to kWarpCap, so a batch
-    // concentrated on a stretch of recent slots still fits); at most 2^10 subtrees, and no
-    // more than half the leaves
+    // about 8 batch entries per subtree (a warp's list holds 512 or 128, so a batch concentrated
+    // on a stretch of recent slots still fits; more take the chunked path); at most 2^10
+    // subtrees, and no more than half the leaves
     const int per = update_entries_per_subtree();
     int P = ilog2_ceil((B + per - 1) / per);
     P = std::min(P, kMaxTopLog);
     P = std::min(P, std::max(t.D - 1, 0));
     a.P = P;
-    a.subs = update_subtrees_per_cta();
+    const bool large = B >= kUpdLargeBatch;
+    const int warps = large ? kUpdLargeWarps : kUpdSmallWarps;
+    a.cap = large ? kUpdLargeCap : kUpdSmallCap;
+    a.subs = update_subtrees_per_cta(warps);
     const unsigned grid = (unsigned)(((1ull << P) + a.subs - 1) / a.subs);
-    return launch_pdl(k_update<kUpdWindow>, grid, kUpdThreads, kUpdSmemBytes, st, a);
+    return launch_pdl(k_update<kUpdWindow>, grid, 32 * warps, kUpdSmemBytes, st, a);
 }
 
 }  // namespace gbper
