@@ -553,20 +553,23 @@ OTHER = {
     "tiny": "tiny: 2^10 leaves, state_dim 8, B=32, alpha 0.6, beta 0.4",
     "dqn": "dqn: 2^20 leaves, state_dim 48 gathered into 64-float rows, B=1024, beta 0.4->1.0 over 341 steps",
     "stress": "stress: 2^24 leaves, state_dim 256, B=8192, 25% duplicate update indices, alpha 0.7, beta 0.5",
-    "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, radix sort + rank sample, alpha 0.7, beta 0.5",
+    "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, order merge (radix sort when rebuilt) + rank sample, alpha 0.7, beta 0.5",
 }
 
 
-def run_other(args, name):
+def run_other(args, name, resort=False):
     """Steps/s of one sample (+IS +gather) and one update per step on another workload; the rank
-    workload's sample call includes the sort.  Same timing rules as the apex step."""
+    workload's sample call brings the slot order up to date (merging the slots written since
+    the previous sample, or with `resort` sorting every slot again).  Same timing rules as the
+    apex step."""
     import ctypes
     import torch
     from rl_infra_gb300 import capi
     from rl_infra_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
     torch.cuda.set_device(0)
-    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0)
+    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0,
+                            flags=capi.PER_FLAG_RANK_RESORT if resort else 0)
     g = wl.rng(0, 55)
     chunk = min(w.capacity, 1 << 18)
     for c in range(w.capacity // chunk):
@@ -639,9 +642,13 @@ def run_other(args, name):
     upd_idx = idx_sets[(W + K + Kop - 1) % NS].cpu().numpy()
     if w.mode == wl.RANK:
         n = w.capacity
-        b_sam = 4 * 16 * n + 4 * n + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
-        b_upd = 12 * B + 4 * len(np.unique(upd_idx))
-        names = ("rank sort + k_sample_rank", "k_update")
+        d = len(np.unique(upd_idx))
+        # order merge: previous keys + slots in, new keys + slots out, the written slots' entries
+        # (slot + raw) once; the sampler's probes, weights and gathered rows
+        b_sort = (16 * n + 8 * d) if not resort else (4 * 16 * n + 4 * n)
+        b_sam = b_sort + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
+        b_upd = 12 * B + 4 * d
+        names = ("rank order + k_sample_rank", "k_update")
     else:
         b_sam = bytes_sample(idx, w.state_dim, w.row_stride, D)
         b_upd = bytes_update(upd_idx, D)
@@ -667,8 +674,11 @@ def run_other(args, name):
                      "unit": "GB/s", "frac": round(achieved / peak, 5), "traffic": None,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
                      "median_launch_us": round(ms * 1e3, 3)},
-        "gpu_launches": (14 if w.mode == wl.RANK else 2) * K,
+        "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 2) * K,
     }
+    if w.mode == wl.RANK:
+        res["config"]["rank_order"] = ("every slot sorted again at each sample (4-pass radix sort)" if resort
+                                       else "previous order merged with the slots written since")
     buf.close()
     return res
 
@@ -755,7 +765,12 @@ def main():
 
     if args.workload != "apex":
         if rank == 0:
-            print(json.dumps(run_other(args, args.workload)))
+            res = run_other(args, args.workload)
+            if args.workload == "rank":
+                full = run_other(args, "rank", resort=True)
+                res["full_resort"] = {k: full[k] for k in ("value", "unit", "step_us_median", "ops_median_us",
+                                                           "bytes_per_step", "roofline")}
+            print(json.dumps(res))
         return
     res = run_gpu(args, rank, world)
     if rank == 0:

@@ -63,7 +63,16 @@ enum {
 /* Bits of the device error word (per_status_device). */
 enum {
     PER_DEVFLAG_BAD_INDEX = 1u, /* an update named an index outside [0, size); it was skipped */
-    PER_DEVFLAG_TIMEOUT = 2u    /* a bounded wait gave up; the call's results are not valid */
+    PER_DEVFLAG_TIMEOUT = 2u,   /* a bounded wait gave up; the call's results are not valid */
+    PER_DEVFLAG_RANK_STALE = 4u /* rank mode: more slots were written between two samples than the
+                                   order merge can take (only reachable by replaying a captured
+                                   sample after more writes than at capture); the order is stale */
+};
+
+/* per_config.flags */
+enum {
+    PER_FLAG_RANK_RESORT = 1u  /* rank mode: sort every filled slot at each sample instead of
+                                  merging the slots written since the previous one (same order) */
 };
 
 typedef struct {
@@ -73,7 +82,7 @@ typedef struct {
     uint32_t row_stride_out; /* floats per gathered state row, >= state_dim (0: state_dim);
                                 columns past state_dim are written as 0.0f */
     uint64_t seed;           /* key of the Philox4x32-10 stream that draws the batches */
-    uint32_t flags;          /* reserved; must be 0 */
+    uint32_t flags;          /* PER_FLAG_* bits; others must be 0 */
     uint32_t reserved;
 } per_config;
 
@@ -133,7 +142,11 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
  * Rank mode ("Sampling Kernels", Rank-based): sorts the filled slots by raw priority
  * descending (ties by slot ascending), draws mass_j = (j + u_j) * (c_size / B) with counter
  * tag 1, takes the rank r whose CDF interval c_{r-1} <= mass < c_r holds it, with
- * c_r = sum_{k<=r} k^-alpha, and weights w = (r / size)^(alpha * beta).
+ * c_r = sum_{k<=r} k^-alpha, and weights w = (r / size)^(alpha * beta).  The order is kept
+ * between calls: when it exists and at most 4096 slots (and at most an eighth of the filled
+ * ones, by the host's count of inserted and updated entries) were written since, only those
+ * slots are merged back into it; otherwise every filled slot is sorted again.  Both give the
+ * same order.
  * Gather ("True Single-Graph Implementation Plan", Task 2/3): row j of d_states and d_next
  * receives the chosen slot's row, padded with 0.0f to row_stride_out floats.
  *   d_idx [B] int64 (required); d_w [B] float; d_states, d_next [B x row_stride_out] float;
@@ -195,7 +208,8 @@ enum {
     PER_STATE_ACTIONS = 7,  /* uint32 [capacity] */
     PER_STATE_REWARDS = 8,  /* float [capacity] */
     PER_STATE_DONES = 9,    /* uint8 [capacity] */
-    PER_STATE_COUNTERS = 10 /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
+    PER_STATE_COUNTERS = 10, /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
+    PER_STATE_RANK_ORDER = 11 /* uint32 [size at the last sample]: slots by rank (rank mode) */
 };
 
 /* per_read_state -- copy `count` elements starting at element `first` of one of the arrays

@@ -27,16 +27,18 @@ PER_MODE_RANK = 1
 
 PER_DEVFLAG_BAD_INDEX = 1
 PER_DEVFLAG_TIMEOUT = 2
+PER_DEVFLAG_RANK_STALE = 4
+PER_FLAG_RANK_RESORT = 1
 
 PER_STATE_LEAVES, PER_STATE_SUMS, PER_STATE_MINS, PER_STATE_RAW, PER_STATE_CDF = 0, 1, 2, 3, 4
 PER_STATE_STATES, PER_STATE_NEXT, PER_STATE_ACTIONS, PER_STATE_REWARDS = 5, 6, 7, 8
-PER_STATE_DONES, PER_STATE_COUNTERS = 9, 10
+PER_STATE_DONES, PER_STATE_COUNTERS, PER_STATE_RANK_ORDER = 9, 10, 11
 
 _STATE_DTYPE = {
     PER_STATE_LEAVES: np.float32, PER_STATE_SUMS: np.float64, PER_STATE_MINS: np.float32,
     PER_STATE_RAW: np.float32, PER_STATE_CDF: np.float64, PER_STATE_STATES: np.float32,
     PER_STATE_NEXT: np.float32, PER_STATE_ACTIONS: np.uint32, PER_STATE_REWARDS: np.float32,
-    PER_STATE_DONES: np.uint8, PER_STATE_COUNTERS: np.uint64,
+    PER_STATE_DONES: np.uint8, PER_STATE_COUNTERS: np.uint64, PER_STATE_RANK_ORDER: np.uint32,
 }
 
 # every symbol include/gbper.h declares
@@ -209,14 +211,14 @@ class ReplayBuffer:
     """One GPU-resident prioritized replay buffer (device memory owned by libgbper)."""
 
     def __init__(self, capacity, state_dim, alpha=0.6, eps=1e-6, mode=PER_MODE_PROPORTIONAL,
-                 row_stride_out=None, seed=0):
+                 row_stride_out=None, seed=0, flags=0):
         import torch
         self.capacity = int(capacity)
         self.state_dim = int(state_dim)
         self.row_stride = int(row_stride_out if row_stride_out is not None else state_dim)
         self.mode = mode
         self.device = torch.device("cuda", torch.cuda.current_device())
-        cfg = per_config(float(alpha), float(eps), int(mode), self.row_stride, int(seed), 0, 0)
+        cfg = per_config(float(alpha), float(eps), int(mode), self.row_stride, int(seed), int(flags), 0)
         self._h = per_create(self.capacity, self.state_dim, cfg)
         self.nleaves = per_nleaves(self._h)[1]
 
@@ -306,7 +308,8 @@ class ReplayBuffer:
                      PER_STATE_STATES: self.capacity * self.state_dim,
                      PER_STATE_NEXT: self.capacity * self.state_dim,
                      PER_STATE_ACTIONS: self.capacity, PER_STATE_REWARDS: self.capacity,
-                     PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 4}[which] - first
+                     PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 4,
+                     PER_STATE_RANK_ORDER: self.size}[which] - first
         buf = np.empty(max(count, 1), dtype=dtype)
         s = per_read_state(self._h, which, first, count, buf.ctypes.data_as(ctypes.c_void_p),
                            _stream(stream))

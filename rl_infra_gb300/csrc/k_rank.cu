@@ -376,6 +376,249 @@ __global__ void __launch_bounds__(1024) k_build_cdf(double *cdf, unsigned long l
     }
 }
 
+// ------------------------------------------------------------------------------------------
+// Incremental order: between two samples only the slots that update and insertion wrote have a
+// new priority (they are marked, each listed once).  The new order is the previous order without
+// those slots, merged with them at their current priority -- the same sequence a full sort gives,
+// since the order is a total order on (key, slot).  One kernel, one 7168-entry tile of the
+// previous order per CTA:
+//   1. the CTA reads every marked entry (key, slot): it counts those at or below the previous
+//      tile's last entry (c0), keeps those up to its own last entry (its own marked entries,
+//      sorted in shared memory), and puts every marked slot in a shared-memory hash set;
+//   2. it drops its tile's marked slots (kept order unchanged) and publishes the kept count;
+//      the kept count of the earlier tiles comes from their published words (look-back, each
+//      wait bounded);
+//   3. a kept entry goes to (kept before it) + c0 + (own marked entries smaller than it);
+//   4. own marked entry j goes to c0 + j + (kept before the tile) + (tile's kept entries smaller);
+//   5. the last CTA to finish clears the marks.
+// ------------------------------------------------------------------------------------------
+constexpr int kMThreads = 1024;
+constexpr int kMItems = 7;
+constexpr int kMTile = kMThreads * kMItems;   // 7168
+constexpr unsigned kMHash = 2 * kMaxDirty;     // hash slots (at least twice the marks)
+constexpr unsigned kMFilter = 1u << 16;        // filter bits: slot mod 2^16 of every marked slot
+constexpr unsigned kEmptySlot = 0xffffffffu;
+constexpr size_t kMergeSmem = (size_t)kMTile * sizeof(unsigned long long)     // kept entries
+                              + (size_t)kMTile * 2 * sizeof(unsigned)           // the tile
+                              + (size_t)kMaxDirty * sizeof(unsigned long long)  // own marked entries
+                              + (size_t)kMHash * sizeof(unsigned)               // marked slots
+                              + (size_t)(kMFilter / 32) * sizeof(unsigned);     // their filter
+
+__device__ __forceinline__ unsigned long long pack_key_slot(unsigned key, unsigned slot)
+{
+    return ((unsigned long long)key << 32) | slot;
+}
+
+// entries of a[0, n) (ascending) that are < x
+__device__ __forceinline__ unsigned count_below(const unsigned long long *a, unsigned n, unsigned long long x)
+{
+    unsigned lo = 0, hi = n;
+    while (lo < hi) {
+        const unsigned mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ unsigned slot_hash(unsigned s, unsigned mask) { return (s * 2654435761u) & mask; }
+
+__global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, const unsigned *keys_in,
+                                                           const unsigned *vals_in, unsigned *keys_out,
+                                                           unsigned *vals_out, unsigned long long n_old,
+                                                           unsigned ntiles, DirtyRefs dirty, unsigned *mctl,
+                                                           unsigned long long *mstatus, unsigned *err)
+{
+    extern __shared__ unsigned long long s_m[];
+    unsigned long long *tk = s_m;                     // [kMTile] kept entries
+    unsigned long long *own = s_m + kMTile;           // [kMaxDirty] own marked entries, ascending
+    unsigned *s_tkey = reinterpret_cast<unsigned *>(own + kMaxDirty), *s_tval = s_tkey + kMTile;  // the tile
+    unsigned *hset = s_tval + kMTile;                 // [kMHash] marked slots
+    unsigned *filt = hset + kMHash;                   // [kMFilter / 32] bit (slot mod 2^16) of each
+    __shared__ unsigned s_tile, s_epoch, s_cnt, s_last, s_nown;
+    __shared__ unsigned s_wsum[kMThreads / 32];
+    __shared__ unsigned long long s_wpart[kMThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_release();
+    if (tid == 0) {
+        s_epoch = *(volatile unsigned *)&mctl[1];
+        s_cnt = *(volatile unsigned *)dirty.count;
+        s_tile = atomicAdd(&mctl[0], 1u);
+        s_nown = 0;
+    }
+    __syncthreads();
+    const unsigned tile = s_tile, epoch = s_epoch, cnt = s_cnt;
+    const bool over = cnt > kMaxDirty;   // more marks than listed: the order cannot be merged
+    const unsigned d = over ? 0u : cnt;
+    if (!over) {
+        unsigned hmask = 63;
+        while (hmask + 1 < 2 * d) hmask = 2 * hmask + 1;
+        for (unsigned i = tid; i <= hmask; i += kMThreads) hset[i] = kEmptySlot;
+        for (unsigned i = tid; i < kMFilter / 32; i += kMThreads) filt[i] = 0u;
+        // the tile of the previous order, coalesced
+        const unsigned long long t0 = (unsigned long long)tile * kMTile;
+        const int nt = (int)(n_old - t0 < (unsigned long long)kMTile ? n_old - t0 : (unsigned long long)kMTile);
+        for (int e = tid; e < nt; e += kMThreads) {
+            s_tkey[e] = keys_in[t0 + e];
+            s_tval[e] = vals_in[t0 + e];
+        }
+        const bool first = tile == 0, lastt = tile + 1 == ntiles;
+        const unsigned long long lo = first ? 0ull : pack_key_slot(keys_in[t0 - 1], vals_in[t0 - 1]);
+        __syncthreads();   // staged tile, cleared hash set and filter
+        const unsigned long long hi = lastt ? ~0ull : pack_key_slot(s_tkey[nt - 1], s_tval[nt - 1]);
+        // 1. the marked entries: count those at or below lo, keep those in (lo, hi], hash the slots
+        unsigned c0 = 0;
+        for (unsigned i = tid; i < d; i += kMThreads) {
+            const unsigned slot = dirty.list[i];
+            const unsigned long long x = pack_key_slot(key_of_raw(raw[slot]), slot);
+            if (!first && x <= lo) ++c0;
+            else if (lastt || x <= hi) own[atomicAdd(&s_nown, 1u)] = x;
+            atomicOr(&filt[(slot & (kMFilter - 1)) >> 5], 1u << (slot & 31));
+            unsigned h = slot_hash(slot, hmask);
+            for (unsigned probe = 0; probe <= hmask; ++probe) {
+                const unsigned prev = atomicCAS(&hset[h], kEmptySlot, slot);
+                if (prev == kEmptySlot || prev == slot) break;
+                h = (h + 1) & hmask;
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) c0 += __shfl_xor_sync(kFull, c0, o);
+        if (lane == 0) s_wsum[warp] = c0;
+        __syncthreads();
+        c0 = 0;
+        for (int w = 0; w < kMThreads / 32; ++w) c0 += s_wsum[w];
+        const unsigned nown = s_nown;
+        // sort the own marked entries (few: one warp's shuffles up to 32, else the block)
+        unsigned m2 = 1;
+        while (m2 < nown) m2 <<= 1;
+        if (m2 <= 32) {
+            if (warp == 0) {
+                unsigned long long x = (unsigned)lane < nown ? own[lane] : ~0ull;
+                for (unsigned k = 2; k <= 32; k <<= 1)
+                    for (unsigned j = k >> 1; j > 0; j >>= 1) {
+                        const unsigned long long y = __shfl_xor_sync(kFull, x, j);
+                        const bool lower = (lane & j) == 0, up = (lane & k) == 0;
+                        if (lower == up ? y < x : y > x) x = y;
+                    }
+                if ((unsigned)lane < nown) own[lane] = x;
+            }
+        } else {
+            for (unsigned i = nown + tid; i < m2; i += kMThreads) own[i] = ~0ull;
+            __syncthreads();
+            for (unsigned k = 2; k <= m2; k <<= 1)
+                for (unsigned j = k >> 1; j > 0; j >>= 1) {
+                    for (unsigned i = tid; i < m2; i += kMThreads) {
+                        const unsigned l = i ^ j;
+                        if (l > i) {
+                            const unsigned long long x = own[i], y = own[l];
+                            if ((i & k) == 0 ? x > y : x < y) {
+                                own[i] = y;
+                                own[l] = x;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+        }
+        __syncthreads();
+        // 2. this tile without its marked slots (thread t takes entries 7t .. 7t+6 of the staged
+        //    tile); kept count published, earlier tiles' summed
+        unsigned keep = 0;
+#pragma unroll
+        for (int i = 0; i < kMItems; ++i) {
+            const int e = tid * kMItems + i;
+            if (e < nt) {
+                const unsigned v = s_tval[e];
+                bool marked = false;
+                if ((filt[(v & (kMFilter - 1)) >> 5] >> (v & 31)) & 1u) {   // else certainly unmarked
+                    unsigned h = slot_hash(v, hmask);
+                    for (unsigned probe = 0; probe <= hmask; ++probe) {
+                        const unsigned q = hset[h];
+                        if (q == v) {
+                            marked = true;
+                            break;
+                        }
+                        if (q == kEmptySlot) break;
+                        h = (h + 1) & hmask;
+                    }
+                }
+                if (!marked) keep |= 1u << i;
+            }
+        }
+        const unsigned c = __popc(keep);
+        unsigned inc = c;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned x = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += x;
+        }
+        __syncthreads();   // every thread read c0's partials from s_wsum
+        if (lane == 31) s_wsum[warp] = inc;
+        __syncthreads();
+        unsigned before = 0, total = 0;
+        for (int w = 0; w < kMThreads / 32; ++w) {
+            const unsigned x = s_wsum[w];
+            if (w < warp) before += x;
+            total += x;
+        }
+        unsigned r = before + inc - c;   // this thread's first kept rank in the tile
+#pragma unroll
+        for (int i = 0; i < kMItems; ++i)
+            if ((keep >> i) & 1u) {
+                const int e = tid * kMItems + i;
+                tk[r++] = pack_key_slot(s_tkey[e], s_tval[e]);
+            }
+        volatile unsigned long long *vst = mstatus;
+        const unsigned want = epoch & 0x3FFFFFFFu;
+        if (tid == 0) vst[tile] = status_word(epoch, kFlagAgg, total);
+        unsigned long long part = 0;
+        bool ok = true;
+        for (unsigned q = tid; q < tile; q += kMThreads) {
+            unsigned long long w = vst[q];
+            int it = 0;
+            while (!word_ready(w, want) && ++it < kSpinLimit) w = vst[q];
+            if (it >= kSpinLimit) ok = false;
+            part += (unsigned)w;
+        }
+        if (!ok) atomicOr(err, kFlagTimeout);
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+        if (lane == 0) s_wpart[warp] = part;
+        __syncthreads();   // tk complete, s_wpart complete
+        unsigned long long pt = 0;
+        for (int w = 0; w < kMThreads / 32; ++w) pt += s_wpart[w];
+        // 3. kept entries in rank order (consecutive ranks land on nearly consecutive positions)
+        for (unsigned rr = tid; rr < total; rr += kMThreads) {
+            const unsigned long long x = tk[rr];
+            const unsigned long long pos = pt + rr + c0 + count_below(own, nown, x);
+            keys_out[pos] = (unsigned)(x >> 32);
+            vals_out[pos] = (unsigned)x;
+        }
+        // 4. own marked entries
+        for (unsigned j = tid; j < nown; j += kMThreads) {
+            const unsigned long long x = own[j];
+            const unsigned long long pos = c0 + j + pt + count_below(tk, total, x);
+            keys_out[pos] = (unsigned)(x >> 32);
+            vals_out[pos] = (unsigned)x;
+        }
+    } else if (tid == 0) {
+        atomicOr(err, kFlagRankStale);
+    }
+    // 5. the last CTA to finish clears the marks (every mark is listed) and the counters
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&mctl[2], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (unsigned i = tid; i < d; i += kMThreads) dirty.bits[dirty.list[i] >> 5] = 0u;
+        if (tid == 0) {
+            if (!over) *dirty.count = 0u;
+            mctl[0] = 0u;
+            mctl[2] = 0u;
+            mctl[1] = epoch + 1u;
+        }
+    }
+}
+
 constexpr size_t kStageSmem = 2ull * kTile * sizeof(unsigned);
 
 // Dynamic shared-memory limits of the sort kernels, set once per device (the sort is also
@@ -392,6 +635,8 @@ cudaError_t ensure_sort_attributes()
     std::lock_guard<std::mutex> lock(g_attr_mu);
     if (g_attr_done[dev]) return cudaSuccess;
     e = cudaFuncSetAttribute(k_rs_hist4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHistSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_rank_merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMergeSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_rs_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageSmem);
     if (e == cudaSuccess) g_attr_done[dev] = true;
@@ -412,6 +657,22 @@ cudaError_t init_rank_kernels(int carveout)
     return cudaSuccess;
 }
 
+unsigned long long rank_merge_tiles(unsigned long long capacity)
+{
+    return (capacity + kMTile - 1) / kMTile;
+}
+
+cudaError_t launch_rank_merge(RankWork &w, const unsigned *keys_in, const unsigned *vals_in, unsigned *keys_out,
+                              unsigned *vals_out, unsigned long long n_old, unsigned long long n_new, cudaStream_t st)
+{
+    (void)n_new;
+    cudaError_t e = ensure_sort_attributes();
+    if (e != cudaSuccess) return e;
+    const unsigned ntiles = (unsigned)std::max<unsigned long long>(rank_merge_tiles(n_old), 1);
+    return launch_pdl(k_rank_merge, ntiles, kMThreads, kMergeSmem, st, (const float *)w.raw, keys_in, vals_in,
+                      keys_out, vals_out, n_old, ntiles, w.dirty, w.merge_ctl, w.merge_status, w.err);
+}
+
 unsigned long long rank_tile_count(unsigned long long capacity)
 {
     return (capacity + kTile - 1) / kTile;
@@ -429,7 +690,8 @@ unsigned long long rank_status_words(unsigned long long capacity)
     return 4ull * (t + (t + kGroup - 1) / kGroup) * 256ull;
 }
 
-cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned **sorted, cudaStream_t st)
+cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned **sorted, cudaStream_t st,
+                             unsigned **keys_out)
 {
     const unsigned long long size = host_size;
     const unsigned ntiles = (unsigned)std::max<unsigned long long>(rank_tile_count(size), 1);
@@ -444,7 +706,7 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
     int cur = 0;
     for (int pass = 0; pass < 4; ++pass) {
         const float *raw = pass == 0 ? w.raw : nullptr;
-        unsigned *kout = pass == 3 ? nullptr : w.keys[cur];
+        unsigned *kout = pass == 3 && !keys_out ? nullptr : w.keys[cur];
         unsigned *vout = w.vals[cur];
         e = launch_pdl(k_rs_onesweep, ntiles, kThreads, kStageSmem, st, raw, kin, vin, kout, vout, size, pass, ntiles,
                        w.digit_hist, (unsigned long long *)w.status, w.sort_ctl, w.err);
@@ -454,6 +716,7 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
         cur ^= 1;
     }
     *sorted = const_cast<unsigned *>(vin);
+    if (keys_out) *keys_out = const_cast<unsigned *>(kin);
     return cudaSuccess;
 }
 

@@ -264,6 +264,7 @@ struct AddArgs {
     RingRefs r;
     float *raw_store;
     Ctl *ctl;
+    DirtyRefs dirty;   // rank mode: slots written are marked for the next order merge
     unsigned long long count, k0;
     const float *states, *next;
     const unsigned *actions;
@@ -449,6 +450,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                         a.t.L[s] = leaf;
                     } else {
                         a.raw_store[s] = raw;
+                        mark_dirty(a.dirty, s);
                     }
                 } else if (a.proportional) {
                     leaf = a.t.L[s];
@@ -672,6 +674,7 @@ struct UpdArgs {
     TreeRefs t;
     float *raw_store;
     Ctl *ctl;
+    DirtyRefs dirty;   // rank mode: slots written are marked for the next order merge
     const long long *idx;
     const float *td;
     unsigned B;
@@ -1149,7 +1152,10 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 if (mine && (31 - __clz(peers)) == lane) {  // the last lane of this chunk for the leaf
                     const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
                     if (a.proportional) a.t.L[i] = leaf_of(raw, a.lp);
-                    else a.raw_store[i] = raw;
+                    else {
+                        a.raw_store[i] = raw;
+                        mark_dirty(a.dirty, (unsigned long long)i);
+                    }
                 }
                 __syncwarp();
             }
@@ -1186,6 +1192,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 warp_climb_regs<W>(a.t, U, shift, lane, base, lane < U ? li : 0u, raw, a.lp, s_lp);
             } else if (lane < U) {
                 a.raw_store[base + li] = raw;
+                mark_dirty(a.dirty, base + li);
             }
         } else {
             int m2 = 2;
@@ -1218,6 +1225,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                         wl.rend[u] = u + 1;
                     } else {
                         a.raw_store[leaf] = raw;
+                        mark_dirty(a.dirty, leaf);
                     }
                 }
                 U += __popc(bal);
@@ -1449,7 +1457,8 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
                        unsigned long long count, const float *states, const float *next,
                        const unsigned *actions, const float *rewards, const unsigned char *dones,
                        const float *prio, double alpha, double eps, bool proportional,
-                       unsigned long long host_cursor, int num_sms, cudaStream_t st)
+                       unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
+                       bool *marked, cudaStream_t st)
 {
     (void)host_cursor;
     AddArgs a;
@@ -1483,6 +1492,8 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     if (ncopy == 0) ncopy = 1;
 
     const bool incremental = cnt + bsz <= C && cnt * 8 <= t.n && cnt <= (1ull << 18);
+    if (marked) *marked = incremental;
+    a.dirty = incremental ? dirty : DirtyRefs{nullptr, nullptr, nullptr};
     if (incremental) {
         a.ntree = (unsigned)(cnt / bsz + 3);
         a.ncopy = ncopy;
@@ -1508,13 +1519,14 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
 
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
-                          bool proportional, int num_sms, cudaStream_t st)
+                          bool proportional, int num_sms, const DirtyRefs &dirty, cudaStream_t st)
 {
     (void)num_sms;
     UpdArgs a;
     a.t = t;
     a.raw_store = raw_store;
     a.ctl = ctl;
+    a.dirty = dirty;
     a.idx = idx;
     a.td = td;
     a.B = B;

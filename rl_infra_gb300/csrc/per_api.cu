@@ -37,6 +37,13 @@ struct per_buffer {
     uint8_t *dones = nullptr;
     Ctl *ctl = nullptr;
     uint64_t host_size = 0, host_cursor = 0;
+    // rank mode: the order kept between samples (keys/vals[order_cur], order_size entries) and
+    // an upper bound on the slots written since (each insertion or update adds its count)
+    bool order_valid = false, always_resort = false;
+    int order_cur = 0;
+    uint64_t order_size = 0, dirty_bound = 0;
+    unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
+    uint64_t dirty_nwords = 0;
     std::string err;
 };
 
@@ -84,6 +91,7 @@ void free_all(per_buffer *h)
 {
     void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
                     h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
+                    h->dirty_words, h->rank.merge_status,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -97,6 +105,37 @@ bool alloc(T **p, uint64_t count)
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Rank mode: bring the slot order (keys/vals[order_cur]) up to date for the filled slots.  When
+// the order exists and at most kMaxDirty slots (and no more than an eighth of them) were written
+// since, the written slots are merged into it; otherwise every slot is sorted again and the
+// marks are cleared.  The decision uses host-side counts only (no synchronisation).
+cudaError_t rank_order(per_buffer *h, cudaStream_t st)
+{
+    RankWork &w = h->rank;
+    cudaError_t e;
+    if (!h->always_resort && h->order_valid && h->dirty_bound <= kMaxDirty && h->dirty_bound * 8 <= h->host_size) {
+        if (h->dirty_bound > 0) {
+            const int c = h->order_cur;
+            e = launch_rank_merge(w, w.keys[c], w.vals[c], w.keys[c ^ 1], w.vals[c ^ 1], h->order_size,
+                                  h->host_size, st);
+            if (e != cudaSuccess) return e;
+            h->order_cur = c ^ 1;
+        }
+    } else {
+        unsigned *sorted = nullptr, *keys = nullptr;
+        e = launch_rank_sort(w, h->host_size, &sorted, st, &keys);
+        if (e != cudaSuccess) return e;
+        h->order_cur = sorted == w.vals[1] ? 1 : 0;
+        e = cudaMemsetAsync(h->dirty_words, 0, h->dirty_nwords * sizeof(unsigned), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(w.dirty.count, 0, sizeof(unsigned), st);
+        if (e != cudaSuccess) return e;
+    }
+    h->order_valid = true;
+    h->order_size = h->host_size;
+    h->dirty_bound = 0;
+    return cudaSuccess;
+}
 
 // Kernel attributes are per device: set them the first time a buffer is created on a device.
 // The carveout (percent of the unified L1/shared array given to shared memory) is the same for
@@ -158,7 +197,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: eps must be finite and > 0");
     if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK)
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown mode");
-    if (c.flags != 0) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: flags must be 0");
+    if (c.flags & ~PER_FLAG_RANK_RESORT) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown flags");
     if (c.mode == PER_MODE_PROPORTIONAL && !((float)std::pow(c.eps, c.alpha) >= 1.17549435e-38f))
         return fail(nullptr, PER_ERR_INVALID_ARG,
                     "per_create: eps^alpha underflows binary32; a leaf of 0 would read as an empty slot");
@@ -188,6 +227,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     h->eps = c.eps;
     h->mode = c.mode;
     h->seed = c.seed;
+    h->always_resort = (c.flags & PER_FLAG_RANK_RESORT) != 0;
 
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
@@ -200,6 +240,15 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         h->rank.sort_ctl = h->rank.digit_hist + 4 * 256;
         h->rank.capacity = capacity;
         h->rank.num_sms = h->num_sms;
+        h->dirty_nwords = capacity / 32 + 1;
+        ok = ok && alloc(&h->dirty_words, h->dirty_nwords + kMaxDirty + 8) &&
+             alloc(&h->rank.merge_status, rank_merge_tiles(capacity));
+        if (ok) {
+            h->rank.dirty.bits = h->dirty_words;
+            h->rank.dirty.list = h->dirty_words + h->dirty_nwords;
+            h->rank.merge_ctl = h->rank.dirty.list + kMaxDirty;   // [0..2] merge, [3] marked count
+            h->rank.dirty.count = h->rank.merge_ctl + 3;
+        }
     }
     ok = ok && alloc(&h->states, capacity * (uint64_t)state_dim) && alloc(&h->next, capacity * (uint64_t)state_dim) &&
          alloc(&h->actions, capacity) && alloc(&h->rewards, capacity) && alloc(&h->dones, capacity);
@@ -222,6 +271,10 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (e == cudaSuccess && h->rank.status)
         e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
     if (e == cudaSuccess && h->rank.digit_hist) e = cudaMemset(h->rank.digit_hist, 0, (4 * 256 + 16) * sizeof(unsigned));
+    if (e == cudaSuccess && h->dirty_words)
+        e = cudaMemset(h->dirty_words, 0, (h->dirty_nwords + kMaxDirty + 8) * sizeof(unsigned));
+    if (e == cudaSuccess && h->rank.merge_status)
+        e = cudaMemset(h->rank.merge_status, 0, rank_merge_tiles(capacity) * sizeof(unsigned long long));
     if (h->rank.raw) h->rank.err = &h->ctl->err_flags;
     if (e == cudaSuccess && h->rank.cdf) e = launch_build_cdf(h->rank.cdf, capacity, h->alpha, 0);
     if (e == cudaSuccess && state_dim) e = cudaMemset(h->states, 0, capacity * (uint64_t)state_dim * sizeof(float));
@@ -268,11 +321,16 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
         (d_raw_prio && reinterpret_cast<uintptr_t>(d_raw_prio) % 4))
         return fail(h, PER_ERR_INVALID_ARG, "per_add: scalar arrays must be 4-byte aligned");
     if (count > (1ull << 40)) return fail(h, PER_ERR_INVALID_ARG, "per_add: count too large");
+    bool marked = false;
     const cudaError_t e = launch_add(tree_of(h), ring_of(h), h->rank.raw, h->ctl, count, d_states, d_next,
                                      d_actions, d_rewards, d_dones, d_raw_prio, h->alpha, h->eps,
                                      h->mode == PER_MODE_PROPORTIONAL, h->host_cursor, h->num_sms,
-                                     as_stream(stream));
+                                     h->rank.dirty, &marked, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "per_add launch");
+    if (h->mode == PER_MODE_RANK) {
+        if (marked) h->dirty_bound += count;
+        else h->order_valid = false;   // rewritten in bulk, unmarked: the next sample sorts again
+    }
     h->host_cursor = (h->host_cursor + count) % h->capacity;
     h->host_size = std::min<uint64_t>(h->host_size + count, h->capacity);
     return PER_OK;
@@ -304,8 +362,8 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
     if (h->mode == PER_MODE_PROPORTIONAL) {
         e = launch_sample_prop(tree_of(h), ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms, as_stream(stream));
     } else {
-        unsigned *sorted = nullptr;
-        e = launch_rank_sort(h->rank, h->host_size, &sorted, as_stream(stream));
+        e = rank_order(h, as_stream(stream));
+        unsigned *sorted = h->rank.vals[h->order_cur];
         if (e == cudaSuccess)
             e = launch_sample_rank(h->rank, sorted, ring_of(h), h->ctl, B, beta, h->alpha, h->seed, o,
                                    h->num_sms, as_stream(stream));
@@ -325,8 +383,9 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
         return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: misaligned input");
     const cudaError_t e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, reinterpret_cast<const long long *>(d_idx),
                                         d_td, h->alpha, h->eps, h->mode == PER_MODE_PROPORTIONAL, h->num_sms,
-                                        as_stream(stream));
+                                        h->rank.dirty, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
+    if (h->mode == PER_MODE_RANK) h->dirty_bound += B;
     return PER_OK;
 }
 
@@ -418,6 +477,13 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
     case PER_STATE_ACTIONS: src = h->actions; elems = h->capacity; esz = 4; break;
     case PER_STATE_REWARDS: src = h->rewards; elems = h->capacity; esz = 4; break;
     case PER_STATE_DONES: src = h->dones; elems = h->capacity; esz = 1; break;
+    case PER_STATE_RANK_ORDER:
+        if (h->mode != PER_MODE_RANK || !h->order_valid)
+            return fail(h, PER_ERR_INVALID_ARG, "per_read_state: no rank order yet (rank mode, after a sample)");
+        src = h->rank.vals[h->order_cur];
+        elems = h->order_size;
+        esz = 4;
+        break;
     case PER_STATE_COUNTERS: {
         if (first + count > 4) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
         Ctl c;

@@ -57,6 +57,29 @@ __device__ __forceinline__ unsigned long long take_call_number(Ctl *c)
 
 constexpr unsigned kFlagBadIndex = 1u;
 constexpr unsigned kFlagTimeout = 2u;
+constexpr unsigned kFlagRankStale = 4u;
+
+// ---- rank mode: slots whose priority changed since the order was last made ------------------
+// Update and insertion mark every slot they write in a bitmap and, the first time, append it to
+// a list of at most kMaxDirty slots; the next sample merges them into the previous order instead
+// of sorting every slot again (k_rank.cu).  Null bits: nothing is marked.
+constexpr unsigned kMaxDirty = 4096;
+
+struct DirtyRefs {
+    unsigned *bits;    // [capacity / 32 + 1]
+    unsigned *list;    // [kMaxDirty]
+    unsigned *count;   // slots marked (the list holds the first kMaxDirty)
+};
+
+__device__ __forceinline__ void mark_dirty(const DirtyRefs &d, unsigned long long slot)
+{
+    if (!d.bits) return;
+    const unsigned bit = 1u << (slot & 31);
+    if (!(atomicOr(&d.bits[slot >> 5], bit) & bit)) {
+        const unsigned i = atomicAdd(d.count, 1u);
+        if (i < kMaxDirty) d.list[i] = (unsigned)slot;
+    }
+}
 
 // ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) -----------------------------------
 // Round: (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0)) with
@@ -145,15 +168,18 @@ struct RingRefs {
 // Host launchers (each returns the launch's cudaError_t).
 cudaError_t launch_fill_mins(float *M, unsigned long long n, cudaStream_t st);
 
+// *marked (may be null) tells whether the insertion marked its slots (the incremental path) or
+// rewrote them in bulk without marks.
 cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, Ctl *ctl,
                        unsigned long long count, const float *states, const float *next,
                        const unsigned *actions, const float *rewards, const unsigned char *dones,
                        const float *prio, double alpha, double eps, bool proportional,
-                       unsigned long long host_cursor, int num_sms, cudaStream_t st);
+                       unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
+                       bool *marked, cudaStream_t st);
 
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
-                          bool proportional, int num_sms, cudaStream_t st);
+                          bool proportional, int num_sms, const DirtyRefs &dirty, cudaStream_t st);
 
 struct SampleOut {
     long long *idx;
@@ -180,6 +206,10 @@ struct RankWork {
     unsigned *err;                 // device error word (PER_DEVFLAG_TIMEOUT)
     unsigned long long capacity;
     int num_sms;                   // grid of the histogram kernel
+    // kept between calls by a buffer (all null for the allocation-free entry point):
+    DirtyRefs dirty;               // slots changed since the order was made
+    unsigned *merge_ctl;           // [8]: [0] tile counter, [1] epoch, [2] arrivals
+    unsigned long long *merge_status;  // [merge tiles] look-back words of the merge
 };
 
 // Words of RankWork scratch the sort needs for `capacity` keys (beyond keys and values).
@@ -189,9 +219,19 @@ cudaError_t launch_build_cdf(double *cdf, unsigned long long capacity, double al
                              cudaStream_t st);
 
 // Sorts the `size` filled slots by raw priority descending, ties by slot ascending, leaving
-// the slot order in *sorted (a pointer into w.vals).
+// the slot order in *sorted (a pointer into w.vals).  With keys_out non-null the last pass also
+// writes the sorted keys there (*keys_out = a pointer into w.keys).
 cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned **sorted,
-                             cudaStream_t st);
+                             cudaStream_t st, unsigned **keys_out = nullptr);
+
+// Brings the order up to date after at most kMaxDirty marked slots: the previous order
+// (keys_in/vals_in, n_old entries) without the marked slots, merged with the marked slots at
+// their current priority, into keys_out/vals_out (n_new entries); clears the marks.
+cudaError_t launch_rank_merge(RankWork &w, const unsigned *keys_in, const unsigned *vals_in,
+                              unsigned *keys_out, unsigned *vals_out, unsigned long long n_old,
+                              unsigned long long n_new, cudaStream_t st);
+
+unsigned long long rank_merge_tiles(unsigned long long capacity);
 
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,
                                Ctl *ctl, unsigned B, float beta, double alpha,

@@ -217,6 +217,46 @@ def test_rank_small(cap, fill):
     p.close()
 
 
+def _assert_rank_order(p):
+    got = p.gpu.read_state(capi.PER_STATE_RANK_ORDER)
+    want = p.orc.rank_order()
+    assert got.shape == want.shape
+    assert np.array_equal(got, want), f"rank order differs at {np.flatnonzero(got != want)[:8]}"
+
+
+@pytest.mark.parametrize("cap,fill,flags", [(50000, 50000, 0), (30000, 20000, 0),
+                                            (30000, 20000, capi.PER_FLAG_RANK_RESORT)])
+def test_rank_order_kept_between_samples(cap, fill, flags):
+    """The slot order after each sample equals the oracle's full sort, whether it was merged
+    from the previous order (a few written slots) or sorted again (many): updates with repeated
+    indices and equal priorities, ring inserts that overwrite slots or grow the filled range,
+    and one large update that forces a full sort."""
+    w = _small("rank", capacity=cap, state_dim=2, row_stride=4)
+    g = wl.rng(21, cap)
+    p = Pair(cap, 2, 4, 0.7, 1e-6, 1, seed=12, flags=flags)
+    prefill(p, w, g, count=fill, chunk=fill)
+    p.sample(512, 0.5)
+    _assert_rank_order(p)
+    for rnd in range(10):
+        size = int(p.orc.size)
+        idx = g.integers(0, size, 600)
+        idx[:150] = idx[150:300]                      # repeated indices: the last writer wins
+        td = wl.td_errors(g, len(idx))
+        td[300:340] = 0.25                            # equal priorities: ties by slot
+        if rnd == 6:
+            idx = g.integers(0, size, size // 4)      # more than an eighth: sorted again
+            td = wl.td_errors(g, len(idx))
+        p.update(idx, td)
+        if rnd % 3 == 1:
+            rows = wl.transitions(g, 300, w)
+            p.add(rows, wl.raw_priorities(g, 300, w.prio))
+        p.sample(512, 0.5)
+        _assert_rank_order(p)
+    p.check_counters()
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
 @pytest.mark.slow
 def test_rank_more_than_a_million_slots():
     """3M slots: more than 256 sort tiles, so the look-back reads group totals in rounds."""
