@@ -40,13 +40,17 @@ constexpr int kHistCopy = 32 * kHistStride;
 constexpr size_t kHistSmem = 4ull * kHistCopy * sizeof(unsigned);   // 131,584 bytes
 
 __global__ void __launch_bounds__(kHistThreads) k_rs_hist4(const float *raw, unsigned long long size,
-                                                            unsigned *digit_hist, unsigned *sort_ctl)
+                                                            unsigned *digit_hist, unsigned *sort_ctl,
+                                                            unsigned *order_cur)
 {
     extern __shared__ unsigned s_h[];   // [4 digits][32 lanes][257]
     for (int i = threadIdx.x; i < 4 * kHistCopy; i += blockDim.x) s_h[i] = 0;
     pdl_wait();
     pdl_release();
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&sort_ctl[4], 1u);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        atomicAdd(&sort_ctl[4], 1u);
+        if (order_cur) *order_cur = 1u;   // the four passes leave the order in keys[1] / vals[1]
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
@@ -423,9 +427,8 @@ __device__ __forceinline__ unsigned count_below(const unsigned long long *a, uns
 
 __device__ __forceinline__ unsigned slot_hash(unsigned s, unsigned mask) { return (s * 2654435761u) & mask; }
 
-__global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, const unsigned *keys_in,
-                                                           const unsigned *vals_in, unsigned *keys_out,
-                                                           unsigned *vals_out, unsigned long long n_old,
+__global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsigned *keys0, unsigned *keys1,
+                                                           unsigned *vals0, unsigned *vals1, unsigned long long n_old,
                                                            unsigned ntiles, DirtyRefs dirty, unsigned *mctl,
                                                            unsigned long long *mstatus, unsigned *err)
 {
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, cons
     unsigned *s_tkey = reinterpret_cast<unsigned *>(own + kMaxDirty), *s_tval = s_tkey + kMTile;  // the tile
     unsigned *hset = s_tval + kMTile;                 // [kMHash] marked slots
     unsigned *filt = hset + kMHash;                   // [kMFilter / 32] bit (slot mod 2^16) of each
-    __shared__ unsigned s_tile, s_epoch, s_cnt, s_last, s_nown;
+    __shared__ unsigned s_tile, s_epoch, s_cnt, s_last, s_nown, s_cur;
     __shared__ unsigned s_wsum[kMThreads / 32];
     __shared__ unsigned long long s_wpart[kMThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -444,11 +447,14 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, cons
     if (tid == 0) {
         s_epoch = *(volatile unsigned *)&mctl[1];
         s_cnt = *(volatile unsigned *)dirty.count;
+        s_cur = *(volatile unsigned *)&mctl[4] & 1u;   // which buffer pair holds the order
         s_tile = atomicAdd(&mctl[0], 1u);
         s_nown = 0;
     }
     __syncthreads();
     const unsigned tile = s_tile, epoch = s_epoch, cnt = s_cnt;
+    const unsigned *keys_in = s_cur ? keys1 : keys0, *vals_in = s_cur ? vals1 : vals0;
+    unsigned *keys_out = s_cur ? keys0 : keys1, *vals_out = s_cur ? vals0 : vals1;
     const bool over = cnt > kMaxDirty;   // more marks than listed: the order cannot be merged
     const unsigned d = over ? 0u : cnt;
     if (!over) {
@@ -611,7 +617,10 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, cons
         __threadfence();
         for (unsigned i = tid; i < d; i += kMThreads) dirty.bits[dirty.list[i] >> 5] = 0u;
         if (tid == 0) {
-            if (!over) *dirty.count = 0u;
+            if (!over) {
+                *dirty.count = 0u;
+                mctl[4] = s_cur ^ 1u;   // the merged order is in the other pair
+            }
             mctl[0] = 0u;
             mctl[2] = 0u;
             mctl[1] = epoch + 1u;
@@ -662,15 +671,13 @@ unsigned long long rank_merge_tiles(unsigned long long capacity)
     return (capacity + kMTile - 1) / kMTile;
 }
 
-cudaError_t launch_rank_merge(RankWork &w, const unsigned *keys_in, const unsigned *vals_in, unsigned *keys_out,
-                              unsigned *vals_out, unsigned long long n_old, unsigned long long n_new, cudaStream_t st)
+cudaError_t launch_rank_merge(RankWork &w, unsigned long long n_old, cudaStream_t st)
 {
-    (void)n_new;
     cudaError_t e = ensure_sort_attributes();
     if (e != cudaSuccess) return e;
     const unsigned ntiles = (unsigned)std::max<unsigned long long>(rank_merge_tiles(n_old), 1);
-    return launch_pdl(k_rank_merge, ntiles, kMThreads, kMergeSmem, st, (const float *)w.raw, keys_in, vals_in,
-                      keys_out, vals_out, n_old, ntiles, w.dirty, w.merge_ctl, w.merge_status, w.err);
+    return launch_pdl(k_rank_merge, ntiles, kMThreads, kMergeSmem, st, (const float *)w.raw, w.keys[0], w.keys[1],
+                      w.vals[0], w.vals[1], n_old, ntiles, w.dirty, w.merge_ctl, w.merge_status, w.err);
 }
 
 unsigned long long rank_tile_count(unsigned long long capacity)
@@ -700,7 +707,7 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
     const unsigned hgrid = (unsigned)std::min<unsigned long long>((size + kHistThreads - 1) / kHistThreads,
                                                                   (unsigned long long)std::max(w.num_sms, 1));
     e = launch_pdl(k_rs_hist4, std::max(hgrid, 1u), kHistThreads, kHistSmem, st, (const float *)w.raw, size,
-                   w.digit_hist, w.sort_ctl);
+                   w.digit_hist, w.sort_ctl, w.merge_ctl ? w.merge_ctl + 4 : (unsigned *)nullptr);
     if (e != cudaSuccess) return e;
     const unsigned *kin = nullptr, *vin = nullptr;
     int cur = 0;

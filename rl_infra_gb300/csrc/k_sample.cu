@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
 // ------------------------------------------------------------------------------------------
 struct RankSampleArgs {
     const double *cdf;
-    const unsigned *sorted;
+    const unsigned *sorted;          // the slot order, unless order_cur is set:
+    const unsigned *vals[2];         //   then vals[*order_cur]
+    const unsigned *order_cur;
     RingRefs r;
     Ctl *ctl;
     unsigned B;
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
     __shared__ unsigned long long s_call;
     pdl_wait();
     pdl_release();
+    const unsigned *sorted = a.order_cur ? a.vals[*a.order_cur & 1u] : a.sorted;
     const unsigned long long size = a.ctl->size;
     if (threadIdx.x == 0) {
         s_call = take_call_number(a.ctl);
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
             hi = pf;  // answer in [lo, pf]; pf itself satisfies the predicate
         }
         unsigned long long r = ans > size ? size : ans;
-        const unsigned long long slot = a.sorted[r - 1];
+        const unsigned long long slot = sorted[r - 1];
         if (lane == 0) {
             a.o.idx[j] = (long long)slot;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn((float)r, fsize), a.ab);
@@ -382,6 +385,9 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
     RankSampleArgs a;
     a.cdf = w.cdf;
     a.sorted = sorted;
+    a.vals[0] = w.vals[0];
+    a.vals[1] = w.vals[1];
+    a.order_cur = w.merge_ctl ? w.merge_ctl + 4 : nullptr;
     a.r = r;
     a.ctl = ctl;
     a.B = B;

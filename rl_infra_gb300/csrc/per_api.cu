@@ -37,10 +37,9 @@ struct per_buffer {
     uint8_t *dones = nullptr;
     Ctl *ctl = nullptr;
     uint64_t host_size = 0, host_cursor = 0;
-    // rank mode: the order kept between samples (keys/vals[order_cur], order_size entries) and
+    // rank mode: the order kept between samples (keys/vals[merge_ctl[4]], order_size entries) and
     // an upper bound on the slots written since (each insertion or update adds its count)
     bool order_valid = false, always_resort = false;
-    int order_cur = 0;
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
     uint64_t dirty_nwords = 0;
@@ -106,7 +105,7 @@ bool alloc(T **p, uint64_t count)
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Rank mode: bring the slot order (keys/vals[order_cur]) up to date for the filled slots.  When
+// Rank mode: bring the slot order (keys/vals[merge_ctl[4]]) up to date for the filled slots.  When
 // the order exists and at most kMaxDirty slots (and no more than an eighth of them) were written
 // since, the written slots are merged into it; otherwise every slot is sorted again and the
 // marks are cleared.  The decision uses host-side counts only (no synchronisation).
@@ -116,17 +115,13 @@ cudaError_t rank_order(per_buffer *h, cudaStream_t st)
     cudaError_t e;
     if (!h->always_resort && h->order_valid && h->dirty_bound <= kMaxDirty && h->dirty_bound * 8 <= h->host_size) {
         if (h->dirty_bound > 0) {
-            const int c = h->order_cur;
-            e = launch_rank_merge(w, w.keys[c], w.vals[c], w.keys[c ^ 1], w.vals[c ^ 1], h->order_size,
-                                  h->host_size, st);
+            e = launch_rank_merge(w, h->order_size, st);
             if (e != cudaSuccess) return e;
-            h->order_cur = c ^ 1;
         }
     } else {
         unsigned *sorted = nullptr, *keys = nullptr;
         e = launch_rank_sort(w, h->host_size, &sorted, st, &keys);
         if (e != cudaSuccess) return e;
-        h->order_cur = sorted == w.vals[1] ? 1 : 0;
         e = cudaMemsetAsync(h->dirty_words, 0, h->dirty_nwords * sizeof(unsigned), st);
         if (e == cudaSuccess) e = cudaMemsetAsync(w.dirty.count, 0, sizeof(unsigned), st);
         if (e != cudaSuccess) return e;
@@ -363,7 +358,7 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
         e = launch_sample_prop(tree_of(h), ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms, as_stream(stream));
     } else {
         e = rank_order(h, as_stream(stream));
-        unsigned *sorted = h->rank.vals[h->order_cur];
+        const unsigned *sorted = h->rank.vals[1];   // unused: the kernel reads the order's buffer
         if (e == cudaSuccess)
             e = launch_sample_rank(h->rank, sorted, ring_of(h), h->ctl, B, beta, h->alpha, h->seed, o,
                                    h->num_sms, as_stream(stream));
@@ -480,7 +475,14 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
     case PER_STATE_RANK_ORDER:
         if (h->mode != PER_MODE_RANK || !h->order_valid)
             return fail(h, PER_ERR_INVALID_ARG, "per_read_state: no rank order yet (rank mode, after a sample)");
-        src = h->rank.vals[h->order_cur];
+        {
+            unsigned cur = 0;
+            cudaError_t e = cudaMemcpyAsync(&cur, h->rank.merge_ctl + 4, sizeof(cur), cudaMemcpyDeviceToHost,
+                                            as_stream(stream));
+            if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+            if (e != cudaSuccess) return cuda_fail(h, e, "per_read_state");
+            src = h->rank.vals[cur & 1u];
+        }
         elems = h->order_size;
         esz = 4;
         break;

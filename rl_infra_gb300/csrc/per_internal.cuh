@@ -208,7 +208,8 @@ struct RankWork {
     int num_sms;                   // grid of the histogram kernel
     // kept between calls by a buffer (all null for the allocation-free entry point):
     DirtyRefs dirty;               // slots changed since the order was made
-    unsigned *merge_ctl;           // [8]: [0] tile counter, [1] epoch, [2] arrivals
+    unsigned *merge_ctl;           // [8]: [0] tile counter, [1] epoch, [2] arrivals, [3] marked count,
+                                   // [4] which of keys/vals[0|1] holds the current order
     unsigned long long *merge_status;  // [merge tiles] look-back words of the merge
 };
 
@@ -225,14 +226,14 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
                              cudaStream_t st, unsigned **keys_out = nullptr);
 
 // Brings the order up to date after at most kMaxDirty marked slots: the previous order
-// (keys_in/vals_in, n_old entries) without the marked slots, merged with the marked slots at
-// their current priority, into keys_out/vals_out (n_new entries); clears the marks.
-cudaError_t launch_rank_merge(RankWork &w, const unsigned *keys_in, const unsigned *vals_in,
-                              unsigned *keys_out, unsigned *vals_out, unsigned long long n_old,
-                              unsigned long long n_new, cudaStream_t st);
+// (n_old entries, in the buffer pair merge_ctl[4] names) without the marked slots, merged with
+// the marked slots at their current priority, into the other pair; flips merge_ctl[4] and
+// clears the marks.  The full sort sets merge_ctl[4] = 1.
+cudaError_t launch_rank_merge(RankWork &w, unsigned long long n_old, cudaStream_t st);
 
 unsigned long long rank_merge_tiles(unsigned long long capacity);
 
+// The slot order is w.vals[merge_ctl[4]] (read on the device), or `sorted` when w.merge_ctl is null.
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,
                                Ctl *ctl, unsigned B, float beta, double alpha,
                                unsigned long long seed, const SampleOut &o, int num_sms,

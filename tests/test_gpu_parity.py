@@ -4,6 +4,8 @@ within 1e-6 relative (built to be bit-identical), IS weights within 1e-5 relativ
 fields byte-exact."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -283,6 +285,65 @@ def test_rank_ties_keep_slot_order():
     p.add(rows, prio)
     for _ in range(3):
         p.sample(1024, 0.5)
+    p.close()
+
+
+# -- CUDA graphs: a captured round replays with the device-resident counters -------------------
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_graph_replayed_rounds(mode):
+    """Insert + sample + update captured once per staging offset as CUDA graphs and replayed:
+    every replay inserts at the device cursor, draws a fresh batch (device call counter) and, in
+    rank mode, merges into whichever buffer holds the order -- each replay's batch and the final
+    state equal the oracle stepping the same rounds."""
+    cap, d, dp, B, I, NO = 4096, 8, 8, 64, 256, 3
+    w = _small("tiny", capacity=cap, state_dim=d, row_stride=dp, mode=mode)
+    g = wl.rng(31, mode)
+    p = Pair(cap, d, dp, 0.6, 1e-6, mode, seed=5)
+    prefill(p, w, g, count=cap, chunk=cap)
+    _, want = p.sample(B, 0.5)                       # rank mode: the first order, sorted eagerly
+    p.update(want["idx"], wl.td_errors(g, B))
+    L, h = capi.load(), p.gpu._h
+    rows = [wl.transitions(g, I, w) for _ in range(NO)]
+    dev_rows = [{k: dev(v) for k, v in r.items()} for r in rows]
+    idx_sets = [g.integers(0, cap, B).astype(np.int64) for _ in range(NO)]
+    td_sets = [wl.td_errors(g, B) for _ in range(NO)]
+    d_idx = [dev(x) for x in idx_sets]
+    d_td = [dev(x) for x in td_sets]
+    out = p.gpu.alloc_batch(B)
+    optr = [out[k].data_ptr() for k in ("idx", "w", "states", "next_states", "actions", "rewards", "dones")]
+    graphs = []
+    for o in range(NO):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            r = dev_rows[o]
+            assert L.per_add(h, I, r["states"].data_ptr(), r["next_states"].data_ptr(), r["actions"].data_ptr(),
+                             r["rewards"].data_ptr(), r["dones"].data_ptr(), None, cs) == 0
+            assert L.per_sample(h, B, ctypes.c_float(0.5), *optr, cs) == 0
+            assert L.per_update_priorities(h, B, d_idx[o].data_ptr(), d_td[o].data_ptr(), cs) == 0
+        graphs.append(gr)
+    for rnd in range(4 * NO):
+        o = rnd % NO
+        graphs[o].replay()
+        torch.cuda.synchronize()
+        r = rows[o]
+        p.orc.add(r["states"], r["next_states"], r["actions"], r["rewards"], r["dones"], None, count=I)
+        want = p.orc.sample(B, 0.5, gather=True)
+        gi = out["idx"].cpu().numpy()
+        harness.assert_indices(gi, want["idx"], want["near"])
+        same = gi == want["idx"]
+        harness.assert_weights_close(out["w"].cpu().numpy(), want["w"], mask=same)
+        for k in ("states", "next_states", "rewards", "dones"):
+            assert np.array_equal(out[k].cpu().numpy()[same].view(np.uint8), want[k][same].view(np.uint8)), k
+        if mode == 1:
+            _assert_rank_order(p)                    # the order this replay's sample used
+        p.orc.update(idx_sets[o], td_sets[o])
+    torch.cuda.synchronize()
+    if mode == 0:
+        p.check_tree()
+    p.check_counters()
+    assert p.gpu.status_device() == 0
     p.close()
 
 
