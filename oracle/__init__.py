@@ -22,6 +22,7 @@ _lib = None
 
 PROPORTIONAL = 0
 RANK = 1
+UNIFORM = 2
 
 
 def build(force: bool = False) -> str:

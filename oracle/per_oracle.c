@@ -42,6 +42,10 @@
  *   R11 rank mode: rank 1 is the largest raw priority, ties by ascending index;
  *      P(r) = r^-alpha / sum_{k<=size} k^-alpha; w = (r / size)^(alpha * beta).
  *   R12 an update index outside [0, size) is skipped and counted.
+ *   R24 uniform mode (the plain replay the pages' PER replaces): every filled slot weighs 1, so
+ *      the stratified draw j (stream tag 2) takes mass (j + u_j) * (size / B) and slot
+ *      floor(mass), weight 1; insertion stores rows (and follows the running maximum as in the
+ *      other modes); updates change nothing.
  */
 #include "per_oracle.h"
 
@@ -186,7 +190,7 @@ orc_per *orc_create(uint64_t capacity, uint32_t state_dim, uint32_t row_stride_o
 {
     if (capacity == 0 || capacity > (1ull << 40) || row_stride_out < state_dim)
         return NULL;
-    if (!(eps > 0.0) || !(alpha >= 0.0) || mode > ORC_RANK)
+    if (!(eps > 0.0) || !(alpha >= 0.0) || mode > ORC_UNIFORM)
         return NULL;
     orc_per *o = (orc_per *)calloc(1, sizeof(orc_per));
     if (!o)
@@ -211,7 +215,7 @@ orc_per *orc_create(uint64_t capacity, uint32_t state_dim, uint32_t row_stride_o
         ok = o->L && o->S && o->M;
         if (ok)
             rebuild_all(o);
-    } else {
+    } else if (mode == ORC_RANK) {
         o->raw = (float *)calloc(capacity, sizeof(float));
         o->cdf = (double *)calloc(capacity + 1, sizeof(double));
         ok = o->raw && o->cdf;
@@ -295,7 +299,7 @@ int orc_add(orc_per *o, uint64_t count, const float *states, const float *next_s
             o->L[slot] = leaf_from_raw(raw, o->alpha);
             if (!bulk)
                 propagate_leaf(o, slot);
-        } else {
+        } else if (o->mode == ORC_RANK) {
             o->raw[slot] = raw;
         }
         if (raw > o->max_raw)
@@ -424,6 +428,36 @@ int orc_sample(orc_per *o, uint32_t B, float beta, int64_t *idx, float *w, float
                 gather_row(o, j, (uint64_t)leaf, out_states, out_next, out_actions, out_rewards,
                            out_dones);
         }
+    } else if (o->mode == ORC_UNIFORM) {
+        /* R24: every filled slot weighs 1, so T = size and the walk is a division: draw j takes
+         * mass (j + u_j) * (size / B), slot floor(mass), weight 1 */
+        double T = (double)o->size;
+        double seg = T / (double)B;
+        for (uint32_t j = 0; j < B; ++j) {
+            double u = orc_uniform53(o->seed, j, call, 2);
+            double mass = ((double)j + u) * seg;
+            double fl = floor(mass);
+            int fell_off = 0;
+            uint64_t slot = (uint64_t)fl;
+            if (slot >= o->size) {
+                slot = o->size - 1;
+                fell_off = 1;
+            }
+            idx[j] = (int64_t)slot;
+            if (w)
+                w[j] = 1.0f;
+            double r = mass - fl;
+            if (near) {
+                double tol = 1e-6 * T;
+                near[j] = (uint8_t)(fell_off || r < tol || (1.0 - r) < tol);
+            }
+            if (rem)
+                rem[j] = r;
+            if (mass_out)
+                mass_out[j] = mass;
+            if (o->with_ring)
+                gather_row(o, j, slot, out_states, out_next, out_actions, out_rewards, out_dones);
+        }
     } else {
         uint64_t s = o->size;
         uint32_t *order = (uint32_t *)malloc(s * sizeof(uint32_t));
@@ -478,6 +512,8 @@ int orc_update(orc_per *o, uint32_t B, const int64_t *idx, const float *td)
 {
     if (!o || (B > 0 && (!idx || !td)))
         return ORC_EINVAL;
+    if (o->mode == ORC_UNIFORM) /* R24: no priorities */
+        return 0;
     float max_at_start = o->max_raw;
     int skipped = 0;
     for (uint32_t j = 0; j < B; ++j) {
@@ -510,6 +546,8 @@ double orc_total(const orc_per *o)
 {
     if (o->mode == ORC_RANK)
         return o->cdf[o->size];
+    if (o->mode == ORC_UNIFORM)
+        return (double)o->size;
     return node_sum(o, 1);
 }
 
@@ -517,6 +555,8 @@ float orc_min(const orc_per *o)
 {
     if (o->mode == ORC_RANK)
         return NAN;
+    if (o->mode == ORC_UNIFORM)
+        return 1.0f;
     return node_min(o, 1);
 }
 

@@ -430,3 +430,100 @@ def test_rank_update_lww(orc):
     assert raw[0] == np.float32(1e-6)
     assert o.max_raw == np.float32(6.0 + 1e-6)
     assert o.rank_order().tolist() == [2, 3, 1, 0]
+
+
+# -- uniform mode (the plain replay that prioritized replay replaces) --------------------------
+
+def _uniform(orc, size, capacity=None, seed=0, with_ring=False, d=0):
+    o = orc.Oracle(capacity or size, d, d, alpha=0.6, mode=orc.UNIFORM, seed=seed,
+                   with_ring=with_ring)
+    g = wl.rng(size)
+    if with_ring:
+        t = wl.transitions(g, size, wl.Workload("u", capacity or size, d, d, 4, 0.6, 0.4, 1e-6, 1))
+        o.add(t["states"], t["next_states"], t["actions"], t["rewards"], t["dones"],
+              g.uniform(0.1, 5, size).astype(np.float32))
+    else:
+        o.add(raw_prio=g.uniform(0.1, 5, size).astype(np.float32), count=size)
+    return o
+
+
+def test_uniform_one_draw_per_slot_when_batch_equals_size(orc):
+    # each stratum is exactly one slot wide, so draw j must land on slot j whatever u_j is
+    for size in (1, 7, 1000, 4096):
+        o = _uniform(orc, size, capacity=2 * size)
+        for _ in range(3):
+            out = o.sample(size, 0.4, gather=False)
+            assert np.array_equal(out["idx"], np.arange(size))
+            assert np.all(out["w"] == 1.0)
+
+
+def test_uniform_strata_bounds_and_weights(orc):
+    # partly filled ring, B neither divides nor is divided by the filled count
+    size, B = 1237, 100
+    o = _uniform(orc, size, capacity=5000, seed=3)
+    assert o.total() == size and o.min() == 1.0
+    j = np.arange(B)
+    lo = (j * size) // B                     # first slot of stratum j
+    hi = -(-((j + 1) * size) // B)           # one past its last (ceil)
+    seen = set()
+    for _ in range(50):
+        out = o.sample(B, 0.7, gather=False)
+        assert np.all(out["idx"] >= lo) and np.all(out["idx"] < hi)
+        assert np.all(out["idx"] < size)
+        assert np.all(out["w"] == 1.0)
+        seen.add(out["idx"].tobytes())
+    assert len(seen) == 50                   # every call draws afresh
+
+
+def test_uniform_chi_square(orc):
+    size, B, calls = 3000, 256, 2000
+    o = _uniform(orc, size, capacity=4096, seed=5)   # 1096 slots never filled
+    counts = np.zeros(4096)
+    for _ in range(calls):
+        counts += np.bincount(o.sample(B, 0.4, gather=False)["idx"], minlength=4096)
+    assert counts[size:].sum() == 0
+    N = counts.sum()
+    assert N == B * calls
+    assert stats.chisquare(counts[:size], np.full(size, N / size)).pvalue > 1e-4
+    # stratification: per call, the draws below slot k are the strata that end at or below k,
+    # plus at most the one stratum that straddles k, so over all calls the prefix counts stay
+    # within [calls * f, calls * (f + 1)], f = floor(k * B / size) -- a bound an unstratified or
+    # biased sampler breaks
+    k = np.arange(1, size + 1)
+    f = (k * B) // size
+    prefix = np.cumsum(counts[:size])
+    assert np.all(prefix >= calls * f) and np.all(prefix <= calls * (f + 1))
+
+
+def test_uniform_update_changes_nothing(orc):
+    a = _uniform(orc, 500, capacity=512, seed=8)
+    b = _uniform(orc, 500, capacity=512, seed=8)
+    g = wl.rng(1)
+    assert a.update(g.integers(0, 500, 300), g.uniform(0, 100, 300).astype(np.float32)) == 0
+    assert a.max_raw == b.max_raw and a.total() == b.total() == 500
+    for _ in range(3):
+        x, y = a.sample(64, 0.4, gather=False), b.sample(64, 0.4, gather=False)
+        assert np.array_equal(x["idx"], y["idx"]) and np.array_equal(x["mass"], y["mass"])
+
+
+def test_uniform_gather_after_wrap(orc):
+    cap, d = 37, 5
+    o = orc.Oracle(cap, d, d + 3, alpha=0.6, mode=orc.UNIFORM, seed=2, with_ring=True)
+    g = wl.rng(77)
+    rows = {}
+    cursor = 0
+    for count in (20, 30, 11):
+        t = wl.transitions(g, count, wl.Workload("u", cap, d, d + 3, 4, 0.6, 0.4, 1e-6, 1))
+        o.add(t["states"], t["next_states"], t["actions"], t["rewards"], t["dones"])
+        for k in range(count):
+            rows[(cursor + k) % cap] = (t["states"][k], t["next_states"][k], t["actions"][k],
+                                        t["rewards"][k], t["dones"][k])
+        cursor = (cursor + count) % cap
+    assert o.size == cap
+    out = o.sample(cap, 0.4)
+    assert np.array_equal(out["idx"], np.arange(cap))
+    for j in range(cap):
+        st, nx, a, r, dn = rows[j]
+        assert np.array_equal(out["states"][j, :d], st) and np.all(out["states"][j, d:] == 0)
+        assert np.array_equal(out["next_states"][j, :d], nx) and np.all(out["next_states"][j, d:] == 0)
+        assert out["actions"][j] == a and out["rewards"][j] == r and out["dones"][j] == dn
