@@ -589,6 +589,7 @@ OTHER = {
     "dqn": "dqn: 2^20 leaves, state_dim 48 gathered into 64-float rows, B=1024, beta 0.4->1.0 over 341 steps",
     "stress": "stress: 2^24 leaves, state_dim 256, B=8192, 25% duplicate update indices, alpha 0.7, beta 0.5",
     "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, order merge (radix sort when rebuilt) + rank sample, alpha 0.7, beta 0.5",
+    "uniform": "uniform: 2^21 slots, state_dim 64, B=512, uniform stratified draws + gather, dones as f32 (the update is a no-op)",
 }
 
 
@@ -603,8 +604,8 @@ def run_other(args, name, resort=False):
     from rl_infra_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
     torch.cuda.set_device(0)
-    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0,
-                            flags=capi.PER_FLAG_RANK_RESORT if resort else 0)
+    flags = (capi.PER_FLAG_RANK_RESORT if resort else 0) | (capi.PER_FLAG_DONES_F32 if w.mode == wl.UNIFORM else 0)
+    buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0, flags=flags)
     g = wl.rng(0, 55)
     chunk = min(w.capacity, 1 << 18)
     for c in range(w.capacity // chunk):
@@ -684,11 +685,18 @@ def run_other(args, name, resort=False):
         b_sam = b_sort + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
         b_upd = 12 * B + 4 * d
         names = ("rank order + k_sample_rank", "k_update")
+    elif w.mode == wl.UNIFORM:
+        # idx + weight out; rows read and written; action, reward in and out; done 1 B in, 4 B out
+        b_sam = B * (8 + 4 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 8 + 8 + 5)
+        b_upd = 0
+        names = ("k_sample_uniform", "update (no kernel in this mode)")
     else:
         b_sam = bytes_sample(idx, w.state_dim, w.row_stride, D)
         b_upd = bytes_update(upd_idx, D)
         names = ("k_sample_prop", "k_update")
     ops = {names[0]: (float(np.median(per[:, 0])), b_sam), names[1]: (float(np.median(per[:, 1])), b_upd)}
+    if w.mode == wl.UNIFORM:
+        del ops[names[1]]
     peak, peak_src = load_peaks()
     dom = max(ops, key=lambda k: ops[k][0])
     ms, byt = ops[dom]
@@ -709,7 +717,7 @@ def run_other(args, name, resort=False):
                      "unit": "GB/s", "frac": round(achieved / peak, 5), "traffic": None,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
                      "median_launch_us": round(ms * 1e3, 3)},
-        "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 2) * K,
+        "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
     }
     if w.mode == wl.RANK:
         res["config"]["rank_order"] = ("every slot sorted again at each sample (4-pass radix sort)" if resort
@@ -768,7 +776,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="apex", choices=["apex", "tiny", "dqn", "stress", "rank"],
+    ap.add_argument("--workload", default="apex", choices=["apex", "tiny", "dqn", "stress", "rank", "uniform"],
                     help="apex is the headline workload; the others are measured with --workload")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip timing the rounds captured as one CUDA graph")

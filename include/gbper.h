@@ -57,7 +57,8 @@ typedef enum {
 /* Sampling modes ("GPU-Resident Prioritized Experience Replay", Sampling Kernels). */
 enum {
     PER_MODE_PROPORTIONAL = 0, /* P(i) = p_i^alpha / sum_k p_k^alpha, sum tree + min tree */
-    PER_MODE_RANK = 1          /* P(i) proportional to 1 / rank(i)^alpha, rank by raw priority */
+    PER_MODE_RANK = 1,         /* P(i) proportional to 1 / rank(i)^alpha, rank by raw priority */
+    PER_MODE_UNIFORM = 2       /* P(i) = 1 / size: the plain replay PER replaces; priorities unused */
 };
 
 /* Bits of the device error word (per_status_device). */
@@ -71,8 +72,11 @@ enum {
 
 /* per_config.flags */
 enum {
-    PER_FLAG_RANK_RESORT = 1u  /* rank mode: sort every filled slot at each sample instead of
+    PER_FLAG_RANK_RESORT = 1u, /* rank mode: sort every filled slot at each sample instead of
                                   merging the slots written since the previous one (same order) */
+    PER_FLAG_DONES_F32 = 2u    /* per_sample writes dones as float 0.0f / 1.0f (d_dones is float*,
+                                  4-byte aligned), the trainer's format ("True Single-Graph
+                                  Implementation Plan", Task 3) */
 };
 
 typedef struct {
@@ -147,10 +151,15 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
  * ones, by the host's count of inserted and updated entries) were written since, only those
  * slots are merged back into it; otherwise every filled slot is sorted again.  Both give the
  * same order.
+ * Uniform mode (the plain replay that PER replaces, "GPU-Resident Prioritized Experience
+ * Replay", Experience Insertion): every filled slot weighs 1, so draw j (counter tag 2) takes
+ * mass_j = (j + u_j) * (size / B) and slot floor(mass_j), clamped to the last filled slot;
+ * w = 1.
  * Gather ("True Single-Graph Implementation Plan", Task 2/3): row j of d_states and d_next
  * receives the chosen slot's row, padded with 0.0f to row_stride_out floats.
  *   d_idx [B] int64 (required); d_w [B] float; d_states, d_next [B x row_stride_out] float;
- *   d_actions [B] uint32; d_rewards [B] float; d_dones [B] uint8 -- each may be NULL to skip.
+ *   d_actions [B] uint32; d_rewards [B] float; d_dones [B] uint8 (float with
+ *   PER_FLAG_DONES_F32) -- each may be NULL to skip.
  *   B in 1 .. 2^24.  beta >= 0.
  * The call counter lives on the device, so each call, captured in a graph or not, draws a
  * fresh batch.  PER_ERR_EMPTY when the buffer holds no transition (host-side count).
@@ -166,7 +175,8 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * when the call began; the leaf becomes raw^alpha.  When an index repeats, the highest batch
  * position wins.  Proportional mode then rebuilds the dirty ancestors of the sum and min
  * trees level by level ("Putting prioritized replay's segment tree on a GPU", Second Port),
- * restricted to the nodes above a changed leaf.  Rank mode stores raw.  The running maximum
+ * restricted to the nodes above a changed leaf.  Rank mode stores raw.  Uniform mode has no
+ * priorities: the call checks its arguments and changes nothing.  The running maximum
  * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
  * PER_DEVFLAG_BAD_INDEX.
  *   d_idx [B] int64, d_td [B] float.  B in 0 .. 2^24 (0 is a no-op).
@@ -174,7 +184,7 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
 per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx,
                                  const float *d_td, void *stream);
 
-/* per_total -- the root of the sum tree (proportional) or c_size (rank), copied to *host_out.
+/* per_total -- the root of the sum tree (proportional), c_size (rank) or size (uniform), copied to *host_out.
  * Synchronises `stream`. */
 per_status per_total(per_buffer *h, double *host_out, void *stream);
 

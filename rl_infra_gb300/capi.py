@@ -24,11 +24,13 @@ PER_ERR_TIMEOUT = 6
 
 PER_MODE_PROPORTIONAL = 0
 PER_MODE_RANK = 1
+PER_MODE_UNIFORM = 2
 
 PER_DEVFLAG_BAD_INDEX = 1
 PER_DEVFLAG_TIMEOUT = 2
 PER_DEVFLAG_RANK_STALE = 4
 PER_FLAG_RANK_RESORT = 1
+PER_FLAG_DONES_F32 = 2
 
 PER_STATE_LEAVES, PER_STATE_SUMS, PER_STATE_MINS, PER_STATE_RAW, PER_STATE_CDF = 0, 1, 2, 3, 4
 PER_STATE_STATES, PER_STATE_NEXT, PER_STATE_ACTIONS, PER_STATE_REWARDS = 5, 6, 7, 8
@@ -217,7 +219,9 @@ class ReplayBuffer:
         self.state_dim = int(state_dim)
         self.row_stride = int(row_stride_out if row_stride_out is not None else state_dim)
         self.mode = mode
+        self.dones_dtype = None  # set below, once torch is imported
         self.device = torch.device("cuda", torch.cuda.current_device())
+        self.dones_dtype = torch.float32 if int(flags) & PER_FLAG_DONES_F32 else torch.uint8
         cfg = per_config(float(alpha), float(eps), int(mode), self.row_stride, int(seed), int(flags), 0)
         self._h = per_create(self.capacity, self.state_dim, cfg)
         self.nleaves = per_nleaves(self._h)[1]
@@ -258,7 +262,7 @@ class ReplayBuffer:
             out["next_states"] = torch.empty((B, self.row_stride), dtype=torch.float32, device=dev)
             out["actions"] = torch.empty(B, dtype=torch.int32, device=dev)
             out["rewards"] = torch.empty(B, dtype=torch.float32, device=dev)
-            out["dones"] = torch.empty(B, dtype=torch.uint8, device=dev)
+            out["dones"] = torch.empty(B, dtype=self.dones_dtype, device=dev)
         return out
 
     def sample(self, B, beta, out=None, gather=True, stream=None):
@@ -269,7 +273,7 @@ class ReplayBuffer:
         s = per_sample(self._h, int(B), float(beta), _ptr(out["idx"], torch.int64, "idx"),
                        g("w", torch.float32), g("states", torch.float32),
                        g("next_states", torch.float32), g("actions", torch.int32),
-                       g("rewards", torch.float32), g("dones", torch.uint8), _stream(stream))
+                       g("rewards", torch.float32), g("dones", self.dones_dtype), _stream(stream))
         self._check(s, "per_sample")
         return out
 

@@ -107,7 +107,10 @@ __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o
     }
     if (lane == 1 && o.actions) o.actions[j] = act;
     if (lane == 2 && o.rewards) o.rewards[j] = rew;
-    if (lane == 3 && o.dones) o.dones[j] = done;
+    if (lane == 3 && o.dones) {
+        if (o.dones_f32) reinterpret_cast<float *>(o.dones)[j] = done ? 1.0f : 0.0f;
+        else o.dones[j] = done;
+    }
 }
 
 // a > b for binary64 values >= +0: their bit patterns order like the values, so the compare
@@ -326,6 +329,49 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
     }
 }
 
+// ------------------------------------------------------------------------------------------
+// Uniform mode (the plain replay that prioritized replay replaces): every filled slot weighs 1,
+// so the stratified walk is a division.  Draw j: u_j from counter (j, call, tag 2),
+// mass_j = (j + u_j) * (size / B), slot floor(mass_j) (clamped to the last filled slot), w = 1.
+// One warp per draw, which then gathers the row like the other modes.
+// ------------------------------------------------------------------------------------------
+struct UniformArgs {
+    RingRefs r;
+    Ctl *ctl;
+    unsigned B;
+    double inv_b;   // 1/B when B is a power of two (exact), else 0
+    unsigned long long seed;
+    SampleOut o;
+    int vec4;
+};
+
+__global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
+{
+    __shared__ unsigned long long s_call;
+    pdl_wait();
+    pdl_release();
+    if (threadIdx.x == 0) s_call = take_call_number(a.ctl);
+    const unsigned long long size = a.ctl->size;
+    const double total = (double)size;
+    const double seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
+    __syncthreads();
+    const unsigned long long call = s_call;
+    const int lane = threadIdx.x & 31;
+    const unsigned wpb = blockDim.x >> 5;
+    const unsigned warps_total = gridDim.x * wpb;
+    for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
+        const double u = draw_uniform(a.seed, j, call, 2);
+        const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
+        unsigned long long slot = (unsigned long long)m;   // m >= 0: truncation is the floor
+        if (slot >= size) slot = size - 1;
+        if (lane == 0) {
+            a.o.idx[j] = (long long)slot;
+            if (a.o.w) a.o.w[j] = 1.0f;
+        }
+        gather_row(a.r, a.o, j, slot, lane, a.vec4);
+    }
+}
+
 int warps_per_cta()
 {
     int w = 8;
@@ -349,7 +395,8 @@ cudaError_t init_sample_kernels(int carveout)
 {
     if (carveout < 0) return cudaSuccess;
     cudaError_t e;
-    const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank};
+    const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank,
+                         (const void *)k_sample_uniform};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (e != cudaSuccess) return e;
@@ -375,6 +422,23 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
+}
+
+cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsigned long long seed,
+                                  const SampleOut &o, int num_sms, cudaStream_t st)
+{
+    UniformArgs a;
+    a.r = r;
+    a.ctl = ctl;
+    a.B = B;
+    a.inv_b = (B & (B - 1)) == 0 ? 1.0 / (double)B : 0.0;
+    a.seed = seed;
+    a.o = o;
+    a.vec4 = rows_vec4(r, o) ? 1 : 0;
+    const int wpb = warps_per_cta();
+    const unsigned long long ctas = (B + wpb - 1) / wpb;
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    return launch_pdl(k_sample_uniform, grid, wpb * 32, 0, st, a);
 }
 
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,

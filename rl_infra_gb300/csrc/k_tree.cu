@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                     if (a.proportional) {
                         leaf = a.prio ? leaf_of(raw, a.lp) : max_leaf;
                         a.t.L[s] = leaf;
-                    } else {
+                    } else if (a.raw_store) {   // rank mode (uniform mode keeps no priorities)
                         a.raw_store[s] = raw;
                         mark_dirty(a.dirty, s);
                     }
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
             mymax = max(mymax, __float_as_uint(raw));
             if (a.proportional)
                 a.t.L[slot] = a.prio ? leaf_of(raw, a.lp) : __uint_as_float(a.ctl->max_leaf_bits);
-            else a.raw_store[slot] = raw;
+            else if (a.raw_store) a.raw_store[slot] = raw;
         }
     }
     const unsigned bm = block_max_u32(mymax);

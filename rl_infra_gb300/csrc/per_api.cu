@@ -40,6 +40,7 @@ struct per_buffer {
     // rank mode: the order kept between samples (keys/vals[merge_ctl[4]], order_size entries) and
     // an upper bound on the slots written since (each insertion or update adds its count)
     bool order_valid = false, always_resort = false;
+    bool dones_f32 = false;   // per_sample writes dones as float
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
     uint64_t dirty_nwords = 0;
@@ -190,9 +191,10 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: alpha must be finite and >= 0");
     if (!(c.eps > 0.0) || !std::isfinite(c.eps))
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: eps must be finite and > 0");
-    if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK)
+    if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK && c.mode != PER_MODE_UNIFORM)
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown mode");
-    if (c.flags & ~PER_FLAG_RANK_RESORT) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown flags");
+    if (c.flags & ~(PER_FLAG_RANK_RESORT | PER_FLAG_DONES_F32))
+        return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown flags");
     if (c.mode == PER_MODE_PROPORTIONAL && !((float)std::pow(c.eps, c.alpha) >= 1.17549435e-38f))
         return fail(nullptr, PER_ERR_INVALID_ARG,
                     "per_create: eps^alpha underflows binary32; a leaf of 0 would read as an empty slot");
@@ -223,11 +225,12 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     h->mode = c.mode;
     h->seed = c.seed;
     h->always_resort = (c.flags & PER_FLAG_RANK_RESORT) != 0;
+    h->dones_f32 = (c.flags & PER_FLAG_DONES_F32) != 0;
 
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
         ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n);
-    } else {
+    } else if (c.mode == PER_MODE_RANK) {
         ok = ok && alloc(&h->rank.raw, capacity) && alloc(&h->rank.cdf, capacity + 1) &&
              alloc(&h->rank.keys[0], capacity) && alloc(&h->rank.keys[1], capacity) &&
              alloc(&h->rank.vals[0], capacity) && alloc(&h->rank.vals[1], capacity) &&
@@ -341,7 +344,8 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
         return fail(h, PER_ERR_INVALID_ARG, "per_sample: beta must be finite and >= 0");
     if (reinterpret_cast<uintptr_t>(d_idx) % 8 || reinterpret_cast<uintptr_t>(d_w) % 4 ||
         reinterpret_cast<uintptr_t>(d_states) % 4 || reinterpret_cast<uintptr_t>(d_next) % 4 ||
-        reinterpret_cast<uintptr_t>(d_actions) % 4 || reinterpret_cast<uintptr_t>(d_rewards) % 4)
+        reinterpret_cast<uintptr_t>(d_actions) % 4 || reinterpret_cast<uintptr_t>(d_rewards) % 4 ||
+        (h->dones_f32 && reinterpret_cast<uintptr_t>(d_dones) % 4))
         return fail(h, PER_ERR_INVALID_ARG, "per_sample: misaligned output pointer");
     if (h->host_size == 0) return fail(h, PER_ERR_EMPTY, "per_sample: the buffer holds no transition");
     SampleOut o;
@@ -352,10 +356,13 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
     o.actions = d_actions;
     o.rewards = d_rewards;
     o.dones = d_dones;
+    o.dones_f32 = h->dones_f32 ? 1 : 0;
     o.dp = h->dp;
     cudaError_t e;
     if (h->mode == PER_MODE_PROPORTIONAL) {
         e = launch_sample_prop(tree_of(h), ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms, as_stream(stream));
+    } else if (h->mode == PER_MODE_UNIFORM) {
+        e = launch_sample_uniform(ring_of(h), h->ctl, B, h->seed, o, h->num_sms, as_stream(stream));
     } else {
         e = rank_order(h, as_stream(stream));
         const unsigned *sorted = h->rank.vals[1];   // unused: the kernel reads the order's buffer
@@ -376,6 +383,7 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
     if (!d_idx || !d_td) return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: NULL input");
     if (reinterpret_cast<uintptr_t>(d_idx) % 8 || reinterpret_cast<uintptr_t>(d_td) % 4)
         return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: misaligned input");
+    if (h->mode == PER_MODE_UNIFORM) return PER_OK;   // no priorities
     const cudaError_t e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, reinterpret_cast<const long long *>(d_idx),
                                         d_td, h->alpha, h->eps, h->mode == PER_MODE_PROPORTIONAL, h->num_sms,
                                         h->rank.dirty, as_stream(stream));
@@ -389,7 +397,13 @@ per_status per_total(per_buffer *h, double *host_out, void *stream)
     if (!h || !host_out) return PER_ERR_INVALID_ARG;
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
-    if (h->mode == PER_MODE_RANK) {
+    if (h->mode == PER_MODE_UNIFORM) {
+        uint64_t size = 0;
+        e = cudaMemcpyAsync(&size, &h->ctl->size, sizeof(size), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        *host_out = (double)size;
+        return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_total");
+    } else if (h->mode == PER_MODE_RANK) {
         e = cudaMemcpyAsync(host_out, h->rank.cdf + h->host_size, sizeof(double), cudaMemcpyDeviceToHost, st);
     } else if (h->D == 0) {
         float v = 0.0f;

@@ -187,13 +187,18 @@ struct SampleOut {
     float *states, *next;
     unsigned *actions;
     float *rewards;
-    unsigned char *dones;
+    unsigned char *dones;      // uint8, or float when dones_f32
+    int dones_f32;
     unsigned dp;
 };
 
 cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, unsigned B,
                                float beta, unsigned long long seed, const SampleOut &o,
                                int num_sms, cudaStream_t st);
+
+// Uniform mode: draw j takes slot floor((j + u_j) * size / B) (counter tag 2), weight 1.
+cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsigned long long seed,
+                                  const SampleOut &o, int num_sms, cudaStream_t st);
 
 struct RankWork {
     float *raw;

@@ -25,6 +25,7 @@ import numpy as np
 
 PROPORTIONAL = 0
 RANK = 1
+UNIFORM = 2
 
 
 @dataclass(frozen=True)
@@ -66,6 +67,9 @@ WORKLOADS = {
                        dup_frac=0.25),
     "rank": Workload("rank", 1 << 20, 64, 64, 1024, 0.7, 0.5, 1e-6, 100, mode=RANK,
                      prio="absnormal"),
+    # the apex shapes drawn uniformly: the plain replay that prioritized replay replaces
+    "uniform": Workload("uniform", 1 << 21, 64, 64, 512, 0.6, 0.4, 1e-6, 1000, mode=UNIFORM,
+                        prio="lognormal"),
 }
 
 

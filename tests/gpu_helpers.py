@@ -55,7 +55,10 @@ class Pair:
         if check_rows:
             for k in ("states", "next_states", "rewards", "dones"):
                 g = got[k].cpu().numpy()
-                assert np.array_equal(g[same].view(np.uint8), want[k][same].view(np.uint8)), k
+                wv = want[k]
+                if k == "dones" and g.dtype == np.float32:   # PER_FLAG_DONES_F32
+                    wv = (wv != 0).astype(np.float32)
+                assert np.array_equal(g[same].view(np.uint8), wv[same].view(np.uint8)), k
             ga = got["actions"].cpu().numpy().view(np.uint32)
             assert np.array_equal(ga[same], want["actions"][same])
         return got, want
@@ -65,6 +68,9 @@ class Pair:
         return self.orc.update(idx, td)
 
     def check_tree(self, full=True):
+        if self.mode == capi.PER_MODE_UNIFORM:
+            assert self.gpu.total() == self.orc.total() == self.orc.size
+            return
         if self.mode == capi.PER_MODE_RANK:
             assert np.array_equal(self.gpu.read_state(capi.PER_STATE_RAW), self.orc.raw())
             return

@@ -67,5 +67,22 @@ def test_workload_table_matches_the_configs():
     assert (W["stress"].capacity, W["stress"].state_dim, W["stress"].batch) == (1 << 24, 256, 8192)
     assert (W["rank"].capacity, W["rank"].mode, W["rank"].alpha, W["rank"].beta) == (
         1 << 20, wl.RANK, 0.7, 0.5)
+    assert (W["uniform"].capacity, W["uniform"].state_dim, W["uniform"].batch, W["uniform"].mode) == (
+        1 << 21, 64, 512, wl.UNIFORM)
     p = wl.raw_priorities(wl.rng(1), 100000, "pareto")
     assert p.min() >= 1.0 and abs(np.median(p) - 2 ** (1 / 1.5)) < 0.03
+
+
+def test_binding_constants_match_the_header():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "gbper.h")).read()
+    consts = {m.group(1): int(m.group(2)) for m in
+              re.finditer(r"\b(PER_(?:MODE|FLAG|STATE|DEVFLAG|ERR)_[A-Z0-9_]+)\s*=\s*(\d+)u?\b", hdr)}
+    assert {"PER_MODE_UNIFORM", "PER_FLAG_DONES_F32", "PER_STATE_RANK_ORDER"} <= consts.keys()
+    for name, v in consts.items():
+        assert getattr(capi, name) == v, name
+    import oracle
+    assert (oracle.PROPORTIONAL, oracle.RANK, oracle.UNIFORM) == (
+        capi.PER_MODE_PROPORTIONAL, capi.PER_MODE_RANK, capi.PER_MODE_UNIFORM)
+    assert (wl.PROPORTIONAL, wl.RANK, wl.UNIFORM) == (
+        capi.PER_MODE_PROPORTIONAL, capi.PER_MODE_RANK, capi.PER_MODE_UNIFORM)

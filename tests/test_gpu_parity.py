@@ -290,7 +290,64 @@ def test_rank_ties_keep_slot_order():
 
 # -- CUDA graphs: a captured round replays with the device-resident counters -------------------
 
-@pytest.mark.parametrize("mode", [0, 1])
+# -- uniform mode and float dones -------------------------------------------------------------
+
+@pytest.mark.parametrize("cap,fill", [(1, 1), (3, 2), (1000, 999), (4096, 4096), (5000, 3001),
+                                      (1 << 16, 1 << 16)])
+def test_uniform_mode(cap, fill):
+    w = _small("tiny", capacity=cap, state_dim=6, row_stride=8, mode=capi.PER_MODE_UNIFORM)
+    g = wl.rng(21, cap)
+    p = Pair(cap, 6, 8, 0.6, 1e-6, capi.PER_MODE_UNIFORM, seed=9)
+    prefill(p, w, g, count=fill, chunk=max(1, fill // 2))
+    p.check_tree()
+    p.check_counters()
+    for B in (1, 5, 64, 100, 1024, fill, 3 * fill + 1):
+        _, want = p.sample(B, 0.4)
+        assert np.all(want["idx"] < fill)
+        assert p.update(want["idx"], wl.td_errors(g, B)) == 0
+        p.check_counters()
+    assert p.stats["mismatch"] == 0, p.stats          # the division has no boundary slack
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
+def test_uniform_mode_wrap_and_update_no_op():
+    cap = 2000
+    w = _small("tiny", capacity=cap, state_dim=4, row_stride=4, mode=capi.PER_MODE_UNIFORM)
+    g = wl.rng(22)
+    p = Pair(cap, 4, 4, 0.6, 1e-6, capi.PER_MODE_UNIFORM, seed=2)
+    for count in (700, 1800, 5003, 1):
+        p.add(wl.transitions(g, count, w), wl.raw_priorities(g, count, "lognormal"))
+        p.check_counters()
+        _, want = p.sample(256, 0.4)
+        p.update(want["idx"], wl.td_errors(g, 256))
+    # updates with out-of-range indices change nothing and raise no device flag in this mode
+    p.update(np.array([-1, cap + 5, 3], np.int64), np.ones(3, np.float32))
+    assert p.gpu.status_device() == 0
+    assert np.array_equal(p.gpu.read_state(capi.PER_STATE_STATES).reshape(cap, 4), p.orc.ring_states())
+    with pytest.raises(capi.PerError):
+        p.gpu.min()
+    p.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_float_dones(mode):
+    cap = 3000
+    w = _small("tiny", capacity=cap, state_dim=8, row_stride=8, mode=mode)
+    g = wl.rng(23, mode)
+    p = Pair(cap, 8, 8, 0.6, 1e-6, mode, seed=4, flags=capi.PER_FLAG_DONES_F32)
+    prefill(p, w, g, count=cap, chunk=cap)
+    for B in (1, 77, 512):
+        got, want = p.sample(B, 0.4)
+        assert got["dones"].dtype == torch.float32
+        d = got["dones"].cpu().numpy()
+        assert set(np.unique(d)) <= {0.0, 1.0}
+        assert d.sum() > 0 or B < 512
+        p.update(want["idx"], wl.td_errors(g, B))
+    p.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_graph_replayed_rounds(mode):
     """Insert + sample + update captured once per staging offset as CUDA graphs and replayed:
     every replay inserts at the device cursor, draws a fresh batch (device call counter) and, in
