@@ -726,6 +726,76 @@ def run_other(args, name, resort=False):
     return res
 
 
+# -- the update's two paths against the batch size ------------------------------------------------
+
+def run_update_crossover(args):
+    """Median time of one per_update_priorities call (L2 flushed before each) by batch size, on
+    the path that climbs from each changed leaf and on the path that scatters and rebuilds every
+    tree level, for the tree sizes of the workloads.  The library's default dispatch picks the
+    rebuild from the batch size where it becomes the faster one."""
+    import ctypes
+    import torch
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    cr = Cudart()
+    rec, memset = cr.lib.cudaEventRecord, cr.lib.cudaMemsetAsync
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    L = capi.load()
+    g = wl.rng(0, 77)
+    reps = max(5, min(args.steps, 40))
+    rows = []
+    configs = [("tiny tree", 1 << 10, wl.PROPORTIONAL), ("2^16 tree", 1 << 16, wl.PROPORTIONAL),
+               ("dqn tree", 1 << 20, wl.PROPORTIONAL), ("apex tree", 1 << 21, wl.PROPORTIONAL),
+               ("stress tree", 1 << 24, wl.PROPORTIONAL), ("rank slots", 1 << 20, wl.RANK)]
+    for label, n, mode in configs:
+        bufs = {}
+        for path, rb in (("climb", capi.REBUILD_NEVER), ("rebuild", 1)):
+            buf = capi.ReplayBuffer(n, 0, 0.6, 1e-6, mode, 0, 0, rebuild_batch=rb)
+            chunk = min(n, 1 << 20)
+            a = torch.zeros(chunk, dtype=torch.int32, device="cuda")
+            r = torch.zeros(chunk, dtype=torch.float32, device="cuda")
+            d = torch.zeros(chunk, dtype=torch.uint8, device="cuda")
+            for c in range(n // chunk):
+                prio = torch.from_numpy(wl.raw_priorities(g, chunk, "lognormal")).cuda()
+                buf.add(None, None, a, r, d, prio)
+            bufs[path] = buf
+        torch.cuda.synchronize()
+        Bs = [b for b in (16, 64, 256, 1024, 4096, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20, 1 << 22)
+              if b <= 4 * n]
+        for B in Bs:
+            idx = torch.from_numpy(g.integers(0, n, B).astype(np.int64)).cuda()
+            td = torch.from_numpy(wl.td_errors(g, B)).cuda()
+            row = {"tree": label, "n": n, "B": B}
+            for path, buf in bufs.items():
+                h = buf._h
+                ev = cr.events(2 * reps)
+                for t in range(3 + reps):
+                    memset(flush.data_ptr(), 0, flush.numel(), st)
+                    if t >= 3:
+                        rec(ev[2 * (t - 3)], st)
+                    _check(L, h, L.per_update_priorities(h, B, idx.data_ptr(), td.data_ptr(), st), "per_update")
+                    if t >= 3:
+                        rec(ev[2 * (t - 3) + 1], st)
+                torch.cuda.synchronize()
+                row[path + "_us"] = round(float(np.median([cr.elapsed_ms(ev[2 * k], ev[2 * k + 1])
+                                                           for k in range(reps)])) * 1e3, 3)
+                cr.destroy(ev)
+            rows.append(row)
+        for buf in bufs.values():
+            if buf.status_device() != 0:
+                raise RuntimeError("device error flag raised during the update sweep")
+            buf.close()
+    cross = {}
+    for label, n, _ in configs:
+        rs = [r for r in rows if r["tree"] == label]
+        first = next((r["B"] for r in rs if r["rebuild_us"] < r["climb_us"]), None)
+        cross[label] = first
+    return {"metric": "per_update_priorities time by batch size, both paths (us, L2 flushed)",
+            "reps": reps, "rows": rows, "rebuild_faster_from_B": cross}
+
+
 # -- the oracle on the host cores ------------------------------------------------------------------
 
 def oracle_steps_per_s(budget_s=12.0, max_steps=None):
@@ -783,6 +853,8 @@ def main():
     ap.add_argument("--l2", default="flush", choices=["flush", "warm"],
                     help="flush L2 between timed steps, or rely on inputs larger than L2")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--update-crossover", action="store_true",
+                    help="time both update paths against the batch size and exit")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -806,6 +878,10 @@ def main():
         print(json.dumps(res))
         return
 
+    if args.update_crossover:
+        if rank == 0:
+            print(json.dumps(run_update_crossover(args)))
+        return
     if args.workload != "apex":
         if rank == 0:
             res = run_other(args, args.workload)

@@ -87,7 +87,11 @@ typedef struct {
                                 columns past state_dim are written as 0.0f */
     uint64_t seed;           /* key of the Philox4x32-10 stream that draws the batches */
     uint32_t flags;          /* PER_FLAG_* bits; others must be 0 */
-    uint32_t reserved;
+    uint32_t rebuild_batch;  /* update batches of at least this many entries scatter their
+                                priorities and rebuild every tree level instead of climbing from
+                                each changed leaf (same result); 0: the crossover measured on
+                                GB300 (max(leaves / 128, 1024) proportional, 1024 rank);
+                                UINT32_MAX: never */
 } per_config;
 
 /*
@@ -175,7 +179,11 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * when the call began; the leaf becomes raw^alpha.  When an index repeats, the highest batch
  * position wins.  Proportional mode then rebuilds the dirty ancestors of the sum and min
  * trees level by level ("Putting prioritized replay's segment tree on a GPU", Second Port),
- * restricted to the nodes above a changed leaf.  Rank mode stores raw.  Uniform mode has no
+ * restricted to the nodes above a changed leaf.  Batches of at least per_config.rebuild_batch
+ * entries instead mark each slot's last batch position in a winner word, write the winners and
+ * rebuild every level of both trees (the post's level-synchronous rebuild, Measuring the
+ * Trade Honestly: O(k + n) beats O(k log n) once k is a large share of n); the trees come out
+ * the same.  Rank mode stores raw.  Uniform mode has no
  * priorities: the call checks its arguments and changes nothing.  The running maximum
  * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
  * PER_DEVFLAG_BAD_INDEX.

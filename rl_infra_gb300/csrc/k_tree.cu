@@ -587,38 +587,313 @@ __global__ void __launch_bounds__(kThreads) k_add_bulk_rows(AddArgs a)
     if (threadIdx.x == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
 }
 
-// Rebuild every node from depth cd-1 up to depth pd (pd < cd) from the nodes at depth cd.
-// Each CTA owns 256 consecutive nodes at depth cd (or the whole level when it is smaller).
-__global__ void __launch_bounds__(kThreads) k_rebuild_levels(TreeRefs t, int cd, int pd)
+// ---- full rebuild of both trees ("Putting prioritized replay's segment tree on a GPU", Second
+// Port: every node from its two children, level after level) ---------------------------------
+// One CTA of 256 threads builds the 11 levels above 2048 consecutive nodes of depth cd (the
+// leaves when cd = D): each thread combines its 8 inputs on registers for 3 levels (stored as
+// 32-, 16- and 8-byte vectors), the next 5 levels run on warp shuffles and the last 3 on warp 0.
+// When the CTA roots number at most 2048, the last CTA to arrive builds the levels above them the
+// same way (or in shared memory when they are fewer than 256) up to the root; otherwise the host
+// launches the next 11 levels.  A tree with fewer than 2048 leaves is built by one CTA.
+// In the large-batch update the leaf level also applies the batch: a slot whose winner word is
+// set takes the winning entry's priority (and the word is cleared) before it enters the sums.
+constexpr int kRbIn = 2048;   // inputs per CTA
+constexpr int kRbLog = 11;
+
+struct RebuildArgs {
+    TreeRefs t;
+    Ctl *ctl;
+    int cd;            // depth of this launch's inputs
+    unsigned *win;     // large-batch update: winner words (entry + 1, or 0); null otherwise
+    const float *td;
+    double eps;
+    LeafPowAlpha lp;
+    int fold;          // fold batch_max_bits into the running maximum once the root is built
+    double alpha;
+};
+
+// binary32 -> binary64 on the integer pipe for leaves (0, +inf or normal numbers: a leaf is at
+// least eps^alpha, which per_create keeps >= the smallest normal binary32)
+__device__ __forceinline__ double leaf_to_double(float f)
 {
-    __shared__ double s_vs[kThreads];
-    __shared__ float s_vm[kThreads];
-    const unsigned long long width = 1ull << cd;
-    const int gl = cd - pd;  // levels this launch builds (<= 8)
-    const unsigned long long first = width + (unsigned long long)blockIdx.x * kThreads;
-    const int tid = threadIdx.x;
-    const int bsz = width < (unsigned long long)kThreads ? (int)width : kThreads;
-    if (tid < bsz) {
-        s_vs[tid] = ld_sum(t, first + tid);
-        s_vm[tid] = ld_min(t, first + tid);
+    const unsigned b = __float_as_uint(f);
+    const unsigned e = b >> 23;
+    if (b == 0u) return 0.0;
+    if (e == 0u) return (double)f;   // subnormal: not a leaf value, kept exact anyway
+    const unsigned long long e64 = e == 255u ? 2047ull : (unsigned long long)(e + (1023 - 127));
+    return __longlong_as_double((long long)((e64 << 52) | ((unsigned long long)(b & 0x7fffffu) << 29)));
+}
+
+// The leaf value of slot i under the large-batch update: the winning entry's leaf when the
+// slot's winner word w is set (then written back, word cleared), else the stored leaf.  `tdv`
+// is the winning entry's TD error, loaded by the caller (all of a thread's loads go out first).
+__device__ __forceinline__ float applied_leaf(const RebuildArgs &a, unsigned long long i, float stored,
+                                              unsigned w, float tdv, float max_prev)
+{
+    if (w == 0u) return stored;
+    const float leaf = leaf_of(td_to_raw(tdv, a.eps, max_prev), a.lp);
+    a.t.L[i] = leaf;
+    a.win[i] = 0u;
+    return leaf;
+}
+
+template <int CNT>
+__device__ __forceinline__ void store_run(const TreeRefs &t, unsigned long long node, const double *v,
+                                          const float *m)
+{
+    if constexpr (CNT == 4) {
+        reinterpret_cast<double2 *>(t.S + node)[0] = make_double2(v[0], v[1]);
+        reinterpret_cast<double2 *>(t.S + node)[1] = make_double2(v[2], v[3]);
+        *reinterpret_cast<float4 *>(t.M + node) = make_float4(m[0], m[1], m[2], m[3]);
+    } else if constexpr (CNT == 2) {
+        *reinterpret_cast<double2 *>(t.S + node) = make_double2(v[0], v[1]);
+        *reinterpret_cast<float2 *>(t.M + node) = make_float2(m[0], m[1]);
+    } else {
+        t.S[node] = v[0];
+        t.M[node] = m[0];
     }
-    for (int h = 1; h <= gl; ++h) {
-        const int cnt = bsz >> h;
-        double sv = 0.0;
-        float mv = 0.0f;
+}
+
+// Builds the log2(256 PER) levels above the 256 PER nodes of depth cd that start at `base`
+// (PER per thread, consecutive); the top node ends in thread 0's registers and in S/M.  Inputs
+// are leaves (with the update applied when a.win is set) or S/M nodes (read from L2 when `cg`,
+// i.e. written by other CTAs of this launch).
+template <int PER>
+__device__ __forceinline__ void build_block(const RebuildArgs &a, unsigned long long base, bool leaves,
+                                            bool cg, float max_prev, unsigned char *smem)
+{
+    const TreeRefs &t = a.t;
+    const int tid = threadIdx.x;
+    const unsigned long long i0 = base + (unsigned long long)PER * tid;
+    double v[PER];
+    float m[PER];
+    if (leaves) {
+        float lf[PER];
+        const unsigned long long l0 = i0 - t.n;
+        if constexpr (PER == 8) {
+            const float4 x = reinterpret_cast<const float4 *>(t.L + l0)[0];
+            const float4 y = reinterpret_cast<const float4 *>(t.L + l0)[1];
+            lf[0] = x.x; lf[1] = x.y; lf[2] = x.z; lf[3] = x.w;
+            lf[4] = y.x; lf[5] = y.y; lf[6] = y.z; lf[7] = y.w;
+            if (a.win) {
+                // the warp's winners (slots whose word is set) go into a list in shared memory
+                // and are computed 32 at a time, so the leaf power runs on full warps
+                const uint4 wx = reinterpret_cast<const uint4 *>(a.win + l0)[0];
+                const uint4 wy = reinterpret_cast<const uint4 *>(a.win + l0)[1];
+                const unsigned w[8] = {wx.x, wx.y, wx.z, wx.w, wy.x, wy.y, wy.z, wy.w};
+                const int lane = tid & 31, wb = (tid >> 5) * 256;
+                unsigned char *s_pos = smem;                                          // [2048]
+                unsigned *s_w = reinterpret_cast<unsigned *>(smem + 2048);            // [2048]
+                float *s_lv = reinterpret_cast<float *>(smem + 2048 + 4 * 2048);      // [2048]
+                int cnt = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) cnt += w[k] != 0u;
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int total = __shfl_sync(0xffffffffu, incl, 31);
+                if (total > 0) {
+                    int off = wb + incl - cnt;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (w[k]) {
+                            s_pos[off] = (unsigned char)(lane * 8 + k);
+                            s_w[off] = w[k];
+                            ++off;
+                        }
+                    }
+                    __syncwarp();
+                    const unsigned long long wl0 = l0 - 8ull * lane;   // the warp's first slot
+                    for (int r = lane; r < total; r += 32) {
+                        const int pos = s_pos[wb + r];
+                        const unsigned ww = s_w[wb + r];
+                        s_lv[wb + pos] = applied_leaf(a, wl0 + pos, 0.0f, ww, __ldg(a.td + (ww - 1u)), max_prev);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (w[k]) lf[k] = s_lv[wb + lane * 8 + k];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                lf[k] = t.L[l0 + k];
+                if (a.win) {
+                    const unsigned w = a.win[l0 + k];
+                    lf[k] = applied_leaf(a, l0 + k, lf[k], w, w ? __ldg(a.td + (w - 1u)) : 0.0f, max_prev);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            v[k] = leaf_to_double(lf[k]);
+            m[k] = leaf_min_value(lf[k]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < PER; k += 2 > PER ? 1 : 2) {
+            if constexpr (PER == 1) {
+                v[0] = cg ? __ldcg(t.S + i0) : t.S[i0];
+            } else {
+                const double2 d = cg ? __ldcg(reinterpret_cast<const double2 *>(t.S + i0 + k))
+                                     : *reinterpret_cast<const double2 *>(t.S + i0 + k);
+                v[k] = d.x;
+                v[k + 1] = d.y;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) m[k] = cg ? __ldcg(t.M + i0 + k) : t.M[i0 + k];
+    }
+    // levels on registers: after step r the thread holds PER >> r nodes at (i0 >> r)
+    int lv = 0;
+#pragma unroll
+    for (int cnt = PER / 2; cnt >= 1; cnt /= 2) {
+        ++lv;
+#pragma unroll
+        for (int k = 0; k < cnt; ++k) {
+            v[k] = v[2 * k] + v[2 * k + 1];
+            m[k] = fmin_tree(m[2 * k], m[2 * k + 1]);
+        }
+        const unsigned long long node = i0 >> lv;
+        if (cnt == 4) store_run<4>(t, node, v, m);
+        else if (cnt == 2) store_run<2>(t, node, v, m);
+        else store_run<1>(t, node, v, m);
+    }
+    double sv = v[0];
+    float mv = m[0];
+    const unsigned long long pr = i0 >> lv;   // = (base >> lv) + tid
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int h = 1; h <= 5; ++h) {
+        const double os = __shfl_down_sync(0xffffffffu, sv, 1 << (h - 1));
+        const float om = __shfl_down_sync(0xffffffffu, mv, 1 << (h - 1));
+        sv = sv + os;
+        mv = fmin_tree(mv, om);
+        if ((lane & ((1 << h) - 1)) == 0) {
+            t.S[pr >> h] = sv;
+            t.M[pr >> h] = mv;
+        }
+    }
+    __shared__ double s_wv[kThreads / 32];
+    __shared__ float s_wm[kThreads / 32];
+    if (lane == 0) {
+        s_wv[warp] = sv;
+        s_wm[warp] = mv;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int nw = kThreads / 32;
+        sv = lane < nw ? s_wv[lane] : 0.0;
+        mv = lane < nw ? s_wm[lane] : __int_as_float(0x7f800000);
+        const unsigned long long pw = (pr >> 5) - (tid >> 5) + lane;   // the warp roots' depth
+#pragma unroll
+        for (int h = 1; h <= 3; ++h) {
+            const double os = __shfl_down_sync(0xffffffffu, sv, 1 << (h - 1));
+            const float om = __shfl_down_sync(0xffffffffu, mv, 1 << (h - 1));
+            sv = sv + os;
+            mv = fmin_tree(mv, om);
+            if ((lane & ((1 << h) - 1)) == 0 && lane < nw) {
+                t.S[pw >> h] = sv;
+                t.M[pw >> h] = mv;
+            }
+        }
+    }
+}
+
+// Every level above the w nodes (a power of two below 256 when called for the top, below 2048
+// for a small tree) of one depth starting at node `first`, in shared memory.
+__device__ void rebuild_smem(const RebuildArgs &a, unsigned long long first, int w, bool cg, float max_prev,
+                             unsigned char *smem)
+{
+    const TreeRefs &t = a.t;
+    double *s_v = reinterpret_cast<double *>(smem);                  // [kRbIn]
+    float *s_m = reinterpret_cast<float *>(smem + 8 * kRbIn);        // [kRbIn]
+    constexpr int kPer = kRbIn / 2 / kThreads;
+    for (int i = threadIdx.x; i < w; i += kThreads) {
+        const unsigned long long node = first + i;
+        if (node >= t.n) {
+            float lf = t.L[node - t.n];
+            if (a.win) {
+                const unsigned w = a.win[node - t.n];
+                lf = applied_leaf(a, node - t.n, lf, w, w ? __ldg(a.td + (w - 1u)) : 0.0f, max_prev);
+            }
+            s_v[i] = leaf_to_double(lf);
+            s_m[i] = leaf_min_value(lf);
+        } else {
+            s_v[i] = cg ? __ldcg(t.S + node) : t.S[node];
+            s_m[i] = cg ? __ldcg(t.M + node) : t.M[node];
+        }
+    }
+    for (int h = 1; (1 << h) <= w; ++h) {
+        const int cnt = w >> h;
+        double v[kPer];
+        float m[kPer];
         __syncthreads();
-        if (tid < cnt) {
-            sv = s_vs[2 * tid] + s_vs[2 * tid + 1];
-            mv = fmin_tree(s_vm[2 * tid], s_vm[2 * tid + 1]);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            if (i < cnt) {
+                v[k] = s_v[2 * i] + s_v[2 * i + 1];
+                m[k] = fmin_tree(s_m[2 * i], s_m[2 * i + 1]);
+            }
         }
         __syncthreads();
-        if (tid < cnt) {
-            s_vs[tid] = sv;
-            s_vm[tid] = mv;
-            const unsigned long long node = (first >> h) + tid;
-            t.S[node] = sv;
-            t.M[node] = mv;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            if (i < cnt) {
+                s_v[i] = v[k];
+                s_m[i] = m[k];
+                const unsigned long long node = (first >> h) + i;
+                t.S[node] = v[k];
+                t.M[node] = m[k];
+            }
         }
+    }
+}
+
+__device__ __forceinline__ void rebuild_fold(const RebuildArgs &a)
+{
+    if (a.fold && threadIdx.x == 0) {
+        fold_running_max(a.ctl, __ldcg(&a.ctl->batch_max_bits), a.alpha);
+        a.ctl->batch_max_bits = 0;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_rebuild_tree(RebuildArgs a)
+{
+    pdl_wait();
+    pdl_release();
+    const int cd = a.cd;
+    // winner lists of the leaf level, or the top levels' nodes (24 KiB)
+    __shared__ __align__(16) unsigned char s_buf[12 * kRbIn];
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);   // folded only at the end
+    if ((1ull << cd) < (unsigned long long)kRbIn) {                  // small tree: one CTA
+        rebuild_smem(a, 1ull << cd, 1 << cd, false, max_prev, s_buf);
+        rebuild_fold(a);
+        return;
+    }
+    const unsigned long long base = (1ull << cd) + (unsigned long long)blockIdx.x * kRbIn;
+    build_block<8>(a, base, cd == a.t.D, false, max_prev, s_buf);
+    const unsigned roots = gridDim.x;
+    if (roots == 1) {
+        rebuild_fold(a);
+        return;
+    }
+    if (roots <= (unsigned)kRbIn && last_to_arrive(&a.ctl->ticket_rebuild)) {
+        if (threadIdx.x == 0) a.ctl->ticket_rebuild = 0;
+        const unsigned long long first = 1ull << (cd - kRbLog);
+        __syncthreads();   // the block builder's shared words are reused below
+        if (roots == 2048) build_block<8>(a, first, false, true, max_prev, s_buf);
+        else if (roots == 1024) build_block<4>(a, first, false, true, max_prev, s_buf);
+        else if (roots == 512) build_block<2>(a, first, false, true, max_prev, s_buf);
+        else if (roots == 256) build_block<1>(a, first, false, true, max_prev, s_buf);
+        else rebuild_smem(a, first, (int)roots, true, max_prev, s_buf);
+        rebuild_fold(a);
     }
 }
 
@@ -638,6 +913,83 @@ __global__ void k_fill(float *p, unsigned long long n, float v)
     for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < n;
          i += (unsigned long long)gridDim.x * blockDim.x)
         p[i] = v;
+}
+
+// ------------------------------------------------------------------------------------------
+// Priority update for batches that touch a large share of the slots ("Putting prioritized
+// replay's segment tree on a GPU", Second Port and Measuring the Trade Honestly: the
+// level-synchronous rebuild of every node costs O(k + n), the per-entry climb O(k log n), and
+// the first wins once k is a large enough share of n).  The last writer wins through one
+// winner word per slot: every valid entry j raises win[i] to j + 1 (atomicMax); the entry that
+// then finds its own j + 1 there writes the slot and zeroes the word, so every word is zero
+// again after the call without a clearing pass.  Proportional mode then rebuilds every level
+// of both trees (k_rebuild_tree) and k_upd_finish folds the batch maximum.
+// ------------------------------------------------------------------------------------------
+struct ScatterArgs {
+    TreeRefs t;
+    float *raw_store;
+    Ctl *ctl;
+    DirtyRefs dirty;
+    unsigned *win;
+    const long long *idx;
+    const float *td;
+    unsigned B;
+    double eps;
+    LeafPowAlpha lp;
+    int proportional;
+};
+
+__global__ void __launch_bounds__(kThreads) k_upd_scatter(ScatterArgs a)
+{
+    pdl_wait();
+    pdl_release();
+    const unsigned long long size = a.ctl->size;
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    unsigned mymax = 0;
+    int bad = 0;
+    for (unsigned j = blockIdx.x * blockDim.x + threadIdx.x; j < a.B; j += gridDim.x * blockDim.x) {
+        const long long i = __ldg(a.idx + j);
+        if (i < 0 || (unsigned long long)i >= size) {
+            bad = 1;
+            continue;
+        }
+        mymax = max(mymax, __float_as_uint(td_to_raw(__ldg(a.td + j), a.eps, max_prev)));
+        atomicMax(a.win + i, j + 1);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
+    const unsigned bm = block_max_u32(mymax);
+    if (threadIdx.x == 0 && bm) atomicMax(&a.ctl->batch_max_bits, bm);
+}
+
+__global__ void __launch_bounds__(kThreads) k_upd_apply(ScatterArgs a)
+{
+    pdl_wait();
+    pdl_release();
+    const unsigned long long size = a.ctl->size;
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);   // not folded until k_upd_finish
+    for (unsigned j = blockIdx.x * blockDim.x + threadIdx.x; j < a.B; j += gridDim.x * blockDim.x) {
+        const long long i = __ldg(a.idx + j);
+        if (i < 0 || (unsigned long long)i >= size) continue;
+        if (__ldcg(a.win + i) != j + 1) continue;   // a later entry holds this slot (or has taken it)
+        a.win[i] = 0;
+        const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
+        if (a.proportional) {
+            a.t.L[i] = leaf_of(raw, a.lp);
+        } else {
+            a.raw_store[i] = raw;
+            mark_dirty(a.dirty, (unsigned long long)i);
+        }
+    }
+}
+
+__global__ void k_upd_finish(Ctl *c, double alpha)
+{
+    pdl_wait();
+    pdl_release();
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        fold_running_max(c, c->batch_max_bits, alpha);
+        c->batch_max_bits = 0;
+    }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1438,7 +1790,8 @@ cudaError_t init_tree_kernels(int carveout)
                                          (int)kUpdSmemBytes);
     if (e != cudaSuccess || carveout < 0) return e;
     const void *fns[] = {(const void *)k_update<kUpdWindow>, (const void *)k_add, (const void *)k_add_bulk_rows,
-                         (const void *)k_rebuild_levels, (const void *)k_add_finish, (const void *)k_fill};
+                         (const void *)k_rebuild_tree, (const void *)k_add_finish, (const void *)k_fill,
+                         (const void *)k_upd_scatter, (const void *)k_upd_apply, (const void *)k_upd_finish};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (e != cudaSuccess) return e;
@@ -1451,6 +1804,40 @@ cudaError_t launch_fill_mins(float *M, unsigned long long n, cudaStream_t st)
     const unsigned grid = (unsigned)std::min<unsigned long long>((n + kThreads - 1) / kThreads, 4096);
     k_fill<<<grid, kThreads, 0, st>>>(M, n, __builtin_huge_valf());
     return cudaGetLastError();
+}
+
+// Both trees rebuilt from the leaves: 11 levels per launch, the last launch's last CTA
+// finishing at the root (one launch up to 2^22 leaves, two up to 2^33).  `base` carries the
+// large-batch update's winner words and the fold of its maximum (win null for insertions).
+cudaError_t launch_rebuild_tree(const RebuildArgs &base, cudaStream_t st)
+{
+    cudaError_t e = cudaSuccess;
+    for (int cd = base.t.D; cd > 0 && e == cudaSuccess; cd -= kRbLog) {
+        const unsigned long long grid = cd < kRbLog ? 1 : 1ull << (cd - kRbLog);
+        RebuildArgs a = base;
+        a.cd = cd;
+        if (cd != base.t.D) a.win = nullptr;   // the leaves are done after the first launch
+        const bool last = grid <= (unsigned long long)kRbIn;
+        a.fold = last ? base.fold : 0;
+        e = launch_pdl(k_rebuild_tree, (unsigned)grid, kThreads, 0, st, a);
+        if (last) break;
+    }
+    return e;
+}
+
+RebuildArgs rebuild_args(const TreeRefs &t, Ctl *ctl)
+{
+    RebuildArgs a{};
+    a.t = t;
+    a.ctl = ctl;
+    a.cd = t.D;
+    a.win = nullptr;
+    a.td = nullptr;
+    a.eps = 0.0;
+    a.lp = make_leaf_pow_alpha(1.0);
+    a.fold = 0;
+    a.alpha = 1.0;
+    return a;
 }
 
 cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, Ctl *ctl,
@@ -1504,17 +1891,48 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     cudaError_t e = launch_pdl(k_add_bulk_rows, ncopy, kThreads, 0, st, a);
     if (e != cudaSuccess) return e;
     if (proportional) {
-        for (int cd = t.D; cd > 0; cd -= 8) {
-            const int pd = std::max(cd - 8, 0);
-            const unsigned long long width = 1ull << cd;
-            const unsigned grid = (unsigned)((width + kThreads - 1) / kThreads);
-            k_rebuild_levels<<<grid, kThreads, 0, st>>>(t, cd, pd);
-            e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
-        }
+        e = launch_rebuild_tree(rebuild_args(t, ctl), st);
+        if (e != cudaSuccess) return e;
     }
     k_add_finish<<<1, 32, 0, st>>>(ctl, count, C, alpha);
     return cudaGetLastError();
+}
+
+cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
+                                  const long long *idx, const float *td, double alpha, double eps,
+                                  bool proportional, int num_sms, const DirtyRefs &dirty, unsigned *win,
+                                  cudaStream_t st)
+{
+    ScatterArgs a;
+    a.t = t;
+    a.raw_store = raw_store;
+    a.ctl = ctl;
+    a.dirty = dirty;
+    a.win = win;
+    a.idx = idx;
+    a.td = td;
+    a.B = B;
+    a.eps = eps;
+    a.lp = make_leaf_pow_alpha(alpha);
+    a.proportional = proportional ? 1 : 0;
+    const unsigned grid = (unsigned)std::min<unsigned long long>((B + kThreads - 1) / kThreads,
+                                                                 (unsigned long long)num_sms * 8);
+    cudaError_t e = launch_pdl(k_upd_scatter, grid, kThreads, 0, st, a);
+    if (e != cudaSuccess) return e;
+    if (proportional && t.D > 0) {
+        // the leaf level of the rebuild applies the winners and the last CTA folds the maximum
+        RebuildArgs r = rebuild_args(t, ctl);
+        r.win = win;
+        r.td = td;
+        r.eps = eps;
+        r.lp = a.lp;
+        r.fold = 1;
+        r.alpha = alpha;
+        return launch_rebuild_tree(r, st);
+    }
+    e = launch_pdl(k_upd_apply, grid, kThreads, 0, st, a);
+    if (e == cudaSuccess) e = launch_pdl(k_upd_finish, 1, 32, 0, st, ctl, alpha);
+    return e;
 }
 
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,

@@ -41,6 +41,10 @@ struct per_buffer {
     // an upper bound on the slots written since (each insertion or update adds its count)
     bool order_valid = false, always_resort = false;
     bool dones_f32 = false;   // per_sample writes dones as float
+    // large-batch update: one winner word per slot (zero between calls) and the batch size from
+    // which it is used (0: the measured default; UINT32_MAX: never)
+    unsigned *win = nullptr;
+    uint32_t rebuild_batch = 0;
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
     uint64_t dirty_nwords = 0;
@@ -91,7 +95,7 @@ void free_all(per_buffer *h)
 {
     void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
                     h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
-                    h->dirty_words, h->rank.merge_status,
+                    h->dirty_words, h->rank.merge_status, h->win,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -105,6 +109,21 @@ bool alloc(T **p, uint64_t count)
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// The batch size from which per_update_priorities scatters (and, proportional, rebuilds every
+// tree level) instead of climbing from each changed leaf: per_config.rebuild_batch, else the
+// crossover measured on GB300 (L2 flushed before each call).  The rebuild costs about
+// 16 us + 5 ns per leaf; the climb about 18-25 us up to a few thousand entries, then grows with
+// the entries per subtree.  They meet near n/128 entries (2^21 leaves: 16384; 2^24: 131072);
+// below 1024 entries the two are within the timer's 2 us resolution at every tree size.  Rank
+// mode only scatters, which is faster from 1024 entries.
+uint64_t update_rebuild_batch(const per_buffer *h)
+{
+    if (h->rebuild_batch == UINT32_MAX) return UINT64_MAX;
+    if (h->rebuild_batch) return h->rebuild_batch;
+    if (h->mode == PER_MODE_RANK) return 1024;
+    return std::max<uint64_t>(h->n / 128, 1024);
+}
 
 // Rank mode: bring the slot order (keys/vals[merge_ctl[4]]) up to date for the filled slots.  When
 // the order exists and at most kMaxDirty slots (and no more than an eighth of them) were written
@@ -226,15 +245,17 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     h->seed = c.seed;
     h->always_resort = (c.flags & PER_FLAG_RANK_RESORT) != 0;
     h->dones_f32 = (c.flags & PER_FLAG_DONES_F32) != 0;
+    h->rebuild_batch = c.rebuild_batch;
 
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
-        ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n);
+        ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n) && alloc(&h->win, h->n);
     } else if (c.mode == PER_MODE_RANK) {
         ok = ok && alloc(&h->rank.raw, capacity) && alloc(&h->rank.cdf, capacity + 1) &&
              alloc(&h->rank.keys[0], capacity) && alloc(&h->rank.keys[1], capacity) &&
              alloc(&h->rank.vals[0], capacity) && alloc(&h->rank.vals[1], capacity) &&
-             alloc(&h->rank.status, rank_status_words(capacity)) && alloc(&h->rank.digit_hist, 4 * 256 + 16);
+             alloc(&h->rank.status, rank_status_words(capacity)) && alloc(&h->rank.digit_hist, 4 * 256 + 16) &&
+             alloc(&h->win, capacity);
         h->rank.sort_ctl = h->rank.digit_hist + 4 * 256;
         h->rank.capacity = capacity;
         h->rank.num_sms = h->num_sms;
@@ -266,6 +287,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (e == cudaSuccess && h->S) e = cudaMemset(h->S, 0, h->n * sizeof(double));
     if (e == cudaSuccess && h->M) e = launch_fill_mins(h->M, h->n, 0);
     if (e == cudaSuccess && h->rank.raw) e = cudaMemset(h->rank.raw, 0, capacity * sizeof(float));
+    if (e == cudaSuccess && h->win) e = cudaMemset(h->win, 0, (h->L ? h->n : capacity) * sizeof(unsigned));
     if (e == cudaSuccess && h->rank.status)
         e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
     if (e == cudaSuccess && h->rank.digit_hist) e = cudaMemset(h->rank.digit_hist, 0, (4 * 256 + 16) * sizeof(unsigned));
@@ -384,9 +406,14 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
     if (reinterpret_cast<uintptr_t>(d_idx) % 8 || reinterpret_cast<uintptr_t>(d_td) % 4)
         return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: misaligned input");
     if (h->mode == PER_MODE_UNIFORM) return PER_OK;   // no priorities
-    const cudaError_t e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, reinterpret_cast<const long long *>(d_idx),
-                                        d_td, h->alpha, h->eps, h->mode == PER_MODE_PROPORTIONAL, h->num_sms,
-                                        h->rank.dirty, as_stream(stream));
+    const long long *idx = reinterpret_cast<const long long *>(d_idx);
+    const bool prop = h->mode == PER_MODE_PROPORTIONAL;
+    const cudaError_t e =
+        B >= update_rebuild_batch(h)
+            ? launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
+                                    h->num_sms, h->rank.dirty, h->win, as_stream(stream))
+            : launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
+                            h->rank.dirty, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
     if (h->mode == PER_MODE_RANK) h->dirty_bound += B;
     return PER_OK;

@@ -24,7 +24,7 @@ struct Ctl {
     unsigned long long size;          // filled slots
     unsigned int max_raw_bits;        // running maximum raw priority (float bits, > 0)
     unsigned int err_flags;           // PER_DEVFLAG_* bits
-    unsigned int ticket_sample;       // (unused)
+    unsigned int ticket_rebuild;      // arrivals in a full tree rebuild
     unsigned int ticket_update;
     unsigned int ticket_add;
     unsigned int batch_max_bits;      // per-call maximum raw priority, folded in by the last CTA
@@ -176,6 +176,14 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
                        const float *prio, double alpha, double eps, bool proportional,
                        unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
                        bool *marked, cudaStream_t st);
+
+// Large batches: last-writer-wins scatter through the winner words `win` (one per slot, zero
+// between calls), then (proportional) a rebuild of every tree level.  Same result as
+// launch_update.
+cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
+                                  const long long *idx, const float *td, double alpha, double eps,
+                                  bool proportional, int num_sms, const DirtyRefs &dirty, unsigned *win,
+                                  cudaStream_t st);
 
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,

@@ -29,6 +29,10 @@ def _lib():
     capi.load()
 
 
+# per_config.rebuild_batch: climb from the changed leaves always, or scatter + rebuild always
+CLIMB, REBUILD = capi.REBUILD_NEVER, 1
+
+
 def _small(name, **kw):
     w = wl.WORKLOADS[name]
     return wl.Workload(**{**w.__dict__, **kw})
@@ -103,11 +107,12 @@ def test_gather_row_shapes(d, dp):
     p.close()
 
 
-def test_update_duplicates_nan_inf_and_bad_indices():
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
+def test_update_duplicates_nan_inf_and_bad_indices(rb):
     cap = 1 << 12
     w = _small("tiny", capacity=cap)
     g = wl.rng(4)
-    p = Pair(cap, 8, 8, 0.7, 1e-6, 0, seed=6)
+    p = Pair(cap, 8, 8, 0.7, 1e-6, 0, seed=6, rebuild_batch=rb)
     prefill(p, w, g, count=cap - 100)
     for rnd in range(6):
         _, want = p.sample(512, 0.5)
@@ -128,12 +133,14 @@ def test_update_duplicates_nan_inf_and_bad_indices():
     p.close()
 
 
-def test_update_all_in_one_subtree_overflow_path():
-    """More entries than one CTA sorts at once land in one subtree: the chunked path."""
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
+def test_update_all_in_one_subtree_overflow_path(rb):
+    """More entries than one CTA sorts at once land in one subtree: the chunked path (or, with
+    the rebuild path, thousands of entries racing for a few hundred winner words)."""
     cap = 1 << 16
     w = _small("tiny", capacity=cap)
     g = wl.rng(5)
-    p = Pair(cap, 8, 8, 0.6, 1e-6, 0, seed=7)
+    p = Pair(cap, 8, 8, 0.6, 1e-6, 0, seed=7, rebuild_batch=rb)
     prefill(p, w, g)
     for B in (4096, 20000):
         idx = g.integers(0, 300, size=B).astype(np.int64)   # all inside the first subtree
@@ -159,12 +166,13 @@ def test_equal_priorities_and_beta_zero():
     p.close()
 
 
-def test_many_sizes_of_batch_and_tree():
-    for D in (1, 4, 5, 6, 9, 10, 11, 15, 16):
+@pytest.mark.parametrize("rb", [0, CLIMB, REBUILD])
+def test_many_sizes_of_batch_and_tree(rb):
+    for D in (0, 1, 4, 5, 6, 9, 10, 11, 15, 16, 17):
         cap = 1 << D
         w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
         g = wl.rng(7, D)
-        p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=D)
+        p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=D, rebuild_batch=rb)
         prefill(p, w, g)
         for B in (1, 31, 32, 33, 257, 2049):
             _, want = p.sample(B, 0.4)
@@ -198,12 +206,13 @@ def test_leaf_values_over_a_wide_range(alpha):
 
 # -- rank-based variant ---------------------------------------------------------------------
 
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
 @pytest.mark.parametrize("cap,fill", [(1, 1), (100, 37), (4095, 4095), (4096, 4096), (4097, 4097),
                                       (100000, 65536)])
-def test_rank_small(cap, fill):
+def test_rank_small(cap, fill, rb):
     w = _small("rank", capacity=cap, state_dim=6, row_stride=8)
     g = wl.rng(8, cap)
-    p = Pair(cap, 6, 8, 0.7, 1e-6, 1, seed=9)
+    p = Pair(cap, 6, 8, 0.7, 1e-6, 1, seed=9, rebuild_batch=rb)
     prefill(p, w, g, count=fill, chunk=max(1, fill // 2))
     cdf = p.gpu.read_state(capi.PER_STATE_CDF)
     harness.assert_sums_close(cdf[1:], p.orc.cdf()[1:], what="rank CDF")
