@@ -23,6 +23,7 @@ _lib = None
 PROPORTIONAL = 0
 RANK = 1
 UNIFORM = 2
+FLAT = 3
 
 
 def build(force: bool = False) -> str:

@@ -46,6 +46,12 @@
  *      the stratified draw j (stream tag 2) takes mass (j + u_j) * (size / B) and slot
  *      floor(mass), weight 1; insertion stores rows (and follows the running maximum as in the
  *      other modes); updates change nothing.
+ *   R26 flat mode (the foxhunt design's own proportional sampler, [GPR] "Sampling Kernels",
+ *      Proportional steps 2-3): the same leaves and the same stratified draws as proportional
+ *      mode (stream tag 0), but no tree: at each sample the cumulative array
+ *      C[i] = C[i-1] + L[i] is summed left to right in binary64 over the filled slots, and draw
+ *      j takes the first i with C[i] > mass_j (binary search).  T = C[size-1]; p_min is the
+ *      smallest filled leaf; weights as R8.  Updates write leaves only.
  */
 #include "per_oracle.h"
 
@@ -190,7 +196,7 @@ orc_per *orc_create(uint64_t capacity, uint32_t state_dim, uint32_t row_stride_o
 {
     if (capacity == 0 || capacity > (1ull << 40) || row_stride_out < state_dim)
         return NULL;
-    if (!(eps > 0.0) || !(alpha >= 0.0) || mode > ORC_UNIFORM)
+    if (!(eps > 0.0) || !(alpha >= 0.0) || mode > ORC_FLAT)
         return NULL;
     orc_per *o = (orc_per *)calloc(1, sizeof(orc_per));
     if (!o)
@@ -215,6 +221,9 @@ orc_per *orc_create(uint64_t capacity, uint32_t state_dim, uint32_t row_stride_o
         ok = o->L && o->S && o->M;
         if (ok)
             rebuild_all(o);
+    } else if (mode == ORC_FLAT) {
+        o->L = (float *)calloc(o->n, sizeof(float));
+        ok = o->L != NULL;
     } else if (mode == ORC_RANK) {
         o->raw = (float *)calloc(capacity, sizeof(float));
         o->cdf = (double *)calloc(capacity + 1, sizeof(double));
@@ -299,6 +308,8 @@ int orc_add(orc_per *o, uint64_t count, const float *states, const float *next_s
             o->L[slot] = leaf_from_raw(raw, o->alpha);
             if (!bulk)
                 propagate_leaf(o, slot);
+        } else if (o->mode == ORC_FLAT) {
+            o->L[slot] = leaf_from_raw(raw, o->alpha);
         } else if (o->mode == ORC_RANK) {
             o->raw[slot] = raw;
         }
@@ -314,8 +325,50 @@ int orc_add(orc_per *o, uint64_t count, const float *states, const float *next_s
 
 /* [SEG "Sampling Is a Descent"]: walk from the root; go left when the left child's sum exceeds
  * the remaining mass, otherwise subtract it and go right. */
+/* R26: the cumulative array of the filled slots, summed left to right in binary64 */
+static double *flat_cumulative(const orc_per *o)
+{
+    double *C = (double *)malloc((o->size ? o->size : 1) * sizeof(double));
+    if (!C)
+        return NULL;
+    double acc = 0.0;
+    for (uint64_t i = 0; i < o->size; ++i) {
+        acc += (double)o->L[i];
+        C[i] = acc;
+    }
+    return C;
+}
+
+/* R26 with R6: the first i in [0, s) with C[i] > mass, or s when there is none */
+static uint64_t flat_search(const double *C, uint64_t s, double mass)
+{
+    uint64_t lo = 0, hi = s;
+    while (lo < hi) {
+        uint64_t mid = lo + (hi - lo) / 2;
+        if (C[mid] > mass)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
 int64_t orc_descend(const orc_per *o, double mass, double *rem)
 {
+    if (o->mode == ORC_FLAT) { /* flat mode locates the mass in the cumulative array */
+        double *C = flat_cumulative(o);
+        if (!C || o->size == 0) {
+            free(C);
+            return -1;
+        }
+        uint64_t i = flat_search(C, o->size, mass);
+        if (rem)
+            *rem = mass - (i == 0 ? 0.0 : C[i - 1]);
+        free(C);
+        return (int64_t)i;
+    }
+    if (o->mode != ORC_PROPORTIONAL) /* the descent needs the tree */
+        return -1;
     uint64_t idx = 1;
     while (idx < o->n) {
         double left = node_sum(o, 2 * idx);
@@ -428,6 +481,46 @@ int orc_sample(orc_per *o, uint32_t B, float beta, int64_t *idx, float *w, float
                 gather_row(o, j, (uint64_t)leaf, out_states, out_next, out_actions, out_rewards,
                            out_dones);
         }
+    } else if (o->mode == ORC_FLAT) {
+        /* R26: the cumulative array over the filled slots, left to right, then a binary search
+         * for the first entry above each stratified mass (R5, R6, R7, R8 as in the tree) */
+        uint64_t s = o->size;
+        double *C = flat_cumulative(o);
+        if (!C)
+            return ORC_ENOMEM;
+        float pmin = INFINITY;
+        for (uint64_t i = 0; i < s; ++i)
+            if (o->L[i] < pmin)
+                pmin = o->L[i];
+        double T = C[s - 1];
+        double seg = T / (double)B;
+        for (uint32_t j = 0; j < B; ++j) {
+            double u = orc_uniform53(o->seed, j, call, 0);
+            double mass = ((double)j + u) * seg;
+            int fell_off = 0;
+            uint64_t leaf = flat_search(C, s, mass);
+            if (leaf >= s) {
+                leaf = s - 1;
+                fell_off = 1;
+            }
+            idx[j] = (int64_t)leaf;
+            float lv = o->L[leaf];
+            if (w)
+                w[j] = (float)pow((double)lv / (double)pmin, -(double)beta);
+            double below = leaf ? C[leaf - 1] : 0.0;
+            double r = mass - below;
+            if (near) {
+                double tol = 1e-6 * T;
+                near[j] = (uint8_t)(fell_off || r < tol || (C[leaf] - mass) < tol);
+            }
+            if (rem)
+                rem[j] = r;
+            if (mass_out)
+                mass_out[j] = mass;
+            if (o->with_ring)
+                gather_row(o, j, leaf, out_states, out_next, out_actions, out_rewards, out_dones);
+        }
+        free(C);
     } else if (o->mode == ORC_UNIFORM) {
         /* R24: every filled slot weighs 1, so T = size and the walk is a division: draw j takes
          * mass (j + u_j) * (size / B), slot floor(mass), weight 1 */
@@ -526,6 +619,8 @@ int orc_update(orc_per *o, uint32_t B, const int64_t *idx, const float *td)
         if (o->mode == ORC_PROPORTIONAL) {
             o->L[i] = leaf_from_raw(raw, o->alpha);
             propagate_leaf(o, (uint64_t)i);
+        } else if (o->mode == ORC_FLAT) {
+            o->L[i] = leaf_from_raw(raw, o->alpha);
         } else {
             o->raw[i] = raw;
         }
@@ -548,6 +643,12 @@ double orc_total(const orc_per *o)
         return o->cdf[o->size];
     if (o->mode == ORC_UNIFORM)
         return (double)o->size;
+    if (o->mode == ORC_FLAT) { /* R26: the last entry of the cumulative array */
+        double acc = 0.0;
+        for (uint64_t i = 0; i < o->size; ++i)
+            acc += (double)o->L[i];
+        return acc;
+    }
     return node_sum(o, 1);
 }
 
@@ -557,6 +658,13 @@ float orc_min(const orc_per *o)
         return NAN;
     if (o->mode == ORC_UNIFORM)
         return 1.0f;
+    if (o->mode == ORC_FLAT) {
+        float m = INFINITY;
+        for (uint64_t i = 0; i < o->size; ++i)
+            if (o->L[i] < m)
+                m = o->L[i];
+        return m;
+    }
     return node_min(o, 1);
 }
 

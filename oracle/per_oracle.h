@@ -18,7 +18,7 @@
 extern "C" {
 #endif
 
-enum { ORC_PROPORTIONAL = 0, ORC_RANK = 1, ORC_UNIFORM = 2 };
+enum { ORC_PROPORTIONAL = 0, ORC_RANK = 1, ORC_UNIFORM = 2, ORC_FLAT = 3 };
 enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_EEMPTY = -2, ORC_ENOMEM = -3 };
 
 typedef struct orc_per orc_per;

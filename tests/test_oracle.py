@@ -527,3 +527,100 @@ def test_uniform_gather_after_wrap(orc):
         assert np.array_equal(out["states"][j, :d], st) and np.all(out["states"][j, d:] == 0)
         assert np.array_equal(out["next_states"][j, :d], nx) and np.all(out["next_states"][j, d:] == 0)
         assert out["actions"][j] == a and out["rewards"][j] == r and out["dones"][j] == dn
+
+
+# -- flat mode: cumulative array + binary search, no tree ---------------------------------------
+
+def _twins(orc, raw, capacity=None, alpha=0.6, seed=0):
+    """The same buffer twice: proportional (tree descent) and flat (scan + search)."""
+    out = []
+    for mode in (orc.PROPORTIONAL, orc.FLAT):
+        o = orc.Oracle(capacity or len(raw), 0, 0, alpha=alpha, mode=mode, seed=seed, with_ring=False)
+        o.add(raw_prio=np.asarray(raw, np.float32), count=len(raw))
+        out.append(o)
+    return out
+
+
+def test_flat_equals_tree_on_exact_sums(orc):
+    # integer leaves (alpha = 1): every prefix and every node sum is exact, so the tree's descent
+    # and the flat search must pick the same leaf for every mass, with the same weights
+    g = wl.rng(31)
+    raw = g.integers(1, 50, 3000).astype(np.float32)
+    tree, flat = _twins(orc, raw, capacity=4096, alpha=1.0, seed=4)
+    assert flat.total() == tree.total() == float(raw.astype(np.float64).sum())
+    assert flat.min() == tree.min() == raw.min()
+    for B in (1, 7, 512, 3000, 6001):
+        a, b = tree.sample(B, 0.4, gather=False), flat.sample(B, 0.4, gather=False)
+        assert np.array_equal(a["mass"], b["mass"])
+        assert np.array_equal(a["idx"], b["idx"])
+        assert np.array_equal(a["w"], b["w"])
+
+
+def test_flat_search_against_numpy_cumsum(orc):
+    # real leaves: the flat oracle's index is numpy's sequential cumsum + searchsorted(right)
+    g = wl.rng(32)
+    raw = g.lognormal(0, 2, 5000).astype(np.float32)
+    (flat,) = _twins(orc, raw, capacity=5000)[1:]
+    C = np.cumsum(flat.leaves()[:5000].astype(np.float64))
+    assert flat.total() == C[-1]
+    for _ in range(4):
+        out = flat.sample(777, 0.5, gather=False)
+        want = np.minimum(np.searchsorted(C, out["mass"], side="right"), 4999)
+        assert np.array_equal(out["idx"], want)
+        below = np.where(want > 0, C[np.maximum(want - 1, 0)], 0.0)
+        assert np.array_equal(out["rem"], out["mass"] - below)
+
+
+def test_flat_matches_tree_away_from_boundaries(orc):
+    # real leaves: the scan and the tree round differently, so only draws the oracle marks as
+    # near a boundary may differ
+    g = wl.rng(33)
+    raw = g.lognormal(0, 1, 1 << 14).astype(np.float32)
+    tree, flat = _twins(orc, raw, seed=9)
+    diff = near = 0
+    for _ in range(20):
+        a, b = tree.sample(1024, 0.4, gather=False), flat.sample(1024, 0.4, gather=False)
+        d = a["idx"] != b["idx"]
+        assert np.all(b["near"][d] | a["near"][d])
+        diff += int(d.sum())
+        near += int(b["near"].sum())
+    assert diff <= 2   # 20480 draws
+
+
+def test_flat_chi_square_and_updates(orc):
+    w = wl.WORKLOADS["tiny"]
+    g = wl.rng(34)
+    raw = wl.raw_priorities(g, w.capacity, "uniform")
+    tree, flat = _twins(orc, raw, alpha=w.alpha)
+    idx = g.integers(0, w.capacity, 300)
+    idx[:50] = idx[50:100]
+    td = wl.td_errors(g, 300)
+    td[5] = np.nan
+    assert tree.update(idx, td) == flat.update(idx, td) == 0
+    assert np.array_equal(tree.leaves(), flat.leaves()) and tree.max_raw == flat.max_raw
+    L = flat.leaves()[: w.capacity].astype(np.float64)
+    counts = np.zeros(w.capacity)
+    for _ in range(500):
+        counts += np.bincount(flat.sample(1024, w.beta, gather=False)["idx"], minlength=w.capacity)
+    N = counts.sum()
+    assert stats.chisquare(counts, N * L / L.sum()).pvalue > 1e-4
+    q = L ** (0.5 / w.alpha)
+    assert stats.chisquare(counts, N * q / q.sum()).pvalue < 1e-10
+    out = flat.sample(2048, 0.7, gather=False)
+    want = (L[out["idx"]] / L.min()) ** -0.7
+    harness.assert_weights_close(out["w"], want)
+
+
+def test_flat_search_every_boundary(orc):
+    # integer leaves: the prefix sums are exact, so a mass equal to C[i] goes to leaf i + 1 (the
+    # strict ">"), one ulp below it stays on leaf i, and the leftover is exact
+    g = wl.rng(35)
+    raw = g.integers(1, 9, 200).astype(np.float32)
+    tree, flat = _twins(orc, raw, capacity=256, alpha=1.0)
+    C = np.cumsum(raw.astype(np.float64))
+    for i in range(len(raw) - 1):
+        for m, want in ((C[i], i + 1), (np.nextafter(C[i], -np.inf), i), (np.nextafter(C[i], np.inf), i + 1)):
+            leaf, rem = flat.descend(m)
+            assert leaf == want and rem == m - (C[want - 1] if want else 0.0)
+            assert tree.descend(m) == (leaf, rem)
+    assert flat.descend(C[-1])[0] == len(raw)      # past the end: the sampler clamps it (R7)
