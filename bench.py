@@ -466,6 +466,81 @@ def run_gpu(args, rank, world):
     return res
 
 
+def run_flat_design(args):
+    """The apex step with the pages' own flat sampler (PER_MODE_FLAT: the leaves summed into a
+    cumulative array at each sample, one search per draw, no tree; updates only scatter leaves)
+    timed like the headline: K steps back to back between two events, then a pass with an event
+    between the calls for the per-call medians."""
+    import ctypes
+    import dataclasses
+    import torch
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    w = dataclasses.replace(wl.WORKLOADS[WORKLOAD], mode=wl.FLAT)
+    buf, staging, g = setup_gpu(torch, w)
+    L, h = capi.load(), buf._h
+    K, W, B, I = args.steps, args.warmup, w.batch, w.ingest
+    TD_SLOTS = 4096
+    td = torch.from_numpy(wl.td_errors(g, TD_SLOTS * B)).cuda()
+    out = buf.alloc_batch(B)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    beta = ctypes.c_float(w.beta)
+    add_args = [(h, I, *_ring_ptrs(staging, o * I), None, st) for o in range(w.staging // I)]
+    sample_args = (h, B, beta, *_out_ptrs(out), st)
+    idx_ptr, td0 = out["idx"].data_ptr(), td.data_ptr()
+    cr = Cudart()
+    rec = cr.lib.cudaEventRecord
+
+    def calls(t, ev=None):
+        if ev is not None:
+            rec(ev[0], st)
+        _check(L, h, L.per_add(*add_args[t % len(add_args)]), "per_add")
+        if ev is not None:
+            rec(ev[1], st)
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        if ev is not None:
+            rec(ev[2], st)
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * (t % TD_SLOTS), st), "per_update")
+        if ev is not None:
+            rec(ev[3], st)
+
+    for t in range(W):
+        calls(t)
+    torch.cuda.synchronize()
+    ca, cb = cr.events(2)
+    rec(ca, st)
+    for t in range(K):
+        calls(W + t)
+    rec(cb, st)
+    torch.cuda.synchronize()
+    cont_s = cr.elapsed_ms(ca, cb) / 1e3
+    cr.destroy([ca, cb])
+    Kop = min(K, 2000)
+    ev = cr.events(4 * Kop)
+    for t in range(Kop):
+        calls(W + K + t, ev[4 * t: 4 * t + 4])
+    torch.cuda.synchronize()
+    per = np.array([[cr.elapsed_ms(ev[4 * t + i], ev[4 * t + i + 1]) for i in range(3)] for t in range(Kop)])
+    cr.destroy(ev)
+    if buf.status_device() != 0:
+        raise RuntimeError("device error flag raised during the flat-design run")
+    n = w.capacity
+    # the scan reads every leaf and writes C (4 + 8 bytes per slot); the search reads about 5
+    # rounds of 32 probes per draw
+    res = {"value": round(K / cont_s, 2), "unit": UNIT, "ms_per_step": round(cont_s * 1e3 / K, 5),
+           "steps": K, "scan_bytes": 12 * n,
+           "ops_median_us": {"per_add (k_add, leaves only)": round(float(np.median(per[:, 0])) * 1e3, 3),
+                             "per_sample (k_flat_scan + k_sample_flat)": round(float(np.median(per[:, 1])) * 1e3, 3),
+                             "per_update (k_upd_scatter + k_upd_apply + k_upd_finish)":
+                                 round(float(np.median(per[:, 2])) * 1e3, 3)},
+           "gpu_launches_per_step": 6,
+           "note": ("the apex step in PER_MODE_FLAT (the pages' cumulative array + search, no tree), "
+                    "K steps back to back between two events; per-call medians from a pass with events "
+                    "between the calls (2.048 us event resolution)")}
+    buf.close()
+    return res
+
+
 def run_e2e(torch, buf, w, staging, g, K, dist):
     """Steps/s through the public C calls with the inputs in pinned host memory: each step copies
     its ingest rows and TD errors host->device (one packed copy) and the sampled batch
@@ -853,6 +928,8 @@ def main():
     ap.add_argument("--l2", default="flush", choices=["flush", "warm"],
                     help="flush L2 between timed steps, or rely on inputs larger than L2")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-flat", action="store_true",
+                    help="skip timing the apex step with the flat cumulative-array sampler")
     ap.add_argument("--update-crossover", action="store_true",
                     help="time both update paths against the batch size and exit")
     args = ap.parse_args()
@@ -892,6 +969,8 @@ def main():
             print(json.dumps(res))
         return
     res = run_gpu(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_flat:
+        res["flat_design"] = run_flat_design(args)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             sps, n, el = oracle_steps_per_s(budget_s=args.cpu_budget)

@@ -58,7 +58,10 @@ typedef enum {
 enum {
     PER_MODE_PROPORTIONAL = 0, /* P(i) = p_i^alpha / sum_k p_k^alpha, sum tree + min tree */
     PER_MODE_RANK = 1,         /* P(i) proportional to 1 / rank(i)^alpha, rank by raw priority */
-    PER_MODE_UNIFORM = 2       /* P(i) = 1 / size: the plain replay PER replaces; priorities unused */
+    PER_MODE_UNIFORM = 2,      /* P(i) = 1 / size: the plain replay PER replaces; priorities unused */
+    PER_MODE_FLAT = 3          /* proportional, located by the pages' own flat design: an inclusive
+                                  sum of the leaves rebuilt at each sample and a search per draw
+                                  ("Sampling Kernels", Proportional steps 2-3); no tree */
 };
 
 /* Bits of the device error word (per_status_device). */
@@ -159,6 +162,13 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
  * Replay", Experience Insertion): every filled slot weighs 1, so draw j (counter tag 2) takes
  * mass_j = (j + u_j) * (size / B) and slot floor(mass_j), clamped to the last filled slot;
  * w = 1.
+ * Flat mode ("Sampling Kernels", Proportional steps 2-5, the pages' own design): the same draws
+ * as proportional mode (tag 0); the call first sums the filled leaves into the inclusive array
+ * C[i] = L[0] + ... + L[i] (fixed-point sums with the unit 2^-52 of the largest leaf's binade,
+ * each prefix rounded once to binary64), then draw j takes the first slot with
+ * C[slot] > mass_j, T = C[size-1], and the same weight with p_min the smallest filled leaf.
+ * The sums round differently from the tree's, so slot choices can differ from proportional
+ * mode only for masses within rounding distance of a boundary.  Flat mode needs alpha <= 1.
  * Gather ("True Single-Graph Implementation Plan", Task 2/3): row j of d_states and d_next
  * receives the chosen slot's row, padded with 0.0f to row_stride_out floats.
  *   d_idx [B] int64 (required); d_w [B] float; d_states, d_next [B x row_stride_out] float;
@@ -183,7 +193,8 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * entries instead mark each slot's last batch position in a winner word, write the winners and
  * rebuild every level of both trees (the post's level-synchronous rebuild, Measuring the
  * Trade Honestly: O(k + n) beats O(k log n) once k is a large share of n); the trees come out
- * the same.  Rank mode stores raw.  Uniform mode has no
+ * the same.  Flat mode writes the leaves only (scatter path always; the next sample sums
+ * them).  Rank mode stores raw.  Uniform mode has no
  * priorities: the call checks its arguments and changes nothing.  The running maximum
  * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
  * PER_DEVFLAG_BAD_INDEX.
@@ -192,12 +203,13 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
 per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx,
                                  const float *d_td, void *stream);
 
-/* per_total -- the root of the sum tree (proportional), c_size (rank) or size (uniform), copied to *host_out.
- * Synchronises `stream`. */
+/* per_total -- the root of the sum tree (proportional), c_size (rank), size (uniform) or C[size-1]
+ * after a fresh scan (flat), copied to *host_out.  Synchronises `stream`. */
 per_status per_total(per_buffer *h, double *host_out, void *stream);
 
-/* per_min -- the root of the min tree: the smallest p^alpha over filled slots (proportional
- * mode only).  Synchronises `stream`.  PER_ERR_EMPTY when no slot is filled. */
+/* per_min -- the smallest p^alpha over filled slots: the root of the min tree (proportional) or
+ * the minimum a fresh scan carries (flat); other modes are rejected.  Synchronises `stream`.
+ * PER_ERR_EMPTY when no slot is filled. */
 per_status per_min(per_buffer *h, float *host_out, void *stream);
 
 /* per_size -- the number of filled slots as the host has counted the per_add calls enqueued
@@ -227,7 +239,9 @@ enum {
     PER_STATE_REWARDS = 8,  /* float [capacity] */
     PER_STATE_DONES = 9,    /* uint8 [capacity] */
     PER_STATE_COUNTERS = 10, /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
-    PER_STATE_RANK_ORDER = 11 /* uint32 [size at the last sample]: slots by rank (rank mode) */
+    PER_STATE_RANK_ORDER = 11, /* uint32 [size at the last sample]: slots by rank (rank mode) */
+    PER_STATE_CUMULATIVE = 12  /* double [size]: C[i] = leaves 0..i summed, as of the last sample,
+                                  per_total or per_min (flat mode) */
 };
 
 /* per_read_state -- copy `count` elements starting at element `first` of one of the arrays

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libgbper.so")
-SOURCES = ["per_api.cu", "k_tree.cu", "k_sample.cu", "k_rank.cu"]
+SOURCES = ["per_api.cu", "k_tree.cu", "k_sample.cu", "k_rank.cu", "k_flat.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -25,6 +25,7 @@ PER_ERR_TIMEOUT = 6
 PER_MODE_PROPORTIONAL = 0
 PER_MODE_RANK = 1
 PER_MODE_UNIFORM = 2
+PER_MODE_FLAT = 3
 
 PER_DEVFLAG_BAD_INDEX = 1
 PER_DEVFLAG_TIMEOUT = 2
@@ -35,13 +36,14 @@ REBUILD_NEVER = 0xFFFFFFFF      # per_config.rebuild_batch: always climb from th
 
 PER_STATE_LEAVES, PER_STATE_SUMS, PER_STATE_MINS, PER_STATE_RAW, PER_STATE_CDF = 0, 1, 2, 3, 4
 PER_STATE_STATES, PER_STATE_NEXT, PER_STATE_ACTIONS, PER_STATE_REWARDS = 5, 6, 7, 8
-PER_STATE_DONES, PER_STATE_COUNTERS, PER_STATE_RANK_ORDER = 9, 10, 11
+PER_STATE_DONES, PER_STATE_COUNTERS, PER_STATE_RANK_ORDER, PER_STATE_CUMULATIVE = 9, 10, 11, 12
 
 _STATE_DTYPE = {
     PER_STATE_LEAVES: np.float32, PER_STATE_SUMS: np.float64, PER_STATE_MINS: np.float32,
     PER_STATE_RAW: np.float32, PER_STATE_CDF: np.float64, PER_STATE_STATES: np.float32,
     PER_STATE_NEXT: np.float32, PER_STATE_ACTIONS: np.uint32, PER_STATE_REWARDS: np.float32,
     PER_STATE_DONES: np.uint8, PER_STATE_COUNTERS: np.uint64, PER_STATE_RANK_ORDER: np.uint32,
+    PER_STATE_CUMULATIVE: np.float64,
 }
 
 # every symbol include/gbper.h declares
@@ -315,7 +317,7 @@ class ReplayBuffer:
                      PER_STATE_NEXT: self.capacity * self.state_dim,
                      PER_STATE_ACTIONS: self.capacity, PER_STATE_REWARDS: self.capacity,
                      PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 4,
-                     PER_STATE_RANK_ORDER: self.size}[which] - first
+                     PER_STATE_RANK_ORDER: self.size, PER_STATE_CUMULATIVE: self.size}[which] - first
         buf = np.empty(max(count, 1), dtype=dtype)
         s = per_read_state(self._h, which, first, count, buf.ctypes.data_as(ctypes.c_void_p),
                            _stream(stream))

@@ -241,6 +241,90 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
     }
 }
 
+// The first position p in [lo, hi) with c[p] > m (c non-decreasing, values >= 0), or hi when
+// there is none: a 32-way search by the warp -- each round probes 32 evenly spaced entries and
+// keeps the bracket that holds the first entry above m (4 rounds for 2^20 entries).
+__device__ __forceinline__ unsigned long long first_above(const double *c, unsigned long long lo,
+                                                          unsigned long long hi, double m, int lane)
+{
+    while (true) {
+        const unsigned long long len = hi - lo;
+        if (len == 0) return hi;
+        if (len <= 32) {
+            const unsigned long long p = lo + lane;
+            const bool pred = p < hi && gt_nonneg(c[p], m);
+            const unsigned b = __ballot_sync(kFull, pred);
+            return b ? lo + (__ffs(b) - 1) : hi;
+        }
+        const unsigned long long step = (len + 31) / 32;
+        unsigned long long p = lo + (unsigned long long)(lane + 1) * step - 1;
+        if (p > hi - 1) p = hi - 1;
+        const bool pred = gt_nonneg(c[p], m);
+        const unsigned b = __ballot_sync(kFull, pred);
+        if (b == 0) return hi;
+        const int f = __ffs(b) - 1;
+        unsigned long long pf = lo + (unsigned long long)(f + 1) * step - 1;
+        if (pf > hi - 1) pf = hi - 1;
+        unsigned long long pprev = lo;
+        if (f > 0) {
+            pprev = lo + (unsigned long long)f * step - 1;
+            if (pprev > hi - 1) pprev = hi - 1;
+            pprev += 1;
+        }
+        lo = pprev;
+        hi = pf;  // the answer is in [lo, pf]; pf itself is above m
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Flat mode ("GPU-Resident Prioritized Experience Replay", Sampling Kernels, Proportional
+// steps 3-5): the same draws as proportional mode (counter tag 0, stratified), located by a
+// search of the cumulative array C that k_flat_scan built; w = (L[i] / p_min)^-beta; gather.
+// ------------------------------------------------------------------------------------------
+struct FlatSampleArgs {
+    const float *L;
+    const double *C;
+    const unsigned long long *res;   // [1] T bits, [2] smallest filled leaf bits
+    RingRefs r;
+    Ctl *ctl;
+    unsigned B;
+    double inv_b;
+    float beta;
+    unsigned long long seed;
+    SampleOut o;
+    int vec4;
+};
+
+__global__ void __launch_bounds__(kThreads, 4) k_sample_flat(FlatSampleArgs a)
+{
+    __shared__ unsigned long long s_call;
+    pdl_wait();
+    pdl_release();
+    if (threadIdx.x == 0) s_call = take_call_number(a.ctl);
+    const unsigned long long size = a.ctl->size;
+    const double total = __longlong_as_double((long long)a.res[1]);
+    const float pmin = __uint_as_float((unsigned)a.res[2]);
+    const double seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
+    __syncthreads();
+    const unsigned long long call = s_call;
+    const float nbeta = -a.beta;
+    const int lane = threadIdx.x & 31;
+    const unsigned wpb = blockDim.x >> 5;
+    const unsigned warps_total = gridDim.x * wpb;
+    for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
+        const double u = draw_uniform(a.seed, j, call, 0);
+        const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
+        unsigned long long slot = first_above(a.C, 0, size, m, lane);
+        if (slot >= size) slot = size - 1;   // ran past the filled slots
+        const float lv = a.L[slot];
+        if (lane == 0) {
+            a.o.idx[j] = (long long)slot;
+            if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
+        }
+        gather_row(a.r, a.o, j, slot, lane, a.vec4);
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // Rank mode ("Sampling Kernels", Rank-based step 2): rank r is drawn with probability
 // r^-alpha / c_size by locating the stratified mass in the CDF c (a 32-way search per warp:
@@ -284,41 +368,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
         const double u = draw_uniform(a.seed, j, call, 1);
         const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         // first position p in [1, size] with cdf[p] > m; size + 1 when there is none
-        unsigned long long lo = 1, hi = size + 1, ans = size + 1;
-        while (true) {
-            const unsigned long long len = hi - lo;
-            if (len == 0) {
-                ans = hi;
-                break;
-            }
-            if (len <= 32) {
-                const unsigned long long p = lo + lane;
-                const bool pred = p < hi && gt_nonneg(a.cdf[p], m);
-                const unsigned b = __ballot_sync(kFull, pred);
-                ans = b ? lo + (__ffs(b) - 1) : hi;
-                break;
-            }
-            const unsigned long long step = (len + 31) / 32;
-            unsigned long long p = lo + (unsigned long long)(lane + 1) * step - 1;
-            if (p > hi - 1) p = hi - 1;
-            const bool pred = gt_nonneg(a.cdf[p], m);
-            const unsigned b = __ballot_sync(kFull, pred);
-            if (b == 0) {
-                ans = hi;
-                break;
-            }
-            const int f = __ffs(b) - 1;
-            unsigned long long pf = lo + (unsigned long long)(f + 1) * step - 1;
-            if (pf > hi - 1) pf = hi - 1;
-            unsigned long long pprev = lo;
-            if (f > 0) {
-                pprev = lo + (unsigned long long)f * step - 1;
-                if (pprev > hi - 1) pprev = hi - 1;
-                pprev += 1;
-            }
-            lo = pprev;
-            hi = pf;  // answer in [lo, pf]; pf itself satisfies the predicate
-        }
+        const unsigned long long ans = first_above(a.cdf, 1, size + 1, m, lane);
         unsigned long long r = ans > size ? size : ans;
         const unsigned long long slot = sorted[r - 1];
         if (lane == 0) {
@@ -396,7 +446,7 @@ cudaError_t init_sample_kernels(int carveout)
     if (carveout < 0) return cudaSuccess;
     cudaError_t e;
     const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank,
-                         (const void *)k_sample_uniform};
+                         (const void *)k_sample_uniform, (const void *)k_sample_flat};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (e != cudaSuccess) return e;
@@ -422,6 +472,28 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
+}
+
+cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRefs &r, Ctl *ctl, unsigned B,
+                               float beta, unsigned long long seed, const SampleOut &o, int num_sms,
+                               cudaStream_t st)
+{
+    FlatSampleArgs a;
+    a.L = L;
+    a.C = fw.C;
+    a.res = fw.res;
+    a.r = r;
+    a.ctl = ctl;
+    a.B = B;
+    a.inv_b = (B & (B - 1)) == 0 ? 1.0 / (double)B : 0.0;
+    a.beta = beta;
+    a.seed = seed;
+    a.o = o;
+    a.vec4 = rows_vec4(r, o) ? 1 : 0;
+    const int wpb = warps_per_cta();
+    const unsigned long long ctas = (B + wpb - 1) / wpb;
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    return launch_pdl(k_sample_flat, grid, wpb * 32, 0, st, a);
 }
 
 cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsigned long long seed,

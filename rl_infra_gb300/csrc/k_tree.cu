@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                     leaf = a.t.L[s];
                 }
             }
-            if (a.proportional) {
+            if (a.proportional && a.t.S) {   // flat mode keeps leaves only
                 // the block's subtree: five levels inside each warp by shuffles, the rest on
                 // warp 0 from the warps' sums
                 const unsigned long long first = a.t.n + ((unsigned long long)blk << a.bl);
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
     if (last_to_arrive(&a.ctl->ticket_add)) {
         unsigned call_max = 0;
         if (tid == 0) call_max = __ldcg(&a.ctl->add_max_bits);   // in flight during the climb
-        if (a.proportional) {
+        if (a.proportional && a.t.S) {
             __shared__ double s_spS0[kTopSpan], s_spS1[kTopSpan];
             __shared__ float s_spM0[kTopSpan], s_spM1[kTopSpan];
             __shared__ double s_exS[64];
@@ -1890,7 +1890,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.ncopy = ncopy;
     cudaError_t e = launch_pdl(k_add_bulk_rows, ncopy, kThreads, 0, st, a);
     if (e != cudaSuccess) return e;
-    if (proportional) {
+    if (proportional && t.S) {
         e = launch_rebuild_tree(rebuild_args(t, ctl), st);
         if (e != cudaSuccess) return e;
     }
@@ -1919,7 +1919,7 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
                                                                  (unsigned long long)num_sms * 8);
     cudaError_t e = launch_pdl(k_upd_scatter, grid, kThreads, 0, st, a);
     if (e != cudaSuccess) return e;
-    if (proportional && t.D > 0) {
+    if (proportional && t.D > 0 && t.S) {
         // the leaf level of the rebuild applies the winners and the last CTA folds the maximum
         RebuildArgs r = rebuild_args(t, ctl);
         r.win = win;

@@ -30,6 +30,10 @@ struct per_buffer {
     float *M = nullptr;
     // rank
     RankWork rank{};
+    // flat
+    FlatWork flat{};
+    void *flat_mem = nullptr;
+    uint64_t flat_bytes = 0;
     // ring
     float *states = nullptr, *next = nullptr;
     uint32_t *actions = nullptr;
@@ -95,7 +99,7 @@ void free_all(per_buffer *h)
 {
     void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
                     h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
-                    h->dirty_words, h->rank.merge_status, h->win,
+                    h->dirty_words, h->rank.merge_status, h->win, h->flat_mem,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -210,11 +214,16 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: alpha must be finite and >= 0");
     if (!(c.eps > 0.0) || !std::isfinite(c.eps))
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: eps must be finite and > 0");
-    if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK && c.mode != PER_MODE_UNIFORM)
+    if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK && c.mode != PER_MODE_UNIFORM &&
+        c.mode != PER_MODE_FLAT)
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown mode");
     if (c.flags & ~(PER_FLAG_RANK_RESORT | PER_FLAG_DONES_F32))
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown flags");
-    if (c.mode == PER_MODE_PROPORTIONAL && !((float)std::pow(c.eps, c.alpha) >= 1.17549435e-38f))
+    if (c.mode == PER_MODE_FLAT && c.alpha > 1.0)
+        return fail(nullptr, PER_ERR_INVALID_ARG,
+                    "per_create: flat mode needs alpha <= 1 (every leaf then stays a finite binary32)");
+    if ((c.mode == PER_MODE_PROPORTIONAL || c.mode == PER_MODE_FLAT) &&
+        !((float)std::pow(c.eps, c.alpha) >= 1.17549435e-38f))
         return fail(nullptr, PER_ERR_INVALID_ARG,
                     "per_create: eps^alpha underflows binary32; a leaf of 0 would read as an empty slot");
 
@@ -250,6 +259,28 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
         ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n) && alloc(&h->win, h->n);
+    } else if (c.mode == PER_MODE_FLAT) {
+        // one block: C [capacity] f64, tile sums and offsets (u64 each), the result words, tile
+        // minima f32, tickets
+        const uint64_t tiles = flat_tiles(capacity);
+        const uint64_t bytes = 8 * capacity + tiles * (8 + 16 + 4) + 4 * 8 + 2 * 4;
+        ok = ok && alloc(&h->L, h->n) && alloc(&h->win, capacity) &&
+             cudaMalloc(&h->flat_mem, bytes) == cudaSuccess;
+        if (ok) {
+            char *p = static_cast<char *>(h->flat_mem);
+            h->flat.C = reinterpret_cast<double *>(p);
+            p += 8 * capacity;
+            h->flat.agg = reinterpret_cast<unsigned long long *>(p);
+            p += 8 * tiles;
+            h->flat.excl = reinterpret_cast<unsigned long long *>(p);
+            p += 16 * tiles;
+            h->flat.res = reinterpret_cast<unsigned long long *>(p);
+            p += 4 * 8;
+            h->flat.tmin = reinterpret_cast<float *>(p);
+            p += 4 * tiles;
+            h->flat.tick = reinterpret_cast<unsigned *>(p);
+            h->flat_bytes = bytes;
+        }
     } else if (c.mode == PER_MODE_RANK) {
         ok = ok && alloc(&h->rank.raw, capacity) && alloc(&h->rank.cdf, capacity + 1) &&
              alloc(&h->rank.keys[0], capacity) && alloc(&h->rank.keys[1], capacity) &&
@@ -287,7 +318,8 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (e == cudaSuccess && h->S) e = cudaMemset(h->S, 0, h->n * sizeof(double));
     if (e == cudaSuccess && h->M) e = launch_fill_mins(h->M, h->n, 0);
     if (e == cudaSuccess && h->rank.raw) e = cudaMemset(h->rank.raw, 0, capacity * sizeof(float));
-    if (e == cudaSuccess && h->win) e = cudaMemset(h->win, 0, (h->L ? h->n : capacity) * sizeof(unsigned));
+    if (e == cudaSuccess && h->win) e = cudaMemset(h->win, 0, (h->S ? h->n : capacity) * sizeof(unsigned));
+    if (e == cudaSuccess && h->flat_mem) e = cudaMemset(h->flat_mem, 0, h->flat_bytes);
     if (e == cudaSuccess && h->rank.status)
         e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
     if (e == cudaSuccess && h->rank.digit_hist) e = cudaMemset(h->rank.digit_hist, 0, (4 * 256 + 16) * sizeof(unsigned));
@@ -344,7 +376,8 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
     bool marked = false;
     const cudaError_t e = launch_add(tree_of(h), ring_of(h), h->rank.raw, h->ctl, count, d_states, d_next,
                                      d_actions, d_rewards, d_dones, d_raw_prio, h->alpha, h->eps,
-                                     h->mode == PER_MODE_PROPORTIONAL, h->host_cursor, h->num_sms,
+                                     h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT,
+                                     h->host_cursor, h->num_sms,
                                      h->rank.dirty, &marked, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "per_add launch");
     if (h->mode == PER_MODE_RANK) {
@@ -385,6 +418,11 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
         e = launch_sample_prop(tree_of(h), ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms, as_stream(stream));
     } else if (h->mode == PER_MODE_UNIFORM) {
         e = launch_sample_uniform(ring_of(h), h->ctl, B, h->seed, o, h->num_sms, as_stream(stream));
+    } else if (h->mode == PER_MODE_FLAT) {
+        e = launch_flat_scan(h->L, h->flat, h->ctl, h->capacity, as_stream(stream));
+        if (e == cudaSuccess)
+            e = launch_sample_flat(h->L, h->flat, ring_of(h), h->ctl, B, beta, h->seed, o, h->num_sms,
+                                   as_stream(stream));
     } else {
         e = rank_order(h, as_stream(stream));
         const unsigned *sorted = h->rank.vals[1];   // unused: the kernel reads the order's buffer
@@ -407,9 +445,9 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
         return fail(h, PER_ERR_INVALID_ARG, "per_update_priorities: misaligned input");
     if (h->mode == PER_MODE_UNIFORM) return PER_OK;   // no priorities
     const long long *idx = reinterpret_cast<const long long *>(d_idx);
-    const bool prop = h->mode == PER_MODE_PROPORTIONAL;
+    const bool prop = h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT;
     const cudaError_t e =
-        B >= update_rebuild_batch(h)
+        (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h))
             ? launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
                                     h->num_sms, h->rank.dirty, h->win, as_stream(stream))
             : launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
@@ -430,6 +468,13 @@ per_status per_total(per_buffer *h, double *host_out, void *stream)
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         *host_out = (double)size;
         return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_total");
+    } else if (h->mode == PER_MODE_FLAT) {
+        if (h->host_size == 0) {
+            *host_out = 0.0;
+            return PER_OK;
+        }
+        e = launch_flat_scan(h->L, h->flat, h->ctl, h->capacity, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, h->flat.res + 1, sizeof(double), cudaMemcpyDeviceToHost, st);
     } else if (h->mode == PER_MODE_RANK) {
         e = cudaMemcpyAsync(host_out, h->rank.cdf + h->host_size, sizeof(double), cudaMemcpyDeviceToHost, st);
     } else if (h->D == 0) {
@@ -448,11 +493,23 @@ per_status per_total(per_buffer *h, double *host_out, void *stream)
 per_status per_min(per_buffer *h, float *host_out, void *stream)
 {
     if (!h || !host_out) return PER_ERR_INVALID_ARG;
-    if (h->mode != PER_MODE_PROPORTIONAL) return fail(h, PER_ERR_INVALID_ARG, "per_min: proportional mode only");
+    if (h->mode != PER_MODE_PROPORTIONAL && h->mode != PER_MODE_FLAT)
+        return fail(h, PER_ERR_INVALID_ARG, "per_min: proportional and flat modes only");
     if (h->host_size == 0) return fail(h, PER_ERR_EMPTY, "per_min: the buffer holds no transition");
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
     float v = 0.0f;
+    if (h->mode == PER_MODE_FLAT) {
+        unsigned long long bits = 0;
+        e = launch_flat_scan(h->L, h->flat, h->ctl, h->capacity, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, h->flat.res + 2, sizeof(bits), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(h, e, "per_min");
+        const unsigned b32 = (unsigned)bits;
+        std::memcpy(&v, &b32, sizeof(v));
+        *host_out = v;
+        return PER_OK;
+    }
     if (h->D == 0) {
         e = cudaMemcpyAsync(&v, h->L, sizeof(float), cudaMemcpyDeviceToHost, st);
     } else {
@@ -526,6 +583,12 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
         }
         elems = h->order_size;
         esz = 4;
+        break;
+    case PER_STATE_CUMULATIVE:
+        if (h->mode != PER_MODE_FLAT) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: flat mode only");
+        src = h->flat.C;
+        elems = h->host_size;
+        esz = 8;
         break;
     case PER_STATE_COUNTERS: {
         if (first + count > 4) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");

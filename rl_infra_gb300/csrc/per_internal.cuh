@@ -208,6 +208,30 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
 cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsigned long long seed,
                                   const SampleOut &o, int num_sms, cudaStream_t st);
 
+// Flat mode ("GPU-Resident Prioritized Experience Replay", Sampling Kernels, Proportional steps
+// 2-3): the cumulative array of the leaves, rebuilt at each sample (fixed-point sums with the unit
+// 2^-52 of the largest leaf's binade, rounded once to binary64), and searched by the sampler.
+struct FlatWork {
+    double *C;                   // [capacity] C[i] = sum of leaves 0..i (filled slots)
+    unsigned long long *agg;     // [tiles] each tile's fixed-point sum
+    unsigned long long *excl;    // [2 tiles] the sum of the tiles before it (128 bits: low, high)
+    float *tmin;                 // [tiles] each tile's smallest filled leaf
+    unsigned *tick;              // [2]: arrivals of the reduce pass
+    unsigned long long *res;     // [4]: [1] T = C[size-1] (binary64 bits), [2] smallest filled leaf (bits)
+};
+
+unsigned long long flat_tiles(unsigned long long capacity);
+
+// Rebuilds C over the filled slots; T and the smallest leaf land in res[1], res[2].
+cudaError_t launch_flat_scan(const float *L, const FlatWork &fw, Ctl *ctl, unsigned long long capacity,
+                             cudaStream_t st);
+
+// Draw j (counter tag 0, as proportional mode): mass_j = (j + u_j) (T / B), the first slot with
+// C[slot] > mass_j, w = (L[slot] / p_min)^-beta, fused gather.
+cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRefs &r, Ctl *ctl, unsigned B,
+                               float beta, unsigned long long seed, const SampleOut &o, int num_sms,
+                               cudaStream_t st);
+
 struct RankWork {
     float *raw;
     double *cdf;

@@ -26,6 +26,7 @@ import numpy as np
 PROPORTIONAL = 0
 RANK = 1
 UNIFORM = 2
+FLAT = 3
 
 
 @dataclass(frozen=True)

@@ -75,6 +75,25 @@ class Pair:
         if self.mode == capi.PER_MODE_RANK:
             assert np.array_equal(self.gpu.read_state(capi.PER_STATE_RAW), self.orc.raw())
             return
+        if self.mode == capi.PER_MODE_FLAT:
+            gl = self.gpu.read_state(capi.PER_STATE_LEAVES)
+            ol = self.orc.leaves()
+            ulp = harness.f32_ulp_diff(gl, ol)
+            assert ulp.max() <= 1, f"leaves differ by {ulp.max()} ulp"
+            self.stats["leaf_ulp"] = int((ulp > 0).sum())
+            n = int(self.orc.size)
+            if n == 0:
+                return
+            # the scan's rounding order differs from the oracle's left-to-right sum: both are
+            # within n * 2^-53 * T of the exact sums (relative 1e-9 covers 2^31 slots)
+            T = self.gpu.total()
+            assert abs(T - self.orc.total()) <= 1e-9 * self.orc.total()
+            C = self.gpu.read_state(capi.PER_STATE_CUMULATIVE)
+            want = np.cumsum(gl[:n].astype(np.float64))
+            assert C.shape == want.shape and np.all(np.abs(C - want) <= 1e-9 * T)
+            assert C[-1] == T
+            assert self.gpu.min() == gl[:n].min()
+            return
         gl = self.gpu.read_state(capi.PER_STATE_LEAVES)
         ol = self.orc.leaves()
         ulp = harness.f32_ulp_diff(gl, ol)

@@ -339,7 +339,98 @@ def test_uniform_mode_wrap_and_update_no_op():
     p.close()
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+# -- flat mode: the pages' own cumulative array + search ----------------------------------------
+
+FLAT = capi.PER_MODE_FLAT
+
+
+@pytest.mark.parametrize("cap,fill", [(1, 1), (3, 2), (2047, 2047), (2048, 2048), (2049, 2049),
+                                      (5000, 3001), (1 << 16, 1 << 16), (100000, 70001)])
+def test_flat_mode(cap, fill):
+    w = _small("tiny", capacity=cap, state_dim=6, row_stride=8, mode=FLAT)
+    g = wl.rng(24, cap)
+    p = Pair(cap, 6, 8, 0.6, 1e-6, FLAT, seed=11)
+    prefill(p, w, g, count=fill, chunk=max(1, fill // 3))
+    p.check_tree()
+    p.check_counters()
+    for B in (1, 7, 512, 3 * fill + 1):
+        _, want = p.sample(B, 0.4)
+        idx = wl.duplicate_positions(g, want["idx"], 0.25) if B > 4 else want["idx"]
+        td = wl.td_errors(g, B)
+        td[:1] = np.nan
+        p.update(idx, td)
+        p.check_tree()
+        p.check_counters()
+    assert p.stats["mismatch"] <= max(1, p.stats["draws"] // 10000), p.stats
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
+def test_flat_mode_wrap_bad_indices_and_gather():
+    cap = 3000
+    w = _small("tiny", capacity=cap, state_dim=5, row_stride=7, mode=FLAT)
+    g = wl.rng(25)
+    p = Pair(cap, 5, 7, 0.6, 1e-6, FLAT, seed=4)
+    for count, with_prio in ((1000, True), (1500, False), (7001, True), (1, False), (3000, True)):
+        rows = wl.transitions(g, count, w)
+        p.add(rows, wl.raw_priorities(g, count, "lognormal") if with_prio else None)
+        p.check_tree()
+        p.check_counters()
+        _, want = p.sample(256, 0.5)
+        p.update(want["idx"], wl.td_errors(g, 256))
+    p.update(np.array([-1, cap + 5, 3], np.int64), np.ones(3, np.float32))
+    assert p.gpu.status_device() == capi.PER_DEVFLAG_BAD_INDEX
+    p.check_tree()
+    p.close()
+
+
+def test_flat_mode_wide_range_and_equal_leaves():
+    """Leaves over 2^-30 .. 2^30 (the fixed-point sums must stay as close to the exact prefix as
+    binary64 summation) and a run of equal leaves (exact sums: every boundary is exact)."""
+    cap = 1 << 15
+    g = wl.rng(27)
+    p = Pair(cap, 0, 0, 1.0, 1e-30, FLAT, seed=2, with_ring=False)
+    raw = np.exp2(g.uniform(-30, 30, cap)).astype(np.float32)
+    p.gpu.add(None, None, dev(np.zeros(cap, np.uint32)), dev(np.zeros(cap, np.float32)),
+              dev(np.zeros(cap, np.uint8)), dev(raw))
+    p.orc.add(raw_prio=raw, count=cap)
+    p.check_tree()
+    for _ in range(4):
+        p.sample(4096, 0.4, check_rows=False)
+    assert p.stats["mismatch"] <= max(1, p.stats["draws"] // 10000), p.stats
+    p.close()
+    q = Pair(4096, 0, 0, 1.0, 1e-6, FLAT, seed=3, with_ring=False)
+    ones = np.full(4096, 0.75, np.float32)
+    q.gpu.add(None, None, dev(np.zeros(4096, np.uint32)), dev(np.zeros(4096, np.float32)),
+              dev(np.zeros(4096, np.uint8)), dev(ones))
+    q.orc.add(raw_prio=ones, count=4096)
+    assert np.array_equal(q.gpu.read_state(capi.PER_STATE_CUMULATIVE) if q.gpu.total() else None,
+                          np.arange(1, 4097) * 0.75)
+    for B in (4096, 1000):
+        got, want = q.sample(B, 0.4, check_rows=False)
+        assert q.stats["mismatch"] == 0
+    q.close()
+
+
+@pytest.mark.slow
+def test_flat_apex_size_rounds():
+    """2^21 slots, B = 512, ingest 4096 per round, the apex shapes, in flat mode."""
+    w = _small("apex", mode=FLAT)
+    g = wl.rng(26)
+    p = Pair(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, FLAT, seed=0, with_ring=True)
+    prefill(p, w, g, chunk=1 << 18)
+    for rnd in range(4):
+        rows = wl.transitions(g, w.ingest, w)
+        p.add(rows, None)
+        _, want = p.sample(w.batch, w.beta, check_rows=(rnd == 3))
+        p.update(want["idx"], wl.td_errors(g, w.batch))
+    p.check_tree()
+    p.check_counters()
+    assert p.stats["mismatch"] <= max(1, p.stats["draws"] // 10000), p.stats
+    p.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_float_dones(mode):
     cap = 3000
     w = _small("tiny", capacity=cap, state_dim=8, row_stride=8, mode=mode)
@@ -356,7 +447,7 @@ def test_float_dones(mode):
     p.close()
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_graph_replayed_rounds(mode):
     """Insert + sample + update captured once per staging offset as CUDA graphs and replayed:
     every replay inserts at the device cursor, draws a fresh batch (device call counter) and, in
@@ -406,7 +497,7 @@ def test_graph_replayed_rounds(mode):
             _assert_rank_order(p)                    # the order this replay's sample used
         p.orc.update(idx_sets[o], td_sets[o])
     torch.cuda.synchronize()
-    if mode == 0:
+    if mode in (0, 3):
         p.check_tree()
     p.check_counters()
     assert p.gpu.status_device() == 0
