@@ -79,17 +79,19 @@ def kernel_source_hash(name):
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel, kernel_file):
-    """Per-launch DRAM bytes (read + write) of a kernel, from the committed ncu summary
-    profiles/traffic.txt (lines of key=value: kernel, file, src_sha, dram_bytes_per_launch), if
-    the kernel's source file is unchanged since the capture (else None)."""
+def traffic_from_profiles(kernel, kernel_file, workload="apex"):
+    """Per-launch DRAM bytes (read + write) of a kernel on a workload, from the committed ncu
+    summary profiles/traffic.txt (lines of key=value: kernel, file, src_sha,
+    dram_bytes_per_launch, workload), if the kernel's source file is unchanged since the capture
+    (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     want = kernel_source_hash(kernel_file)
     for line in open(p):
         parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-        if parts.get("kernel") == kernel and parts.get("file") == kernel_file and parts.get("src_sha") == want:
+        if (parts.get("kernel") == kernel and parts.get("file") == kernel_file and parts.get("src_sha") == want
+                and parts.get("workload") == workload):
             try:
                 return float(parts["dram_bytes_per_launch"])
             except (KeyError, ValueError):
@@ -659,6 +661,8 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
 
 # -- the other workloads (sample + update steps; rank adds the sort) -------------------------------
 
+KERNEL_FILES = {"k_sample_prop": "k_sample.cu", "k_update": "k_tree.cu", "k_sample_uniform": "k_sample.cu"}
+
 OTHER = {
     "tiny": "tiny: 2^10 leaves, state_dim 8, B=32, alpha 0.6, beta 0.4",
     "dqn": "dqn: 2^20 leaves, state_dim 48 gathered into 64-float rows, B=1024, beta 0.4->1.0 over 341 steps",
@@ -789,7 +793,8 @@ def run_other(args, name, resort=False):
         "bytes_per_step": {k: int(v[1]) for k, v in ops.items()},
         "hbm_gbs_algorithmic": round((b_sam + b_upd) / (total_s / K) / 1e9, 2),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 5), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 5),
+                     "traffic": traffic_from_profiles(dom, KERNEL_FILES[dom], name) if dom in KERNEL_FILES else None,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
                      "median_launch_us": round(ms * 1e3, 3)},
         "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
@@ -824,6 +829,9 @@ def run_update_crossover(args):
     configs = [("tiny tree", 1 << 10, wl.PROPORTIONAL), ("2^16 tree", 1 << 16, wl.PROPORTIONAL),
                ("dqn tree", 1 << 20, wl.PROPORTIONAL), ("apex tree", 1 << 21, wl.PROPORTIONAL),
                ("stress tree", 1 << 24, wl.PROPORTIONAL), ("rank slots", 1 << 20, wl.RANK)]
+    if args.crossover_trees:
+        keep = set(args.crossover_trees.split(","))
+        configs = [c for c in configs if c[0].split()[0] in keep]
     for label, n, mode in configs:
         bufs = {}
         for path, rb in (("climb", capi.REBUILD_NEVER), ("rebuild", 1)):
@@ -864,6 +872,8 @@ def run_update_crossover(args):
             buf.close()
     cross = {}
     for label, n, _ in configs:
+        if not any(r["tree"] == label for r in rows):
+            continue
         rs = [r for r in rows if r["tree"] == label]
         first = next((r["B"] for r in rs if r["rebuild_us"] < r["climb_us"]), None)
         cross[label] = first
@@ -932,6 +942,9 @@ def main():
                     help="skip timing the apex step with the flat cumulative-array sampler")
     ap.add_argument("--update-crossover", action="store_true",
                     help="time both update paths against the batch size and exit")
+    ap.add_argument("--crossover-trees", default="",
+                    help="comma-separated first words of the sweep's tree labels (tiny, 2^16, dqn, apex, "
+                         "stress, rank); all when empty")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
