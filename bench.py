@@ -763,7 +763,7 @@ def run_other(args, name, resort=False):
         b_sort = (16 * n + 8 * d) if not resort else (4 * 16 * n + 4 * n)
         b_sam = b_sort + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
         b_upd = 12 * B + 4 * d
-        names = ("rank order + k_sample_rank", "k_update")
+        names = ("rank order + k_sample_rank", "update (k_upd_scatter + k_upd_apply + k_upd_finish)")
     elif w.mode == wl.UNIFORM:
         # idx + weight out; rows read and written; action, reward in and out; done 1 B in, 4 B out
         b_sam = B * (8 + 4 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 8 + 8 + 5)
@@ -797,7 +797,8 @@ def run_other(args, name, resort=False):
                      "traffic": traffic_from_profiles(dom, KERNEL_FILES[dom], name) if dom in KERNEL_FILES else None,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
                      "median_launch_us": round(ms * 1e3, 3)},
-        "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
+        # rank: order (merge, or histogram + 4 sort passes) + sampler + the 3 scatter-path update kernels
+        "gpu_launches": ((9 if resort else 5) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
     }
     if w.mode == wl.RANK:
         res["config"]["rank_order"] = ("every slot sorted again at each sample (4-pass radix sort)" if resort
@@ -834,8 +835,11 @@ def run_update_crossover(args):
         configs = [c for c in configs if c[0].split()[0] in keep]
     for label, n, mode in configs:
         bufs = {}
-        for path, rb in (("climb", capi.REBUILD_NEVER), ("rebuild", 1)):
-            buf = capi.ReplayBuffer(n, 0, 0.6, 1e-6, mode, 0, 0, rebuild_batch=rb)
+        paths = [("climb", capi.REBUILD_NEVER, capi.ELEMENT_NEVER), ("rebuild", 1, capi.ELEMENT_NEVER)]
+        if mode == wl.PROPORTIONAL:
+            paths.append(("element", capi.REBUILD_NEVER, capi.ELEMENT_ALWAYS))
+        for path, rb, eb in paths:
+            buf = capi.ReplayBuffer(n, 0, 0.6, 1e-6, mode, 0, 0, rebuild_batch=rb, element_batch=eb)
             chunk = min(n, 1 << 20)
             a = torch.zeros(chunk, dtype=torch.int32, device="cuda")
             r = torch.zeros(chunk, dtype=torch.float32, device="cuda")
@@ -845,13 +849,15 @@ def run_update_crossover(args):
                 buf.add(None, None, a, r, d, prio)
             bufs[path] = buf
         torch.cuda.synchronize()
-        Bs = [b for b in (16, 64, 256, 1024, 4096, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20, 1 << 22)
-              if b <= 4 * n]
+        Bs = [b for b in (1, 4, 16, 64, 256, 1024, 4096, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20,
+                          1 << 22) if b <= 4 * n]
         for B in Bs:
             idx = torch.from_numpy(g.integers(0, n, B).astype(np.int64)).cuda()
             td = torch.from_numpy(wl.td_errors(g, B)).cuda()
             row = {"tree": label, "n": n, "B": B}
             for path, buf in bufs.items():
+                if path == "element" and B > 1024:
+                    continue   # one entry after another: about 1.5 us each
                 h = buf._h
                 ev = cr.events(2 * reps)
                 for t in range(3 + reps):
@@ -870,15 +876,16 @@ def run_update_crossover(args):
             if buf.status_device() != 0:
                 raise RuntimeError("device error flag raised during the update sweep")
             buf.close()
-    cross = {}
+    cross, elem = {}, {}
     for label, n, _ in configs:
         if not any(r["tree"] == label for r in rows):
             continue
         rs = [r for r in rows if r["tree"] == label]
-        first = next((r["B"] for r in rs if r["rebuild_us"] < r["climb_us"]), None)
-        cross[label] = first
-    return {"metric": "per_update_priorities time by batch size, both paths (us, L2 flushed)",
-            "reps": reps, "rows": rows, "rebuild_faster_from_B": cross}
+        cross[label] = next((r["B"] for r in rs if r["rebuild_us"] < r["climb_us"]), None)
+        if any("element_us" in r for r in rs):
+            elem[label] = next((r["B"] for r in rs if "element_us" in r and r["element_us"] > r["climb_us"]), None)
+    return {"metric": "per_update_priorities time by batch size, each path (us, L2 flushed)",
+            "reps": reps, "rows": rows, "rebuild_faster_from_B": cross, "element_slower_from_B": elem}
 
 
 # -- the oracle on the host cores ------------------------------------------------------------------

@@ -93,8 +93,14 @@ typedef struct {
     uint32_t rebuild_batch;  /* update batches of at least this many entries scatter their
                                 priorities and rebuild every tree level instead of climbing from
                                 each changed leaf (same result); 0: the crossover measured on
-                                GB300 (max(leaves / 128, 1024) proportional, 1024 rank);
+                                GB300 (max(leaves / 128, 1024) proportional; rank mode
+                                always scatters);
                                 UINT32_MAX: never */
+    uint32_t element_batch;  /* proportional mode: update batches of fewer entries than this
+                                propagate entry by entry, each from its leaf to the root (same
+                                result); 0: the crossover measured on GB300 (3: batches of
+                                one or two entries); 1: never; UINT32_MAX: always */
+    uint32_t reserved;       /* 0 */
 } per_config;
 
 /*

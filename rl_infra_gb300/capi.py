@@ -32,7 +32,9 @@ PER_DEVFLAG_TIMEOUT = 2
 PER_DEVFLAG_RANK_STALE = 4
 PER_FLAG_RANK_RESORT = 1
 PER_FLAG_DONES_F32 = 2
-REBUILD_NEVER = 0xFFFFFFFF      # per_config.rebuild_batch: always climb from the changed leaves
+REBUILD_NEVER = 0xFFFFFFFF      # per_config.rebuild_batch: never scatter + rebuild
+ELEMENT_NEVER = 1               # per_config.element_batch: never propagate entry by entry
+ELEMENT_ALWAYS = 0xFFFFFFFF     # per_config.element_batch: always propagate entry by entry
 
 PER_STATE_LEAVES, PER_STATE_SUMS, PER_STATE_MINS, PER_STATE_RAW, PER_STATE_CDF = 0, 1, 2, 3, 4
 PER_STATE_STATES, PER_STATE_NEXT, PER_STATE_ACTIONS, PER_STATE_REWARDS = 5, 6, 7, 8
@@ -55,7 +57,8 @@ EXPORTS = ("per_create", "per_destroy", "per_add", "per_sample", "per_update_pri
 class per_config(ctypes.Structure):
     _fields_ = [("alpha", ctypes.c_double), ("eps", ctypes.c_double), ("mode", ctypes.c_uint32),
                 ("row_stride_out", ctypes.c_uint32), ("seed", ctypes.c_uint64),
-                ("flags", ctypes.c_uint32), ("rebuild_batch", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("rebuild_batch", ctypes.c_uint32),
+                ("element_batch", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class PerError(RuntimeError):
@@ -216,7 +219,7 @@ class ReplayBuffer:
     """One GPU-resident prioritized replay buffer (device memory owned by libgbper)."""
 
     def __init__(self, capacity, state_dim, alpha=0.6, eps=1e-6, mode=PER_MODE_PROPORTIONAL,
-                 row_stride_out=None, seed=0, flags=0, rebuild_batch=0):
+                 row_stride_out=None, seed=0, flags=0, rebuild_batch=0, element_batch=0):
         import torch
         self.capacity = int(capacity)
         self.state_dim = int(state_dim)
@@ -226,7 +229,7 @@ class ReplayBuffer:
         self.device = torch.device("cuda", torch.cuda.current_device())
         self.dones_dtype = torch.float32 if int(flags) & PER_FLAG_DONES_F32 else torch.uint8
         cfg = per_config(float(alpha), float(eps), int(mode), self.row_stride, int(seed), int(flags),
-                         int(rebuild_batch))
+                         int(rebuild_batch), int(element_batch), 0)
         self._h = per_create(self.capacity, self.state_dim, cfg)
         self.nleaves = per_nleaves(self._h)[1]
 

@@ -916,6 +916,85 @@ __global__ void k_fill(float *p, unsigned long long n, float v)
 }
 
 // ------------------------------------------------------------------------------------------
+// Priority update for a few entries: the per-element propagation the post measures its level
+// rebuild against ("Putting prioritized replay's segment tree on a GPU", Measuring the Trade
+// Honestly: each changed leaf walks to the root).  One warp takes the entries in batch order;
+// for each it writes the leaf, loads the sibling of every ancestor at once (lane l the sibling
+// at height l) and recomputes the ancestors bottom-up, each the binary64 sum of its two
+// children, lane l storing the node at height l + 1.  The warp orders its memory between
+// entries, so a later entry sees an earlier one's nodes: the last writer wins and every node
+// ends as the sum of its final children, as in a sequential update.
+// ------------------------------------------------------------------------------------------
+struct ElementArgs {
+    TreeRefs t;
+    Ctl *ctl;
+    const long long *idx;
+    const float *td;
+    unsigned B;
+    double alpha, eps;
+    LeafPowAlpha lp;
+};
+
+__global__ void __launch_bounds__(32) k_upd_element(ElementArgs a)
+{
+    pdl_wait();
+    pdl_release();
+    const int lane = threadIdx.x;
+    const TreeRefs t = a.t;
+    const int D = t.D;
+    const unsigned long long size = a.ctl->size;
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    unsigned batch_max = 0;
+    bool bad = false;
+    for (unsigned j0 = 0; j0 < a.B; j0 += 32) {
+        const unsigned jl = j0 + lane;
+        const long long iv = jl < a.B ? __ldg(a.idx + jl) : -1;
+        const float tv = jl < a.B ? __ldg(a.td + jl) : 0.0f;
+        const unsigned cnt = a.B - j0 < 32u ? a.B - j0 : 32u;
+        for (unsigned q = 0; q < cnt; ++q) {
+            const long long i = __shfl_sync(0xffffffffu, iv, (int)q);
+            const float tq = __shfl_sync(0xffffffffu, tv, (int)q);
+            if (i < 0 || (unsigned long long)i >= size) {
+                bad = true;
+                continue;
+            }
+            const float raw = td_to_raw(tq, a.eps, max_prev);
+            batch_max = max(batch_max, __float_as_uint(raw));
+            const float leaf = leaf_of(raw, a.lp);
+            const unsigned long long v0 = t.n + (unsigned long long)i;
+            double sv = 0.0;
+            float sm = __int_as_float(0x7f800000);
+            if (lane < D) {
+                const unsigned long long sib = (v0 >> lane) ^ 1ull;
+                sv = ld_sum_cg(t, sib);
+                sm = ld_min_cg(t, sib);
+            }
+            if (lane == 0) t.L[i] = leaf;
+            double v = (double)leaf, mine_v = 0.0;
+            float m = leaf_min_value(leaf), mine_m = 0.0f;
+            for (int l = 0; l < D; ++l) {
+                v = v + __shfl_sync(0xffffffffu, sv, l);
+                m = fmin_tree(m, __shfl_sync(0xffffffffu, sm, l));
+                if (lane == l) {
+                    mine_v = v;
+                    mine_m = m;
+                }
+            }
+            if (lane < D) {
+                const unsigned long long node = v0 >> (lane + 1);
+                t.S[node] = mine_v;
+                t.M[node] = mine_m;
+            }
+            __syncwarp();
+        }
+    }
+    if (lane == 0) {
+        if (bad) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
+        fold_running_max(a.ctl, batch_max, a.alpha);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
 // Priority update for batches that touch a large share of the slots ("Putting prioritized
 // replay's segment tree on a GPU", Second Port and Measuring the Trade Honestly: the
 // level-synchronous rebuild of every node costs O(k + n), the per-entry climb O(k log n), and
@@ -1791,7 +1870,8 @@ cudaError_t init_tree_kernels(int carveout)
     if (e != cudaSuccess || carveout < 0) return e;
     const void *fns[] = {(const void *)k_update<kUpdWindow>, (const void *)k_add, (const void *)k_add_bulk_rows,
                          (const void *)k_rebuild_tree, (const void *)k_add_finish, (const void *)k_fill,
-                         (const void *)k_upd_scatter, (const void *)k_upd_apply, (const void *)k_upd_finish};
+                         (const void *)k_upd_scatter, (const void *)k_upd_apply, (const void *)k_upd_finish,
+                         (const void *)k_upd_element};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
         if (e != cudaSuccess) return e;
@@ -1896,6 +1976,21 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     }
     k_add_finish<<<1, 32, 0, st>>>(ctl, count, C, alpha);
     return cudaGetLastError();
+}
+
+cudaError_t launch_update_element(const TreeRefs &t, Ctl *ctl, unsigned B, const long long *idx,
+                                  const float *td, double alpha, double eps, cudaStream_t st)
+{
+    ElementArgs a;
+    a.t = t;
+    a.ctl = ctl;
+    a.idx = idx;
+    a.td = td;
+    a.B = B;
+    a.alpha = alpha;
+    a.eps = eps;
+    a.lp = make_leaf_pow_alpha(alpha);
+    return launch_pdl(k_upd_element, 1, 32, 0, st, a);
 }
 
 cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,

@@ -49,6 +49,7 @@ struct per_buffer {
     // which it is used (0: the measured default; UINT32_MAX: never)
     unsigned *win = nullptr;
     uint32_t rebuild_batch = 0;
+    uint32_t element_batch = 0;   // per_config.element_batch
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
     uint64_t dirty_nwords = 0;
@@ -114,19 +115,33 @@ bool alloc(T **p, uint64_t count)
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Measured on GB300 (L2 flushed before each call): one entry propagates in about 10 us (the
+// climb takes 16-21 us at any small batch), each further entry adds about 3 us, so one or two
+// entries go entry by entry.
+constexpr uint64_t kDefaultElementBatch = 3;
+
 // The batch size from which per_update_priorities scatters (and, proportional, rebuilds every
 // tree level) instead of climbing from each changed leaf: per_config.rebuild_batch, else the
 // crossover measured on GB300 (L2 flushed before each call).  The rebuild costs about
 // 16 us + 5 ns per leaf; the climb about 18-25 us up to a few thousand entries, then grows with
 // the entries per subtree.  They meet near n/128 entries (2^21 leaves: 16384; 2^24: 131072);
-// below 1024 entries the two are within the timer's 2 us resolution at every tree size.  Rank
-// mode only scatters, which is faster from 1024 entries.
+// below 1024 entries the two are within the timer's 2 us resolution at every tree size.  In
+// rank mode (no tree) the scatter is at least as fast as the climb at every batch size.
 uint64_t update_rebuild_batch(const per_buffer *h)
 {
     if (h->rebuild_batch == UINT32_MAX) return UINT64_MAX;
     if (h->rebuild_batch) return h->rebuild_batch;
-    if (h->mode == PER_MODE_RANK) return 1024;
+    if (h->mode == PER_MODE_RANK) return 1;
     return std::max<uint64_t>(h->n / 128, 1024);
+}
+
+// Proportional batches of fewer entries than this propagate entry by entry (per_config.element_batch,
+// else the crossover measured on GB300).
+uint64_t update_element_batch(const per_buffer *h)
+{
+    if (h->mode != PER_MODE_PROPORTIONAL || h->D == 0) return 0;
+    if (h->element_batch) return h->element_batch;
+    return kDefaultElementBatch;
 }
 
 // Rank mode: bring the slot order (keys/vals[merge_ctl[4]]) up to date for the filled slots.  When
@@ -217,6 +232,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (c.mode != PER_MODE_PROPORTIONAL && c.mode != PER_MODE_RANK && c.mode != PER_MODE_UNIFORM &&
         c.mode != PER_MODE_FLAT)
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown mode");
+    if (c.reserved != 0) return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: reserved must be 0");
     if (c.flags & ~(PER_FLAG_RANK_RESORT | PER_FLAG_DONES_F32))
         return fail(nullptr, PER_ERR_INVALID_ARG, "per_create: unknown flags");
     if (c.mode == PER_MODE_FLAT && c.alpha > 1.0)
@@ -255,6 +271,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     h->always_resort = (c.flags & PER_FLAG_RANK_RESORT) != 0;
     h->dones_f32 = (c.flags & PER_FLAG_DONES_F32) != 0;
     h->rebuild_batch = c.rebuild_batch;
+    h->element_batch = c.element_batch;
 
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
@@ -447,7 +464,9 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
     const long long *idx = reinterpret_cast<const long long *>(d_idx);
     const bool prop = h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT;
     const cudaError_t e =
-        (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h))
+        B < update_element_batch(h)
+            ? launch_update_element(tree_of(h), h->ctl, B, idx, d_td, h->alpha, h->eps, as_stream(stream))
+        : (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h))
             ? launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
                                     h->num_sms, h->rank.dirty, h->win, as_stream(stream))
             : launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,

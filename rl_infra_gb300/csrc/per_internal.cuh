@@ -177,6 +177,11 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
                        unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
                        bool *marked, cudaStream_t st);
 
+// A few entries (proportional mode, with a tree): one warp propagates them one after another,
+// each from its leaf to the root.  Same result as launch_update.
+cudaError_t launch_update_element(const TreeRefs &t, Ctl *ctl, unsigned B, const long long *idx,
+                                  const float *td, double alpha, double eps, cudaStream_t st);
+
 // Large batches: last-writer-wins scatter through the winner words `win` (one per slot, zero
 // between calls), then (proportional) a rebuild of every tree level.  Same result as
 // launch_update.

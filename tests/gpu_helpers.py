@@ -23,11 +23,11 @@ def dev(a):
 
 class Pair:
     def __init__(self, capacity, d, dp=None, alpha=0.6, eps=1e-6, mode=0, seed=0,
-                 with_ring=True, flags=0, rebuild_batch=0):
+                 with_ring=True, flags=0, rebuild_batch=0, element_batch=0):
         dp = d if dp is None else dp
         self.d, self.dp, self.mode = d, dp, mode
         self.gpu = capi.ReplayBuffer(capacity, d, alpha, eps, mode, dp, seed, flags=flags,
-                                     rebuild_batch=rebuild_batch)
+                                     rebuild_batch=rebuild_batch, element_batch=element_batch)
         self.orc = oracle.Oracle(capacity, d, dp, alpha, eps, mode, seed, with_ring)
         self.stats = {"draws": 0, "mismatch": 0, "near": 0, "leaf_ulp": 0}
 

@@ -29,8 +29,13 @@ def _lib():
     capi.load()
 
 
-# per_config.rebuild_batch: climb from the changed leaves always, or scatter + rebuild always
-CLIMB, REBUILD = capi.REBUILD_NEVER, 1
+# the update's three paths, each forced through per_config: climb from the changed leaves,
+# scatter + rebuild every level, or propagate entry by entry
+CLIMB = dict(rebuild_batch=capi.REBUILD_NEVER, element_batch=capi.ELEMENT_NEVER)
+REBUILD = dict(rebuild_batch=1, element_batch=capi.ELEMENT_NEVER)
+ELEMENT = dict(rebuild_batch=capi.REBUILD_NEVER, element_batch=capi.ELEMENT_ALWAYS)
+DEFAULT = dict()
+PATH_IDS = ["climb", "rebuild", "element"]
 
 
 def _small(name, **kw):
@@ -107,12 +112,12 @@ def test_gather_row_shapes(d, dp):
     p.close()
 
 
-@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD, ELEMENT], ids=PATH_IDS)
 def test_update_duplicates_nan_inf_and_bad_indices(rb):
     cap = 1 << 12
     w = _small("tiny", capacity=cap)
     g = wl.rng(4)
-    p = Pair(cap, 8, 8, 0.7, 1e-6, 0, seed=6, rebuild_batch=rb)
+    p = Pair(cap, 8, 8, 0.7, 1e-6, 0, seed=6, **rb)
     prefill(p, w, g, count=cap - 100)
     for rnd in range(6):
         _, want = p.sample(512, 0.5)
@@ -133,14 +138,14 @@ def test_update_duplicates_nan_inf_and_bad_indices(rb):
     p.close()
 
 
-@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD], ids=PATH_IDS[:2])
 def test_update_all_in_one_subtree_overflow_path(rb):
     """More entries than one CTA sorts at once land in one subtree: the chunked path (or, with
     the rebuild path, thousands of entries racing for a few hundred winner words)."""
     cap = 1 << 16
     w = _small("tiny", capacity=cap)
     g = wl.rng(5)
-    p = Pair(cap, 8, 8, 0.6, 1e-6, 0, seed=7, rebuild_batch=rb)
+    p = Pair(cap, 8, 8, 0.6, 1e-6, 0, seed=7, **rb)
     prefill(p, w, g)
     for B in (4096, 20000):
         idx = g.integers(0, 300, size=B).astype(np.int64)   # all inside the first subtree
@@ -166,13 +171,13 @@ def test_equal_priorities_and_beta_zero():
     p.close()
 
 
-@pytest.mark.parametrize("rb", [0, CLIMB, REBUILD])
+@pytest.mark.parametrize("rb", [DEFAULT, CLIMB, REBUILD, ELEMENT], ids=["default"] + PATH_IDS)
 def test_many_sizes_of_batch_and_tree(rb):
     for D in (0, 1, 4, 5, 6, 9, 10, 11, 15, 16, 17):
         cap = 1 << D
         w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
         g = wl.rng(7, D)
-        p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=D, rebuild_batch=rb)
+        p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=D, **rb)
         prefill(p, w, g)
         for B in (1, 31, 32, 33, 257, 2049):
             _, want = p.sample(B, 0.4)
@@ -206,13 +211,13 @@ def test_leaf_values_over_a_wide_range(alpha):
 
 # -- rank-based variant ---------------------------------------------------------------------
 
-@pytest.mark.parametrize("rb", [CLIMB, REBUILD])
+@pytest.mark.parametrize("rb", [CLIMB, REBUILD], ids=PATH_IDS[:2])
 @pytest.mark.parametrize("cap,fill", [(1, 1), (100, 37), (4095, 4095), (4096, 4096), (4097, 4097),
                                       (100000, 65536)])
 def test_rank_small(cap, fill, rb):
     w = _small("rank", capacity=cap, state_dim=6, row_stride=8)
     g = wl.rng(8, cap)
-    p = Pair(cap, 6, 8, 0.7, 1e-6, 1, seed=9, rebuild_batch=rb)
+    p = Pair(cap, 6, 8, 0.7, 1e-6, 1, seed=9, **rb)
     prefill(p, w, g, count=fill, chunk=max(1, fill // 2))
     cdf = p.gpu.read_state(capi.PER_STATE_CDF)
     harness.assert_sums_close(cdf[1:], p.orc.cdf()[1:], what="rank CDF")
