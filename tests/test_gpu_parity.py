@@ -156,6 +156,33 @@ def test_update_all_in_one_subtree_overflow_path(rb):
     p.close()
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_large_batch_climb(mode):
+    """Batches of 4096 entries and more on the climb path (CTAs of 16 warps, lists of 128):
+    duplicates, bad indices, NaN/Inf, and one subtree holding more entries than its list."""
+    cap = 1 << 17
+    w = _small("tiny", capacity=cap, state_dim=4, row_stride=4, mode=mode)
+    g = wl.rng(13, mode)
+    p = Pair(cap, 4, 4, 0.6, 1e-6, mode, seed=3, **CLIMB)
+    prefill(p, w, g)
+    for rnd in range(4):
+        B = (4096, 8192, 20000, 5000)[rnd]
+        idx = g.integers(0, cap, B).astype(np.int64)
+        idx = wl.duplicate_positions(g, idx, 0.25)
+        td = wl.td_errors(g, B)
+        if rnd == 1:
+            idx[:3] = [-1, cap + 7, 1 << 40]
+            td[5:8] = [np.nan, np.inf, -np.inf]
+        if rnd == 2:
+            idx[:3000] = g.integers(0, 200, 3000)   # one subtree: more than its list holds
+        p.update(idx, td)
+        p.check_tree()
+        p.check_counters()
+        assert p.gpu.status_device() == (capi.PER_DEVFLAG_BAD_INDEX if rnd == 1 else 0)
+        _, want = p.sample(1024, 0.4, check_rows=False)
+    p.close()
+
+
 def test_equal_priorities_and_beta_zero():
     cap = 1 << 12
     w = _small("tiny", capacity=cap)
@@ -415,6 +442,24 @@ def test_flat_mode_wide_range_and_equal_leaves():
         got, want = q.sample(B, 0.4, check_rows=False)
         assert q.stats["mismatch"] == 0
     q.close()
+
+
+def test_flat_mode_over_a_thousand_tiles():
+    """More than 1024 tiles of 2048 leaves, a ragged last tile, and the reduce pass's last CTA
+    scanning more than 4 tile sums per thread."""
+    cap = (1 << 21) + 4099
+    g = wl.rng(28)
+    p = Pair(cap, 0, 0, 0.6, 1e-6, FLAT, seed=5, with_ring=False)
+    raw = wl.raw_priorities(g, cap, "lognormal")
+    p.gpu.add(None, None, dev(np.zeros(cap, np.uint32)), dev(np.zeros(cap, np.float32)),
+              dev(np.zeros(cap, np.uint8)), dev(raw))
+    p.orc.add(raw_prio=raw, count=cap)
+    for _ in range(3):
+        _, want = p.sample(2048, 0.4, check_rows=False)
+        p.update(want["idx"], wl.td_errors(g, 2048))
+    p.check_tree()
+    assert p.stats["mismatch"] <= max(1, p.stats["draws"] // 10000), p.stats
+    p.close()
 
 
 @pytest.mark.slow
