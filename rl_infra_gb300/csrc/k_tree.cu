@@ -637,6 +637,52 @@ __device__ __forceinline__ float applied_leaf(const RebuildArgs &a, unsigned lon
     return leaf;
 }
 
+// Sums of 8 leaves for the three register levels as exact integers: each leaf (0 or a normal
+// binary32) is its 24-bit significand shifted by (exponent - elo), elo the smallest exponent among
+// them; when the exponents span at most 26 binades every partial sum is below 2^53, so it is the
+// exact value a binary64 add of the two children gives.  Returns false (sums unset) otherwise, or
+// for an infinite or subnormal leaf.
+__device__ __forceinline__ bool exact_leaf_sums(const float *lf, unsigned long long *isum, int &elo)
+{
+    int lo = 255, hi = 0;
+    bool special = false;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const unsigned b = __float_as_uint(lf[k]);
+        const int e = (int)(b >> 23);
+        if (b != 0u) {
+            lo = min(lo, e);
+            hi = max(hi, e);
+            special |= e == 0 || e == 255;
+        }
+    }
+    if (special || (hi >= lo && hi - lo > 26)) return false;
+    if (hi < lo) lo = 127;   // every leaf is 0
+    unsigned long long iv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const unsigned b = __float_as_uint(lf[k]);
+        iv[k] = b ? (unsigned long long)((b & 0x7fffffu) | 0x800000u) << ((int)(b >> 23) - lo) : 0ull;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) isum[k] = iv[2 * k] + iv[2 * k + 1];
+    isum[4] = isum[0] + isum[1];
+    isum[5] = isum[2] + isum[3];
+    isum[6] = isum[4] + isum[5];
+    elo = lo;
+    return true;
+}
+
+// x * 2^(elo - 150) for an integer x < 2^53: exact, assembled on the integer pipe
+__device__ __forceinline__ double fixed_to_double_exact(unsigned long long x, int elo)
+{
+    if (x == 0ull) return 0.0;
+    const int p = 63 - __clzll((long long)x);
+    const unsigned long long mant = x << (52 - p);
+    const unsigned long long e = (unsigned long long)(p + elo - 150 + 1023);
+    return __longlong_as_double((long long)((e << 52) | (mant & ((1ull << 52) - 1ull))));
+}
+
 template <int CNT>
 __device__ __forceinline__ void store_run(const TreeRefs &t, unsigned long long node, const double *v,
                                           const float *m)
@@ -667,6 +713,9 @@ __device__ __forceinline__ void build_block(const RebuildArgs &a, unsigned long 
     const unsigned long long i0 = base + (unsigned long long)PER * tid;
     double v[PER];
     float m[PER];
+    bool exact = false;             // leaves whose three register levels are exact integer sums
+    unsigned long long isum[7] = {}; // those sums: level 1 [0..3], level 2 [4..5], level 3 [6]
+    int elo = 0;                    // their unit is 2^(elo - 150)
     if (leaves) {
         float lf[PER];
         const unsigned long long l0 = i0 - t.n;
@@ -733,6 +782,7 @@ __device__ __forceinline__ void build_block(const RebuildArgs &a, unsigned long 
             v[k] = leaf_to_double(lf[k]);
             m[k] = leaf_min_value(lf[k]);
         }
+        if constexpr (PER == 8) exact = exact_leaf_sums(lf, isum, elo);
     } else {
 #pragma unroll
         for (int k = 0; k < PER; k += 2 > PER ? 1 : 2) {
@@ -748,20 +798,43 @@ __device__ __forceinline__ void build_block(const RebuildArgs &a, unsigned long 
 #pragma unroll
         for (int k = 0; k < PER; ++k) m[k] = cg ? __ldcg(t.M + i0 + k) : t.M[i0 + k];
     }
-    // levels on registers: after step r the thread holds PER >> r nodes at (i0 >> r)
+    // levels on registers: after step r the thread holds PER >> r nodes at (i0 >> r); for 8 leaves
+    // whose exponents span at most 26 binades the sums are exact integers (converted on the
+    // integer pipe), else binary64 adds
     int lv = 0;
+    bool done = false;
+    if constexpr (PER == 8) {
+        if (exact) {
+            double d[7];
 #pragma unroll
-    for (int cnt = PER / 2; cnt >= 1; cnt /= 2) {
-        ++lv;
+            for (int k = 0; k < 7; ++k) d[k] = fixed_to_double_exact(isum[k], elo);
 #pragma unroll
-        for (int k = 0; k < cnt; ++k) {
-            v[k] = v[2 * k] + v[2 * k + 1];
-            m[k] = fmin_tree(m[2 * k], m[2 * k + 1]);
+            for (int k = 0; k < 4; ++k) m[k] = fmin_tree(m[2 * k], m[2 * k + 1]);
+            store_run<4>(t, i0 >> 1, d, m);
+            m[0] = fmin_tree(m[0], m[1]);
+            m[1] = fmin_tree(m[2], m[3]);
+            store_run<2>(t, i0 >> 2, d + 4, m);
+            m[0] = fmin_tree(m[0], m[1]);
+            store_run<1>(t, i0 >> 3, d + 6, m);
+            v[0] = d[6];
+            lv = 3;
+            done = true;
         }
-        const unsigned long long node = i0 >> lv;
-        if (cnt == 4) store_run<4>(t, node, v, m);
-        else if (cnt == 2) store_run<2>(t, node, v, m);
-        else store_run<1>(t, node, v, m);
+    }
+    if (!done) {
+#pragma unroll
+        for (int cnt = PER / 2; cnt >= 1; cnt /= 2) {
+            ++lv;
+#pragma unroll
+            for (int k = 0; k < cnt; ++k) {
+                v[k] = v[2 * k] + v[2 * k + 1];
+                m[k] = fmin_tree(m[2 * k], m[2 * k + 1]);
+            }
+            const unsigned long long node = i0 >> lv;
+            if (cnt == 4) store_run<4>(t, node, v, m);
+            else if (cnt == 2) store_run<2>(t, node, v, m);
+            else store_run<1>(t, node, v, m);
+        }
     }
     double sv = v[0];
     float mv = m[0];
