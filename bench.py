@@ -295,7 +295,7 @@ def run_gpu(args, rank, world):
     rec, memset = cr.lib.cudaEventRecord, cr.lib.cudaMemsetAsync
     flush_ptr, flush_n = flush.data_ptr(), flush.numel()
 
-    def step(t, ev=None):
+    def step(t, ev=None, flush=True):
         if ev is not None:
             rec(ev[0], st)
         _check(L, h, L.per_add(*add_args[t % n_ofs]), "per_add")
@@ -308,7 +308,7 @@ def run_gpu(args, rank, world):
                "per_update")
         if ev is not None:
             rec(ev[3], st)
-        if flush_l2:
+        if flush_l2 and flush:
             # evict L2 between steps, outside the step's events: write 512 MiB, then read 256 MiB
             # so the next step starts on clean, unrelated lines rather than a write-back backlog
             memset(flush_ptr, 0, flush_n, st)
@@ -357,13 +357,13 @@ def run_gpu(args, rank, world):
     cr.destroy([ca, cb])
     cont_s = max_over_ranks(cont_s, dist)
 
-    # per-kernel breakdown (for the roofline): a second pass with an event between the calls.
-    # Each event pair also carries a launch (about 4 us on this GPU for an empty kernel), so
-    # these durations are upper bounds.
+    # per-kernel breakdown (for the roofline): a second pass with an event between the calls and,
+    # like the timed region, no flush between steps.  Each event pair also carries a launch
+    # without the programmatic overlap, so these durations are upper bounds.
     Kop = min(K, 4000)
     flat = cr.events(4 * Kop)
     for t in range(Kop):
-        step(W + K + t, flat[4 * t: 4 * t + 4])
+        step(W + K + t, flat[4 * t: 4 * t + 4], flush=False)
     torch.cuda.synchronize()
     per = np.array([[cr.elapsed_ms(flat[4 * t + i], flat[4 * t + i + 1]) for i in range(3)]
                     for t in range(Kop)])
@@ -440,7 +440,7 @@ def run_gpu(args, rank, world):
                           "ones); per_step_l2_flushed: 512 MiB write + 256 MiB read between steps"),
                    "timing": ("value: K steps back to back on one stream between two CUDA events, "
                               "synchronised on both sides; per-kernel figures from a separate pass "
-                              "with an event between the calls"),
+                              "with an event between the calls and no flush (as the timed region)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "wall_s_timed_loop": round(wall, 4), "host_enqueue_s": round(host_s, 4)},
         "hbm_gbs_algorithmic": round(step_bytes / (cont_s / K) / 1e9 / world, 2),

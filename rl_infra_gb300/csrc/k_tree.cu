@@ -1189,6 +1189,7 @@ struct UpdArgs {
     double alpha, eps;
     LeafPowAlpha lp;
     int proportional;
+    int cluster;   // the grid is one thread-block cluster: CTA 0 builds the top after a cluster barrier
 };
 
 // One warp's entry lists in shared memory, `cap` entries each (36 bytes per entry).
@@ -1739,8 +1740,17 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
         }
     }
 
-    // 3. the last CTA rebuilds the top P levels and folds in the batch maximum
-    if (last_to_arrive(&a.ctl->ticket_update)) {
+    // 3. the last CTA rebuilds the top P levels and folds in the batch maximum (when the grid
+    //    is one cluster: CTA 0, after a cluster barrier, without the arrival ticket)
+    bool top;
+    if (a.cluster) {
+        __threadfence();
+        cluster_sync_all();
+        top = cluster_cta_rank() == 0;
+    } else {
+        top = last_to_arrive(&a.ctl->ticket_update);
+    }
+    if (top) {
         if (a.proportional && a.P > 0 && a.P <= 8) {
             // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
             // node of depth 5 in registers, or starts from depth-P node l (P < 5); every level
@@ -1913,6 +1923,16 @@ int update_subtrees_per_cta(int warps)
     return v < 1 ? warps : (v > warps ? warps : v);
 }
 
+// Small update grids (at most 16 CTAs) run as one cluster (GBPER_UPD_CLUSTER=0 turns it off).
+bool update_cluster_enabled()
+{
+    static const bool on = [] {
+        const char *e = std::getenv("GBPER_UPD_CLUSTER");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 // Target batch entries per subtree of the update kernel (GBPER_UPD_PER, 1..64; default 8).
 int update_entries_per_subtree()
 {
@@ -1940,6 +1960,7 @@ cudaError_t init_tree_kernels(int carveout)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kUpdSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess || carveout < 0) return e;
     const void *fns[] = {(const void *)k_update<kUpdWindow>, (const void *)k_add, (const void *)k_add_bulk_rows,
                          (const void *)k_rebuild_tree, (const void *)k_add_finish, (const void *)k_fill,
@@ -2134,6 +2155,11 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.cap = large ? kUpdLargeCap : kUpdSmallCap;
     a.subs = update_subtrees_per_cta(warps);
     const unsigned grid = (unsigned)(((1ull << P) + a.subs - 1) / a.subs);
+    a.cluster = 0;
+    if (grid > 1 && grid <= 16 && update_cluster_enabled()) {
+        a.cluster = 1;
+        return launch_pdl_cluster(k_update<kUpdWindow>, grid, 32 * warps, kUpdSmemBytes, st, a);
+    }
     return launch_pdl(k_update<kUpdWindow>, grid, 32 * warps, kUpdSmemBytes, st, a);
 }
 
