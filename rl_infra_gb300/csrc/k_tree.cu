@@ -426,6 +426,12 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
     const unsigned long long C = a.r.capacity;
     const AddGeom g = add_geometry(a, cursor);
     const int tid = threadIdx.x;
+    // Every CTA arrives once; the last to arrive climbs and advances the counters, which every
+    // CTA has read above before it arrives.  Copy CTAs arrive before copying, so the climb does
+    // not wait for the rows (the next kernel waits for this whole grid), unless rows overwritten
+    // within this call (k < k0) feed the running maximum through them.
+    const bool copies_late = a.k0 > 0 && a.prio;
+    bool last = false;
 
     if (blockIdx.x < a.ntree) {
         const unsigned b = blockIdx.x;
@@ -504,22 +510,25 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
         }
         const unsigned bm = block_max_u32(mymax);
         if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
+        last = last_to_arrive(&a.ctl->ticket_add);
     } else {
+        if (!copies_late) last = last_to_arrive(&a.ctl->ticket_add);
         // rows that a later row of the same call overwrites still count toward the running
         // maximum, as if they had been inserted one after another
-        unsigned mymax = 0;
-        if (a.prio) {
+        if (copies_late) {
+            unsigned mymax = 0;
             const unsigned long long t0 = (unsigned long long)(blockIdx.x - a.ntree) * kThreads + tid;
             for (unsigned long long k = t0; k < a.k0; k += (unsigned long long)a.ncopy * kThreads)
                 mymax = max(mymax, __float_as_uint(prio_to_raw(__ldg(a.prio + k), a.eps, max_prev)));
+            const unsigned bm = block_max_u32(mymax);
+            if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
         }
-        const unsigned bm = block_max_u32(mymax);
-        if (tid == 0 && bm) atomicMax(&a.ctl->add_max_bits, bm);
         copy_rows_flat(a, g, (unsigned long long)(blockIdx.x - a.ntree) * kThreads + tid,
                        (unsigned long long)a.ncopy * kThreads);
+        if (copies_late) last = last_to_arrive(&a.ctl->ticket_add);
     }
 
-    if (last_to_arrive(&a.ctl->ticket_add)) {
+    if (last) {
         unsigned call_max = 0;
         if (tid == 0) call_max = __ldcg(&a.ctl->add_max_bits);   // in flight during the climb
         if (a.proportional && a.t.S) {
