@@ -422,11 +422,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
     }
 }
 
-int warps_per_cta()
+// Draws (warps) per CTA of the samplers, measured on GB300 (steps/s of each workload's step):
+// 2 for batches of at most 512 or at least 4096 draws (the apex step 35.7K against 34.8K with 8;
+// the stress step 20.9K against 20.1K), 8 in between (the dqn step 42.3K against 40.0K with 2
+// or 4; the rank step 25.8K against 24.8K).  GBPER_SAMPLE_WARPS overrides it.
+int warps_per_cta(unsigned B)
 {
-    int w = 8;
-    if (const char *e = std::getenv("GBPER_SAMPLE_WARPS")) w = std::atoi(e);
-    if (w < 1) w = 1;
+    static const int forced = [] {
+        const char *e = std::getenv("GBPER_SAMPLE_WARPS");
+        return e ? std::atoi(e) : 0;
+    }();
+    int w = forced > 0 ? forced : ((B <= 512 || B >= 4096) ? 2 : 8);
     if (w > kThreads / 32) w = kThreads / 32;
     return w;
 }
@@ -468,7 +474,7 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     a.seed = seed;
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
-    const int wpb = warps_per_cta();
+    const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
@@ -490,7 +496,7 @@ cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRef
     a.seed = seed;
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
-    const int wpb = warps_per_cta();
+    const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_flat, grid, wpb * 32, 0, st, a);
@@ -507,7 +513,7 @@ cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsig
     a.seed = seed;
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
-    const int wpb = warps_per_cta();
+    const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_uniform, grid, wpb * 32, 0, st, a);
@@ -531,7 +537,7 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
     a.seed = seed;
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
-    const int wpb = warps_per_cta();
+    const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
     return launch_pdl(k_sample_rank, grid, wpb * 32, 0, st, a);
