@@ -2055,9 +2055,16 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.vec4 = (r.d % 4 == 0) && ((reinterpret_cast<uintptr_t>(states) | reinterpret_cast<uintptr_t>(next)) % 16 == 0);
     if (r.d == 0) a.vec4 = 0;
 
-    // rows: about two elements of each array per copy thread, at most 4 CTAs per SM
+    // rows: about `per` elements of each array per copy thread, at most 4 CTAs per SM.  8 (16
+    // float4 loads in flight per thread) measured best on GB300 for the apex step: 36.7K steps/s
+    // against 35.7K with 2 (128 copy CTAs) and 35.4K with 16.  GBPER_ADD_COPY_PER overrides it.
+    static const unsigned long long per = [] {
+        const char *e = std::getenv("GBPER_ADD_COPY_PER");
+        const int v = e ? std::atoi(e) : 8;
+        return (unsigned long long)(v < 1 ? 1 : (v > 16 ? 16 : v));
+    }();
     const unsigned long long elems = a.vec4 ? cnt * (r.d / 4) : cnt * (unsigned long long)std::max(r.d, 1u);
-    unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + 2ull * kThreads - 1) / (2ull * kThreads),
+    unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + per * kThreads - 1) / (per * kThreads),
                                                             (unsigned long long)num_sms * 4);
     if (ncopy == 0) ncopy = 1;
 
