@@ -172,9 +172,12 @@ cudaError_t rank_order(per_buffer *h, cudaStream_t st)
 }
 
 // Kernel attributes are per device: set them the first time a buffer is created on a device.
-// The carveout (percent of the unified L1/shared array given to shared memory) is the same for
-// every kernel of the library when GBPER_CARVEOUT is set (measured: no effect on this path, so
-// by default the driver chooses).
+// The carveout (percent of the unified L1/shared array preferred for shared memory; a kernel
+// still gets the shared memory it needs), measured on GB300: the tree kernels prefer L1 (0):
+// the apex step 37.2K steps/s against 36.8K with the driver's choice; the samplers keep the
+// driver's choice (with 0 the stress sample took 35.6 us against 27.1); so do the rank
+// kernels, which stage whole tiles in shared memory.  GBPER_CARVEOUT sets one value for every
+// kernel; GBPER_CARVEOUT_TREE and GBPER_CARVEOUT_SAMPLE set one family (-1: the driver's).
 cudaError_t init_kernels_once(int device)
 {
     static std::mutex mu;
@@ -182,11 +185,14 @@ cudaError_t init_kernels_once(int device)
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (done[device]) return cudaSuccess;
-    int carveout = -1;
-    if (const char *env = std::getenv("GBPER_CARVEOUT")) carveout = std::atoi(env);
-    cudaError_t e = init_tree_kernels(carveout);
-    if (e == cudaSuccess) e = init_sample_kernels(carveout);
-    if (e == cudaSuccess) e = init_rank_kernels(carveout);
+    int tree_carveout = 0, sample_carveout = -1, rank_carveout = -1;
+    if (const char *env = std::getenv("GBPER_CARVEOUT"))
+        tree_carveout = sample_carveout = rank_carveout = std::atoi(env);
+    if (const char *env = std::getenv("GBPER_CARVEOUT_TREE")) tree_carveout = std::atoi(env);
+    if (const char *env = std::getenv("GBPER_CARVEOUT_SAMPLE")) sample_carveout = std::atoi(env);
+    cudaError_t e = init_tree_kernels(tree_carveout);
+    if (e == cudaSuccess) e = init_sample_kernels(sample_carveout);
+    if (e == cudaSuccess) e = init_rank_kernels(rank_carveout);
     if (e == cudaSuccess) done[device] = true;
     return e;
 }
