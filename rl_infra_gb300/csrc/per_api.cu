@@ -469,14 +469,20 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
     if (h->mode == PER_MODE_UNIFORM) return PER_OK;   // no priorities
     const long long *idx = reinterpret_cast<const long long *>(d_idx);
     const bool prop = h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT;
-    const cudaError_t e =
-        B < update_element_batch(h)
-            ? launch_update_element(tree_of(h), h->ctl, B, idx, d_td, h->alpha, h->eps, as_stream(stream))
-        : (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h))
-            ? launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
-                                    h->num_sms, h->rank.dirty, h->win, as_stream(stream))
-            : launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
-                            h->rank.dirty, as_stream(stream));
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e;
+    if (B < update_element_batch(h)) {
+        // one or two entries: each from its leaf to the root
+        e = launch_update_element(tree_of(h), h->ctl, B, idx, d_td, h->alpha, h->eps, st);
+    } else if (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h)) {
+        // winners scattered, then (with a tree) every level rebuilt
+        e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
+                                  h->num_sms, h->rank.dirty, h->win, st);
+    } else {
+        // the dirty-ancestor climb
+        e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
+                          h->rank.dirty, st);
+    }
     if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
     if (h->mode == PER_MODE_RANK) h->dirty_bound += B;
     return PER_OK;
