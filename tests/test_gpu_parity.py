@@ -664,4 +664,30 @@ def test_invalid_arguments_rejected():
         capi.ReplayBuffer(16, 8, row_stride_out=4)
     with pytest.raises(capi.PerError):
         capi.ReplayBuffer(16, 8, eps=0.0)
+    with pytest.raises(capi.PerError):      # unknown mode
+        capi.ReplayBuffer(16, 8, mode=7)
+    with pytest.raises(capi.PerError):      # unknown flag bit
+        capi.ReplayBuffer(16, 8, flags=1 << 9)
+    with pytest.raises(capi.PerError):      # flat mode needs every leaf finite: alpha <= 1
+        capi.ReplayBuffer(16, 8, alpha=1.5, mode=capi.PER_MODE_FLAT)
+    with pytest.raises(capi.PerError):      # eps^alpha below the smallest normal binary32
+        capi.ReplayBuffer(16, 8, alpha=4.0, eps=1e-12)
+    cfg = capi.per_config(0.6, 1e-6, 0, 8, 0, 0, 0, 0, 1)   # reserved must be 0
+    with pytest.raises(capi.PerError):
+        capi.per_create(16, 8, cfg)
+    # min is proportional/flat only; uniform updates are checked but change nothing
+    u = capi.ReplayBuffer(64, 0, mode=capi.PER_MODE_UNIFORM)
+    s, _ = capi.per_min(u._h, None)
+    assert s == capi.PER_ERR_INVALID_ARG
+    assert capi.per_update_priorities(u._h, 4, None, None, None) == capi.PER_ERR_INVALID_ARG
+    u.close()
+    # float dones need a 4-byte aligned destination
+    f = capi.ReplayBuffer(64, 0, flags=capi.PER_FLAG_DONES_F32)
+    z = torch.zeros(64, dtype=torch.float32, device="cuda")
+    f.add(None, None, torch.zeros(64, dtype=torch.int32, device="cuda"), z,
+          torch.zeros(64, dtype=torch.uint8, device="cuda"))
+    dst = torch.zeros(40, dtype=torch.uint8, device="cuda")
+    s = capi.per_sample(f._h, 8, 0.4, idx.data_ptr(), None, None, None, None, None, dst.data_ptr() + 1, None)
+    assert s == capi.PER_ERR_INVALID_ARG
+    f.close()
     b.close()
