@@ -182,7 +182,10 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
  *   PER_FLAG_DONES_F32) -- each may be NULL to skip.
  *   B in 1 .. 2^24.  beta >= 0.
  * The call counter lives on the device, so each call, captured in a graph or not, draws a
- * fresh batch.  PER_ERR_EMPTY when the buffer holds no transition (host-side count).
+ * fresh batch.  PER_ERR_EMPTY when the buffer holds no transition (host-side count).  In rank
+ * mode the slot order's length is fixed at launch, so a call made during stream capture while
+ * the buffer is not yet full is refused (PER_ERR_INVALID_ARG): capture rank-mode rounds once the
+ * ring is full.
  */
 per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, float *d_w,
                       float *d_states, float *d_next, uint32_t *d_actions, float *d_rewards,

@@ -426,6 +426,14 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
         (h->dones_f32 && reinterpret_cast<uintptr_t>(d_dones) % 4))
         return fail(h, PER_ERR_INVALID_ARG, "per_sample: misaligned output pointer");
     if (h->host_size == 0) return fail(h, PER_ERR_EMPTY, "per_sample: the buffer holds no transition");
+    if (h->mode == PER_MODE_RANK && h->host_size < h->capacity) {
+        // the slot order's length is a launch argument: a graph captured now would keep sorting
+        // this many slots while later replays fill the buffer further
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(as_stream(stream), &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+            return fail(h, PER_ERR_INVALID_ARG,
+                        "per_sample: in rank mode, capture a graph only once the buffer is full");
+    }
     SampleOut o;
     o.idx = reinterpret_cast<long long *>(d_idx);
     o.w = d_w;

@@ -554,6 +554,35 @@ def test_graph_replayed_rounds(mode):
     p.close()
 
 
+def test_rank_mode_refuses_capture_before_full():
+    """A rank-mode sample captured while the ring is filling would keep sorting the captured
+    number of slots on every replay; the call is refused during capture until the ring is full."""
+    cap, d = 4096, 4
+    w = _small("rank", capacity=cap, state_dim=d, row_stride=d)
+    g = wl.rng(33)
+    p = Pair(cap, d, d, 0.7, 1e-6, 1, seed=3)
+    prefill(p, w, g, count=1000, chunk=1000)
+    L, h = capi.load(), p.gpu._h
+    out = p.gpu.alloc_batch(64)
+    optr = [out[k].data_ptr() for k in ("idx", "w", "states", "next_states", "actions", "rewards", "dones")]
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert L.per_sample(h, 64, ctypes.c_float(0.5), *optr, cs) == capi.PER_ERR_INVALID_ARG
+    del gr
+    p.sample(64, 0.5)                      # outside capture the call runs as usual
+    prefill(p, w, g, count=cap - 1000, chunk=cap - 1000)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert L.per_sample(h, 64, ctypes.c_float(0.5), *optr, cs) == 0
+    gr.replay()
+    torch.cuda.synchronize()
+    want = p.orc.sample(64, 0.5, gather=False)
+    harness.assert_indices(out["idx"].cpu().numpy(), want["idx"], want["near"])
+    p.close()
+
+
 # -- the full-size workloads (sampled checks) -------------------------------------------------
 
 @pytest.mark.slow
