@@ -58,7 +58,7 @@ __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o
     if (lane == 1 && o.actions) act = __ldg(r.actions + slot);
     if (lane == 2 && o.rewards) rew = __ldg(r.rewards + slot);
     if (lane == 3 && o.dones) done = __ldg(r.dones + slot);
-    const bool rows = d && (o.states || o.next);
+    const bool rows = dp && (o.states || o.next);   // with d = 0 the rows are all padding
     if (rows && vec4 && 2 * (dp >> 2) <= 32 * kGatherV) {
         // up to 32 kGatherV float4 per row pair: kGatherV per lane, all loaded before any store
         const unsigned d4 = d >> 2, dp4 = dp >> 2;

@@ -98,7 +98,7 @@ def test_ring_wrap_and_oversized_insert():
     p.close()
 
 
-@pytest.mark.parametrize("d,dp", [(0, 0), (1, 1), (3, 8), (8, 8), (48, 64), (64, 64), (63, 65)])
+@pytest.mark.parametrize("d,dp", [(0, 0), (0, 1), (0, 4), (1, 1), (3, 8), (8, 8), (48, 64), (64, 64), (63, 65)])
 def test_gather_row_shapes(d, dp):
     cap = 4096
     w = _small("tiny", capacity=cap, state_dim=d, row_stride=dp)
@@ -581,6 +581,38 @@ def test_rank_mode_refuses_capture_before_full():
     want = p.orc.sample(64, 0.5, gather=False)
     harness.assert_indices(out["idx"].cpu().numpy(), want["idx"], want["near"])
     p.close()
+
+
+def test_random_configurations():
+    """Seeded random mixes of mode, capacity, row shape, insert sizes (wrapping), batch sizes and
+    update path, every call checked against the oracle."""
+    g = wl.rng(99)
+    modes = [0, 1, 2, 3]
+    paths = [DEFAULT, CLIMB, REBUILD, ELEMENT]
+    for case in range(24):
+        mode = modes[case % 4]
+        cap = int(g.integers(1, 6000))
+        d = int(g.choice([0, 1, 3, 4, 8, 17]))
+        dp = d + int(g.choice([0, 0, 1, 4]))
+        path = paths[int(g.integers(0, 4))] if mode == 0 else (DEFAULT if mode != 1 else paths[int(g.integers(0, 3))])
+        alpha = float(g.choice([0.0, 0.5, 0.6, 1.0]))
+        w = _small("tiny", capacity=cap, state_dim=d, row_stride=dp, mode=mode)
+        p = Pair(cap, d, dp, alpha, 1e-6, mode, seed=case, **path)
+        for rnd in range(4):
+            count = int(g.integers(1, 2 * cap + 2))
+            rows = wl.transitions(g, count, w)
+            prio = wl.raw_priorities(g, count, "lognormal") if g.random() < 0.7 else None
+            p.add(rows, prio)
+            p.check_counters()
+            B = int(g.integers(1, 700))
+            _, want = p.sample(B, float(g.uniform(0, 1)))
+            idx = want["idx"].copy()
+            if B > 3 and g.random() < 0.5:
+                idx = wl.duplicate_positions(g, idx, 0.3)
+            p.update(idx, wl.td_errors(g, B))
+            p.check_tree()
+        assert p.gpu.status_device() == 0, (case, mode, cap)
+        p.close()
 
 
 # -- the full-size workloads (sampled checks) -------------------------------------------------
