@@ -583,28 +583,30 @@ def test_rank_mode_refuses_capture_before_full():
     p.close()
 
 
-def test_random_configurations():
-    """Seeded random mixes of mode, capacity, row shape, insert sizes (wrapping), batch sizes and
-    update path, every call checked against the oracle."""
-    g = wl.rng(99)
+@pytest.mark.parametrize("seed", [99, 7, 2024])
+def test_random_configurations(seed):
+    """Seeded random mixes of mode, capacity, row shape, insert sizes (wrapping), batch sizes,
+    float dones and update path, every call checked against the oracle."""
+    g = wl.rng(seed)
     modes = [0, 1, 2, 3]
     paths = [DEFAULT, CLIMB, REBUILD, ELEMENT]
     for case in range(24):
         mode = modes[case % 4]
-        cap = int(g.integers(1, 6000))
+        cap = int(g.integers(1, 6000)) if case % 3 else int(g.integers(1, 40000))
         d = int(g.choice([0, 1, 3, 4, 8, 17]))
         dp = d + int(g.choice([0, 0, 1, 4]))
         path = paths[int(g.integers(0, 4))] if mode == 0 else (DEFAULT if mode != 1 else paths[int(g.integers(0, 3))])
         alpha = float(g.choice([0.0, 0.5, 0.6, 1.0]))
         w = _small("tiny", capacity=cap, state_dim=d, row_stride=dp, mode=mode)
-        p = Pair(cap, d, dp, alpha, 1e-6, mode, seed=case, **path)
+        flags = capi.PER_FLAG_DONES_F32 if g.random() < 0.3 else 0
+        p = Pair(cap, d, dp, alpha, 1e-6, mode, seed=case, flags=flags, **path)
         for rnd in range(4):
             count = int(g.integers(1, 2 * cap + 2))
             rows = wl.transitions(g, count, w)
             prio = wl.raw_priorities(g, count, "lognormal") if g.random() < 0.7 else None
             p.add(rows, prio)
             p.check_counters()
-            B = int(g.integers(1, 700))
+            B = int(g.integers(1, 2000))
             _, want = p.sample(B, float(g.uniform(0, 1)))
             idx = want["idx"].copy()
             if B > 3 and g.random() < 0.5:
