@@ -249,8 +249,8 @@ enum {
     PER_STATE_DONES = 9,    /* uint8 [capacity] */
     PER_STATE_COUNTERS = 10, /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
     PER_STATE_RANK_ORDER = 11, /* uint32 [size at the last sample]: slots by rank (rank mode) */
-    PER_STATE_CUMULATIVE = 12  /* double [size]: C[i] = leaves 0..i summed, as of the last sample,
-                                  per_total or per_min (flat mode) */
+    PER_STATE_CUMULATIVE = 12  /* double [size on the device]: C[i] = leaves 0..i summed, as of the
+                                  last sample, per_total or per_min (flat mode) */
 };
 
 /* per_read_state -- copy `count` elements starting at element `first` of one of the arrays

@@ -312,6 +312,8 @@ class ReplayBuffer:
 
     def read_state(self, which, first=0, count=None, stream=None):
         dtype = _STATE_DTYPE[which]
+        if count is None and which == PER_STATE_CUMULATIVE:   # the device's filled size
+            count = int(self.read_state(PER_STATE_COUNTERS, 2, 1)[0]) - first
         if count is None:
             count = {PER_STATE_LEAVES: self.nleaves, PER_STATE_SUMS: self.nleaves,
                      PER_STATE_MINS: self.nleaves, PER_STATE_RAW: self.capacity,
@@ -320,7 +322,7 @@ class ReplayBuffer:
                      PER_STATE_NEXT: self.capacity * self.state_dim,
                      PER_STATE_ACTIONS: self.capacity, PER_STATE_REWARDS: self.capacity,
                      PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 4,
-                     PER_STATE_RANK_ORDER: self.size, PER_STATE_CUMULATIVE: self.size}[which] - first
+                     PER_STATE_RANK_ORDER: self.size}[which] - first
         buf = np.empty(max(count, 1), dtype=dtype)
         s = per_read_state(self._h, which, first, count, buf.ctypes.data_as(ctypes.c_void_p),
                            _stream(stream))

@@ -623,12 +623,19 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
         elems = h->order_size;
         esz = 4;
         break;
-    case PER_STATE_CUMULATIVE:
+    case PER_STATE_CUMULATIVE: {
         if (h->mode != PER_MODE_FLAT) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: flat mode only");
+        // the device's filled size (graph replays advance it without the host counting)
+        uint64_t dsize = 0;
+        cudaError_t e = cudaMemcpyAsync(&dsize, &h->ctl->size, sizeof(dsize), cudaMemcpyDeviceToHost,
+                                        as_stream(stream));
+        if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "per_read_state");
         src = h->flat.C;
-        elems = h->host_size;
+        elems = dsize;
         esz = 8;
         break;
+    }
     case PER_STATE_COUNTERS: {
         if (first + count > 4) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
         Ctl c;

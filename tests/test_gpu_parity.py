@@ -554,6 +554,54 @@ def test_graph_replayed_rounds(mode):
     p.close()
 
 
+@pytest.mark.parametrize("mode", [0, 2, 3])
+def test_graph_replayed_while_filling(mode):
+    """Rounds captured while the ring is still filling: every replay inserts at the device cursor
+    and the filled size grows on the device, which the samplers (and the flat scan) read there."""
+    cap, d, B, I, NO = 4096, 4, 64, 300, 2
+    w = _small("tiny", capacity=cap, state_dim=d, row_stride=d, mode=mode)
+    g = wl.rng(34, mode)
+    p = Pair(cap, d, d, 0.6, 1e-6, mode, seed=6)
+    prefill(p, w, g, count=500, chunk=500)
+    L, h = capi.load(), p.gpu._h
+    rows = [wl.transitions(g, I, w) for _ in range(NO)]
+    dev_rows = [{k: dev(v) for k, v in r.items()} for r in rows]
+    td = [wl.td_errors(g, B) for _ in range(NO)]
+    d_td = [dev(x) for x in td]
+    out = p.gpu.alloc_batch(B)
+    optr = [out[k].data_ptr() for k in ("idx", "w", "states", "next_states", "actions", "rewards", "dones")]
+    graphs = []
+    for o in range(NO):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            r = dev_rows[o]
+            assert L.per_add(h, I, r["states"].data_ptr(), r["next_states"].data_ptr(), r["actions"].data_ptr(),
+                             r["rewards"].data_ptr(), r["dones"].data_ptr(), None, cs) == 0
+            assert L.per_sample(h, B, ctypes.c_float(0.5), *optr, cs) == 0
+            assert L.per_update_priorities(h, B, out["idx"].data_ptr(), d_td[o].data_ptr(), cs) == 0
+        graphs.append(gr)
+    for rnd in range(16):                      # 500 + 16 * 300 > 4096: the ring fills and wraps
+        o = rnd % NO
+        graphs[o].replay()
+        torch.cuda.synchronize()
+        r = rows[o]
+        p.orc.add(r["states"], r["next_states"], r["actions"], r["rewards"], r["dones"], None, count=I)
+        want = p.orc.sample(B, 0.5, gather=True)
+        gi = out["idx"].cpu().numpy()
+        harness.assert_indices(gi, want["idx"], want["near"])
+        same = gi == want["idx"]
+        assert np.array_equal(out["states"].cpu().numpy()[same], want["states"][same])
+        p.orc.update(want["idx"], td[o])
+    c = p.counters()                           # the device's counters (the host counted no replay)
+    assert (c["calls"], c["cursor"], c["size"]) == (p.orc.sample_calls, p.orc.cursor, p.orc.size)
+    assert c["max_raw"] == np.float32(p.orc.max_raw)
+    if mode != 2:
+        p.check_tree()
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
 def test_rank_mode_refuses_capture_before_full():
     """A rank-mode sample captured while the ring is filling would keep sorting the captured
     number of slots on every replay; the call is refused during capture until the ring is full."""
