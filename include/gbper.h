@@ -222,7 +222,8 @@ per_status per_total(per_buffer *h, double *host_out, void *stream);
 per_status per_min(per_buffer *h, float *host_out, void *stream);
 
 /* per_size -- the number of filled slots as the host has counted the per_add calls enqueued
- * so far.  No device access. */
+ * so far.  No device access.  Calls replayed from a CUDA graph are not counted here; the
+ * device's own count is PER_STATE_COUNTERS[2] (per_read_state). */
 per_status per_size(const per_buffer *h, uint64_t *out);
 
 /* per_status_device -- read and clear the device error word (PER_DEVFLAG_* bits) into
