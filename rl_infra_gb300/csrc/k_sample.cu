@@ -426,6 +426,18 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
 // 2 for batches of at most 512 or at least 4096 draws (the apex step 35.7K against 34.8K with 8;
 // the stress step 20.9K against 20.1K), 8 in between (the dqn step 42.3K against 40.0K with 2
 // or 4; the rank step 25.8K against 24.8K).  GBPER_SAMPLE_WARPS overrides it.
+// CTAs per SM the samplers' grids stop at (larger batches loop over their draws):
+// GBPER_SAMPLE_CTAS_PER_SM, default 16.
+unsigned long long sampler_ctas_per_sm()
+{
+    static const unsigned long long v = [] {
+        const char *e = std::getenv("GBPER_SAMPLE_CTAS_PER_SM");
+        const int x = e ? std::atoi(e) : 16;
+        return (unsigned long long)(x < 1 ? 1 : (x > 32 ? 32 : x));
+    }();
+    return v;
+}
+
 int warps_per_cta(unsigned B)
 {
     static const int forced = [] {
@@ -476,7 +488,7 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
-    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
     return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
 }
 
@@ -498,7 +510,7 @@ cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRef
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
-    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
     return launch_pdl(k_sample_flat, grid, wpb * 32, 0, st, a);
 }
 
@@ -515,7 +527,7 @@ cudaError_t launch_sample_uniform(const RingRefs &r, Ctl *ctl, unsigned B, unsig
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
-    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
     return launch_pdl(k_sample_uniform, grid, wpb * 32, 0, st, a);
 }
 
@@ -539,7 +551,7 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta(B);
     const unsigned long long ctas = (B + wpb - 1) / wpb;
-    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * 16);
+    const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
     return launch_pdl(k_sample_rank, grid, wpb * 32, 0, st, a);
 }
 
