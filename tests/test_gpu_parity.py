@@ -300,6 +300,39 @@ def test_rank_order_kept_between_samples(cap, fill, flags):
     p.close()
 
 
+@pytest.mark.parametrize("seed", [3, 17, 31])
+def test_rank_order_random_operations(seed):
+    """Seeded random rank-mode histories (inserts of every size, some wrapping or larger than the
+    ring, updates with repeats, NaN/Inf and equal priorities): after every sample the kept order
+    is the oracle's full order."""
+    g = wl.rng(seed, 5)
+    cap = int(g.integers(2000, 30000))
+    w = _small("rank", capacity=cap, state_dim=2, row_stride=2)
+    p = Pair(cap, 2, 2, 0.7, 1e-6, 1, seed=seed)
+    prefill(p, w, g, count=int(g.integers(1, cap)), chunk=cap)
+    for rnd in range(12):
+        op = g.random()
+        if op < 0.4:
+            count = int(g.integers(1, 3000)) if g.random() < 0.8 else int(g.integers(cap, 2 * cap))
+            p.add(wl.transitions(g, count, w), wl.raw_priorities(g, count, w.prio) if g.random() < 0.7 else None)
+        else:
+            size = int(p.orc.size)
+            B = int(g.integers(1, 3000))
+            idx = g.integers(0, size, B)
+            if B > 4:
+                idx = wl.duplicate_positions(g, idx, 0.3)
+            td = wl.td_errors(g, B)
+            if B > 10:
+                td[:3] = [np.nan, np.inf, 0.0]
+                td[3:8] = 0.5
+            p.update(idx, td)
+        p.sample(int(g.integers(1, 1025)), 0.5, check_rows=False)
+        _assert_rank_order(p)
+    p.check_counters()
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
 @pytest.mark.slow
 def test_rank_more_than_a_million_slots():
     """3M slots: more than 256 sort tiles, so the look-back reads group totals in rounds."""
