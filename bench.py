@@ -314,6 +314,11 @@ def run_gpu(args, rank, world):
             memset(flush_ptr, 0, flush_n, st)
             torch.sum(evict, 0, out=evict_out)
 
+    # the clock sampler starts before the warm-up, so the timed steps follow the warm-up directly
+    clocks = ClockSampler(dev) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     for t in range(W):
         step(t)
     torch.cuda.synchronize()
@@ -322,13 +327,9 @@ def run_gpu(args, rank, world):
     # timed region: K steps, each bracketed by two events on the launching stream (no events
     # between the three calls, so each kernel's launch overlaps its predecessor's tail)
     sev = cr.events(2 * K)
-    clocks = ClockSampler(dev) if rank == 0 else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
     t0 = time.perf_counter()
     for t in range(K):
         step(W + t, (sev[2 * t], None, None, sev[2 * t + 1]))
@@ -345,11 +346,13 @@ def run_gpu(args, rank, world):
     ca, cb = cr.events(2)
     torch.cuda.synchronize()
     rec(ca, st)
+    t1 = time.perf_counter()
     for t in range(K):
         _check(L, h, L.per_add(*add_args[(W + t) % n_ofs]), "per_add")
         _check(L, h, L.per_sample(*sample_args), "per_sample")
         _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * ((W + t) % TD_SLOTS), st),
                "per_update")
+    cont_host_s = time.perf_counter() - t1
     rec(cb, st)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None   # the sampler spans both timed loops
@@ -442,7 +445,8 @@ def run_gpu(args, rank, world):
                               "synchronised on both sides; per-kernel figures from a separate pass "
                               "with an event between the calls and no flush (as the timed region)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "wall_s_timed_loop": round(wall, 4), "host_enqueue_s": round(host_s, 4)},
+                   "wall_s_timed_loop": round(wall, 4), "host_enqueue_s": round(host_s, 4),
+                   "host_enqueue_us_per_step": round(cont_host_s * 1e6 / K, 3)},
         "hbm_gbs_algorithmic": round(step_bytes / (cont_s / K) / 1e9 / world, 2),
         "bytes_per_step": {"k_add": int(b_add), "k_sample_prop": int(b_sam), "k_update": int(b_upd)},
         "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
@@ -532,10 +536,10 @@ def run_flat_design(args):
     res = {"value": round(K / cont_s, 2), "unit": UNIT, "ms_per_step": round(cont_s * 1e3 / K, 5),
            "steps": K, "scan_bytes": 12 * n,
            "ops_median_us": {"per_add (k_add, leaves only)": round(float(np.median(per[:, 0])) * 1e3, 3),
-                             "per_sample (k_flat_scan + k_sample_flat)": round(float(np.median(per[:, 1])) * 1e3, 3),
+                             "per_sample (k_flat_reduce + k_flat_scan + k_sample_flat)": round(float(np.median(per[:, 1])) * 1e3, 3),
                              "per_update (k_upd_scatter + k_upd_apply + k_upd_finish)":
                                  round(float(np.median(per[:, 2])) * 1e3, 3)},
-           "gpu_launches_per_step": 6,
+           "gpu_launches_per_step": 7,
            "note": ("the apex step in PER_MODE_FLAT (the pages' cumulative array + search, no tree), "
                     "K steps back to back between two events; per-call medians from a pass with events "
                     "between the calls (2.048 us event resolution)")}

@@ -1204,14 +1204,12 @@ struct UpdArgs {
 // One warp's entry lists in shared memory, `cap` entries each (36 bytes per entry).
 struct WarpLists {
     unsigned long long *keys;  // (leaf offset << pb) | position
-    double *vs;
     unsigned *pay;             // entry slot carried through the sort
     float *rawv;               // raw priority by entry slot
     unsigned *ulist;           // distinct leaves, ascending (absolute)
-    float *vm;
-    int *rend;
+    float *uraw;               // raw priority of each distinct leaf
 };
-constexpr size_t kListBytesPerEntry = 36;
+constexpr size_t kListBytesPerEntry = 24;
 
 __device__ __forceinline__ WarpLists warp_lists(unsigned char *smem, int w, int cap)
 {
@@ -1219,17 +1217,13 @@ __device__ __forceinline__ WarpLists warp_lists(unsigned char *smem, int w, int 
     WarpLists l;
     l.keys = reinterpret_cast<unsigned long long *>(b);
     b += 8 * (size_t)cap;
-    l.vs = reinterpret_cast<double *>(b);
-    b += 8 * (size_t)cap;
     l.pay = reinterpret_cast<unsigned *>(b);
     b += 4 * (size_t)cap;
     l.rawv = reinterpret_cast<float *>(b);
     b += 4 * (size_t)cap;
     l.ulist = reinterpret_cast<unsigned *>(b);
     b += 4 * (size_t)cap;
-    l.vm = reinterpret_cast<float *>(b);
-    b += 4 * (size_t)cap;
-    l.rend = reinterpret_cast<int *>(b);
+    l.uraw = reinterpret_cast<float *>(b);
     return l;
 }
 
@@ -1461,111 +1455,6 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane, u
     }
 }
 
-// Climb one warp's subtree from its U distinct leaves (ulist ascending, vs/vm seeded with the
-// new leaf values, rend[k] = k + 1) up to the subtree root at depth D - shift.
-template <int W>
-__device__ void warp_upsweep(const TreeRefs &t, const WarpLists &wl, int U, int shift, int lane)
-{
-    const unsigned long long n = t.n;
-    if (U <= 32) {
-        const int k = lane;
-        const bool have = k < U;
-        const unsigned long long myleaf = have ? (unsigned long long)wl.ulist[k] + n : 0;
-        const unsigned long long prevleaf = (have && k > 0) ? (unsigned long long)wl.ulist[k - 1] + n : 0;
-        for (int h0 = 0; h0 < shift; h0 += W) {
-            double ps[W];
-            float pmn[W];
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const int h = h0 + w;
-                ps[w] = 0.0;
-                pmn[w] = 0.0f;
-                if (have && h < shift) {
-                    const unsigned long long v = myleaf >> h;
-                    if (k == 0 || (prevleaf >> h) != v) {
-                        ps[w] = ld_sum(t, v ^ 1ull);
-                        pmn[w] = ld_min(t, v ^ 1ull);
-                    }
-                }
-            }
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const int h = h0 + w;
-                if (h >= shift) break;
-                if (have) {
-                    const unsigned long long v = myleaf >> h;
-                    if (k == 0 || (prevleaf >> h) != v) {
-                        const double ms = wl.vs[k];
-                        const float mm = wl.vm[k];
-                        int ne = wl.rend[k];
-                        bool compute = true;
-                        double sum;
-                        float mn;
-                        if ((v & 1ull) == 0) {
-                            const int e = ne;
-                            if (e < U && ((((unsigned long long)wl.ulist[e] + n) >> h) == v + 1)) {
-                                sum = ms + wl.vs[e];
-                                mn = fmin_tree(mm, wl.vm[e]);
-                                ne = wl.rend[e];
-                            } else {
-                                sum = ms + ps[w];
-                                mn = fmin_tree(mm, pmn[w]);
-                            }
-                        } else if (k > 0 && (prevleaf >> h) == v - 1) {
-                            compute = false;  // the left sibling's owner combines this pair
-                        } else {
-                            sum = ps[w] + ms;
-                            mn = fmin_tree(pmn[w], mm);
-                        }
-                        if (compute) {
-                            wl.vs[k] = sum;
-                            wl.vm[k] = mn;
-                            wl.rend[k] = ne;
-                            t.S[v >> 1] = sum;
-                            t.M[v >> 1] = mn;
-                        }
-                    }
-                }
-                __syncwarp();
-            }
-        }
-        return;
-    }
-    for (int h = 0; h < shift; ++h) {
-        for (int k = lane; k < U; k += 32) {
-            const unsigned long long v = ((unsigned long long)wl.ulist[k] + n) >> h;
-            const unsigned long long pv = k > 0 ? ((unsigned long long)wl.ulist[k - 1] + n) >> h : 0;
-            if (k > 0 && pv == v) continue;  // not the first entry under this node
-            const double ms = wl.vs[k];
-            const float mm = wl.vm[k];
-            int ne = wl.rend[k];
-            double sum;
-            float mn;
-            if ((v & 1ull) == 0) {
-                const int e = ne;
-                if (e < U && ((((unsigned long long)wl.ulist[e] + n) >> h) == v + 1)) {
-                    sum = ms + wl.vs[e];
-                    mn = fmin_tree(mm, wl.vm[e]);
-                    ne = wl.rend[e];
-                } else {
-                    sum = ms + ld_sum(t, v + 1);
-                    mn = fmin_tree(mm, ld_min(t, v + 1));
-                }
-            } else {
-                if (k > 0 && pv == v - 1) continue;
-                sum = ld_sum(t, v - 1) + ms;
-                mn = fmin_tree(ld_min(t, v - 1), mm);
-            }
-            wl.vs[k] = sum;
-            wl.vm[k] = mn;
-            wl.rend[k] = ne;
-            t.S[v >> 1] = sum;
-            t.M[v >> 1] = mn;
-        }
-        __syncwarp();
-    }
-}
-
 // Files the batch entries of this CTA's subtrees under their warp's list (slot order is the
 // order of arrival; the sort below restores batch order).  Returns this thread's largest raw
 // priority among the filed entries.
@@ -1627,11 +1516,18 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     pdl_release();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int D = a.t.D;
-    const int shift = D - a.P;
-    const unsigned long long nsub = 1ull << a.P;
-    const unsigned long long first_sub = (unsigned long long)blockIdx.x * a.subs;
     const unsigned long long n = a.t.n;
     const unsigned long long size = a.ctl->size;
+    // While the ring fills, every valid index lies below `size`.  The 2^P subtrees are then
+    // taken at depth P + skip, the subtree of node 2^skip split in 2^P, where skip is the
+    // largest such that [0, n >> skip) still holds [0, size): the batch spreads over every warp
+    // instead of the few whose subtrees hold the filled slots.  Nodes above depth skip off the
+    // left spine cover only unused slots; the spine is rebuilt at the end.
+    int skip = 0;
+    while (a.P + skip + 1 <= D - 1 && size <= (n >> (skip + 1))) ++skip;
+    const int shift = D - a.P - skip;
+    const unsigned long long nsub = 1ull << a.P;
+    const unsigned long long first_sub = (unsigned long long)blockIdx.x * a.subs;
     const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
     if (tid < kUpdMaxWarps) s_cnt[tid] = 0;
     if (tid == 0) s_max = 0;
@@ -1732,11 +1628,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 if (win) {
                     wl.ulist[u] = (unsigned)leaf;
                     if (a.proportional) {
-                        const float lv = leaf_of(raw, a.lp);
-                        a.t.L[leaf] = lv;
-                        wl.vs[u] = (double)lv;
-                        wl.vm[u] = leaf_min_value(lv);
-                        wl.rend[u] = u + 1;
+                        wl.uraw[u] = raw;
                     } else {
                         a.raw_store[leaf] = raw;
                         mark_dirty(a.dirty, leaf);
@@ -1745,7 +1637,19 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 U += __popc(bal);
             }
             __syncwarp();
-            if (a.proportional) warp_upsweep<W>(a.t, wl, U, shift, lane);
+            if (a.proportional) {
+                // 32 distinct leaves at a time in ascending order, each group after the previous
+                // one has stored its nodes: a later group reads the earlier groups' nodes as its
+                // siblings and rewrites the ancestors they share
+                for (int c0 = 0; c0 < U; c0 += 32) {
+                    const int Uc = min(32, U - c0);
+                    const bool have = lane < Uc;
+                    const unsigned li = have ? wl.ulist[c0 + lane] - (unsigned)base : 0u;
+                    const float raw = have ? wl.uraw[c0 + lane] : 0.0f;
+                    warp_climb_regs<W>(a.t, Uc, shift, lane, base, li, raw, a.lp, s_lp);
+                    __syncwarp();
+                }
+            }
         }
     }
 
@@ -1773,7 +1677,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     const int g = 1 << (P - 5);
                     double gs[8];
                     float gm[8];
-                    const unsigned long long c0 = (1ull << P) + (unsigned long long)lane * g;
+                    const unsigned long long c0 = (1ull << (P + skip)) + (unsigned long long)lane * g;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         gs[i] = i < g ? ld_sum_cg(a.t, c0 + i) : 0.0;
@@ -1791,20 +1695,20 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                             const int dlev = 5 + (31 - __clz(half));
 #pragma unroll
                             for (int i = 0; i < half; ++i) {
-                                const unsigned long long node = (1ull << dlev) + (unsigned long long)lane * half + i;
+                                const unsigned long long node = (1ull << (dlev + skip)) + (unsigned long long)lane * half + i;
                                 a.t.S[node] = gs[i];
                                 a.t.M[node] = gm[i];
                             }
                         }
                     }
-                    sv = gs[0];   // depth-5 node 32 + lane
+                    sv = gs[0];   // depth-(5 + skip) node 32 * 2^skip + lane
                     mv = gm[0];
                     w = 32;
                 } else {
                     w = 1 << P;
                     if (lane < w) {
-                        sv = ld_sum_cg(a.t, (unsigned long long)w + lane);
-                        mv = ld_min_cg(a.t, (unsigned long long)w + lane);
+                        sv = ld_sum_cg(a.t, ((unsigned long long)w << skip) + lane);
+                        mv = ld_min_cg(a.t, ((unsigned long long)w << skip) + lane);
                     }
                 }
                 for (int st = 1; w > 1; st <<= 1, w >>= 1) {
@@ -1813,7 +1717,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     if ((lane & (2 * st - 1)) == 0 && lane < w * st) {
                         sv = sv + os;
                         mv = fmin_tree(mv, om);
-                        const int node = (w >> 1) + lane / (2 * st);
+                        const unsigned long long node = ((unsigned long long)(w >> 1) << skip) + lane / (2 * st);
                         a.t.S[node] = sv;
                         a.t.M[node] = mv;
                     }
@@ -1830,7 +1734,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
             if (warp < 4) {
             double gs[8];
             float gm[8];
-            const unsigned long long c0 = (1ull << P) + ((unsigned long long)warp << (P - 2)) + (unsigned long long)lane * g;
+            const unsigned long long c0 = (1ull << (P + skip)) + ((unsigned long long)warp << (P - 2)) + (unsigned long long)lane * g;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 gs[i] = i < g ? ld_sum_cg(a.t, c0 + i) : 0.0;
@@ -1847,7 +1751,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     const int dlev = 7 + (31 - __clz(half));   // depth of these sums
 #pragma unroll
                     for (int i = 0; i < half; ++i) {
-                        const unsigned long long node = (1ull << dlev) + ((unsigned long long)warp << (dlev - 2)) +
+                        const unsigned long long node = (1ull << (dlev + skip)) + ((unsigned long long)warp << (dlev - 2)) +
                                                         (unsigned long long)lane * half + i;
                         a.t.S[node] = gs[i];
                         a.t.M[node] = gm[i];
@@ -1862,7 +1766,8 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 if ((lane & (2 * st - 1)) == 0) {
                     sv = sv + os;
                     mv = fmin_tree(mv, om);
-                    const int node = (1 << (dep - 1)) + (warp << (dep - 3)) + lane / (2 * st);
+                    const unsigned long long node = (1ull << (dep - 1 + skip)) + ((unsigned long long)warp << (dep - 3)) +
+                                                    lane / (2 * st);
                     a.t.S[node] = sv;
                     a.t.M[node] = mv;
                 }
@@ -1882,7 +1787,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     if ((lane & (2 * st - 1)) == 0 && lane < w * st) {
                         qv = qv + os;
                         qm = fmin_tree(qm, om);
-                        const int node = (w >> 1) + lane / (2 * st);
+                        const unsigned long long node = ((unsigned long long)(w >> 1) << skip) + lane / (2 * st);
                         a.t.S[node] = qv;
                         a.t.M[node] = qm;
                     }
@@ -1894,8 +1799,8 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
             const int P = a.P;
             const int width = 1 << P;
             for (int i = tid; i < width; i += blockDim.x) {
-                heapS[width + i] = ld_sum_cg(a.t, (unsigned long long)width + i);
-                heapM[width + i] = ld_min_cg(a.t, (unsigned long long)width + i);
+                heapS[width + i] = ld_sum_cg(a.t, ((unsigned long long)width << skip) + i);
+                heapM[width + i] = ld_min_cg(a.t, ((unsigned long long)width << skip) + i);
             }
             for (int l = P - 1; l >= 0; --l) {
                 __syncthreads();
@@ -1906,8 +1811,37 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     const float mn = fmin_tree(heapM[2 * node], heapM[2 * node + 1]);
                     heapS[node] = sum;
                     heapM[node] = mn;
-                    a.t.S[node] = sum;
-                    a.t.M[node] = mn;
+                    a.t.S[((unsigned long long)lw << skip) + i] = sum;
+                    a.t.M[((unsigned long long)lw << skip) + i] = mn;
+                }
+            }
+        }
+        if (a.proportional && skip > 0) {
+            // the left spine from node 2^skip (rebuilt above, or the single subtree's root) up to
+            // the root; each right sibling on it covers slots at or beyond n >> skip, untouched
+            __syncthreads();
+            if (tid == 0) {
+                double sv = ld_sum_cg(a.t, 1ull << skip);
+                float mv = ld_min_cg(a.t, 1ull << skip);
+                for (int j0 = skip; j0 >= 1; j0 -= 8) {
+                    double rs[8];
+                    float rm[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 - u;
+                        rs[u] = j >= 1 ? ld_sum_cg(a.t, (1ull << j) + 1) : 0.0;
+                        rm[u] = j >= 1 ? ld_min_cg(a.t, (1ull << j) + 1) : 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int j = j0 - u;
+                        if (j >= 1) {
+                            sv = sv + rs[u];
+                            mv = fmin_tree(mv, rm[u]);
+                            a.t.S[1ull << (j - 1)] = sv;
+                            a.t.M[1ull << (j - 1)] = mv;
+                        }
+                    }
                 }
             }
         }
