@@ -173,11 +173,13 @@ cudaError_t rank_order(per_buffer *h, cudaStream_t st)
 
 // Kernel attributes are per device: set them the first time a buffer is created on a device.
 // The carveout (percent of the unified L1/shared array preferred for shared memory; a kernel
-// still gets the shared memory it needs), measured on GB300: the tree kernels prefer L1 (0):
-// the apex step 37.2K steps/s against 36.8K with the driver's choice; the samplers keep the
-// driver's choice (with 0 the stress sample took 35.6 us against 27.1); so do the rank
-// kernels, which stage whole tiles in shared memory.  GBPER_CARVEOUT sets one value for every
-// kernel; GBPER_CARVEOUT_TREE and GBPER_CARVEOUT_SAMPLE set one family (-1: the driver's).
+// still gets the shared memory it needs), measured on GB300: the tree kernels but the level
+// rebuild prefer L1 (0): the apex step 37.2K steps/s against 36.8K with the driver's choice
+// (the rebuild's shared memory needs the larger configurations for more than one CTA per SM);
+// the samplers keep the driver's choice (with 0 the stress sample took 35.6 us against 27.1);
+// so do the rank kernels, which stage whole tiles in shared memory.  GBPER_CARVEOUT sets one
+// value for every kernel but the rebuild; GBPER_CARVEOUT_TREE and GBPER_CARVEOUT_SAMPLE set
+// one family (-1: the driver's).
 cudaError_t init_kernels_once(int device)
 {
     static std::mutex mu;
