@@ -74,9 +74,37 @@ def bytes_update(idx, D):
     return 12 * B + 4 * len(np.unique(idx)) + 36 * nodes
 
 
+def strip_c_comments(src: str) -> str:
+    """C/CUDA source with its comments removed and every run of whitespace made one space, so
+    that an edit of comments or layout alone leaves the result unchanged (string and character
+    literals are kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(name):
+    """First 16 hex digits of the sha256 of a kernel source file, comments and layout aside."""
     p = os.path.join(ROOT, "rl_infra_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    code = strip_c_comments(open(p, encoding="utf-8").read())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def traffic_from_profiles(kernel, kernel_file, workload="apex"):

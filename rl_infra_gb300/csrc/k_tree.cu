@@ -1157,14 +1157,17 @@ __global__ void k_upd_finish(Ctl *c, double alpha)
 // Priority update: last-writer-wins scatter + dirty-ancestor upsweep, one launch.
 // The tree below depth P is cut into 2^P subtrees and each subtree belongs to one warp (a CTA
 // holds 4 or 16 of them), so nothing below depth P needs more than warp synchronisation:
-//   1. the CTA reads the batch once, coalesced, and files each entry under its subtree's warp;
-//   2. each warp sorts its entries by (leaf, batch position) in shared memory, keeps the last
-//      position of every leaf, writes those leaves and climbs its subtree level by level.  On
-//      a level the first entry of each run of entries under one node owns the node; the owner
-//      of a left child reaches the owner of a dirty right sibling through a run-end pointer
-//      (pointer jumping); clean siblings are loaded from global memory, a window of levels at
-//      a time, before the window is combined;
-//   3. the last CTA to arrive rebuilds the 2^P - 1 nodes above the subtree roots and folds the
+//   1. every CTA reads the whole batch, coalesced, and files each entry of its subtrees under
+//      the subtree's warp (while the ring fills, the subtrees split only the part that holds
+//      filled slots);
+//   2. each warp sorts its entries by (leaf, batch position), in registers up to 32 and in
+//      shared memory beyond, keeps the last position of every leaf and climbs its subtree 32
+//      distinct leaves at a time: one round of loads fetches every sibling a lane owns up to
+//      16 levels, the plan (which lane adds at which height, which takes a dirty sibling's
+//      value from another lane) comes from owner ballots while the loads are in flight, and a
+//      chain of binary64 adds carries nothing else;
+//   3. the last CTA to arrive (or CTA 0 after a cluster barrier) rebuilds the 2^P - 1 nodes
+//      above the subtree roots, and the spine above them while the ring fills, and folds the
 //      batch maximum into the running maximum.
 // A warp whose subtree receives more entries than its shared-memory list holds applies the
 // batch in position order 32 entries at a time (later chunks overwrite earlier ones, so the
