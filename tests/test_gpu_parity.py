@@ -189,18 +189,26 @@ def test_climb_crowded_and_partly_filled(mode, size):
     """The climb path on a full ring and on rings holding 5000 or 3 of 2^16 slots (the subtrees
     then split only the filled part; the spine above it is rebuilt), with batches that give one
     subtree (2^0, 2^3, 2^6, 2^9 and 2^10 of them) 33 to 600 entries, more than one warp's group
-    of 32 and more than its list."""
+    of 32 and more than its list, packed into 256 or 1024 slots (also spanning a whole aligned
+    block of 1024) or spread over 8192."""
     cap = 1 << 16
     w = _small("tiny", capacity=cap, state_dim=4, row_stride=4, mode=mode)
     g = wl.rng(21, 10 * mode + (size % 7))
     p = Pair(cap, 4, 4, 0.6, 1e-6, mode, seed=5, **CLIMB)
     prefill(p, w, g, count=size)
     for B in (5, 40, 300, 600, 2100, 5000):
-        for crowd in (False, True):
+        for crowd in ("none", "dense", "spread", "ends"):
             idx = g.integers(0, size, B).astype(np.int64)
-            if crowd:
-                lo = int(g.integers(0, max(size - 256, 1)))
-                idx[: (3 * B) // 4] = lo + g.integers(0, min(256, size), (3 * B) // 4)
+            width = {"none": 0, "dense": 256, "spread": 8192, "ends": 1024}[crowd]
+            if width:
+                # most entries in one stretch of `width` slots
+                width = min(width, size)
+                lo = int(g.integers(0, size - width + 1))
+                k = (9 * B) // 10
+                idx[:k] = lo + g.integers(0, width, k)
+                if crowd == "ends" and B - k >= 2:
+                    blk = (lo // width) * width   # both ends of an aligned block
+                    idx[k:k + 2] = [blk, min(blk + width, size) - 1]
             idx = wl.duplicate_positions(g, idx, 0.2) if B > 4 else idx
             p.update(idx, wl.td_errors(g, B))
             p.check_tree()
