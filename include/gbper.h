@@ -278,21 +278,29 @@ per_status per_nleaves(const per_buffer *h, uint64_t *out);
  * while a CUDA graph is being captured (cudaMalloc is not permitted then), real-time loops
  * that forbid allocator latency, or hosts whose device memory belongs to another framework's
  * pool.  The call itself makes no cudaMalloc, cudaFree or other allocating call.
- *   d_raw   [n] float, device, > 0 and finite (caller-owned input).
- *   d_order [n] uint32, device (caller-owned output).
- *   n       1 .. 262144 (2^18); larger n returns PER_ERR_INVALID_ARG.
+ *   d_raw    [n] float, device, > 0 and finite (caller-owned input).
+ *   d_order  [n] uint32, device (caller-owned output).
+ *   d_status one uint32, device, or NULL (caller-owned output): receives 0, or the
+ *            PER_DEVFLAG_* bits of what the device met (PER_DEVFLAG_TIMEOUT: a bounded wait of
+ *            the sort gave up).  The call returns before the GPU runs it, so its return value
+ *            cannot carry this; read the word after the stream has reached it.
+ *   n        1 .. 262144 (2^18); larger n returns PER_ERR_INVALID_ARG.
+ * When a wait gave up, every entry of d_order is 0xFFFFFFFF (a value no valid slot has)
+ * instead of a partial order, whether or not d_status is given.
  * Scratch: a fixed device array of about 4.3 MiB compiled into the library, which every GPU
  * that loads the library holds until the process exits.  The first call on a device looks up
  * that array's device address (cudaGetSymbolAddress) and caches it; make that first call on
  * each device before any stream capture begins.  All calls share the one array and it keeps
- * the last call's contents (every call overwrites all it reads, so nothing has to start at
- * zero); calls whose GPU work overlaps -- on different streams, or concurrently from several
- * host threads -- race on it and must be serialised by the caller.
+ * the last call's contents; every call first clears, with cudaMemsetAsync (no allocation), the
+ * digit histograms, tile counters and error word that must start at zero, so a call that
+ * stopped part way does not spoil the next.  Calls whose GPU work overlaps -- on different
+ * streams, or concurrently from several host threads -- race on the array and must be
+ * serialised by the caller.
  * Errors: PER_ERR_INVALID_ARG (NULL or misaligned pointer, n out of range), PER_ERR_CUDA.
  * It records no message for per_last_error.
  */
 per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uint32_t *d_order,
-                                  void *stream);
+                                  uint32_t *d_status, void *stream);
 
 #ifdef __cplusplus
 }

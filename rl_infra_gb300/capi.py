@@ -113,7 +113,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.per_last_error.restype = ctypes.c_char_p
         L.per_read_state.argtypes = [vp, u32, u64, u64, vp, vp]
         L.per_read_state.restype = st
-        L.per_rank_order_noalloc.argtypes = [vp, u32, vp, vp]
+        L.per_rank_order_noalloc.argtypes = [vp, u32, vp, vp, vp]
         L.per_rank_order_noalloc.restype = st
         _lib = L
         return L
@@ -187,9 +187,10 @@ def per_read_state(h, which, first, count, host_dst, stream):
     return load().per_read_state(h, which, first, count, host_dst, stream)
 
 
-def per_rank_order_noalloc(d_raw, n, d_order, stream):
-    """Slot order by raw priority, descending, without any device allocation (n <= 2^18)."""
-    return load().per_rank_order_noalloc(d_raw, n, d_order, stream)
+def per_rank_order_noalloc(d_raw, n, d_order, d_status, stream):
+    """Slot order by raw priority, descending, without any device allocation (n <= 2^18);
+    d_status (a device uint32, or None) receives the device's PER_DEVFLAG_* bits."""
+    return load().per_rank_order_noalloc(d_raw, n, d_order, d_status, stream)
 
 
 # -- torch-facing convenience ---------------------------------------------------------------

@@ -731,8 +731,9 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
 
 // ------------------------------------------------------------------------------------------
 // per_rank_order_noalloc: the same descending sort for callers that may not allocate device
-// memory.  Its scratch (key and value ping-pong buffers, tile histograms) is a file-scope
-// device array of fixed size, resolved to a device address once per device.
+// memory.  Its scratch (key and value ping-pong buffers, digit histograms, control words and
+// look-back words) is a file-scope device array of fixed size, resolved to a device address
+// once per device.
 // ------------------------------------------------------------------------------------------
 #include "gbper.h"
 
@@ -744,13 +745,15 @@ namespace {
 constexpr unsigned long long kNoAllocMaxKeys = 1ull << 18;
 constexpr unsigned long long kNoAllocTiles = (kNoAllocMaxKeys + kTile - 1) / kTile;
 constexpr unsigned long long kNoAllocGroups = (kNoAllocTiles + kGroup - 1) / kGroup;
-// keys[2], values[2], digit histograms, sort control, then 64-bit look-back words
+// keys[2], values[2], digit histograms [1024], sort control [16], then 64-bit look-back words
 constexpr unsigned long long kNoAllocWords =
     4 * kNoAllocMaxKeys + 1024 + 16 + 2 * (4 * (kNoAllocTiles + kNoAllocGroups) * 256);
 constexpr int kNoAllocMaxDevices = 64;
 
-// About 4.3 MiB per device, held by every device that loads the library until exit;
-// zero at load, which the sort's histograms, control words and epoch tags rely on.
+// About 4.3 MiB per device, held by every device that loads the library until exit.  Zero at
+// load; the look-back words rely on that (each sort tags them with a new epoch, so a word left
+// by an earlier call never reads as this call's).  The histograms, tile counters and error word
+// are cleared by every call.
 __device__ __align__(256) unsigned g_noalloc_scratch[kNoAllocWords];
 
 std::mutex g_noalloc_mu;
@@ -775,16 +778,30 @@ cudaError_t noalloc_scratch(unsigned **out)
     return cudaSuccess;
 }
 
+// Copies the sorted slots to the caller's order and reports the sort's error word: when a
+// look-back wait gave up, every entry becomes 0xFFFFFFFF (no valid slot) instead of a wrong
+// order, and *status (if given) receives the flag bits.  Launched without programmatic
+// serialization, so it starts once the last sort pass has completed.
+__global__ void k_noalloc_emit(const unsigned *sorted, unsigned n, const unsigned *err, unsigned *order,
+                               unsigned *status)
+{
+    const unsigned flags = *(const volatile unsigned *)err;
+    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) order[i] = flags ? 0xFFFFFFFFu : sorted[i];
+    if (status && i == 0) *status = flags;
+}
+
 }  // namespace
 
 }  // namespace gbper
 
 extern "C" per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uint32_t *d_order,
-                                             void *stream)
+                                             uint32_t *d_status, void *stream)
 {
     using namespace gbper;
     if (!d_raw || !d_order || n == 0 || n > kNoAllocMaxKeys) return PER_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(d_raw) % 4 || reinterpret_cast<uintptr_t>(d_order) % 4)
+    if (reinterpret_cast<uintptr_t>(d_raw) % 4 || reinterpret_cast<uintptr_t>(d_order) % 4 ||
+        reinterpret_cast<uintptr_t>(d_status) % 4)
         return PER_ERR_INVALID_ARG;
     unsigned *base = nullptr;
     if (noalloc_scratch(&base) != cudaSuccess) {
@@ -809,9 +826,17 @@ extern "C" per_status per_rank_order_noalloc(const float *d_raw, uint32_t n, uin
         return PER_ERR_CUDA;
     }
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // A call that stopped part way (a failed launch, a captured call never replayed) may have
+    // left histogram counts, tile counters or the error word set: clear them (the epoch in
+    // sort_ctl[4] stays, it tags this sort's look-back words).  cudaMemsetAsync allocates nothing.
+    cudaError_t e = cudaMemsetAsync(w.digit_hist, 0, (1024 + 4) * sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.err, 0, sizeof(unsigned), st);
     unsigned *sorted = nullptr;
-    cudaError_t e = launch_rank_sort(w, n, &sorted, st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(d_order, sorted, (size_t)n * sizeof(unsigned), cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess) e = launch_rank_sort(w, n, &sorted, st);
+    if (e == cudaSuccess) {
+        k_noalloc_emit<<<(n + 255) / 256, 256, 0, st>>>(sorted, n, w.err, d_order, d_status);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) cudaGetLastError();
     return e == cudaSuccess ? PER_OK : PER_ERR_CUDA;
 }
