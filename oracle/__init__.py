@@ -18,7 +18,7 @@ _SRC = os.path.join(_HERE, "per_oracle.c")
 _HDR = os.path.join(_HERE, "per_oracle.h")
 _LIB = os.path.join(_HERE, "_build", "libper_oracle.so")
 _lock = threading.Lock()
-_lib = None
+_libs: dict = {}
 
 PROPORTIONAL = 0
 RANK = 1
@@ -26,24 +26,30 @@ UNIFORM = 2
 FLAT = 3
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (binary64 as written: no contraction, no fast-math)."""
+def _lib_path(plant: int) -> str:
+    return _LIB if plant == 0 else _LIB.replace(".so", f"_plant{plant}.so")
+
+
+def build(force: bool = False, plant: int = 0) -> str:
+    """Compile the oracle with gcc (binary64 as written: no contraction, no fast-math).
+    `plant` > 0 builds a separate test copy with one known mistake planted in the
+    near-boundary rule (ORC_PLANT in per_oracle.c), for the tests that show its pins catch it."""
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    out = _lib_path(plant)
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
-        tmp = _LIB + f".tmp{os.getpid()}"
+    if force or not os.path.exists(out) or os.path.getmtime(out) < newest:
+        tmp = out + f".tmp{os.getpid()}"
         subprocess.check_call([
             "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-            "-shared", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB)
-    return _LIB
+            f"-DORC_PLANT={int(plant)}", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, out)
+    return out
 
 
-def lib() -> ctypes.CDLL:
-    global _lib
+def lib(plant: int = 0) -> ctypes.CDLL:
     with _lock:
-        if _lib is None:
-            L = ctypes.CDLL(build())
+        if plant not in _libs:
+            L = ctypes.CDLL(build(plant=plant))
             u32, u64, i64, f32, f64, vp = (ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64,
                                            ctypes.c_float, ctypes.c_double, ctypes.c_void_p)
             L.orc_philox4x32_10.argtypes = [vp, vp, vp]
@@ -62,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.orc_update.restype = ctypes.c_int
             L.orc_descend.argtypes = [vp, f64, vp]
             L.orc_descend.restype = i64
+            L.orc_locate.argtypes = [vp, f64, vp, vp, vp]
+            L.orc_locate.restype = ctypes.c_int
             L.orc_rank_order.argtypes = [vp, vp]
             L.orc_rank_order.restype = i64
             for name in ("orc_capacity", "orc_nleaves", "orc_size", "orc_cursor",
@@ -78,8 +86,8 @@ def lib() -> ctypes.CDLL:
                          "orc_ring_states", "orc_ring_next"):
                 getattr(L, name).argtypes = [vp]
                 getattr(L, name).restype = vp
-            _lib = L
-    return _lib
+            _libs[plant] = L
+    return _libs[plant]
 
 
 def _p(a):
@@ -106,21 +114,22 @@ class Oracle:
     """One replay buffer held by the oracle (host memory only)."""
 
     def __init__(self, capacity, state_dim, row_stride_out=None, alpha=0.6, eps=1e-6,
-                 mode=PROPORTIONAL, seed=0, with_ring=True):
+                 mode=PROPORTIONAL, seed=0, with_ring=True, plant=0):
         self.capacity = int(capacity)
         self.d = int(state_dim)
         self.dp = int(row_stride_out if row_stride_out is not None else state_dim)
         self.mode = mode
         self.with_ring = bool(with_ring)
-        self._h = lib().orc_create(self.capacity, self.d, self.dp, float(alpha), float(eps),
+        self._L = lib(plant)
+        self._h = self._L.orc_create(self.capacity, self.d, self.dp, float(alpha), float(eps),
                                    int(mode), int(seed), int(with_ring))
         if not self._h:
             raise OracleError("orc_create rejected its arguments or ran out of memory")
-        self.n = int(lib().orc_nleaves(self._h))
+        self.n = int(self._L.orc_nleaves(self._h))
 
     def close(self):
         if self._h:
-            lib().orc_destroy(self._h)
+            self._L.orc_destroy(self._h)
             self._h = None
 
     def __del__(self):
@@ -138,7 +147,7 @@ class Oracle:
                 for a, t in ((states, np.float32), (next_states, np.float32),
                              (actions, np.uint32), (rewards, np.float32),
                              (dones, np.uint8), (raw_prio, np.float32))]
-        rc = lib().orc_add(self._h, int(count), *[_p(a) for a in arrs])
+        rc = self._L.orc_add(self._h, int(count), *[_p(a) for a in arrs])
         if rc != 0:
             raise OracleError(f"orc_add -> {rc}")
 
@@ -156,7 +165,7 @@ class Oracle:
             out["actions"] = np.zeros(B, np.uint32)
             out["rewards"] = np.zeros(B, np.float32)
             out["dones"] = np.zeros(B, np.uint8)
-        rc = lib().orc_sample(
+        rc = self._L.orc_sample(
             self._h, B, float(beta), _p(out["idx"]), _p(out["w"]),
             _p(out.get("states")), _p(out.get("next_states")), _p(out.get("actions")),
             _p(out.get("rewards")), _p(out.get("dones")), _p(out["near"]), _p(out["rem"]),
@@ -169,19 +178,31 @@ class Oracle:
     def update(self, idx, td) -> int:
         idx = np.ascontiguousarray(idx, dtype=np.int64)
         td = np.ascontiguousarray(td, dtype=np.float32)
-        rc = lib().orc_update(self._h, len(idx), _p(idx), _p(td))
+        rc = self._L.orc_update(self._h, len(idx), _p(idx), _p(td))
         if rc < 0:
             raise OracleError(f"orc_update -> {rc}")
         return rc
 
     def descend(self, mass):
         rem = ctypes.c_double(0.0)
-        leaf = lib().orc_descend(self._h, float(mass), ctypes.byref(rem))
+        leaf = self._L.orc_descend(self._h, float(mass), ctypes.byref(rem))
         return int(leaf), rem.value
+
+    def locate(self, mass):
+        """(slot, mass above the slot's extent start, near-boundary flag) of one mass, by the
+        same step sample() takes for each draw."""
+        slot = ctypes.c_int64(0)
+        rem = ctypes.c_double(0.0)
+        near = ctypes.c_uint8(0)
+        rc = self._L.orc_locate(self._h, float(mass), ctypes.byref(slot), ctypes.byref(rem),
+                                ctypes.byref(near))
+        if rc != 0:
+            raise OracleError(f"orc_locate -> {rc}")
+        return int(slot.value), rem.value, bool(near.value)
 
     def rank_order(self) -> np.ndarray:
         out = np.zeros(max(self.size, 1), np.uint32)
-        s = lib().orc_rank_order(self._h, _p(out))
+        s = self._L.orc_rank_order(self._h, _p(out))
         if s < 0:
             raise OracleError(f"orc_rank_order -> {s}")
         return out[:s]
@@ -189,28 +210,28 @@ class Oracle:
     # -- state ----------------------------------------------------------------------------
     @property
     def size(self):
-        return int(lib().orc_size(self._h))
+        return int(self._L.orc_size(self._h))
 
     @property
     def cursor(self):
-        return int(lib().orc_cursor(self._h))
+        return int(self._L.orc_cursor(self._h))
 
     @property
     def sample_calls(self):
-        return int(lib().orc_sample_calls(self._h))
+        return int(self._L.orc_sample_calls(self._h))
 
     @property
     def max_raw(self):
-        return float(lib().orc_max_raw(self._h))
+        return float(self._L.orc_max_raw(self._h))
 
     def total(self):
-        return float(lib().orc_total(self._h))
+        return float(self._L.orc_total(self._h))
 
     def min(self):
-        return float(lib().orc_min(self._h))
+        return float(self._L.orc_min(self._h))
 
     def _view(self, fn, dtype, count):
-        ptr = getattr(lib(), fn)(self._h)
+        ptr = getattr(self._L, fn)(self._h)
         if not ptr:
             return None
         buf = (ctypes.c_char * (count * np.dtype(dtype).itemsize)).from_address(ptr)

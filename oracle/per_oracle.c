@@ -440,6 +440,157 @@ static void gather_row(const orc_per *o, uint32_t j, uint64_t slot, float *out_s
         out_dones[j] = o->dones[slot];
 }
 
+/* ------------------------------------------------------------------------------------------
+ * Locating one draw.  Every mode maps a mass m in [0, T) to the slot whose extent
+ * [C(i-1), C(i)) holds it (R6): the tree by the descent, flat mode by a search of the
+ * cumulative array, uniform mode by a division, rank mode by a search of the CDF (then the slot
+ * of that rank).  The draw lies near a boundary -- the parity bar's excuse for an index
+ * mismatch -- when it fell off the end (R7) or when its mass is within 1e-6 * T of either end
+ * of the extent: m - C(i-1) < 1e-6 T or C(i) - m < 1e-6 T.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Test builds only: ORC_PLANT = 1..4 plants one known mistake in the near-boundary rule, so a
+ * test can show that the rule's pins catch it (1: an absolute tolerance of 1e-6; 2: a fall-off
+ * not counted; 3: the tree's upper distance taken against the next leaf; 4: the upper end not
+ * tested).  The oracle proper is built with ORC_PLANT = 0. */
+#ifndef ORC_PLANT
+#define ORC_PLANT 0
+#endif
+
+typedef struct {
+    double T;        /* the call's total */
+    double *C;       /* flat mode: cumulative array of the filled slots */
+    uint32_t *order; /* rank mode: slots by rank */
+} locate_ctx;
+
+static int locate_begin(const orc_per *o, locate_ctx *c)
+{
+    c->C = NULL;
+    c->order = NULL;
+    if (o->mode == ORC_PROPORTIONAL) {
+        c->T = node_sum(o, 1);
+    } else if (o->mode == ORC_FLAT) {
+        c->C = flat_cumulative(o);
+        if (!c->C)
+            return ORC_ENOMEM;
+        c->T = c->C[o->size - 1];
+    } else if (o->mode == ORC_UNIFORM) {
+        c->T = (double)o->size;
+    } else {
+        c->order = (uint32_t *)malloc(o->size * sizeof(uint32_t));
+        if (!c->order)
+            return ORC_ENOMEM;
+        orc_rank_order(o, c->order);
+        c->T = o->cdf[o->size];
+    }
+    return ORC_OK;
+}
+
+static void locate_end(locate_ctx *c)
+{
+    free(c->C);
+    free(c->order);
+}
+
+/* below = m - C(i-1), above = C(i) - m */
+static int near_boundary(int fell_off, double below, double above, double T)
+{
+    double tol = 1e-6 * T;
+#if ORC_PLANT == 1
+    tol = 1e-6;
+#elif ORC_PLANT == 2
+    fell_off = 0;
+#elif ORC_PLANT == 4
+    above = INFINITY;
+#endif
+    return fell_off || below < tol || above < tol;
+}
+
+/* The slot of one mass; *rank (rank mode) the rank, *rem the mass above the extent's start,
+ * *near the boundary flag. */
+static uint64_t locate(const orc_per *o, const locate_ctx *c, double mass, uint64_t *rank,
+                       double *rem, int *near)
+{
+    uint64_t s = o->size, slot = 0;
+    int fell_off = 0;
+    double below = 0.0, above = 0.0;
+    if (o->mode == ORC_PROPORTIONAL) {
+        double r = 0.0;
+        int64_t leaf = orc_descend(o, mass, &r);
+        if ((uint64_t)leaf >= s) { /* R7 */
+            leaf = (int64_t)s - 1;
+            fell_off = 1;
+        }
+        slot = (uint64_t)leaf;
+        below = r;
+        above = (double)o->L[slot] - r;
+#if ORC_PLANT == 3
+        if (slot + 1 < o->n)
+            above = (double)o->L[slot + 1] - r;
+#endif
+    } else if (o->mode == ORC_FLAT) {
+        /* R26: the first entry of the cumulative array above the mass */
+        slot = flat_search(c->C, s, mass);
+        if (slot >= s) {
+            slot = s - 1;
+            fell_off = 1;
+        }
+        below = mass - (slot ? c->C[slot - 1] : 0.0);
+        above = c->C[slot] - mass;
+    } else if (o->mode == ORC_UNIFORM) {
+        /* R24: every filled slot weighs 1, so the walk is a division */
+        double fl = floor(mass);
+        slot = (uint64_t)fl;
+        if (slot >= s) {
+            slot = s - 1;
+            fell_off = 1;
+        }
+        below = mass - fl;
+        above = 1.0 - below;
+    } else {
+        /* smallest r in [1, s] with cdf[r] > mass (binary search over the CDF) */
+        uint64_t lo = 1, hi = s + 1;
+        while (lo < hi) {
+            uint64_t mid = lo + (hi - lo) / 2;
+            if (o->cdf[mid] > mass)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        uint64_t r = lo;
+        if (r > s) {
+            r = s;
+            fell_off = 1;
+        }
+        slot = c->order[r - 1];
+        below = mass - o->cdf[r - 1];
+        above = o->cdf[r] - mass;
+        *rank = r;
+    }
+    *rem = below;
+    *near = near_boundary(fell_off, below, above, c->T);
+    return slot;
+}
+
+int orc_locate(const orc_per *o, double mass, int64_t *slot, double *rem, uint8_t *near)
+{
+    if (!o || !slot || o->size == 0)
+        return o && o->size == 0 ? ORC_EEMPTY : ORC_EINVAL;
+    locate_ctx c;
+    if (locate_begin(o, &c) != ORC_OK)
+        return ORC_ENOMEM;
+    uint64_t r = 0;
+    double left = 0.0;
+    int nb = 0;
+    *slot = (int64_t)locate(o, &c, mass, &r, &left, &nb);
+    if (rem)
+        *rem = left;
+    if (near)
+        *near = (uint8_t)nb;
+    locate_end(&c);
+    return ORC_OK;
+}
+
 int orc_sample(orc_per *o, uint32_t B, float beta, int64_t *idx, float *w, float *out_states,
                float *out_next, uint32_t *out_actions, float *out_rewards, uint8_t *out_dones,
                uint8_t *near, double *rem, double *mass_out)
@@ -451,151 +602,47 @@ int orc_sample(orc_per *o, uint32_t B, float beta, int64_t *idx, float *w, float
     if (o->size == 0)
         return ORC_EEMPTY;
     uint64_t call = o->calls;
+    locate_ctx c;
+    if (locate_begin(o, &c) != ORC_OK)
+        return ORC_ENOMEM;
+    /* p_min (R8): the min tree's root, or the smallest filled leaf without a tree */
+    float pmin = INFINITY;
     if (o->mode == ORC_PROPORTIONAL) {
-        double T = node_sum(o, 1);
-        float pmin = node_min(o, 1);
-        double seg = T / (double)B;
-        for (uint32_t j = 0; j < B; ++j) {
-            double u = orc_uniform53(o->seed, j, call, 0);
-            double mass = ((double)j + u) * seg; /* R5 */
-            double r = 0.0;
-            int64_t leaf = orc_descend(o, mass, &r);
-            int fell_off = 0;
-            if ((uint64_t)leaf >= o->size) { /* R7 */
-                leaf = (int64_t)o->size - 1;
-                fell_off = 1;
-            }
-            idx[j] = leaf;
-            float lv = o->L[leaf];
-            if (w) /* R8 */
-                w[j] = (float)pow((double)lv / (double)pmin, -(double)beta);
-            if (near) {
-                double tol = 1e-6 * T;
-                near[j] = (uint8_t)(fell_off || r < tol || ((double)lv - r) < tol);
-            }
-            if (rem)
-                rem[j] = r;
-            if (mass_out)
-                mass_out[j] = mass;
-            if (o->with_ring)
-                gather_row(o, j, (uint64_t)leaf, out_states, out_next, out_actions, out_rewards,
-                           out_dones);
-        }
+        pmin = node_min(o, 1);
     } else if (o->mode == ORC_FLAT) {
-        /* R26: the cumulative array over the filled slots, left to right, then a binary search
-         * for the first entry above each stratified mass (R5, R6, R7, R8 as in the tree) */
-        uint64_t s = o->size;
-        double *C = flat_cumulative(o);
-        if (!C)
-            return ORC_ENOMEM;
-        float pmin = INFINITY;
-        for (uint64_t i = 0; i < s; ++i)
+        for (uint64_t i = 0; i < o->size; ++i)
             if (o->L[i] < pmin)
                 pmin = o->L[i];
-        double T = C[s - 1];
-        double seg = T / (double)B;
-        for (uint32_t j = 0; j < B; ++j) {
-            double u = orc_uniform53(o->seed, j, call, 0);
-            double mass = ((double)j + u) * seg;
-            int fell_off = 0;
-            uint64_t leaf = flat_search(C, s, mass);
-            if (leaf >= s) {
-                leaf = s - 1;
-                fell_off = 1;
-            }
-            idx[j] = (int64_t)leaf;
-            float lv = o->L[leaf];
-            if (w)
-                w[j] = (float)pow((double)lv / (double)pmin, -(double)beta);
-            double below = leaf ? C[leaf - 1] : 0.0;
-            double r = mass - below;
-            if (near) {
-                double tol = 1e-6 * T;
-                near[j] = (uint8_t)(fell_off || r < tol || (C[leaf] - mass) < tol);
-            }
-            if (rem)
-                rem[j] = r;
-            if (mass_out)
-                mass_out[j] = mass;
-            if (o->with_ring)
-                gather_row(o, j, leaf, out_states, out_next, out_actions, out_rewards, out_dones);
-        }
-        free(C);
-    } else if (o->mode == ORC_UNIFORM) {
-        /* R24: every filled slot weighs 1, so T = size and the walk is a division: draw j takes
-         * mass (j + u_j) * (size / B), slot floor(mass), weight 1 */
-        double T = (double)o->size;
-        double seg = T / (double)B;
-        for (uint32_t j = 0; j < B; ++j) {
-            double u = orc_uniform53(o->seed, j, call, 2);
-            double mass = ((double)j + u) * seg;
-            double fl = floor(mass);
-            int fell_off = 0;
-            uint64_t slot = (uint64_t)fl;
-            if (slot >= o->size) {
-                slot = o->size - 1;
-                fell_off = 1;
-            }
-            idx[j] = (int64_t)slot;
-            if (w)
-                w[j] = 1.0f;
-            double r = mass - fl;
-            if (near) {
-                double tol = 1e-6 * T;
-                near[j] = (uint8_t)(fell_off || r < tol || (1.0 - r) < tol);
-            }
-            if (rem)
-                rem[j] = r;
-            if (mass_out)
-                mass_out[j] = mass;
-            if (o->with_ring)
-                gather_row(o, j, slot, out_states, out_next, out_actions, out_rewards, out_dones);
-        }
-    } else {
-        uint64_t s = o->size;
-        uint32_t *order = (uint32_t *)malloc(s * sizeof(uint32_t));
-        if (!order)
-            return ORC_ENOMEM;
-        orc_rank_order(o, order);
-        double T = o->cdf[s];
-        double seg = T / (double)B;
-        for (uint32_t j = 0; j < B; ++j) {
-            double u = orc_uniform53(o->seed, j, call, 1);
-            double mass = ((double)j + u) * seg;
-            /* smallest r in [1, s] with cdf[r] > mass (binary search over the CDF) */
-            uint64_t lo = 1, hi = s + 1;
-            while (lo < hi) {
-                uint64_t mid = lo + (hi - lo) / 2;
-                if (o->cdf[mid] > mass)
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            int fell_off = 0;
-            uint64_t r = lo;
-            if (r > s) {
-                r = s;
-                fell_off = 1;
-            }
-            uint64_t slot = order[r - 1];
-            idx[j] = (int64_t)slot;
-            if (w) /* R11: (n P(r))^-beta / max_w = (r / n)^(alpha beta) */
-                w[j] = (float)pow((double)r / (double)s, o->alpha * (double)beta);
-            double below = mass - o->cdf[r - 1];
-            if (near) {
-                double tol = 1e-6 * T;
-                near[j] = (uint8_t)(fell_off || below < tol || (o->cdf[r] - mass) < tol);
-            }
-            if (rem)
-                rem[j] = below;
-            if (mass_out)
-                mass_out[j] = mass;
-            if (o->with_ring)
-                gather_row(o, j, slot, out_states, out_next, out_actions, out_rewards,
-                           out_dones);
-        }
-        free(order);
     }
+    /* counter tags: 0 proportional and flat (the same draws), 1 rank, 2 uniform */
+    uint32_t tag = o->mode == ORC_RANK ? 1u : (o->mode == ORC_UNIFORM ? 2u : 0u);
+    double seg = c.T / (double)B;
+    for (uint32_t j = 0; j < B; ++j) {
+        double u = orc_uniform53(o->seed, j, call, tag);
+        double mass = ((double)j + u) * seg; /* R5 */
+        uint64_t r = 0;
+        double left = 0.0;
+        int nb = 0;
+        uint64_t slot = locate(o, &c, mass, &r, &left, &nb);
+        idx[j] = (int64_t)slot;
+        if (w) {
+            if (o->mode == ORC_RANK) /* R11: (n P(r))^-beta / max_w = (r / n)^(alpha beta) */
+                w[j] = (float)pow((double)r / (double)o->size, o->alpha * (double)beta);
+            else if (o->mode == ORC_UNIFORM)
+                w[j] = 1.0f;
+            else /* R8 */
+                w[j] = (float)pow((double)o->L[slot] / (double)pmin, -(double)beta);
+        }
+        if (near)
+            near[j] = (uint8_t)nb;
+        if (rem)
+            rem[j] = left;
+        if (mass_out)
+            mass_out[j] = mass;
+        if (o->with_ring)
+            gather_row(o, j, slot, out_states, out_next, out_actions, out_rewards, out_dones);
+    }
+    locate_end(&c);
     o->calls = call + 1;
     return ORC_OK;
 }

@@ -52,6 +52,11 @@ int orc_sample(orc_per *o, uint32_t B, float beta, int64_t *idx, float *w, float
                float *out_next, uint32_t *out_actions, float *out_rewards, uint8_t *out_dones,
                uint8_t *near, double *rem, double *mass);
 
+/* Where one mass lands, by the same step orc_sample takes for each draw (every mode): *slot
+ * the chosen slot (after clamping), *rem the mass above the start of its extent, *near the
+ * near-boundary flag.  rem and near may be NULL.  ORC_EEMPTY when no slot is filled. */
+int orc_locate(const orc_per *o, double mass, int64_t *slot, double *rem, uint8_t *near);
+
 /* Scatter new priorities from TD errors.  Returns the number of skipped entries (index outside
  * the filled slots) or a negative error. */
 int orc_update(orc_per *o, uint32_t B, const int64_t *idx, const float *td);

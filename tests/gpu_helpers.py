@@ -5,6 +5,8 @@ updates.  Nothing the CUDA path returns is ever fed to the oracle.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -19,6 +21,31 @@ def dev(a):
     if a.dtype == np.uint32:
         a = a.view(np.int32)
     return torch.from_numpy(a).cuda()
+
+
+# Boundary-draw counts of every sampled batch compared in this process, by configuration: the
+# parity bar counts index mismatches (each must be a draw the oracle flags as near a boundary)
+# and near-boundary draws, and reports both; tests/conftest.py prints them at the end of the run.
+BOUNDARY_COUNTS: dict = {}
+
+_FULL_SIZE = {"test_tiny_workload_rounds": "tiny (2^10, B=32)",
+              "test_apex_full_size_rounds": "apex (2^21, B=512)",
+              "test_dqn_full_size_steps": "dqn (2^20, B=1024)",
+              "test_stress_full_size_sampled": "stress (2^24, B=8192)",
+              "test_rank_full_size_steps": "rank (2^20, B=1024)",
+              "test_flat_apex_size_rounds": "flat (2^21, B=512)"}
+_MODE_NAMES = {0: "proportional", 1: "rank", 2: "uniform", 3: "flat"}
+
+
+def _config_label(mode: int) -> str:
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0].split("::")[-1].split("[")[0]
+    return _FULL_SIZE.get(test, f"{_MODE_NAMES.get(mode, mode)}, other cases")
+
+
+def record_boundary(mode: int, r: dict):
+    c = BOUNDARY_COUNTS.setdefault(_config_label(mode), {"draws": 0, "mismatch": 0, "near": 0})
+    for k in c:
+        c[k] += int(r[k])
 
 
 class Pair:
@@ -49,6 +76,7 @@ class Pair:
         want = self.orc.sample(B, beta, gather=check_rows)
         gi = got["idx"].cpu().numpy()
         r = harness.assert_indices(gi, want["idx"], want["near"])
+        record_boundary(self.mode, r)
         for k in ("draws", "mismatch", "near"):
             self.stats[k] += r[k]
         same = gi == want["idx"]
