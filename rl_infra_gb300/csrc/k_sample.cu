@@ -425,29 +425,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
 // Draws (warps) per CTA of the samplers, measured on GB300 (steps/s of each workload's step):
 // 2 for batches of at most 512 or at least 4096 draws (the apex step 35.7K against 34.8K with 8;
 // the stress step 20.9K against 20.1K), 8 in between (the dqn step 42.3K against 40.0K with 2
-// or 4; the rank step 25.8K against 24.8K).  GBPER_SAMPLE_WARPS overrides it.
-// CTAs per SM the samplers' grids stop at (larger batches loop over their draws):
-// GBPER_SAMPLE_CTAS_PER_SM, default 16.
-unsigned long long sampler_ctas_per_sm()
-{
-    static const unsigned long long v = [] {
-        const char *e = std::getenv("GBPER_SAMPLE_CTAS_PER_SM");
-        const int x = e ? std::atoi(e) : 16;
-        return (unsigned long long)(x < 1 ? 1 : (x > 32 ? 32 : x));
-    }();
-    return v;
-}
+// or 4; the rank step 25.8K against 24.8K).
+// CTAs per SM the samplers' grids stop at (larger batches loop over their draws): 16 (24 or 32
+// slowed the stress sample from 26.6 to 28.6-32.6 us).
+unsigned long long sampler_ctas_per_sm() { return 16; }
 
-int warps_per_cta(unsigned B)
-{
-    static const int forced = [] {
-        const char *e = std::getenv("GBPER_SAMPLE_WARPS");
-        return e ? std::atoi(e) : 0;
-    }();
-    int w = forced > 0 ? forced : ((B <= 512 || B >= 4096) ? 2 : 8);
-    if (w > kThreads / 32) w = kThreads / 32;
-    return w;
-}
+int warps_per_cta(unsigned B) { return (B <= 512 || B >= 4096) ? 2 : 8; }
 
 bool rows_vec4(const RingRefs &r, const SampleOut &o)
 {

@@ -1173,9 +1173,6 @@ __global__ void k_upd_finish(Ctl *c, double alpha)
 // batch in position order 32 entries at a time (later chunks overwrite earlier ones, so the
 // last writer wins) and then rebuilds its whole subtree.
 // ------------------------------------------------------------------------------------------
-#ifndef GBPER_UPD_WINDOW
-#define GBPER_UPD_WINDOW 8
-#endif
 // Two CTA shapes: 4 warps with lists of 512 entries (batches below 4096 entries), or 16 warps
 // with lists of 128 (larger batches: a quarter as many CTAs read the whole batch, each in one
 // round).  Both take the same shared memory.
@@ -1184,7 +1181,7 @@ constexpr int kUpdMaxThreads = 32 * kUpdMaxWarps;
 constexpr int kUpdSmallWarps = 4, kUpdSmallCap = 512;
 constexpr int kUpdLargeWarps = 16, kUpdLargeCap = 128;
 constexpr unsigned kUpdLargeBatch = 4096;
-constexpr int kUpdWindow = GBPER_UPD_WINDOW; // tree levels whose clean siblings load in one round
+constexpr int kUpdWindow = 8;  // tree levels whose clean siblings load in one round
 
 struct UpdArgs {
     TreeRefs t;
@@ -1857,38 +1854,17 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     }
 }
 
-// Subtrees per CTA of the update kernel, at most its warps: fewer per CTA spreads the climbs
-// over more SMs (GBPER_UPD_SUBS; default: one per warp).
-int update_subtrees_per_cta(int warps)
-{
-    static const int v = [] {
-        int s = 0;
-        if (const char *e = std::getenv("GBPER_UPD_SUBS")) s = std::atoi(e);
-        return s;
-    }();
-    return v < 1 ? warps : (v > warps ? warps : v);
-}
+// Subtrees per CTA of the update kernel: one per warp (measured on GB300 against 2 or 1 per
+// CTA, which spread the climbs over more SMs: 36.8K and 36.0K against 37.0K apex steps/s).
+int update_subtrees_per_cta(int warps) { return warps; }
 
-// Small update grids (at most 16 CTAs) run as one cluster (GBPER_UPD_CLUSTER=0 turns it off).
-bool update_cluster_enabled()
-{
-    static const bool on = [] {
-        const char *e = std::getenv("GBPER_UPD_CLUSTER");
-        return !(e && e[0] == '0');
-    }();
-    return on;
-}
+// Small update grids (at most 16 CTAs) run as one cluster (measured on GB300: the apex step
+// 34.3K against 33.9K steps/s with the arrival ticket).
+bool update_cluster_enabled() { return true; }
 
-// Target batch entries per subtree of the update kernel (GBPER_UPD_PER, 1..64; default 8).
-int update_entries_per_subtree()
-{
-    static const int v = [] {
-        int s = 8;
-        if (const char *e = std::getenv("GBPER_UPD_PER")) s = std::atoi(e);
-        return s < 1 ? 1 : (s > 64 ? 64 : s);
-    }();
-    return v;
-}
+// Target batch entries per subtree of the update kernel: 8 (measured on GB300 against 4 and 2:
+// 37.0K against 36.3K and 35.6K apex steps/s).
+int update_entries_per_subtree() { return 8; }
 
 int ilog2_ceil(unsigned long long v)
 {
@@ -1996,12 +1972,8 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
 
     // rows: about `per` elements of each array per copy thread, at most 4 CTAs per SM.  8 (16
     // float4 loads in flight per thread) measured best on GB300 for the apex step: 36.7K steps/s
-    // against 35.7K with 2 (128 copy CTAs) and 35.4K with 16.  GBPER_ADD_COPY_PER overrides it.
-    static const unsigned long long per = [] {
-        const char *e = std::getenv("GBPER_ADD_COPY_PER");
-        const int v = e ? std::atoi(e) : 8;
-        return (unsigned long long)(v < 1 ? 1 : (v > 16 ? 16 : v));
-    }();
+    // against 35.7K with 2 (128 copy CTAs) and 35.4K with 16.
+    constexpr unsigned long long per = 8;
     const unsigned long long elems = a.vec4 ? cnt * (r.d / 4) : cnt * (unsigned long long)std::max(r.d, 1u);
     unsigned ncopy = (unsigned)std::min<unsigned long long>((elems + per * kThreads - 1) / (per * kThreads),
                                                             (unsigned long long)num_sms * 4);

@@ -287,8 +287,8 @@ unsigned long long rank_tile_count(unsigned long long capacity);
 // Every hot kernel is launched with programmatic stream serialization: its CTAs may be scheduled
 // while the previous kernel in the stream is still finishing, and they wait in pdl_wait() --
 // before reading any state a predecessor may write -- until that kernel has completed and its
-// memory is visible.  pdl_release() lets the next kernel begin launching early.  Launched
-// without the attribute (GBPER_PDL=0), both are no-ops.
+// memory is visible.  pdl_release() lets the next kernel begin launching early.  In a kernel
+// launched without the attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
