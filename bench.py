@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "PER steps/s at 2^21 leaves, B=512 (sample+IS+gather+update); HBM GB/s"
 UNIT = "steps/s"
 WORKLOAD = "apex"
+APEX_WORKLOAD = "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step, alpha 0.6, beta 0.4"
 
 
 def load_peaks():
@@ -464,8 +465,7 @@ def run_gpu(args, rank, world):
         "steps": K, "warmup": W, "ms_per_step": round(cont_s * 1e3 / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; rows N(0,1) drawn on the device, lognormal(0,1) priorities)",
-        "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step, "
-                               "alpha 0.6, beta 0.4",
+        "config": {"workload": APEX_WORKLOAD,
                    "l2": ("value: not flushed, inputs larger than L2 (1 GiB ring + 48 MiB trees + "
                           "32 MiB staging vs 129 MB L2; each step ingests new rows and gathers random "
                           "ones); per_step_l2_flushed: 512 MiB write + 256 MiB read between steps"),
@@ -493,6 +493,40 @@ def run_gpu(args, rank, world):
         res["clocks"] = clk
     if graph_res:
         res["graph"] = graph_res
+
+    # steady state: right after the prefill every new row enters at the running maximum, so the
+    # draws crowd the last rows written until the ring has turned over once (2^21 / 4096 = 512
+    # steps); the same step timed back to back once that pass is complete
+    done = int(buf.read_state(capi.PER_STATE_COUNTERS, 0, 1)[0])    # sample calls = steps so far
+    ring_pass = w.capacity // I
+    t_next = W + K + Kop + K
+    for t in range(max(0, ring_pass + 64 - done)):
+        _check(L, h, L.per_add(*add_args[(t_next + t) % n_ofs]), "per_add")
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * ((t_next + t) % TD_SLOTS), st),
+               "per_update")
+    torch.cuda.synchronize()
+    after = int(buf.read_state(capi.PER_STATE_COUNTERS, 0, 1)[0])
+    Ks = max(K, 2000)
+    sa, sb = cr.events(2)
+    rec(sa, st)
+    for t in range(Ks):
+        _check(L, h, L.per_add(*add_args[(t_next + t) % n_ofs]), "per_add")
+        _check(L, h, L.per_sample(*sample_args), "per_sample")
+        _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * ((t_next + t) % TD_SLOTS), st),
+               "per_update")
+    rec(sb, st)
+    torch.cuda.synchronize()
+    ss_s = max_over_ranks(cr.elapsed_ms(sa, sb) / 1e3, dist)
+    cr.destroy([sa, sb])
+    if buf.status_device() != 0:
+        raise RuntimeError("device error flag raised during the steady-state steps")
+    res["steady_state"] = {"value": round(aggregate_throughput(world, Ks, ss_s), 2), "unit": UNIT,
+                           "ms_per_step": round(ss_s * 1e3 / Ks, 5), "steps": Ks, "after_steps": after,
+                           "note": ("the same step, back to back between two events, once the ring has "
+                                    "turned over (every slot rewritten since the prefill); `value` times "
+                                    "the K steps right after the warm-up, while new rows entered at the "
+                                    "running maximum still crowd the draws")}
     res["e2e"] = run_e2e(torch, buf, w, staging, g, min(K, 4000), dist)
     buf.close()
     if dist:
@@ -726,11 +760,12 @@ OTHER = {
 }
 
 
-def run_other(args, name, resort=False):
+def run_other(args, name, resort=False, steps=None, warmup=None, op_steps=None):
     """Steps/s of one sample (+IS +gather) and one update per step on another workload; the rank
     workload's sample call brings the slot order up to date (merging the slots written since
     the previous sample, or with `resort` sorting every slot again).  Same timing rules as the
-    apex step."""
+    apex step: `steps` steps (default --steps) after `warmup` untimed ones, two events around
+    each step and L2 flushed between steps; per-call medians from `op_steps` further steps."""
     import ctypes
     import torch
     from rl_infra_gb300 import capi
@@ -749,7 +784,9 @@ def run_other(args, name, resort=False):
         del sd, nd
     torch.cuda.synchronize()
     L, h = capi.load(), buf._h
-    K, W, B = args.steps, args.warmup, w.batch
+    K = args.steps if steps is None else steps
+    W = args.warmup if warmup is None else warmup
+    B = w.batch
     out = buf.alloc_batch(B)
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     # update batches: the sampled indices, or (stress) a copy with 25% duplicated positions
@@ -797,7 +834,7 @@ def run_other(args, name, resort=False):
     wall = time.perf_counter() - t0
     step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
     cr.destroy(sev)
-    Kop = min(K, 1000)
+    Kop = min(K, 1000) if op_steps is None else op_steps
     fl = cr.events(3 * Kop)
     for t in range(Kop):
         step(W + K + t, fl[3 * t: 3 * t + 3])
@@ -859,6 +896,26 @@ def run_other(args, name, resort=False):
                                        else "previous order merged with the slots written since")
     buf.close()
     return res
+
+
+def run_workloads(args):
+    """The larger configurations beside the headline (one GPU): dqn, stress and rank (the order
+    kept between samples, and sorted again at each sample), each timed like run_other: the
+    driver's --steps steps after --warmup, L2 flushed between steps, per-call medians from at
+    least 200 further steps.  Each buffer is freed before the next is made (stress holds 32 GiB)."""
+    import torch
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "step_us_median", "ops_median_us",
+            "bytes_per_step", "hbm_gbs_algorithmic", "roofline", "gpu_launches", "config")
+    out = {}
+    for name in ("dqn", "stress", "rank"):
+        r = run_other(args, name, op_steps=max(args.steps, 200))
+        rec = {k: r[k] for k in keep if k in r}
+        if name == "rank":
+            full = run_other(args, "rank", resort=True, op_steps=max(args.steps, 200))
+            rec["full_resort"] = {k: full[k] for k in keep if k in full}
+        out[name] = rec
+        torch.cuda.empty_cache()
+    return out
 
 
 # -- the update's two paths against the batch size ------------------------------------------------
@@ -946,26 +1003,31 @@ def run_update_crossover(args):
 
 def oracle_steps_per_s(budget_s=12.0, max_steps=None, warmup=0):
     """The oracle's apex steps per second on one host core: `warmup` untimed steps after the
-    prefill, then steps timed until `max_steps` or `budget_s` seconds, whichever comes first."""
+    prefill, then steps timed until `max_steps` or `budget_s` seconds, whichever comes first.
+    The prefill priorities and the TD errors come from the same seeded stream, in the same
+    order, as the GPU arm's (setup_gpu, run_gpu), so both arms run the same step on the same
+    priorities; the rows (which the step only copies) come from a host stream of their own."""
     import oracle
     from rl_infra_gb300 import workloads as wl
     w = wl.WORKLOADS[WORKLOAD]
-    g = wl.rng(0, 99)
+    g = wl.rng(0, 77)          # priorities, then TD errors: the GPU arm's stream
+    rows_g = wl.rng(0, 99)
     o = oracle.Oracle(w.capacity, w.state_dim, w.row_stride, w.alpha, w.eps, w.mode, 0, True)
     chunk = 1 << 18
     for _ in range(w.capacity // chunk):
-        rows = wl.transitions(g, chunk, w)
+        rows = wl.transitions(rows_g, chunk, w)
         o.add(rows["states"], rows["next_states"], rows["actions"], rows["rewards"],
               rows["dones"], wl.raw_priorities(g, chunk, w.prio))
-    staging = wl.transitions(g, w.staging, w)
-    td = wl.td_errors(g, 64 * w.batch).reshape(64, w.batch)
+    staging = wl.transitions(rows_g, w.staging, w)
+    TD_SLOTS = 4096
+    td = wl.td_errors(g, TD_SLOTS * w.batch).reshape(TD_SLOTS, w.batch)
 
     def one(t):
         lo = (t * w.ingest) % w.staging
         o.add(*(staging[k][lo:lo + w.ingest] for k in
                 ("states", "next_states", "actions", "rewards", "dones")), None)
         s = o.sample(w.batch, w.beta)
-        o.update(s["idx"], td[t % 64])
+        o.update(s["idx"], td[t % TD_SLOTS])
 
     for t in range(warmup):
         one(t)
@@ -1009,6 +1071,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-flat", action="store_true",
                     help="skip timing the apex step with the flat cumulative-array sampler")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the dqn, stress and rank records of the default run")
     ap.add_argument("--update-crossover", action="store_true",
                     help="time both update paths against the batch size and exit")
     ap.add_argument("--crossover-trees", default="",
@@ -1030,7 +1094,7 @@ def main():
                "steps": n, "warmup": args.warmup, "ms_per_step": round(1e3 / sps, 4),
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                "data": "synthetic (seeded)", "impl": "reference",
-               "config": {"workload": "apex: 2^21 leaves, state_dim 64, B=512, ingest 4096/step"},
+               "config": {"workload": APEX_WORKLOAD},
                "cpu_baseline": {"value": round(sps, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{n} apex steps in {el:.1f} s" + (
                                     f" (of {args.steps}: the {budget:.0f} s budget ran out)"
@@ -1057,6 +1121,8 @@ def main():
     res = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_flat:
         res["flat_design"] = run_flat_design(args)
+    if rank == 0 and world == 1 and not args.no_workloads:
+        res["workloads"] = run_workloads(args)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             sps, n, el = oracle_steps_per_s(budget_s=args.cpu_budget)
