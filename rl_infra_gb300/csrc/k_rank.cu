@@ -28,8 +28,6 @@ constexpr int kGroup = 16;                        // tiles per look-back group
 constexpr int kMaxGroups = 16;                    // group totals read per round
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ unsigned key_of_raw(float raw) { return ~__float_as_uint(raw); }
-
 // All four digit histograms at once: they depend on the key set, not on its order.  Every lane
 // counts into its own copy of the 4 x 256 bins, laid out with a stride of 257 words, so lanes
 // that meet the same digit (the high digits of floats of similar magnitude) hit distinct banks.
@@ -41,7 +39,7 @@ constexpr size_t kHistSmem = 4ull * kHistCopy * sizeof(unsigned);   // 131,584 b
 
 __global__ void __launch_bounds__(kHistThreads) k_rs_hist4(const float *raw, unsigned long long size,
                                                             unsigned *digit_hist, unsigned *sort_ctl,
-                                                            unsigned *order_cur)
+                                                            unsigned *mctl)
 {
     extern __shared__ unsigned s_h[];   // [4 digits][32 lanes][257]
     for (int i = threadIdx.x; i < 4 * kHistCopy; i += blockDim.x) s_h[i] = 0;
@@ -49,7 +47,14 @@ __global__ void __launch_bounds__(kHistThreads) k_rs_hist4(const float *raw, uns
     pdl_release();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         atomicAdd(&sort_ctl[4], 1u);
-        if (order_cur) *order_cur = 1u;   // the four passes leave the order in keys[1] / vals[1]
+        if (mctl) {
+            // a buffer's order: the four passes leave it in keys[1] / vals[1] (mctl[4]); every
+            // mark is void once every slot is sorted, so a new mark epoch opens (mctl[1]) with an
+            // empty list (mctl[3])
+            mctl[4] = 1u;
+            mctl[1] += 1u;
+            mctl[3] = 0u;
+        }
     }
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -62,7 +67,7 @@ __global__ void __launch_bounds__(kHistThreads) k_rs_hist4(const float *raw, uns
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const unsigned long long p = p0 + u * stride;
-            k[u] = p < size ? key_of_raw(__ldg(raw + p)) : 0u;
+            k[u] = p < size ? order_key(__ldg(raw + p)) : 0u;
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) k_rs_onesweep(const float *raw, cons
 #pragma unroll
         for (int i = 0; i < kItems; ++i) {
             const bool ok = i * 32 + lane < wvalid;
-            k[i] = ok ? (rp ? key_of_raw(__ldg(rp + i * 32)) : __ldg(kp + i * 32)) : 0u;
+            k[i] = ok ? (rp ? order_key(__ldg(rp + i * 32)) : __ldg(kp + i * 32)) : 0u;
             v[i] = ok ? (rp ? (unsigned)(w0 + i * 32) : __ldg(vp + i * 32)) : 0u;
         }
     }
@@ -380,33 +385,62 @@ __global__ void __launch_bounds__(1024) k_build_cdf(double *cdf, unsigned long l
     }
 }
 
+// guide[k] = the first r in [1, C] with cdf[r] > fl(k * delta) (C + 1 if none), k = 0 .. K, and
+// guide[K + 1] = C + 1.  The sampler forms fl(k * delta) with the same binary64 product.
+__global__ void k_build_guide(const double *cdf, unsigned long long C, unsigned *guide, unsigned K, double delta)
+{
+    for (unsigned long long k = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; k <= (unsigned long long)K + 1;
+         k += (unsigned long long)gridDim.x * blockDim.x) {
+        if (k == (unsigned long long)K + 1) {
+            guide[k] = (unsigned)(C + 1);
+            continue;
+        }
+        const double thr = __dmul_rn((double)k, delta);
+        unsigned long long lo = 1, hi = C + 1;
+        while (lo < hi) {
+            const unsigned long long mid = lo + (hi - lo) / 2;
+            if (cdf[mid] > thr) hi = mid;
+            else lo = mid + 1;
+        }
+        guide[k] = (unsigned)lo;
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // Incremental order: between two samples only the slots that update and insertion wrote have a
-// new priority (they are marked, each listed once).  The new order is the previous order without
-// those slots, merged with them at their current priority -- the same sequence a full sort gives,
-// since the order is a total order on (key, slot).  One kernel, one 7168-entry tile of the
-// previous order per CTA:
-//   1. the CTA reads every marked entry (key, slot): it counts those at or below the previous
-//      tile's last entry (c0), keeps those up to its own last entry (its own marked entries,
-//      sorted in shared memory), and puts every marked slot in a shared-memory hash set;
-//   2. it drops its tile's marked slots (kept order unchanged) and publishes the kept count;
-//      the kept count of the earlier tiles comes from their published words (look-back, each
-//      wait bounded);
-//   3. a kept entry goes to (kept before it) + c0 + (own marked entries smaller than it);
-//   4. own marked entry j goes to c0 + j + (kept before the tile) + (tile's kept entries smaller);
-//   5. the last CTA to finish clears the marks.
+// new priority; each is listed once, with the key it held in the order.  The new order is the
+// previous order without those slots' old entries, merged with their new entries -- the same
+// sequence a full sort gives, since the order is a total order on (key, slot).  One kernel, one
+// 8192-entry tile of the previous order per CTA, no CTA waiting for another.  Every listed slot
+// gives an old entry (old key, slot), which is an entry of the previous order, and a new entry
+// (current key, slot).  With `lo` the previous tile's last entry and `x_last` this tile's:
+//   1. the CTA stages its tile in shared memory (asynchronous 16-byte copies); it reads the listed slots: c_old = old entries at or below lo, c_new = new
+//      entries at or below lo, the dropped entries (old entries in (lo, x_last]: they are in this
+//      tile) and the own new entries (in (lo, x_last], or above lo for the last tile);
+//   2. each dropped entry is located in the tile by binary search and marked in a bitmap of the
+//      tile's 8192 entries (with per-word prefix counts, the dropped entries below any index are
+//      one lookup away: they need no sort, which matters because the top ranks, where the draws
+//      concentrate, collect most of them); the own new entries (few, spread like the order) are
+//      located as they are found (i tile entries lie below an own entry) and sorted with that
+//      count;
+//   3. the tile's output starts at base = t0 - c_old + c_new (t0 entries of the previous order
+//      lie at or below lo, c_old of them dropped, and c_new new entries precede the tile).  Tile
+//      entry e, unless dropped, goes to e - (dropped below e) + (own with i <= e); own entry j
+//      goes to i_j - (dropped below i_j) + j.  The stores are coalesced between those few
+//      break points;
+//   4. the last CTA to finish opens a new mark epoch (which unmarks every slot) and flips the
+//      buffer pair.
 // ------------------------------------------------------------------------------------------
-constexpr int kMThreads = 1024;
-constexpr int kMItems = 7;
-constexpr int kMTile = kMThreads * kMItems;   // 7168
-constexpr unsigned kMHash = 2 * kMaxDirty;     // hash slots (at least twice the marks)
-constexpr unsigned kMFilter = 1u << 16;        // filter bits: slot mod 2^16 of every marked slot
-constexpr unsigned kEmptySlot = 0xffffffffu;
-constexpr size_t kMergeSmem = (size_t)kMTile * sizeof(unsigned long long)     // kept entries
-                              + (size_t)kMTile * 2 * sizeof(unsigned)           // the tile
-                              + (size_t)kMaxDirty * sizeof(unsigned long long)  // own marked entries
-                              + (size_t)kMHash * sizeof(unsigned)               // marked slots
-                              + (size_t)(kMFilter / 32) * sizeof(unsigned);     // their filter
+constexpr int kMThreads = 512;                               // 16 warps: registers enough for no spills
+constexpr int kMItems = 16;
+constexpr int kMTile = kMThreads * kMItems;                  // 8192
+constexpr int kMPre = 2;   // listed slots per thread loaded with the tile (more are read after)
+constexpr int kMWords = kMTile / 32;                         // words of the tile's dropped bitmap
+static_assert(kMTile % 4 == 0, "the tile's slot array must start 16 bytes after a multiple");
+constexpr size_t kMergeSmem = (size_t)kMTile * 2 * sizeof(unsigned)             // the tile: keys, slots
+                              + (size_t)kMaxDirty * sizeof(unsigned long long)  // own new entries
+                              + (size_t)kMaxDirty * sizeof(unsigned)            // their places in the tile
+                              + (size_t)2 * (kMWords + 1) * sizeof(unsigned);   // dropped bitmap, prefix counts
 
 __device__ __forceinline__ unsigned long long pack_key_slot(unsigned key, unsigned slot)
 {
@@ -414,7 +448,8 @@ __device__ __forceinline__ unsigned long long pack_key_slot(unsigned key, unsign
 }
 
 // entries of a[0, n) (ascending) that are < x
-__device__ __forceinline__ unsigned count_below(const unsigned long long *a, unsigned n, unsigned long long x)
+template <typename T>
+__device__ __forceinline__ unsigned count_below(const T *a, unsigned n, T x)
 {
     unsigned lo = 0, hi = n;
     while (lo < hi) {
@@ -425,205 +460,254 @@ __device__ __forceinline__ unsigned count_below(const unsigned long long *a, uns
     return lo;
 }
 
-__device__ __forceinline__ unsigned slot_hash(unsigned s, unsigned mask) { return (s * 2654435761u) & mask; }
+// entries of the staged tile (keys tk[], slots tv[], ascending as pairs) that are < x
+__device__ __forceinline__ unsigned tile_below(const unsigned *tk, const unsigned *tv, unsigned n,
+                                               unsigned long long x)
+{
+    unsigned lo = 0, hi = n;
+    while (lo < hi) {
+        const unsigned mid = (lo + hi) >> 1;
+        if (pack_key_slot(tk[mid], tv[mid]) < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// 16 bytes global -> shared without passing through registers (L2 only)
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// entries of a[0, n) (ascending) that are <= x
+__device__ __forceinline__ unsigned count_at_most(const unsigned *a, unsigned n, unsigned x)
+{
+    unsigned lo = 0, hi = n;
+    while (lo < hi) {
+        const unsigned mid = (lo + hi) >> 1;
+        if (a[mid] <= x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Sorts a[0, n) ascending, carrying p[0, n) along, n <= kMaxDirty: one warp's shuffles up to 32
+// entries (warp `w` of the CTA), else the CTA (every thread must call it with the same n).
+__device__ __forceinline__ void sort_small(unsigned long long *a, unsigned *p, unsigned n, int w)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (n <= 32) {
+        if (warp == w) {
+            unsigned long long x = (unsigned)lane < n ? a[lane] : ~0ull;
+            unsigned px = (unsigned)lane < n ? p[lane] : 0u;
+            for (unsigned kk = 2; kk <= 32; kk <<= 1)
+                for (unsigned j = kk >> 1; j > 0; j >>= 1) {
+                    const unsigned long long y = __shfl_xor_sync(kFull, x, j);
+                    const unsigned py = __shfl_xor_sync(kFull, px, j);
+                    const bool lower = (lane & j) == 0, up = (lane & kk) == 0;
+                    if (lower == up ? y < x : y > x) {
+                        x = y;
+                        px = py;
+                    }
+                }
+            if ((unsigned)lane < n) {
+                a[lane] = x;
+                p[lane] = px;
+            }
+        }
+        return;
+    }
+    unsigned m2 = 64;
+    while (m2 < n) m2 <<= 1;
+    for (unsigned i = n + tid; i < m2; i += blockDim.x) a[i] = ~0ull;
+    __syncthreads();
+    for (unsigned kk = 2; kk <= m2; kk <<= 1)
+        for (unsigned j = kk >> 1; j > 0; j >>= 1) {
+            for (unsigned i = tid; i < m2; i += blockDim.x) {
+                const unsigned l = i ^ j;
+                if (l > i) {
+                    const unsigned long long x = a[i], y = a[l];
+                    if ((i & kk) == 0 ? x > y : x < y) {
+                        a[i] = y;
+                        a[l] = x;
+                        const unsigned t = p[i];
+                        p[i] = p[l];
+                        p[l] = t;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+}
 
 __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsigned *keys0, unsigned *keys1,
                                                            unsigned *vals0, unsigned *vals1, unsigned long long n_old,
-                                                           unsigned ntiles, DirtyRefs dirty, unsigned *mctl,
-                                                           unsigned long long *mstatus, unsigned *err)
+                                                           DirtyRefs dirty, unsigned *mctl, unsigned *err)
 {
-    extern __shared__ unsigned long long s_m[];
-    unsigned long long *tk = s_m;                     // [kMTile] kept entries
-    unsigned long long *own = s_m + kMTile;           // [kMaxDirty] own marked entries, ascending
-    unsigned *s_tkey = reinterpret_cast<unsigned *>(own + kMaxDirty), *s_tval = s_tkey + kMTile;  // the tile
-    unsigned *hset = s_tval + kMTile;                 // [kMHash] marked slots
-    unsigned *filt = hset + kMHash;                   // [kMFilter / 32] bit (slot mod 2^16) of each
-    __shared__ unsigned s_tile, s_epoch, s_cnt, s_last, s_nown, s_cur;
-    __shared__ unsigned s_wsum[kMThreads / 32];
-    __shared__ unsigned long long s_wpart[kMThreads / 32];
+    extern __shared__ __align__(16) unsigned long long s_m[];
+    // the tile first: the asynchronous copies write it 16 bytes at a time, at 16-byte offsets
+    unsigned *tk = reinterpret_cast<unsigned *>(s_m), *tv = tk + kMTile;   // [kMTile] each: the tile
+    unsigned long long *nl = reinterpret_cast<unsigned long long *>(tv + kMTile);   // [kMaxDirty] own new entries
+    unsigned *nins = reinterpret_cast<unsigned *>(nl + kMaxDirty);   // [kMaxDirty] tile entries below each
+    unsigned *dbits = nins + kMaxDirty;                   // [kMWords + 1] dropped tile entries
+    unsigned *dpre = dbits + kMWords + 1;                 // [kMWords + 1] dropped entries in earlier words
+    __shared__ unsigned s_nn;
+    __shared__ unsigned s_wo[kMThreads / 32], s_wn[kMThreads / 32], s_wd[kMWords / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_nn = 0;
+    for (int i = tid; i <= kMWords; i += kMThreads) dbits[i] = 0u;
     pdl_wait();
     pdl_release();
-    if (tid == 0) {
-        s_epoch = *(volatile unsigned *)&mctl[1];
-        s_cnt = *(volatile unsigned *)dirty.count;
-        s_cur = *(volatile unsigned *)&mctl[4] & 1u;   // which buffer pair holds the order
-        s_tile = atomicAdd(&mctl[0], 1u);
-        s_nown = 0;
-    }
-    __syncthreads();
-    const unsigned tile = s_tile, epoch = s_epoch, cnt = s_cnt;
-    const unsigned *keys_in = s_cur ? keys1 : keys0, *vals_in = s_cur ? vals1 : vals0;
-    unsigned *keys_out = s_cur ? keys0 : keys1, *vals_out = s_cur ? vals0 : vals1;
-    const bool over = cnt > kMaxDirty;   // more marks than listed: the order cannot be merged
-    const unsigned d = over ? 0u : cnt;
+    const unsigned tile = blockIdx.x;
+    const unsigned cnt = *(volatile unsigned *)dirty.count;       // nothing writes these during the
+    const unsigned cur = *(volatile unsigned *)&mctl[4] & 1u;     // merge: the same for every thread
+    const unsigned *keys_in = cur ? keys1 : keys0, *vals_in = cur ? vals1 : vals0;
+    unsigned *keys_out = cur ? keys0 : keys1, *vals_out = cur ? vals0 : vals1;
+    const bool over = cnt > kMaxDirty;   // more slots than listed: the order cannot be merged
     if (!over) {
-        unsigned hmask = 63;
-        while (hmask + 1 < 2 * d) hmask = 2 * hmask + 1;
-        for (unsigned i = tid; i <= hmask; i += kMThreads) hset[i] = kEmptySlot;
-        for (unsigned i = tid; i < kMFilter / 32; i += kMThreads) filt[i] = 0u;
-        // the tile of the previous order, coalesced
         const unsigned long long t0 = (unsigned long long)tile * kMTile;
         const int nt = (int)(n_old - t0 < (unsigned long long)kMTile ? n_old - t0 : (unsigned long long)kMTile);
-        for (int e = tid; e < nt; e += kMThreads) {
-            s_tkey[e] = keys_in[t0 + e];
-            s_tval[e] = vals_in[t0 + e];
-        }
-        const bool first = tile == 0, lastt = tile + 1 == ntiles;
-        const unsigned long long lo = first ? 0ull : pack_key_slot(keys_in[t0 - 1], vals_in[t0 - 1]);
-        __syncthreads();   // staged tile, cleared hash set and filter
-        const unsigned long long hi = lastt ? ~0ull : pack_key_slot(s_tkey[nt - 1], s_tval[nt - 1]);
-        // 1. the marked entries: count those at or below lo, keep those in (lo, hi], hash the slots
-        unsigned c0 = 0;
-        for (unsigned i = tid; i < d; i += kMThreads) {
-            const unsigned slot = dirty.list[i];
-            const unsigned long long x = pack_key_slot(key_of_raw(raw[slot]), slot);
-            if (!first && x <= lo) ++c0;
-            else if (lastt || x <= hi) own[atomicAdd(&s_nown, 1u)] = x;
-            atomicOr(&filt[(slot & (kMFilter - 1)) >> 5], 1u << (slot & 31));
-            unsigned h = slot_hash(slot, hmask);
-            for (unsigned probe = 0; probe <= hmask; ++probe) {
-                const unsigned prev = atomicCAS(&hset[h], kEmptySlot, slot);
-                if (prev == kEmptySlot || prev == slot) break;
-                h = (h + 1) & hmask;
-            }
-        }
-        for (int o = 16; o > 0; o >>= 1) c0 += __shfl_xor_sync(kFull, c0, o);
-        if (lane == 0) s_wsum[warp] = c0;
-        __syncthreads();
-        c0 = 0;
-        for (int w = 0; w < kMThreads / 32; ++w) c0 += s_wsum[w];
-        const unsigned nown = s_nown;
-        // sort the own marked entries (few: one warp's shuffles up to 32, else the block)
-        unsigned m2 = 1;
-        while (m2 < nown) m2 <<= 1;
-        if (m2 <= 32) {
-            if (warp == 0) {
-                unsigned long long x = (unsigned)lane < nown ? own[lane] : ~0ull;
-                for (unsigned k = 2; k <= 32; k <<= 1)
-                    for (unsigned j = k >> 1; j > 0; j >>= 1) {
-                        const unsigned long long y = __shfl_xor_sync(kFull, x, j);
-                        const bool lower = (lane & j) == 0, up = (lane & k) == 0;
-                        if (lower == up ? y < x : y > x) x = y;
-                    }
-                if ((unsigned)lane < nown) own[lane] = x;
-            }
-        } else {
-            for (unsigned i = nown + tid; i < m2; i += kMThreads) own[i] = ~0ull;
-            __syncthreads();
-            for (unsigned k = 2; k <= m2; k <<= 1)
-                for (unsigned j = k >> 1; j > 0; j >>= 1) {
-                    for (unsigned i = tid; i < m2; i += kMThreads) {
-                        const unsigned l = i ^ j;
-                        if (l > i) {
-                            const unsigned long long x = own[i], y = own[l];
-                            if ((i & k) == 0 ? x > y : x < y) {
-                                own[i] = y;
-                                own[l] = x;
-                            }
-                        }
-                    }
-                    __syncthreads();
-                }
-        }
-        __syncthreads();
-        // 2. this tile without its marked slots (thread t takes entries 7t .. 7t+6 of the staged
-        //    tile); kept count published, earlier tiles' summed
-        unsigned keep = 0;
+        const bool first = tile == 0, lastt = tile + 1 == gridDim.x;
+        // 1. the tile into shared memory (asynchronous 16-byte copies), its boundary entries and
+        //    this thread's listed slots
 #pragma unroll
-        for (int i = 0; i < kMItems; ++i) {
-            const int e = tid * kMItems + i;
-            if (e < nt) {
-                const unsigned v = s_tval[e];
-                bool marked = false;
-                if ((filt[(v & (kMFilter - 1)) >> 5] >> (v & 31)) & 1u) {   // else certainly unmarked
-                    unsigned h = slot_hash(v, hmask);
-                    for (unsigned probe = 0; probe <= hmask; ++probe) {
-                        const unsigned q = hset[h];
-                        if (q == v) {
-                            marked = true;
-                            break;
-                        }
-                        if (q == kEmptySlot) break;
-                        h = (h + 1) & hmask;
-                    }
+        for (int c = 0; c < kMItems / 4; ++c) {
+            const int e = (c * kMThreads + tid) * 4;
+            if (e + 4 <= nt) {
+                cp_async16(tk + e, keys_in + t0 + e);
+                cp_async16(tv + e, vals_in + t0 + e);
+            } else {
+                for (int i = e; i < nt; ++i) {
+                    tk[i] = __ldg(keys_in + t0 + i);
+                    tv[i] = __ldg(vals_in + t0 + i);
                 }
-                if (!marked) keep |= 1u << i;
             }
         }
-        const unsigned c = __popc(keep);
-        unsigned inc = c;
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned x = __shfl_up_sync(kFull, inc, o);
-            if (lane >= o) inc += x;
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const unsigned long long lo = first ? 0ull : pack_key_slot(__ldg(keys_in + t0 - 1), __ldg(vals_in + t0 - 1));
+        const unsigned long long x_last = pack_key_slot(__ldg(keys_in + t0 + nt - 1), __ldg(vals_in + t0 + nt - 1));
+        unsigned ls[kMPre], lk[kMPre], lr[kMPre];
+#pragma unroll
+        for (int q = 0; q < kMPre; ++q) {
+            const unsigned i = tid + q * kMThreads;
+            ls[q] = i < cnt ? dirty.list[i] : 0u;
+            lk[q] = i < cnt ? dirty.oldkey[i] : 0u;
         }
-        __syncthreads();   // every thread read c0's partials from s_wsum
-        if (lane == 31) s_wsum[warp] = inc;
-        __syncthreads();
-        unsigned before = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < kMPre; ++q) lr[q] = tid + q * kMThreads < cnt ? order_key(raw[ls[q]]) : 0u;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();   // the staged tile, s_nn, the cleared bitmap
+        // 2. the listed slots: counts at or below lo, dropped entries marked at their index,
+        //    own new entries collected
+        unsigned c_old = 0, c_new = 0;
+        for (unsigned i = tid; i < cnt; i += kMThreads) {
+            const int q = (int)(i / kMThreads);
+            unsigned slot, okey, nkey;
+            if (q < kMPre) {
+                slot = q == 0 ? ls[0] : ls[1];
+                okey = q == 0 ? lk[0] : lk[1];
+                nkey = q == 0 ? lr[0] : lr[1];
+            } else {
+                slot = dirty.list[i];
+                okey = dirty.oldkey[i];
+                nkey = order_key(raw[slot]);
+            }
+            const unsigned long long xo = pack_key_slot(okey, slot);
+            const unsigned long long xn = pack_key_slot(nkey, slot);
+            if (!first && xo <= lo) {
+                ++c_old;
+            } else if (xo <= x_last) {   // an entry of this tile
+                const unsigned d = tile_below(tk, tv, (unsigned)nt, xo);
+                atomicOr(&dbits[d >> 5], 1u << (d & 31));
+            }
+            if (!first && xn <= lo) {
+                ++c_new;
+            } else if (lastt || xn <= x_last) {   // own: with the count of tile entries below it
+                const unsigned j = atomicAdd(&s_nn, 1u);
+                nl[j] = xn;
+                nins[j] = tile_below(tk, tv, (unsigned)nt, xn);
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            c_old += __shfl_xor_sync(kFull, c_old, o);
+            c_new += __shfl_xor_sync(kFull, c_new, o);
+        }
+        if (lane == 0) {
+            s_wo[warp] = c_old;
+            s_wn[warp] = c_new;
+        }
+        __syncthreads();   // dropped bitmap, own list, partial counts
+        const unsigned nn = s_nn;
+        if (warp < kMWords / 32) {   // prefix counts of the dropped bitmap, 32 words per warp
+            const unsigned c = __popc(dbits[warp * 32 + lane]);
+            unsigned inc = c;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned x = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += x;
+            }
+            dpre[warp * 32 + lane] = inc - c;   // within the warp's 32 words, fixed up below
+            if (lane == 31) s_wd[warp] = inc;
+        }
+        c_old = 0;
+        c_new = 0;
         for (int w = 0; w < kMThreads / 32; ++w) {
-            const unsigned x = s_wsum[w];
-            if (w < warp) before += x;
-            total += x;
+            c_old += s_wo[w];
+            c_new += s_wn[w];
         }
-        unsigned r = before + inc - c;   // this thread's first kept rank in the tile
+        __syncthreads();   // the warps' bitmap totals
+        if (warp < kMWords / 32) {
+            unsigned before = 0;
+            for (int w = 0; w < warp; ++w) before += s_wd[w];
+            dpre[warp * 32 + lane] += before;
+            if (warp == kMWords / 32 - 1 && lane == 31) dpre[kMWords] = before + s_wd[warp];
+        }
+        sort_small(nl, nins, nn, kMWords / 32);   // a warp that does not build the prefix, when short
+        __syncthreads();   // dpre, own entries sorted with their places
+        // 3. the tile's output from base = t0 - c_old + c_new
+        const unsigned long long base = t0 - c_old + c_new;
+        // this thread's entries rise with q, so the own entries at or below each are counted by one
+        // pointer that only moves forward (found for the first entry by binary search)
+        unsigned sn = count_at_most(nins, nn, (unsigned)tid);
+        unsigned nxt = sn < nn ? nins[sn] : 0xffffffffu;
 #pragma unroll
-        for (int i = 0; i < kMItems; ++i)
-            if ((keep >> i) & 1u) {
-                const int e = tid * kMItems + i;
-                tk[r++] = pack_key_slot(s_tkey[e], s_tval[e]);
+        for (int q = 0; q < kMItems; ++q) {
+            const unsigned e = tid + q * kMThreads;
+            if ((int)e >= nt) break;
+            while (nxt <= e) {
+                ++sn;
+                nxt = sn < nn ? nins[sn] : 0xffffffffu;
             }
-        volatile unsigned long long *vst = mstatus;
-        const unsigned want = epoch & 0x3FFFFFFFu;
-        if (tid == 0) vst[tile] = status_word(epoch, kFlagAgg, total);
-        unsigned long long part = 0;
-        bool ok = true;
-        for (unsigned q = tid; q < tile; q += kMThreads) {
-            unsigned long long w = vst[q];
-            int it = 0;
-            while (!word_ready(w, want) && ++it < kSpinLimit) w = vst[q];
-            if (it >= kSpinLimit) ok = false;
-            part += (unsigned)w;
+            const unsigned wd = dbits[e >> 5], bit = 1u << (e & 31);
+            if (wd & bit) continue;   // dropped
+            const unsigned sd = dpre[e >> 5] + __popc(wd & (bit - 1u));
+            const unsigned long long o = base + e - sd + sn;
+            keys_out[o] = tk[e];
+            vals_out[o] = tv[e];
         }
-        if (!ok) atomicOr(err, kFlagTimeout);
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
-        if (lane == 0) s_wpart[warp] = part;
-        __syncthreads();   // tk complete, s_wpart complete
-        unsigned long long pt = 0;
-        for (int w = 0; w < kMThreads / 32; ++w) pt += s_wpart[w];
-        // 3. kept entries in rank order (consecutive ranks land on nearly consecutive positions)
-        for (unsigned rr = tid; rr < total; rr += kMThreads) {
-            const unsigned long long x = tk[rr];
-            const unsigned long long pos = pt + rr + c0 + count_below(own, nown, x);
-            keys_out[pos] = (unsigned)(x >> 32);
-            vals_out[pos] = (unsigned)x;
+        for (unsigned j = tid; j < nn; j += kMThreads) {
+            const unsigned i = nins[j];
+            const unsigned sd = dpre[i >> 5] + __popc(dbits[i >> 5] & ((1u << (i & 31)) - 1u));
+            const unsigned long long o = base + i - sd + j;
+            const unsigned long long y = nl[j];
+            keys_out[o] = (unsigned)(y >> 32);
+            vals_out[o] = (unsigned)y;
         }
-        // 4. own marked entries
-        for (unsigned j = tid; j < nown; j += kMThreads) {
-            const unsigned long long x = own[j];
-            const unsigned long long pos = c0 + j + pt + count_below(tk, total, x);
-            keys_out[pos] = (unsigned)(x >> 32);
-            vals_out[pos] = (unsigned)x;
-        }
-    } else if (tid == 0) {
+    } else if (tid == 0 && tile == 0) {
         atomicOr(err, kFlagRankStale);
     }
-    // 5. the last CTA to finish clears the marks (every mark is listed) and the counters
-    __threadfence();
+    // the last CTA to arrive (every CTA has read the control words by then) opens a new mark
+    // epoch, which unmarks every slot, empties the list and flips the buffer pair
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&mctl[2], 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (s_last) {
+    if (tid == 0) {
         __threadfence();
-        for (unsigned i = tid; i < d; i += kMThreads) dirty.bits[dirty.list[i] >> 5] = 0u;
-        if (tid == 0) {
+        if (atomicAdd(&mctl[2], 1u) == gridDim.x - 1) {
             if (!over) {
                 *dirty.count = 0u;
-                mctl[4] = s_cur ^ 1u;   // the merged order is in the other pair
+                mctl[1] += 1u;
+                mctl[4] = cur ^ 1u;   // the merged order is in the other pair
             }
-            mctl[0] = 0u;
             mctl[2] = 0u;
-            mctl[1] = epoch + 1u;
         }
     }
 }
@@ -666,18 +750,21 @@ cudaError_t init_rank_kernels(int carveout)
     return cudaSuccess;
 }
 
-unsigned long long rank_merge_tiles(unsigned long long capacity)
-{
-    return (capacity + kMTile - 1) / kMTile;
-}
-
 cudaError_t launch_rank_merge(RankWork &w, unsigned long long n_old, cudaStream_t st)
 {
     cudaError_t e = ensure_sort_attributes();
     if (e != cudaSuccess) return e;
-    const unsigned ntiles = (unsigned)std::max<unsigned long long>(rank_merge_tiles(n_old), 1);
+    const unsigned ntiles = (unsigned)std::max<unsigned long long>((n_old + kMTile - 1) / kMTile, 1);
     return launch_pdl(k_rank_merge, ntiles, kMThreads, kMergeSmem, st, (const float *)w.raw, w.keys[0], w.keys[1],
-                      w.vals[0], w.vals[1], n_old, ntiles, w.dirty, w.merge_ctl, w.merge_status, w.err);
+                      w.vals[0], w.vals[1], n_old, w.dirty, w.merge_ctl, w.err);
+}
+
+cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, unsigned *guide, unsigned K,
+                               double delta, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)std::min<unsigned long long>(((unsigned long long)K + 2 + 255) / 256, 4096);
+    k_build_guide<<<grid, 256, 0, st>>>(cdf, capacity, guide, K, delta);
+    return cudaGetLastError();
 }
 
 unsigned long long rank_tile_count(unsigned long long capacity)
@@ -707,7 +794,7 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
     const unsigned hgrid = (unsigned)std::min<unsigned long long>((size + kHistThreads - 1) / kHistThreads,
                                                                   (unsigned long long)std::max(w.num_sms, 1));
     e = launch_pdl(k_rs_hist4, std::max(hgrid, 1u), kHistThreads, kHistSmem, st, (const float *)w.raw, size,
-                   w.digit_hist, w.sort_ctl, w.merge_ctl ? w.merge_ctl + 4 : (unsigned *)nullptr);
+                   w.digit_hist, w.sort_ctl, w.merge_ctl);
     if (e != cudaSuccess) return e;
     const unsigned *kin = nullptr, *vin = nullptr;
     int cur = 0;

@@ -43,11 +43,11 @@ struct SampleArgs {
     int vec4;  // rows move as float4
 };
 
-constexpr int kGatherV = 4;   // float4 per lane in the single-round gather: rows of up to 256 floats
-
-// The sampled row: every load of the warp's share (states, next_states, and the action, reward
-// and done fields on lanes 1-3) is issued before the first store, so the gather costs one memory
-// round trip.  Rows shorter than the output stride are padded with zeros.
+// The sampled row, copied by the G lanes that served the draw: every load of a chunk of G V
+// float4 of the row pair (and the action, reward and done fields on lanes 1-3) is issued before
+// the chunk's first store, so the gather costs one memory round trip per chunk (one for rows of up
+// to 256 floats with G V = 128).  Rows shorter than the output stride are padded with zeros.
+template <int G, int V>
 __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o, unsigned j,
                                            unsigned long long slot, int lane, int vec4)
 {
@@ -59,44 +59,33 @@ __device__ __forceinline__ void gather_row(const RingRefs &r, const SampleOut &o
     if (lane == 2 && o.rewards) rew = __ldg(r.rewards + slot);
     if (lane == 3 && o.dones) done = __ldg(r.dones + slot);
     const bool rows = dp && (o.states || o.next);   // with d = 0 the rows are all padding
-    if (rows && vec4 && 2 * (dp >> 2) <= 32 * kGatherV) {
-        // up to 32 kGatherV float4 per row pair: kGatherV per lane, all loaded before any store
-        const unsigned d4 = d >> 2, dp4 = dp >> 2;
-        const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
-        const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
-        float4 v[kGatherV];
-        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < kGatherV; ++q) {
-            const unsigned c = lane + 32 * q;
-            const bool second = c >= dp4;
-            const unsigned cc = second ? c - dp4 : c;
-            v[q] = zero;
-            if (c < 2 * dp4 && cc < d4 && (second ? o.next : o.states)) v[q] = __ldg((second ? srcN : srcS) + cc);
-        }
-#pragma unroll
-        for (int q = 0; q < kGatherV; ++q) {
-            const unsigned c = lane + 32 * q;
-            const bool second = c >= dp4;
-            const unsigned cc = second ? c - dp4 : c;
-            float *base = second ? o.next : o.states;
-            if (c < 2 * dp4 && base) reinterpret_cast<float4 *>(base + (unsigned long long)j * dp)[cc] = v[q];
-        }
-    } else if (rows && vec4) {
+    if (rows && vec4) {
+        // the row pair as 2 dp4 float4, in chunks of G V: V per lane, all loaded before any store
         const unsigned d4 = d >> 2, dp4 = dp >> 2;
         const float4 *srcS = reinterpret_cast<const float4 *>(r.states + slot * d);
         const float4 *srcN = reinterpret_cast<const float4 *>(r.next + slot * d);
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (unsigned c = lane; c < 2 * dp4; c += 32) {
-            const bool second = c >= dp4;
-            const unsigned cc = second ? c - dp4 : c;
-            float *base = second ? o.next : o.states;
-            if (!base) continue;
-            reinterpret_cast<float4 *>(base + (unsigned long long)j * dp)[cc] =
-                cc < d4 ? __ldg((second ? srcN : srcS) + cc) : zero;
+        for (unsigned c0 = 0; c0 < 2 * dp4; c0 += G * V) {
+            float4 v[V];
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+                const unsigned c = c0 + lane + G * q;
+                const bool second = c >= dp4;
+                const unsigned cc = second ? c - dp4 : c;
+                v[q] = zero;
+                if (c < 2 * dp4 && cc < d4 && (second ? o.next : o.states)) v[q] = __ldg((second ? srcN : srcS) + cc);
+            }
+#pragma unroll
+            for (int q = 0; q < V; ++q) {
+                const unsigned c = c0 + lane + G * q;
+                const bool second = c >= dp4;
+                const unsigned cc = second ? c - dp4 : c;
+                float *base = second ? o.next : o.states;
+                if (c < 2 * dp4 && base) reinterpret_cast<float4 *>(base + (unsigned long long)j * dp)[cc] = v[q];
+            }
         }
     } else if (rows) {
-        for (unsigned c = lane; c < 2 * dp; c += 32) {
+        for (unsigned c = lane; c < 2 * dp; c += G) {
             const bool second = c >= dp;
             const unsigned cc = second ? c - dp : c;
             float *dst = second ? o.next : o.states;
@@ -120,25 +109,47 @@ __device__ __forceinline__ bool gt_nonneg(double a, double b)
     return __double_as_longlong(a) > __double_as_longlong(b);
 }
 
-// One round of the walk: k <= 7 levels below `node`.  The 2^k - 1 left children the walk may
-// read are loaded at once, four per lane (child i of the round sits in lane i % 32, slot i / 32),
-// and the k decisions then run on registers and shuffles.  When `last`, the deepest level is
-// the leaves: the 2^k leaves under `node` are one contiguous stretch, four per lane, and *lv
-// receives the chosen leaf's value.  The loads (walk_load) and the decisions (walk_decide) are
-// separate so that the first round's loads, which do not depend on the draw, can be issued
-// before the call number is known.
+// One round of the walk: k levels below `node`, served by G lanes holding S slots each, so
+// k <= log2(G S + 1).  The 2^k - 1 left children the walk may read are loaded at once (child i of
+// the round sits in lane i % G, slot i / G), and the k decisions then run on registers and
+// shuffles within the G lanes.  When `last`, the deepest level is the leaves: the 2^k leaves
+// under `node` are one contiguous stretch, S per lane, and *lv receives the chosen leaf's value.
+// The loads (walk_load) and the decisions (walk_decide) are separate so that the first round's
+// loads, which do not depend on the draw, can be issued before the call number is known.
+template <int S>
 struct WalkRegs {
-    double v[4];
-    float lf[4];
+    double v[S];
+    float lf[S];
 };
 
+template <int S>
+__device__ __forceinline__ double pick_slot(const double (&v)[S], int r)
+{
+    double x = v[0];
+#pragma unroll
+    for (int q = 1; q < S; ++q)
+        if (r == q) x = v[q];
+    return x;
+}
+
+template <int S>
+__device__ __forceinline__ float pick_slot(const float (&v)[S], int r)
+{
+    float x = v[0];
+#pragma unroll
+    for (int q = 1; q < S; ++q)
+        if (r == q) x = v[q];
+    return x;
+}
+
+template <int G, int S>
 __device__ __forceinline__ void walk_load(const TreeRefs &t, unsigned long long node, int k, bool last,
-                                          int lane, WalkRegs &w)
+                                          int lane, WalkRegs<S> &w)
 {
     const int ninternal = (1 << (last ? k - 1 : k)) - 1;  // left children that are internal nodes
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = lane + 32 * r;
+    for (int r = 0; r < S; ++r) {
+        const int i = lane + G * r;
         w.v[r] = 0.0;
         if (i < ninternal) {
             const int lev = 32 - __clz(i + 1);
@@ -150,17 +161,16 @@ __device__ __forceinline__ void walk_load(const TreeRefs &t, unsigned long long 
     }
 }
 
+template <int G, int S>
 __device__ __forceinline__ unsigned long long walk_decide(unsigned long long node, int k, bool last,
-                                                          double &m, int lane, const WalkRegs &w,
+                                                          double &m, int lane, const WalkRegs<S> &w,
                                                           float *lv)
 {
     int q = 0;
     const int kint = last ? k - 1 : k;
     for (int lev = 1; lev <= kint; ++lev) {
         const int i = (1 << (lev - 1)) - 1 + q;
-        const int r = i >> 5;
-        const double mine = r == 0 ? w.v[0] : r == 1 ? w.v[1] : r == 2 ? w.v[2] : w.v[3];
-        const double left = __shfl_sync(kFull, mine, i & 31);
+        const double left = __shfl_sync(kFull, pick_slot<S>(w.v, i / G), i & (G - 1), G);
         if (gt_nonneg(left, m)) {
             q = 2 * q;
         } else {
@@ -170,24 +180,29 @@ __device__ __forceinline__ unsigned long long walk_decide(unsigned long long nod
     }
     if (last) {
         const int i = 2 * q;  // the left leaf of the final pair
-        const int r = i >> 5;
-        const float mine = r == 0 ? w.lf[0] : r == 1 ? w.lf[1] : r == 2 ? w.lf[2] : w.lf[3];
-        const double left = (double)__shfl_sync(kFull, mine, i & 31);
+        const double left = (double)__shfl_sync(kFull, pick_slot<S>(w.lf, i / G), i & (G - 1), G);
         if (gt_nonneg(left, m)) {
             q = 2 * q;
         } else {
             m = __dsub_rn(m, left);
             q = 2 * q + 1;
         }
-        const int rr = q >> 5;
-        const float pick = rr == 0 ? w.lf[0] : rr == 1 ? w.lf[1] : rr == 2 ? w.lf[2] : w.lf[3];
-        *lv = __shfl_sync(kFull, pick, q & 31);
+        *lv = __shfl_sync(kFull, pick_slot<S>(w.lf, q / G), q & (G - 1), G);
     }
     return (node << k) + q;
 }
 
+// G lanes serve one draw (32 / G draws per warp at once), each lane holding S nodes of a round:
+// rounds of K = log2(G S + 1) levels (7 for 32 x 4; 6 for 16 x 4 and 8 x 8).  Every level of the
+// walk is one binary64 subtraction per warp instruction, and GB300's binary64 pipe retires about
+// one warp instruction every 19 cycles per SM, so large batches share each instruction among 2
+// or 4 draws; the deepest round also reads 17 sectors of nodes and leaves instead of 33.
+template <int G, int S>
 __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
 {
+    constexpr int K = G * S >= 127 ? 7 : (G * S >= 63 ? 6 : 5);   // levels per round
+    constexpr int GV = G >= 16 ? 128 / G : 8;                      // float4 per lane per gather chunk
+    constexpr int per_warp = 32 / G;
     __shared__ unsigned long long s_call;
     pdl_wait();
     pdl_release();
@@ -199,20 +214,29 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
     const double total = D == 0 ? (double)a.t.L[0] : a.t.S[1];
     const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
     const unsigned long long size = a.ctl->size;
-    const int rounds = (D + 6) / 7;                 // 7 levels per round; the first takes the rest
-    const int first = D - 7 * (rounds - 1);
-    const int lane = threadIdx.x & 31;
-    WalkRegs w0;
-    if (D > 0) walk_load(a.t, 1, first, rounds == 1, lane, w0);
+    const int rounds = (D + K - 1) / K;             // K levels per round; the first takes the rest
+    const int first = D - K * (rounds - 1);
+    const int lane = threadIdx.x & (G - 1);
+    const unsigned sub = (threadIdx.x & 31) / G;
+    // the first round's nodes are preloaded (before the call number arrives) when they fit the
+    // register budget beside the gather (one draw per warp); otherwise each draw loads them (L1)
+    constexpr bool kPre = G == 32;
+    WalkRegs<S> w0;
+    if (kPre && D > 0) walk_load<G, S>(a.t, 1, first, rounds == 1, lane, w0);
     // stratum width T / B: one exact scaling when B is a power of two
     const double seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
     __syncthreads();
     const unsigned long long call = s_call;
     const float nbeta = -a.beta;
     const unsigned wpb = blockDim.x >> 5;
-    const unsigned warps_total = gridDim.x * wpb;
+    const unsigned long long stride = (unsigned long long)gridDim.x * wpb * per_warp;
 
-    for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
+    for (unsigned long long j0 = ((unsigned long long)blockIdx.x * wpb + (threadIdx.x >> 5)) * per_warp; j0 < a.B;
+         j0 += stride) {
+        // every lane of the warp walks (the shuffles need them all); a sub-warp past the batch
+        // walks draw j0 again and stores nothing
+        const bool active = j0 + sub < a.B;
+        const unsigned j = (unsigned)(active ? j0 + sub : j0);
         const double u = draw_uniform(a.seed, j, call, 0);
         double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         unsigned long long leaf;
@@ -221,11 +245,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
             leaf = 0;
             lv = a.t.L[0];
         } else {
-            unsigned long long node = walk_decide(1, first, rounds == 1, m, lane, w0, &lv);
+            if (!kPre) walk_load<G, S>(a.t, 1, first, rounds == 1, lane, w0);
+            unsigned long long node = walk_decide<G, S>(1, first, rounds == 1, m, lane, w0, &lv);
             for (int rd = 1; rd < rounds; ++rd) {
-                WalkRegs w;
-                walk_load(a.t, node, 7, rd == rounds - 1, lane, w);
-                node = walk_decide(node, 7, rd == rounds - 1, m, lane, w, &lv);
+                WalkRegs<S> w;
+                walk_load<G, S>(a.t, node, K, rd == rounds - 1, lane, w);
+                node = walk_decide<G, S>(node, K, rd == rounds - 1, m, lane, w, &lv);
             }
             leaf = node - n;
         }
@@ -233,11 +258,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
             leaf = size - 1;
             lv = a.t.L[leaf];
         }
-        if (lane == 0) {
-            a.o.idx[j] = (long long)leaf;
-            if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
+        if (active) {
+            if (lane == 0) {
+                a.o.idx[j] = (long long)leaf;
+                if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
+            }
+            gather_row<G, GV>(a.r, a.o, j, leaf, lane, a.vec4);
         }
-        gather_row(a.r, a.o, j, leaf, lane, a.vec4);
+        // the first round again for the next draw (reloaded here, from L1 or L2, rather than kept
+        // in registers through the gather)
+        if (kPre && D > 0 && j0 + stride < a.B) walk_load<G, S>(a.t, 1, first, rounds == 1, lane, w0);
     }
 }
 
@@ -321,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_flat(FlatSampleArgs a)
             a.o.idx[j] = (long long)slot;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn(lv, pmin), nbeta);
         }
-        gather_row(a.r, a.o, j, slot, lane, a.vec4);
+        gather_row<32, 4>(a.r, a.o, j, slot, lane, a.vec4);
     }
 }
 
@@ -333,6 +363,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_flat(FlatSampleArgs a)
 // ------------------------------------------------------------------------------------------
 struct RankSampleArgs {
     const double *cdf;
+    const unsigned *guide;           // guide[0 .. guide_k + 1] (see RankWork), or null
+    unsigned guide_k;
+    double guide_delta, guide_inv;
     const unsigned *sorted;          // the slot order, unless order_cur is set:
     const unsigned *vals[2];         //   then vals[*order_cur]
     const unsigned *order_cur;
@@ -367,15 +400,29 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
     for (unsigned j = blockIdx.x * wpb + (threadIdx.x >> 5); j < a.B; j += warps_total) {
         const double u = draw_uniform(a.seed, j, call, 1);
         const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
-        // first position p in [1, size] with cdf[p] > m; size + 1 when there is none
-        const unsigned long long ans = first_above(a.cdf, 1, size + 1, m, lane);
+        // first position p in [1, size] with cdf[p] > m; size + 1 when there is none.  The
+        // guide brackets it: with fl(k delta) <= m < fl((k+1) delta), the rank lies in
+        // [guide[k], guide[k+1]], so the search covers that stretch only (same comparisons)
+        unsigned long long lo = 1, hi = size + 1;
+        if (a.guide) {
+            long long k = (long long)__dmul_rn(m, a.guide_inv);
+            if (k > (long long)a.guide_k) k = a.guide_k;
+            if (k < 0) k = 0;
+            while (k > 0 && __dmul_rn((double)k, a.guide_delta) > m) --k;
+            while (k < (long long)a.guide_k && __dmul_rn((double)(k + 1), a.guide_delta) <= m) ++k;
+            const unsigned long long g0 = __ldg(a.guide + k), g1 = __ldg(a.guide + k + 1);
+            if (g0 > lo) lo = g0;
+            if (g1 < hi) hi = g1;
+            if (lo > hi) lo = hi;
+        }
+        const unsigned long long ans = first_above(a.cdf, lo, hi, m, lane);
         unsigned long long r = ans > size ? size : ans;
         const unsigned long long slot = sorted[r - 1];
         if (lane == 0) {
             a.o.idx[j] = (long long)slot;
             if (a.o.w) a.o.w[j] = powf(__fdiv_rn((float)r, fsize), a.ab);
         }
-        gather_row(a.r, a.o, j, slot, lane, a.vec4);
+        gather_row<32, 4>(a.r, a.o, j, slot, lane, a.vec4);
     }
 }
 
@@ -418,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
             a.o.idx[j] = (long long)slot;
             if (a.o.w) a.o.w[j] = 1.0f;
         }
-        gather_row(a.r, a.o, j, slot, lane, a.vec4);
+        gather_row<32, 4>(a.r, a.o, j, slot, lane, a.vec4);
     }
 }
 
@@ -431,6 +478,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_uniform(UniformArgs a)
 unsigned long long sampler_ctas_per_sm() { return 16; }
 
 int warps_per_cta(unsigned B) { return (B <= 512 || B >= 4096) ? 2 : 8; }
+
+// Batches from which the proportional sampler serves two draws per warp (16 lanes each), and
+// four (8 lanes each).
+constexpr unsigned kHalfWarpBatch = 4096;
+constexpr unsigned kQuarterWarpBatch = 8192;
 
 bool rows_vec4(const RingRefs &r, const SampleOut &o)
 {
@@ -446,7 +498,8 @@ cudaError_t init_sample_kernels(int carveout)
 {
     if (carveout < 0) return cudaSuccess;
     cudaError_t e;
-    const void *fns[] = {(const void *)k_sample_prop, (const void *)k_sample_rank,
+    const void *fns[] = {(const void *)k_sample_prop<32, 4>, (const void *)k_sample_prop<16, 4>,
+                         (const void *)k_sample_prop<8, 8>, (const void *)k_sample_rank,
                          (const void *)k_sample_uniform, (const void *)k_sample_flat};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
@@ -470,9 +523,14 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     a.o = o;
     a.vec4 = rows_vec4(r, o) ? 1 : 0;
     const int wpb = warps_per_cta(B);
-    const unsigned long long ctas = (B + wpb - 1) / wpb;
+    // several draws per warp for large batches, where the walk keeps its number of rounds
+    const int r7 = (t.D + 6) / 7, r6 = (t.D + 5) / 6;
+    const int per_warp = (B >= kQuarterWarpBatch && r6 == r7) ? 4 : (B >= kHalfWarpBatch && r6 == r7) ? 2 : 1;
+    const unsigned long long ctas = (B + wpb * per_warp - 1) / (wpb * per_warp);
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
-    return launch_pdl(k_sample_prop, grid, wpb * 32, 0, st, a);
+    if (per_warp == 4) return launch_pdl(k_sample_prop<8, 8>, grid, wpb * 32, 0, st, a);
+    if (per_warp == 2) return launch_pdl(k_sample_prop<16, 4>, grid, wpb * 32, 0, st, a);
+    return launch_pdl(k_sample_prop<32, 4>, grid, wpb * 32, 0, st, a);
 }
 
 cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRefs &r, Ctl *ctl, unsigned B,
@@ -521,6 +579,10 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
 {
     RankSampleArgs a;
     a.cdf = w.cdf;
+    a.guide = w.guide;
+    a.guide_k = w.guide_k;
+    a.guide_delta = w.guide_delta;
+    a.guide_inv = w.guide_delta > 0.0 ? 1.0 / w.guide_delta : 0.0;
     a.sorted = sorted;
     a.vals[0] = w.vals[0];
     a.vals[1] = w.vals[1];

@@ -455,8 +455,9 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                         leaf = a.prio ? leaf_of(raw, a.lp) : max_leaf;
                         a.t.L[s] = leaf;
                     } else if (a.raw_store) {   // rank mode (uniform mode keeps no priorities)
+                        const float old = a.raw_store[s];
                         a.raw_store[s] = raw;
-                        mark_dirty(a.dirty, s);
+                        mark_dirty(a.dirty, s, old);
                     }
                 } else if (a.proportional) {
                     leaf = a.t.L[s];
@@ -1095,7 +1096,7 @@ struct ScatterArgs {
     const long long *idx;
     const float *td;
     unsigned B;
-    double eps;
+    double eps, alpha;
     LeafPowAlpha lp;
     int proportional;
 };
@@ -1137,9 +1138,135 @@ __global__ void __launch_bounds__(kThreads) k_upd_apply(ScatterArgs a)
         if (a.proportional) {
             a.t.L[i] = leaf_of(raw, a.lp);
         } else {
+            const float old = a.raw_store[i];
             a.raw_store[i] = raw;
-            mark_dirty(a.dirty, (unsigned long long)i);
+            mark_dirty(a.dirty, (unsigned long long)i, old);
         }
+    }
+}
+
+// Batches of at most kBlockBatch entries without a tree to climb (rank and flat modes): one
+// thread-block cluster of kBlockCtas CTAs does what k_upd_scatter, k_upd_apply and k_upd_finish
+// do, in one launch (the random accesses of one batch, spread over kBlockCtas SMs rather than
+// issued by one; hardware cluster barriers separate the phases).  Each thread keeps its entries in
+// registers: it loads index and TD error, then at once raises the slot's winner word and (rank
+// mode) reads the slot's raw priority and mark; after a cluster barrier, the entry that still
+// finds its own position stores its priority and clears the word.  Rank mode marks each slot not
+// yet marked in this epoch (the mark read before says which: this launch is the slot's only
+// writer), with one counter increment per CTA for the list positions.  CTA 0 folds the batch
+// maximum after a last cluster barrier.
+constexpr int kBlockCtas = 8;
+constexpr int kBlockThreads = 256;
+constexpr int kBlockPer = 4;   // entries per thread, at most
+constexpr unsigned kBlockBatch = (unsigned)(kBlockCtas * kBlockThreads * kBlockPer);   // 8192
+
+__global__ void __launch_bounds__(kBlockThreads) k_upd_block(ScatterArgs a)
+{
+    __shared__ unsigned s_w[kBlockThreads / 32];
+    __shared__ unsigned s_base;
+    pdl_wait();
+    pdl_release();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned gtid = cluster_cta_rank() * kBlockThreads + tid, gthreads = kBlockCtas * kBlockThreads;
+    const unsigned long long size = a.ctl->size;
+    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    const bool rank = !a.proportional;
+    const unsigned epoch = rank && a.dirty.mark ? __ldcg(a.dirty.epoch) : 0u;
+    constexpr unsigned kNone = 0xffffffffu;   // no entry, or an index outside the filled slots
+    unsigned iv[kBlockPer];
+    float tv[kBlockPer], oldv[kBlockPer];
+    unsigned mword[kBlockPer];
+#pragma unroll
+    for (int u = 0; u < kBlockPer; ++u) {
+        const unsigned j = gtid + u * gthreads;
+        const long long i = j < a.B ? __ldg(a.idx + j) : -1;
+        tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
+        iv[u] = (i < 0 || (unsigned long long)i >= size) ? kNone : (unsigned)i;
+    }
+    unsigned mymax = 0;
+    int bad = 0;
+#pragma unroll
+    for (int u = 0; u < kBlockPer; ++u) {
+        const unsigned j = gtid + u * gthreads;
+        const unsigned i = iv[u];
+        oldv[u] = 0.0f;
+        mword[u] = 0u;
+        if (j >= a.B) continue;
+        if (i == kNone) {
+            bad = 1;
+            continue;
+        }
+        mymax = max(mymax, __float_as_uint(td_to_raw(tv[u], a.eps, max_prev)));
+        atomicMax(a.win + i, j + 1);
+        if (rank) {
+            oldv[u] = a.raw_store[i];
+            if (a.dirty.mark) mword[u] = a.dirty.mark[i];
+        }
+    }
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
+    cluster_sync_all();   // every winner word raised
+    unsigned newmark = 0;   // bit u: entry u marks its slot for the first time
+#pragma unroll
+    for (int u = 0; u < kBlockPer; ++u) {
+        const unsigned j = gtid + u * gthreads;
+        const unsigned i = iv[u];
+        if (i == kNone) continue;
+        if (__ldcg(a.win + i) != j + 1) continue;   // a later entry holds this slot (or has taken it)
+        a.win[i] = 0;
+        const float raw = td_to_raw(tv[u], a.eps, max_prev);
+        if (!rank) {
+            a.t.L[i] = leaf_of(raw, a.lp);
+        } else {
+            a.raw_store[i] = raw;
+            if (a.dirty.mark && mword[u] != epoch) {
+                a.dirty.mark[i] = epoch;
+                newmark |= 1u << u;
+            }
+        }
+    }
+    if (rank && a.dirty.mark) {
+        // list positions for the new marks: a CTA-wide exclusive count, one counter increment
+        const unsigned c = __popc(newmark);
+        unsigned inc = c;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned x = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += x;
+        }
+        if (lane == 31) s_w[warp] = inc;
+        __syncthreads();
+        unsigned before = 0, total = 0;
+        for (int w = 0; w < kBlockThreads / 32; ++w) {
+            const unsigned x = s_w[w];
+            if (w < warp) before += x;
+            total += x;
+        }
+        if (tid == 0) s_base = total ? atomicAdd(a.dirty.count, total) : 0u;
+        __syncthreads();
+        unsigned pos = s_base + before + inc - c;
+#pragma unroll
+        for (int u = 0; u < kBlockPer; ++u)
+            if ((newmark >> u) & 1u) {
+                if (pos < kMaxDirty) {
+                    a.dirty.list[pos] = iv[u];
+                    a.dirty.oldkey[pos] = order_key(oldv[u]);
+                }
+                ++pos;
+            }
+        __syncthreads();   // s_w is reused below
+    }
+    for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
+    if (lane == 0) s_w[warp] = mymax;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned bm = 0;
+        for (int w = 0; w < kBlockThreads / 32; ++w) bm = max(bm, s_w[w]);
+        if (bm) atomicMax(&a.ctl->batch_max_bits, bm);
+    }
+    cluster_sync_all();   // every CTA's maximum in
+    if (cluster_cta_rank() == 0 && tid == 0) {
+        Ctl *c = a.ctl;
+        fold_running_max(c, __ldcg(&c->batch_max_bits), a.alpha);   // L2: this SM's L1 may hold the line
+        c->batch_max_bits = 0;
     }
 }
 
@@ -1563,8 +1690,9 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     const float raw = td_to_raw(__ldg(a.td + j), a.eps, max_prev);
                     if (a.proportional) a.t.L[i] = leaf_of(raw, a.lp);
                     else {
+                        const float old = a.raw_store[i];
                         a.raw_store[i] = raw;
-                        mark_dirty(a.dirty, (unsigned long long)i);
+                        mark_dirty(a.dirty, (unsigned long long)i, old);
                     }
                 }
                 __syncwarp();
@@ -1601,8 +1729,9 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
             if (a.proportional) {
                 warp_climb_regs<W>(a.t, U, shift, lane, base, lane < U ? li : 0u, raw, a.lp, s_lp);
             } else if (lane < U) {
+                const float old = a.raw_store[base + li];
                 a.raw_store[base + li] = raw;
-                mark_dirty(a.dirty, base + li);
+                mark_dirty(a.dirty, base + li, old);
             }
         } else {
             int m2 = 2;
@@ -1630,8 +1759,9 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     if (a.proportional) {
                         wl.uraw[u] = raw;
                     } else {
+                        const float old = a.raw_store[leaf];
                         a.raw_store[leaf] = raw;
-                        mark_dirty(a.dirty, leaf);
+                        mark_dirty(a.dirty, leaf, old);
                     }
                 }
                 U += __popc(bal);
@@ -1981,7 +2111,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
 
     const bool incremental = cnt + bsz <= C && cnt * 8 <= t.n && cnt <= (1ull << 18);
     if (marked) *marked = incremental;
-    a.dirty = incremental ? dirty : DirtyRefs{nullptr, nullptr, nullptr};
+    a.dirty = incremental ? dirty : DirtyRefs{nullptr, nullptr, nullptr, nullptr, nullptr};
     if (incremental) {
         a.ntree = (unsigned)(cnt / bsz + 3);
         a.ncopy = ncopy;
@@ -2029,13 +2159,16 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
     a.td = td;
     a.B = B;
     a.eps = eps;
+    a.alpha = alpha;
     a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
+    const bool tree = proportional && t.D > 0 && t.S;
+    if (!tree && B <= kBlockBatch) return launch_pdl_cluster(k_upd_block, kBlockCtas, kBlockThreads, 0, st, a);
     const unsigned grid = (unsigned)std::min<unsigned long long>((B + kThreads - 1) / kThreads,
                                                                  (unsigned long long)num_sms * 8);
     cudaError_t e = launch_pdl(k_upd_scatter, grid, kThreads, 0, st, a);
     if (e != cudaSuccess) return e;
-    if (proportional && t.D > 0 && t.S) {
+    if (tree) {
         // the leaf level of the rebuild applies the winners and the last CTA folds the maximum
         RebuildArgs r = rebuild_args(t, ctl);
         r.win = win;

@@ -51,8 +51,8 @@ struct per_buffer {
     uint32_t rebuild_batch = 0;
     uint32_t element_batch = 0;   // per_config.element_batch
     uint64_t order_size = 0, dirty_bound = 0;
-    unsigned *dirty_words = nullptr;   // bitmap [dirty_nwords] + list [kMaxDirty] + control [8]
-    uint64_t dirty_nwords = 0;
+    unsigned *dirty_words = nullptr;   // slot marks [dirty_nwords] + list, old keys [kMaxDirty each] + control [8]
+    uint64_t dirty_nwords = 0;         // words of slot marks (one per slot)
     std::string err;
 };
 
@@ -98,9 +98,9 @@ RingRefs ring_of(const per_buffer *h)
 
 void free_all(per_buffer *h)
 {
-    void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.keys[0], h->rank.keys[1],
+    void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.guide, h->rank.keys[0], h->rank.keys[1],
                     h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
-                    h->dirty_words, h->rank.merge_status, h->win, h->flat_mem,
+                    h->dirty_words, h->win, h->flat_mem,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -158,11 +158,9 @@ cudaError_t rank_order(per_buffer *h, cudaStream_t st)
             if (e != cudaSuccess) return e;
         }
     } else {
+        // the sort's first kernel also opens a new mark epoch with an empty list
         unsigned *sorted = nullptr, *keys = nullptr;
         e = launch_rank_sort(w, h->host_size, &sorted, st, &keys);
-        if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(h->dirty_words, 0, h->dirty_nwords * sizeof(unsigned), st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(w.dirty.count, 0, sizeof(unsigned), st);
         if (e != cudaSuccess) return e;
     }
     h->order_valid = true;
@@ -304,13 +302,15 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         h->rank.sort_ctl = h->rank.digit_hist + 4 * 256;
         h->rank.capacity = capacity;
         h->rank.num_sms = h->num_sms;
-        h->dirty_nwords = capacity / 32 + 1;
-        ok = ok && alloc(&h->dirty_words, h->dirty_nwords + kMaxDirty + 8) &&
-             alloc(&h->rank.merge_status, rank_merge_tiles(capacity));
+        h->dirty_nwords = capacity;   // one mark epoch per slot
+        ok = ok && alloc(&h->dirty_words, h->dirty_nwords + 2 * kMaxDirty + 8);
         if (ok) {
-            h->rank.dirty.bits = h->dirty_words;
+            h->rank.dirty.mark = h->dirty_words;
             h->rank.dirty.list = h->dirty_words + h->dirty_nwords;
-            h->rank.merge_ctl = h->rank.dirty.list + kMaxDirty;   // [0..2] merge, [3] marked count
+            h->rank.dirty.oldkey = h->rank.dirty.list + kMaxDirty;
+            // [1] mark epoch, [2] merge arrivals, [3] listed count, [4] which pair holds the order
+            h->rank.merge_ctl = h->rank.dirty.oldkey + kMaxDirty;
+            h->rank.dirty.epoch = h->rank.merge_ctl + 1;
             h->rank.dirty.count = h->rank.merge_ctl + 3;
         }
     }
@@ -338,11 +338,34 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
     if (e == cudaSuccess && h->rank.digit_hist) e = cudaMemset(h->rank.digit_hist, 0, (4 * 256 + 16) * sizeof(unsigned));
     if (e == cudaSuccess && h->dirty_words)
-        e = cudaMemset(h->dirty_words, 0, (h->dirty_nwords + kMaxDirty + 8) * sizeof(unsigned));
-    if (e == cudaSuccess && h->rank.merge_status)
-        e = cudaMemset(h->rank.merge_status, 0, rank_merge_tiles(capacity) * sizeof(unsigned long long));
+        e = cudaMemset(h->dirty_words, 0, (h->dirty_nwords + 2 * kMaxDirty + 8) * sizeof(unsigned));
+    if (e == cudaSuccess && h->dirty_words) {   // the first mark epoch is 1: no slot is marked
+        const unsigned one_epoch = 1u;
+        e = cudaMemcpy(h->rank.merge_ctl + 1, &one_epoch, sizeof(one_epoch), cudaMemcpyHostToDevice);
+    }
     if (h->rank.raw) h->rank.err = &h->ctl->err_flags;
     if (e == cudaSuccess && h->rank.cdf) e = launch_build_cdf(h->rank.cdf, capacity, h->alpha, 0);
+    if (e == cudaSuccess && h->rank.cdf) {
+        // the CDF's guide: about 16 ranks per bucket of mass where ranks are sparsest in mass
+        // (the last, each of mass capacity^-alpha), at most two entries per slot
+        double T = 0.0;
+        e = cudaMemcpy(&T, h->rank.cdf + capacity, sizeof(double), cudaMemcpyDeviceToHost);
+        uint64_t K = 1024, cap2 = 2;
+        while (cap2 < capacity) cap2 <<= 1;
+        cap2 *= 2;
+        const double est = T * std::pow((double)capacity, h->alpha) / 16.0;
+        while ((double)K < est && K < cap2) K <<= 1;
+        if (e == cudaSuccess && !alloc(&h->rank.guide, K + 2)) {
+            cudaGetLastError();
+            free_all(h);
+            delete h;
+            return fail(nullptr, PER_ERR_OOM, "per_create: device allocation failed");
+        }
+        h->rank.guide_k = (unsigned)K;
+        h->rank.guide_delta = T / (double)K;
+        if (e == cudaSuccess) e = launch_build_guide(h->rank.cdf, capacity, h->rank.guide, (unsigned)K,
+                                                     h->rank.guide_delta, 0);
+    }
     if (e == cudaSuccess && state_dim) e = cudaMemset(h->states, 0, capacity * (uint64_t)state_dim * sizeof(float));
     if (e == cudaSuccess && state_dim) e = cudaMemset(h->next, 0, capacity * (uint64_t)state_dim * sizeof(float));
     if (e == cudaSuccess) e = cudaMemset(h->actions, 0, capacity * sizeof(uint32_t));

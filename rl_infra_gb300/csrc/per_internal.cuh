@@ -60,24 +60,37 @@ constexpr unsigned kFlagTimeout = 2u;
 constexpr unsigned kFlagRankStale = 4u;
 
 // ---- rank mode: slots whose priority changed since the order was last made ------------------
-// Update and insertion mark every slot they write in a bitmap and, the first time, append it to
-// a list of at most kMaxDirty slots; the next sample merges them into the previous order instead
-// of sorting every slot again (k_rank.cu).  Null bits: nothing is marked.
+// Update and insertion mark every slot they write with the current mark epoch and, the first
+// time in that epoch, append it to a list of at most kMaxDirty slots together with the order key
+// it had before that first write (the key it holds in the order); the next sample merges them
+// into the previous order instead of sorting every slot again (k_rank.cu), then opens a new epoch,
+// which unmarks every slot at once.  Null mark: nothing is marked.
 constexpr unsigned kMaxDirty = 4096;
 
 struct DirtyRefs {
-    unsigned *bits;    // [capacity / 32 + 1]
-    unsigned *list;    // [kMaxDirty]
-    unsigned *count;   // slots marked (the list holds the first kMaxDirty)
+    unsigned *mark;          // [capacity] the epoch in which each slot was last marked
+    const unsigned *epoch;   // the current epoch (never 0, so a cleared mark is not current)
+    unsigned *list;          // [kMaxDirty] marked slots
+    unsigned *oldkey;        // [kMaxDirty] their order key before the first write (~bits of the raw)
+    unsigned *count;         // slots marked in this epoch (the list holds the first kMaxDirty)
 };
 
-__device__ __forceinline__ void mark_dirty(const DirtyRefs &d, unsigned long long slot)
+// The order key of a raw priority: raw > 0, so ascending ~bits is descending raw (an empty
+// slot's 0 gives the largest key).
+__device__ __forceinline__ unsigned order_key(float raw) { return ~__float_as_uint(raw); }
+
+// Called by the one writer of `slot` in a launch, with the raw priority the slot held before
+// this write.
+__device__ __forceinline__ void mark_dirty(const DirtyRefs &d, unsigned long long slot, float old_raw)
 {
-    if (!d.bits) return;
-    const unsigned bit = 1u << (slot & 31);
-    if (!(atomicOr(&d.bits[slot >> 5], bit) & bit)) {
+    if (!d.mark) return;
+    const unsigned e = __ldcg(d.epoch);
+    if (atomicExch(&d.mark[slot], e) != e) {
         const unsigned i = atomicAdd(d.count, 1u);
-        if (i < kMaxDirty) d.list[i] = (unsigned)slot;
+        if (i < kMaxDirty) {
+            d.list[i] = (unsigned)slot;
+            d.oldkey[i] = order_key(old_raw);
+        }
     }
 }
 
@@ -240,6 +253,12 @@ cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRef
 struct RankWork {
     float *raw;
     double *cdf;
+    // guide to the CDF: guide[k] = the first rank r with cdf[r] > fl(k * guide_delta), for
+    // k = 0 .. guide_k (guide_k + 1 past the end: capacity + 1), so a mass in
+    // [fl(k delta), fl((k+1) delta)) has its rank in [guide[k], guide[k+1]]
+    unsigned *guide;
+    unsigned guide_k;
+    double guide_delta;
     unsigned *keys[2];
     unsigned *vals[2];
     unsigned *digit_hist;          // [4][256] digit counts of the sort in progress (zero between sorts)
@@ -250,9 +269,8 @@ struct RankWork {
     int num_sms;                   // grid of the histogram kernel
     // kept between calls by a buffer (all null for the allocation-free entry point):
     DirtyRefs dirty;               // slots changed since the order was made
-    unsigned *merge_ctl;           // [8]: [0] tile counter, [1] epoch, [2] arrivals, [3] marked count,
+    unsigned *merge_ctl;           // [8]: [1] mark epoch, [2] arrivals of the merge, [3] marked count,
                                    // [4] which of keys/vals[0|1] holds the current order
-    unsigned long long *merge_status;  // [merge tiles] look-back words of the merge
 };
 
 // Words of RankWork scratch the sort needs for `capacity` keys (beyond keys and values).
@@ -260,6 +278,10 @@ unsigned long long rank_status_words(unsigned long long capacity);
 
 cudaError_t launch_build_cdf(double *cdf, unsigned long long capacity, double alpha,
                              cudaStream_t st);
+
+// guide[0 .. K + 1] for a CDF of `capacity` ranks (K = guide_k, delta = guide_delta).
+cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, unsigned *guide, unsigned K,
+                               double delta, cudaStream_t st);
 
 // Sorts the `size` filled slots by raw priority descending, ties by slot ascending, leaving
 // the slot order in *sorted (a pointer into w.vals).  With keys_out non-null the last pass also
@@ -272,8 +294,6 @@ cudaError_t launch_rank_sort(RankWork &w, unsigned long long host_size, unsigned
 // the marked slots at their current priority, into the other pair; flips merge_ctl[4] and
 // clears the marks.  The full sort sets merge_ctl[4] = 1.
 cudaError_t launch_rank_merge(RankWork &w, unsigned long long n_old, cudaStream_t st);
-
-unsigned long long rank_merge_tiles(unsigned long long capacity);
 
 // The slot order is w.vals[merge_ctl[4]] (read on the device), or `sorted` when w.merge_ctl is null.
 cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const RingRefs &r,

@@ -251,6 +251,24 @@ def test_many_sizes_of_batch_and_tree(rb):
         p.close()
 
 
+@pytest.mark.parametrize("D,cap", [(0, 1), (3, 5), (6, 64), (10, 1000), (12, 1 << 12), (16, 40000),
+                                   (18, 1 << 18)])
+def test_large_batches_two_draws_per_warp(D, cap):
+    """Batches of 4096 draws or more walk on 16-lane halves of a warp in rounds of up to 6 levels
+    (for trees whose round count that keeps); odd batch sizes leave one half without a draw."""
+    w = _small("tiny", capacity=cap, state_dim=64, row_stride=64)
+    g = wl.rng(17, D)
+    p = Pair(cap, 64, 64, 0.7, 1e-6, 0, seed=D)
+    prefill(p, w, g)
+    for B in (4096, 5001, 8192, 8195):
+        _, want = p.sample(B, 0.5)
+        idx = wl.duplicate_positions(g, want["idx"], 0.25)
+        p.update(idx, wl.td_errors(g, B))
+    p.check_tree()
+    p.check_counters()
+    p.close()
+
+
 @pytest.mark.parametrize("alpha", [0.6, 0.5, 1.5, 0.123456789])
 def test_leaf_values_over_a_wide_range(alpha):
     """Leaves p^alpha for priorities spread over 2^-30 .. 2^30 (and exact powers of two),
