@@ -609,6 +609,71 @@ def run_flat_design(args):
     return res
 
 
+def run_crowded(args):
+    """Lasting crowding on the apex shape: every slot prefilled at raw priority 1e-6, each step
+    inserts 512 rows at the running maximum (they keep nearly all the mass, so the draws crowd
+    the newest rows), samples 512 and updates them with TD errors of order 1e-3.  Steps/s with
+    the default update dispatch (which follows the crowding) and with each update path forced,
+    K steps back to back between two events after W + 64 untimed steps."""
+    import ctypes
+    import torch
+    from rl_infra_gb300 import capi
+    from rl_infra_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    K, W, B, I = args.steps, args.warmup, w.batch, 512
+    res = {"note": ("apex shape (2^21 slots, state_dim 64, B=512) with every slot prefilled at raw "
+                    "priority 1e-6, 512 rows a step inserted at the running maximum, TD errors N(0,1) x 1e-3; "
+                    "K steps back to back between two events")}
+    for label, rb in (("default", 0), ("climb", capi.REBUILD_NEVER), ("rebuild", 1)):
+        buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0,
+                                rebuild_batch=rb)
+        chunk = 1 << 18
+        for c in range(w.capacity // chunk):
+            sd, nd = wl.device_rows(torch, 0, c, chunk, w.state_dim)
+            a, r, d = wl.device_scalars(torch, 0, c, chunk, w)
+            buf.add(sd, nd, a, r, d, torch.full((chunk,), 1e-6, dtype=torch.float32, device="cuda"))
+        sd, nd = wl.device_rows(torch, 1, 0, 1 << 14, w.state_dim)
+        a, r, d = wl.device_scalars(torch, 1, 0, 1 << 14, w)
+        staging = {"states": sd, "next_states": nd, "actions": a, "rewards": r, "dones": d}
+        g = wl.rng(0, 88)
+        td = torch.from_numpy(wl.td_errors(g, 64 * B) * np.float32(1e-3)).cuda()
+        out = buf.alloc_batch(B)
+        L, h = capi.load(), buf._h
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        add_args = [(h, I, *_ring_ptrs(staging, o * I), None, st) for o in range((1 << 14) // I)]
+        sample_args = (h, B, ctypes.c_float(w.beta), *_out_ptrs(out), st)
+        idx_ptr, td0 = out["idx"].data_ptr(), td.data_ptr()
+
+        def one(t):
+            _check(L, h, L.per_add(*add_args[t % len(add_args)]), "per_add")
+            _check(L, h, L.per_sample(*sample_args), "per_sample")
+            _check(L, h, L.per_update_priorities(h, B, idx_ptr, td0 + 4 * B * (t % 64), st), "per_update")
+
+        for t in range(W + 64):
+            one(t)
+            if t % 8 == 7:
+                torch.cuda.synchronize()   # let the crowding count reach the host
+        torch.cuda.synchronize()
+        cr = Cudart()
+        e0, e1 = cr.events(2)
+        cr.lib.cudaEventRecord(e0, st)
+        for t in range(K):
+            one(W + 64 + t)
+        cr.lib.cudaEventRecord(e1, st)
+        torch.cuda.synchronize()
+        secs = cr.elapsed_ms(e0, e1) / 1e3
+        cr.destroy([e0, e1])
+        crowd = int(buf.read_state(capi.PER_STATE_COUNTERS, 4, 1)[0])
+        if buf.status_device() != 0:
+            raise RuntimeError("device error flag raised during the crowded run")
+        res[label] = {"value": round(K / secs, 2), "unit": UNIT, "us_per_step": round(secs * 1e6 / K, 3),
+                      "steps": K, "crowd_last": crowd}
+        buf.close()
+        del staging, td, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_e2e(torch, buf, w, staging, g, K, dist):
     """Steps/s through the public C calls with the inputs in pinned host memory: each step copies
     its ingest rows and TD errors host->device (one packed copy) and the sampled batch
@@ -749,13 +814,14 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
 
 # -- the other workloads (sample + update steps; rank adds the sort) -------------------------------
 
-KERNEL_FILES = {"k_sample_prop": "k_sample.cu", "k_update": "k_tree.cu", "k_sample_uniform": "k_sample.cu"}
+KERNEL_FILES = {"k_sample_prop": "k_sample.cu", "k_update": "k_tree.cu", "k_sample_uniform": "k_sample.cu",
+                "k_rank_merge": "k_rank.cu", "k_sample_rank": "k_sample.cu"}
 
 OTHER = {
     "tiny": "tiny: 2^10 leaves, state_dim 8, B=32, alpha 0.6, beta 0.4",
     "dqn": "dqn: 2^20 leaves, state_dim 48 gathered into 64-float rows, B=1024, beta 0.4->1.0 over 341 steps",
     "stress": "stress: 2^24 leaves, state_dim 256, B=8192, 25% duplicate update indices, alpha 0.7, beta 0.5",
-    "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, order merge (radix sort when rebuilt) + rank sample, alpha 0.7, beta 0.5",
+    "rank": "rank-based: 2^20 slots, state_dim 64, B=1024, order brought up to date (merge, or radix sort when rebuilt) + rank sample + update, alpha 0.7, beta 0.5",
     "uniform": "uniform: 2^21 slots, state_dim 64, B=512, uniform stratified draws + gather, dones as f32 (the update is a no-op)",
 }
 
@@ -808,65 +874,86 @@ def run_other(args, name, resort=False, steps=None, warmup=None, op_steps=None):
     rec, memset = cr.lib.cudaEventRecord, cr.lib.cudaMemsetAsync
     flush_l2 = args.l2 == "flush"
 
-    def step(t, ev):
+    rank = w.mode == wl.RANK
+
+    def calls(t):
+        """The step's C calls: (rank) the order brought up to date, the sample, the update."""
         beta = ctypes.c_float(w.beta_at(t % max(w.rounds, 1)))
         k = t % NS
-        rec(ev[0], st)
-        _check(L, h, L.per_sample(h, B, beta, *ptrs, st), "per_sample")
-        if ev[1] is not None:
-            rec(ev[1], st)
-        _check(L, h, L.per_update_priorities(h, B, idx_sets[k].data_ptr(), td[k].data_ptr(), st),
-               "per_update")
-        rec(ev[2], st)
+        out_ = []
+        if rank:
+            out_.append(lambda: _check(L, h, L.per_rank_refresh(h, st), "per_rank_refresh"))
+        out_.append(lambda: _check(L, h, L.per_sample(h, B, beta, *ptrs, st), "per_sample"))
+        out_.append(lambda: _check(L, h, L.per_update_priorities(h, B, idx_sets[k].data_ptr(), td[k].data_ptr(), st),
+                                   "per_update"))
+        return out_
+
+    NC = len(calls(0))
+
+    def step(t, ev):
+        """One step; ev holds NC + 1 events (None: no event at that point)."""
+        for i, c in enumerate(calls(t)):
+            if ev[i] is not None:
+                rec(ev[i], st)
+            c()
+        rec(ev[NC], st)
         if flush_l2:
             memset(flush.data_ptr(), 0, flush.numel(), st)
             torch.sum(evict, 0, out=evict_out)
 
-    warm = cr.events(3)
+    warm = cr.events(NC + 1)
     for t in range(W):
         step(t, warm)
     torch.cuda.synchronize()
     sev = cr.events(2 * K)
     t0 = time.perf_counter()
     for t in range(K):
-        step(W + t, (sev[2 * t], None, sev[2 * t + 1]))
+        step(W + t, [sev[2 * t]] + [None] * (NC - 1) + [sev[2 * t + 1]])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     step_ms = np.array([cr.elapsed_ms(sev[2 * t], sev[2 * t + 1]) for t in range(K)])
     cr.destroy(sev)
     Kop = min(K, 1000) if op_steps is None else op_steps
-    fl = cr.events(3 * Kop)
+    fl = cr.events((NC + 1) * Kop)
     for t in range(Kop):
-        step(W + K + t, fl[3 * t: 3 * t + 3])
+        step(W + K + t, fl[(NC + 1) * t: (NC + 1) * (t + 1)])
     torch.cuda.synchronize()
-    per = np.array([[cr.elapsed_ms(fl[3 * t + i], fl[3 * t + i + 1]) for i in range(2)] for t in range(Kop)])
+    per = np.array([[cr.elapsed_ms(fl[(NC + 1) * t + i], fl[(NC + 1) * t + i + 1]) for i in range(NC)]
+                    for t in range(Kop)])
     cr.destroy(fl + warm)
     if buf.status_device() != 0:
         raise RuntimeError("device error flag raised during the benchmark")
     idx = out["idx"].cpu().numpy()
     D = int(np.log2(buf.nleaves))
     upd_idx = idx_sets[(W + K + Kop - 1) % NS].cpu().numpy()
-    if w.mode == wl.RANK:
+    if rank:
         n = w.capacity
         d = len(np.unique(upd_idx))
-        # order merge: previous keys + slots in, new keys + slots out, the written slots' entries
-        # (slot + raw) once; the sampler's probes, weights and gathered rows
-        b_sort = (16 * n + 8 * d) if not resort else (4 * 16 * n + 4 * n)
-        b_sam = b_sort + B * (8 + 8 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18 + 8)
-        b_upd = 12 * B + 4 * d
-        names = ("rank order + k_sample_rank", "update (k_upd_scatter + k_upd_apply + k_upd_finish)")
+        # order merge: previous keys + slots in, new keys + slots out (16 B per slot), and the
+        # listed slots' entries (slot, old key, raw: 12 B) once; the full sort: the histogram pass
+        # reads 4 B per key, passes 0-2 read and write 8 B per key, pass 3 reads 8 and writes 4 B
+        b_ord = (16 * n + 12 * d) if not resort else (4 * n + 3 * 16 * n + 12 * n)
+        # the sampler: CDF guide and probes (about 2 x 8 B), the order entry (4 B), weight and
+        # index (12 B), rows read and written, action, reward, done in and out
+        b_sam = B * (16 + 4 + 12 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 18)
+        b_upd = 12 * B + 8 * d
+        names = ("sort (k_rs_hist4 + 4 k_rs_onesweep)" if resort else "k_rank_merge", "k_sample_rank",
+                 "k_upd_block")
+        byts = (b_ord, b_sam, b_upd)
     elif w.mode == wl.UNIFORM:
         # idx + weight out; rows read and written; action, reward in and out; done 1 B in, 4 B out
         b_sam = B * (8 + 4 + 2 * (4 * w.state_dim + 4 * w.row_stride) + 8 + 8 + 5)
-        b_upd = 0
         names = ("k_sample_uniform", "update (no kernel in this mode)")
+        byts = (b_sam, 0)
     else:
         b_sam = bytes_sample(idx, w.state_dim, w.row_stride, D)
         b_upd = bytes_update(upd_idx, D)
         names = ("k_sample_prop", "k_update")
-    ops = {names[0]: (float(np.median(per[:, 0])), b_sam), names[1]: (float(np.median(per[:, 1])), b_upd)}
+        byts = (b_sam, b_upd)
+    ops = {nm: (float(np.median(per[:, i])), byts[i]) for i, nm in enumerate(names)}
     if w.mode == wl.UNIFORM:
         del ops[names[1]]
+    b_step = sum(byts)
     peak, peak_src = load_peaks()
     dom = max(ops, key=lambda k: ops[k][0])
     ms, byt = ops[dom]
@@ -882,14 +969,14 @@ def run_other(args, name, resort=False, steps=None, warmup=None, op_steps=None):
         "step_us_median": round(float(np.median(step_ms)) * 1e3, 3),
         "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
         "bytes_per_step": {k: int(v[1]) for k, v in ops.items()},
-        "hbm_gbs_algorithmic": round((b_sam + b_upd) / (total_s / K) / 1e9, 2),
+        "hbm_gbs_algorithmic": round(b_step / (total_s / K) / 1e9, 2),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 5),
                      "traffic": traffic_from_profiles(dom, KERNEL_FILES[dom], name) if dom in KERNEL_FILES else None,
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": int(byt),
                      "median_launch_us": round(ms * 1e3, 3)},
-        # rank: order (merge, or histogram + 4 sort passes) + sampler + the 3 scatter-path update kernels
-        "gpu_launches": ((9 if resort else 5) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
+        # rank: order (merge, or histogram + 4 sort passes) + sampler + the cluster update kernel
+        "gpu_launches": ((7 if resort else 3) if w.mode == wl.RANK else 1 if w.mode == wl.UNIFORM else 2) * K,
     }
     if w.mode == wl.RANK:
         res["config"]["rank_order"] = ("every slot sorted again at each sample (4-pass radix sort)" if resort
@@ -1062,7 +1149,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="apex", choices=["apex", "tiny", "dqn", "stress", "rank", "uniform"],
+    ap.add_argument("--workload", default="apex",
+                    choices=["apex", "tiny", "dqn", "stress", "rank", "uniform", "crowded"],
                     help="apex is the headline workload; the others are measured with --workload")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip timing the rounds captured as one CUDA graph")
@@ -1109,6 +1197,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_update_crossover(args)))
         return
+    if args.workload == "crowded":
+        if rank == 0:
+            print(json.dumps(run_crowded(args)))
+        return
     if args.workload != "apex":
         if rank == 0:
             res = run_other(args, args.workload)
@@ -1123,6 +1215,7 @@ def main():
         res["flat_design"] = run_flat_design(args)
     if rank == 0 and world == 1 and not args.no_workloads:
         res["workloads"] = run_workloads(args)
+        res["workloads"]["apex_lasting_crowding"] = run_crowded(args)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             sps, n, el = oracle_steps_per_s(budget_s=args.cpu_budget)

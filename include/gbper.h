@@ -94,13 +94,10 @@ typedef struct {
                                 priorities and rebuild every tree level instead of climbing from
                                 each changed leaf (same result); 0: the crossover measured on
                                 GB300 (max(leaves / 128, 1024) proportional; rank mode
-                                always scatters);
-                                UINT32_MAX: never.  1 (always) suits buffers whose draws
-                                keep crowding a few subtrees, e.g. new rows at the running
-                                maximum that hold most of the mass: the climb then takes
-                                32 leaves of a subtree at a time (at 2^21 leaves and
-                                B = 512 such a step measured 79-103 us climbing and 33 us
-                                rebuilding, against 27 us for spread draws) */
+                                always scatters), and smaller batches too while recent
+                                updates crowded a subtree (see per_update_priorities);
+                                UINT32_MAX: never; any other value: from that size, with
+                                no regard to crowding */
     uint32_t element_batch;  /* proportional mode: update batches of fewer entries than this
                                 propagate entry by entry, each from its leaf to the root (same
                                 result); 0: the crossover measured on GB300 (3: batches of
@@ -207,8 +204,16 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * entries instead mark each slot's last batch position in a winner word, write the winners and
  * rebuild every level of both trees (the post's level-synchronous rebuild, Measuring the
  * Trade Honestly: O(k + n) beats O(k log n) once k is a large share of n); the trees come out
- * the same.  Flat mode writes the leaves only (scatter path always; the next sample sums
- * them).  Rank mode stores raw.  Uniform mode has no
+ * the same.  Batches below that size rebuild as well while recent updates crowded one subtree:
+ * the climb serves a subtree's entries 32 distinct leaves at a time, one group after the other,
+ * so when one subtree (of the update's 2^P, about 8 entries each) received at least
+ * 32 (2 + leaves / 2^20) entries, as when new rows entering at the running maximum keep most of
+ * the mass, the next calls rebuild (measured on GB300 at 2^21 leaves, B = 512: up to 465 entries
+ * in one subtree climbed in 68-104 us, rebuilt in 33 us), and return to the climb once the
+ * counts the rebuild keeps fall below it.  The count reaches the host through mapped host
+ * memory without a synchronisation, a few calls late; PER_STATE_COUNTERS[4] reads it.  A
+ * rebuild_batch other than 0 turns this off.  Flat mode writes the leaves only (scatter path
+ * always; the next sample sums them).  Rank mode stores raw.  Uniform mode has no
  * priorities: the call checks its arguments and changes nothing.  The running maximum
  * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
  * PER_DEVFLAG_BAD_INDEX.
@@ -216,6 +221,20 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  */
 per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx,
                                  const float *d_td, void *stream);
+
+/*
+ * per_rank_refresh -- rank mode: bring the slot order up to date now, the step per_sample takes
+ * first ("GPU-Resident Prioritized Experience Replay", Sampling Kernels, Rank-based step 1: the
+ * filled slots sorted by raw priority descending, ties by slot ascending).  When the order exists
+ * and at most 4096 slots (and at most an eighth of the filled ones) were written since it was
+ * made, the written slots are merged into it; otherwise every filled slot is sorted again.  A
+ * per_sample that follows with no write in between samples from this order without redoing it;
+ * PER_STATE_RANK_ORDER reads it.  A buffer with no filled slot is left as it is.  No host
+ * synchronisation.  As for per_sample, a call made during stream capture while the buffer is not
+ * yet full is refused.
+ * Errors: PER_ERR_INVALID_ARG (not rank mode, or the capture case), PER_ERR_CUDA.
+ */
+per_status per_rank_refresh(per_buffer *h, void *stream);
 
 /* per_total -- the root of the sum tree (proportional), c_size (rank), size (uniform) or C[size-1]
  * after a fresh scan (flat), copied to *host_out.  Synchronises `stream`. */
@@ -253,7 +272,9 @@ enum {
     PER_STATE_ACTIONS = 7,  /* uint32 [capacity] */
     PER_STATE_REWARDS = 8,  /* float [capacity] */
     PER_STATE_DONES = 9,    /* uint8 [capacity] */
-    PER_STATE_COUNTERS = 10, /* uint64 [4]: sample calls, cursor, size, max raw (float bits) */
+    PER_STATE_COUNTERS = 10, /* uint64 [5]: sample calls, cursor, size, max raw (float bits), and
+                                (proportional mode) the most entries one update subtree received in
+                                the latest update that measured it (see per_update_priorities) */
     PER_STATE_RANK_ORDER = 11, /* uint32 [size at the last sample]: slots by rank (rank mode) */
     PER_STATE_CUMULATIVE = 12  /* double [size on the device]: C[i] = leaves 0..i summed, as of the
                                   last sample, per_total or per_min (flat mode) */

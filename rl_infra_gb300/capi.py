@@ -51,7 +51,7 @@ _STATE_DTYPE = {
 # every symbol include/gbper.h declares
 EXPORTS = ("per_create", "per_destroy", "per_add", "per_sample", "per_update_priorities",
            "per_total", "per_min", "per_size", "per_status_device", "per_last_error",
-           "per_read_state", "per_nleaves", "per_rank_order_noalloc")
+           "per_read_state", "per_nleaves", "per_rank_order_noalloc", "per_rank_refresh")
 
 
 class per_config(ctypes.Structure):
@@ -114,6 +114,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.per_read_state.argtypes = [vp, u32, u64, u64, vp, vp]
         L.per_read_state.restype = st
         L.per_rank_order_noalloc.argtypes = [vp, u32, vp, vp, vp]
+        L.per_rank_refresh.argtypes = [vp, vp]
+        L.per_rank_refresh.restype = st
         L.per_rank_order_noalloc.restype = st
         _lib = L
         return L
@@ -185,6 +187,11 @@ def per_last_error(h):
 
 def per_read_state(h, which, first, count, host_dst, stream):
     return load().per_read_state(h, which, first, count, host_dst, stream)
+
+
+def per_rank_refresh(h, stream):
+    """Rank mode: bring the slot order up to date (the step per_sample takes first)."""
+    return load().per_rank_refresh(h, stream)
 
 
 def per_rank_order_noalloc(d_raw, n, d_order, d_status, stream):
@@ -322,7 +329,7 @@ class ReplayBuffer:
                      PER_STATE_STATES: self.capacity * self.state_dim,
                      PER_STATE_NEXT: self.capacity * self.state_dim,
                      PER_STATE_ACTIONS: self.capacity, PER_STATE_REWARDS: self.capacity,
-                     PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 4,
+                     PER_STATE_DONES: self.capacity, PER_STATE_COUNTERS: 5,
                      PER_STATE_RANK_ORDER: self.size}[which] - first
         buf = np.empty(max(count, 1), dtype=dtype)
         s = per_read_state(self._h, which, first, count, buf.ctypes.data_as(ctypes.c_void_p),

@@ -620,6 +620,7 @@ struct RebuildArgs {
     LeafPowAlpha lp;
     int fold;          // fold batch_max_bits into the running maximum once the root is built
     double alpha;
+    CrowdRefs crowd;   // hist non-null: the fold also reports (and clears) the subtree counts
 };
 
 // binary32 -> binary64 on the integer pipe for leaves (0, +inf or normal numbers: a leaf is at
@@ -939,11 +940,26 @@ __device__ void rebuild_smem(const RebuildArgs &a, unsigned long long first, int
     }
 }
 
+// The last CTA, once the root is built (every thread of it calls this).
 __device__ __forceinline__ void rebuild_fold(const RebuildArgs &a)
 {
     if (a.fold && threadIdx.x == 0) {
         fold_running_max(a.ctl, __ldcg(&a.ctl->batch_max_bits), a.alpha);
         a.ctl->batch_max_bits = 0;
+    }
+    if (a.crowd.hist) {   // the most entries in one subtree, to the host; the counts cleared
+        __shared__ unsigned s_cmax;
+        if (threadIdx.x == 0) s_cmax = 0;
+        __syncthreads();
+        unsigned m = 0;
+        for (unsigned i = threadIdx.x; i < a.crowd.nsub; i += blockDim.x) {
+            m = max(m, __ldcg(a.crowd.hist + i));
+            a.crowd.hist[i] = 0u;
+        }
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0 && m) atomicMax(&s_cmax, m);
+        __syncthreads();
+        if (threadIdx.x == 0 && a.crowd.host) *(volatile unsigned *)a.crowd.host = s_cmax;
     }
 }
 
@@ -1099,6 +1115,7 @@ struct ScatterArgs {
     double eps, alpha;
     LeafPowAlpha lp;
     int proportional;
+    CrowdRefs crowd;   // hist non-null: count the entries per subtree
 };
 
 __global__ void __launch_bounds__(kThreads) k_upd_scatter(ScatterArgs a)
@@ -1117,6 +1134,7 @@ __global__ void __launch_bounds__(kThreads) k_upd_scatter(ScatterArgs a)
         }
         mymax = max(mymax, __float_as_uint(td_to_raw(__ldg(a.td + j), a.eps, max_prev)));
         atomicMax(a.win + i, j + 1);
+        if (a.crowd.hist) atomicAdd(a.crowd.hist + ((unsigned long long)i >> a.crowd.shift), 1u);
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(&a.ctl->err_flags, kFlagBadIndex);
     const unsigned bm = block_max_u32(mymax);
@@ -1326,6 +1344,7 @@ struct UpdArgs {
     LeafPowAlpha lp;
     int proportional;
     int cluster;   // the grid is one thread-block cluster: CTA 0 builds the top after a cluster barrier
+    unsigned *crowd_host;   // the most entries in one subtree goes here (host-mapped), or null
 };
 
 // One warp's entry lists in shared memory, `cap` entries each (36 bytes per entry).
@@ -1671,6 +1690,11 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     if (lane == 0 && mymax) atomicMax(&s_max, mymax);
     __syncthreads();
     if (tid == 0 && s_max) atomicMax(&a.ctl->batch_max_bits, s_max);
+    if (tid == 0 && a.crowd_host) {   // crowding: the most entries one of this CTA's subtrees received
+        int m = 0;
+        for (int w = 0; w < a.subs; ++w) m = max(m, s_cnt[w]);
+        if (m) atomicMax(&a.ctl->crowd_max, (unsigned)m);
+    }
 
     // 2. one warp per subtree
     const unsigned long long sub = first_sub + warp;
@@ -1793,6 +1817,8 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     } else {
         top = last_to_arrive(&a.ctl->ticket_update);
     }
+    if (top && tid == 0 && a.crowd_host)   // every CTA's count is in: to the host, and reset
+        *(volatile unsigned *)a.crowd_host = atomicExch(&a.ctl->crowd_max, 0u);
     if (top) {
         if (a.proportional && a.P > 0 && a.P <= 8) {
             // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
@@ -2065,6 +2091,7 @@ RebuildArgs rebuild_args(const TreeRefs &t, Ctl *ctl)
     a.lp = make_leaf_pow_alpha(1.0);
     a.fold = 0;
     a.alpha = 1.0;
+    a.crowd = CrowdRefs{nullptr, nullptr, 0, 0};
     return a;
 }
 
@@ -2147,7 +2174,7 @@ cudaError_t launch_update_element(const TreeRefs &t, Ctl *ctl, unsigned B, const
 cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                                   const long long *idx, const float *td, double alpha, double eps,
                                   bool proportional, int num_sms, const DirtyRefs &dirty, unsigned *win,
-                                  cudaStream_t st)
+                                  const CrowdRefs &crowd, cudaStream_t st)
 {
     ScatterArgs a;
     a.t = t;
@@ -2163,6 +2190,7 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
     a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
     const bool tree = proportional && t.D > 0 && t.S;
+    a.crowd = tree ? crowd : CrowdRefs{nullptr, nullptr, 0, 0};
     if (!tree && B <= kBlockBatch) return launch_pdl_cluster(k_upd_block, kBlockCtas, kBlockThreads, 0, st, a);
     const unsigned grid = (unsigned)std::min<unsigned long long>((B + kThreads - 1) / kThreads,
                                                                  (unsigned long long)num_sms * 8);
@@ -2177,6 +2205,7 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
         r.lp = a.lp;
         r.fold = 1;
         r.alpha = alpha;
+        r.crowd = a.crowd;
         return launch_rebuild_tree(r, st);
     }
     e = launch_pdl(k_upd_apply, grid, kThreads, 0, st, a);
@@ -2184,9 +2213,21 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
     return e;
 }
 
+int update_subtree_log(unsigned B, int D)
+{
+    // about 8 batch entries per subtree (a warp's list holds 512 or 128, so a batch concentrated
+    // on a stretch of recent slots still fits; more take the chunked path); at most 2^10
+    // subtrees, and no more than half the leaves
+    const int per = update_entries_per_subtree();
+    int P = ilog2_ceil((B + per - 1) / per);
+    P = std::min(P, kMaxTopLog);
+    return std::min(P, std::max(D - 1, 0));
+}
+
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
-                          bool proportional, int num_sms, const DirtyRefs &dirty, cudaStream_t st)
+                          bool proportional, int num_sms, const DirtyRefs &dirty, const CrowdRefs &crowd,
+                          cudaStream_t st)
 {
     (void)num_sms;
     UpdArgs a;
@@ -2202,13 +2243,8 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.eps = eps;
     a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
-    // about 8 batch entries per subtree (a warp's list holds 512 or 128, so a batch concentrated
-    // on a stretch of recent slots still fits; more take the chunked path); at most 2^10
-    // subtrees, and no more than half the leaves
-    const int per = update_entries_per_subtree();
-    int P = ilog2_ceil((B + per - 1) / per);
-    P = std::min(P, kMaxTopLog);
-    P = std::min(P, std::max(t.D - 1, 0));
+    a.crowd_host = proportional && t.S ? crowd.host : nullptr;
+    const int P = update_subtree_log(B, t.D);
     a.P = P;
     const bool large = B >= kUpdLargeBatch;
     const int warps = large ? kUpdLargeWarps : kUpdSmallWarps;

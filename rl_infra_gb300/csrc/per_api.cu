@@ -50,6 +50,9 @@ struct per_buffer {
     unsigned *win = nullptr;
     uint32_t rebuild_batch = 0;
     uint32_t element_batch = 0;   // per_config.element_batch
+    // crowding of update batches (proportional mode): a host-mapped word the update kernels
+    // write (crowd_host on the host, crowd_dev on the device) and the rebuild's subtree counts
+    unsigned *crowd_host = nullptr, *crowd_dev = nullptr, *crowd_hist = nullptr;
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // slot marks [dirty_nwords] + list, old keys [kMaxDirty each] + control [8]
     uint64_t dirty_nwords = 0;         // words of slot marks (one per slot)
@@ -98,9 +101,10 @@ RingRefs ring_of(const per_buffer *h)
 
 void free_all(per_buffer *h)
 {
+    if (h->crowd_host) cudaFreeHost(h->crowd_host);
     void *ptrs[] = {h->L, h->S, h->M, h->rank.raw, h->rank.cdf, h->rank.guide, h->rank.keys[0], h->rank.keys[1],
                     h->rank.vals[0], h->rank.vals[1], h->rank.status, h->rank.digit_hist,
-                    h->dirty_words, h->win, h->flat_mem,
+                    h->dirty_words, h->win, h->flat_mem, h->crowd_hist,
                     h->states, h->next, h->actions, h->rewards, h->dones, h->ctl};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -135,6 +139,25 @@ uint64_t update_rebuild_batch(const per_buffer *h)
     return std::max<uint64_t>(h->n / 128, 1024);
 }
 
+// Crowding: the climb serves a subtree's entries 32 distinct leaves at a time, one group after
+// the other, so a batch whose draws crowd a few subtrees (new rows entering at the running
+// maximum keep most of the mass, say) climbs for several times as long, while the level rebuild
+// does not care where the entries fall.  The most entries one subtree received in the latest
+// measured update reaches the host through a word in mapped host memory (no synchronisation: it
+// lags the enqueued calls by the few the GPU has not run yet).  From 32 (2 + leaves / 2^20)
+// entries -- measured on GB300 at 2^21 leaves and B = 512: 63 entries in a subtree climbed in
+// 22.6 us, as long as the rebuild's 22.5 us, and lasting crowding of up to 465 climbed in
+// 68-104 us against 33 us rebuilding -- the next updates below the size crossover rebuild too,
+// until the counts the rebuild keeps fall below it.  per_config.rebuild_batch other than 0 keeps
+// the choice by batch size alone.  A call captured in a CUDA graph keeps the choice made at
+// capture.
+bool update_crowded(const per_buffer *h)
+{
+    if (!h->crowd_host || h->rebuild_batch != 0) return false;
+    const unsigned last = *reinterpret_cast<volatile const unsigned *>(h->crowd_host);
+    return (uint64_t)last >= 32 * (2 + (h->n >> 20));
+}
+
 // Proportional batches of fewer entries than this propagate entry by entry (per_config.element_batch,
 // else the crossover measured on GB300).
 uint64_t update_element_batch(const per_buffer *h)
@@ -152,6 +175,9 @@ cudaError_t rank_order(per_buffer *h, cudaStream_t st)
 {
     RankWork &w = h->rank;
     cudaError_t e;
+    // nothing written since the order was made (per_rank_refresh just ran, say): it is current,
+    // and sorting it again (PER_FLAG_RANK_RESORT) would give the same order
+    if (h->order_valid && h->dirty_bound == 0 && h->order_size == h->host_size) return cudaSuccess;
     if (!h->always_resort && h->order_valid && h->dirty_bound <= kMaxDirty && h->dirty_bound * 8 <= h->host_size) {
         if (h->dirty_bound > 0) {
             e = launch_rank_merge(w, h->order_size, st);
@@ -270,7 +296,18 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
 
     bool ok = alloc(&h->ctl, 1);
     if (c.mode == PER_MODE_PROPORTIONAL) {
-        ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n) && alloc(&h->win, h->n);
+        ok = ok && alloc(&h->L, h->n) && alloc(&h->S, h->n) && alloc(&h->M, h->n) && alloc(&h->win, h->n) &&
+             alloc(&h->crowd_hist, 1024);
+        if (ok && h->D > 0) {
+            void *hp = nullptr, *dp = nullptr;
+            ok = cudaHostAlloc(&hp, 64, cudaHostAllocMapped) == cudaSuccess;
+            if (ok) {
+                h->crowd_host = static_cast<unsigned *>(hp);
+                std::memset(hp, 0, 64);
+                ok = cudaHostGetDevicePointer(&dp, hp, 0) == cudaSuccess;
+                h->crowd_dev = static_cast<unsigned *>(dp);
+            }
+        }
     } else if (c.mode == PER_MODE_FLAT) {
         // one block: C [capacity] f64, tile sums and offsets (u64 each), the result words, tile
         // minima f32, tickets
@@ -333,6 +370,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (e == cudaSuccess && h->M) e = launch_fill_mins(h->M, h->n, 0);
     if (e == cudaSuccess && h->rank.raw) e = cudaMemset(h->rank.raw, 0, capacity * sizeof(float));
     if (e == cudaSuccess && h->win) e = cudaMemset(h->win, 0, (h->S ? h->n : capacity) * sizeof(unsigned));
+    if (e == cudaSuccess && h->crowd_hist) e = cudaMemset(h->crowd_hist, 0, 1024 * sizeof(unsigned));
     if (e == cudaSuccess && h->flat_mem) e = cudaMemset(h->flat_mem, 0, h->flat_bytes);
     if (e == cudaSuccess && h->rank.status)
         e = cudaMemset(h->rank.status, 0, rank_status_words(capacity) * sizeof(unsigned long long));
@@ -479,6 +517,22 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
     return PER_OK;
 }
 
+per_status per_rank_refresh(per_buffer *h, void *stream)
+{
+    if (!h) return PER_ERR_INVALID_ARG;
+    if (h->mode != PER_MODE_RANK) return fail(h, PER_ERR_INVALID_ARG, "per_rank_refresh: rank mode only");
+    if (h->host_size == 0) return PER_OK;   // no filled slot: nothing to order
+    if (h->host_size < h->capacity) {
+        // as in per_sample: the order's length is a launch argument
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(as_stream(stream), &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+            return fail(h, PER_ERR_INVALID_ARG,
+                        "per_rank_refresh: capture a graph only once the buffer is full");
+    }
+    const cudaError_t e = rank_order(h, as_stream(stream));
+    return e == cudaSuccess ? PER_OK : cuda_fail(h, e, "per_rank_refresh launch");
+}
+
 per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx, const float *d_td,
                                  void *stream)
 {
@@ -493,17 +547,26 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
     const bool prop = h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT;
     cudaStream_t st = as_stream(stream);
     cudaError_t e;
+    const CrowdRefs none{nullptr, nullptr, 0, 0};
     if (B < update_element_batch(h)) {
         // one or two entries: each from its leaf to the root
         e = launch_update_element(tree_of(h), h->ctl, B, idx, d_td, h->alpha, h->eps, st);
     } else if (h->mode == PER_MODE_FLAT || B >= update_rebuild_batch(h)) {
         // winners scattered, then (with a tree) every level rebuilt
         e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
-                                  h->num_sms, h->rank.dirty, h->win, st);
+                                  h->num_sms, h->rank.dirty, h->win, none, st);
+    } else if (update_crowded(h)) {
+        // the same, chosen because recent batches crowded a subtree; the crowding is measured
+        // on the way, so that the choice can return to the climb
+        const int P = update_subtree_log(B, h->D);
+        const CrowdRefs c{h->crowd_dev, h->crowd_hist, h->D - P, 1u << P};
+        e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
+                                  h->num_sms, h->rank.dirty, h->win, c, st);
     } else {
-        // the dirty-ancestor climb
+        // the dirty-ancestor climb (measuring the crowding)
+        const CrowdRefs c{h->crowd_dev, nullptr, 0, 0};
         e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
-                          h->rank.dirty, st);
+                          h->rank.dirty, c, st);
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
     if (h->mode == PER_MODE_RANK) h->dirty_bound += B;
@@ -651,13 +714,14 @@ per_status per_read_state(per_buffer *h, uint32_t which, uint64_t first, uint64_
         break;
     }
     case PER_STATE_COUNTERS: {
-        if (first + count > 4) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
+        if (first > 5 || count > 5 - first) return fail(h, PER_ERR_INVALID_ARG, "per_read_state: range");
         Ctl c;
         cudaStream_t st = as_stream(stream);
         cudaError_t e = cudaMemcpyAsync(&c, h->ctl, sizeof(Ctl), cudaMemcpyDeviceToHost, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return cuda_fail(h, e, "per_read_state");
-        const uint64_t v[4] = {c.call_tix >> kCallShift, c.cursor, c.size, c.max_raw_bits};
+        const uint64_t crowd = h->crowd_host ? *reinterpret_cast<volatile const unsigned *>(h->crowd_host) : 0u;
+        const uint64_t v[5] = {c.call_tix >> kCallShift, c.cursor, c.size, c.max_raw_bits, crowd};
         std::memcpy(host_dst, v + first, count * sizeof(uint64_t));
         return PER_OK;
     }

@@ -30,7 +30,20 @@ struct Ctl {
     unsigned int batch_max_bits;      // per-call maximum raw priority, folded in by the last CTA
     unsigned int add_max_bits;
     unsigned int max_leaf_bits;       // fl32(pow(running maximum, alpha)): the leaf of a new row
-    unsigned int pad[2];
+    unsigned int crowd_max;           // the update's most entries in one subtree (reset by the top CTA)
+    unsigned int pad;
+};
+
+// Crowding of update batches (proportional mode): the most entries one update subtree receives,
+// written to host-mapped memory for the host's choice between climbing and rebuilding (see
+// per_update_priorities).  The climb measures it while filing its batch; a rebuild chosen because
+// of crowding measures it with a histogram of 2^P subtrees (P the climb's subtree count for the
+// batch) so that the choice can return to the climb.
+struct CrowdRefs {
+    unsigned *host;    // device alias of the host-mapped word; null: not measured
+    unsigned *hist;    // [1024] per-subtree counts (rebuild path), zero between calls; null: not kept
+    int shift;         // slot >> shift is the subtree (rebuild path)
+    unsigned nsub;     // subtrees (rebuild path)
 };
 
 // Fold a call's maximum raw priority into the running maximum and keep the cached leaf value
@@ -201,11 +214,15 @@ cudaError_t launch_update_element(const TreeRefs &t, Ctl *ctl, unsigned B, const
 cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                                   const long long *idx, const float *td, double alpha, double eps,
                                   bool proportional, int num_sms, const DirtyRefs &dirty, unsigned *win,
-                                  cudaStream_t st);
+                                  const CrowdRefs &crowd, cudaStream_t st);
 
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
-                          bool proportional, int num_sms, const DirtyRefs &dirty, cudaStream_t st);
+                          bool proportional, int num_sms, const DirtyRefs &dirty, const CrowdRefs &crowd,
+                          cudaStream_t st);
+
+// log2 of the update kernel's subtree count for a batch of B entries on a tree of depth D
+int update_subtree_log(unsigned B, int D);
 
 struct SampleOut {
     long long *idx;

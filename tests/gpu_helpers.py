@@ -144,7 +144,7 @@ class Pair:
     def counters(self):
         c = self.gpu.read_state(capi.PER_STATE_COUNTERS)
         return {"calls": int(c[0]), "cursor": int(c[1]), "size": int(c[2]),
-                "max_raw": float(np.array([c[3]], np.uint32).view(np.float32)[0])}
+                "max_raw": float(np.array([c[3]], np.uint32).view(np.float32)[0]), "crowd": int(c[4])}
 
     def check_counters(self):
         c = self.counters()

@@ -220,6 +220,43 @@ def test_climb_crowded_and_partly_filled(mode, size):
     p.close()
 
 
+def test_update_dispatch_follows_lasting_crowding():
+    """With the default dispatch, updates whose entries keep crowding one subtree switch to the
+    level rebuild, and the rebuild's own counts switch them back once the draws spread; the
+    trees match the oracle after every round on both paths.  Crowding: every slot prefilled at
+    priority 1e-6, each round inserts 512 rows at the running maximum (they hold nearly all the
+    mass), samples 512 and updates them with TD errors of order 1e-3.  Spread: one large update
+    gives every slot a priority of order 1, then rounds insert rows at such priorities."""
+    cap = 1 << 16                     # 2^16 leaves: crowding from 64 entries in one of 64 subtrees
+    w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
+    g = wl.rng(31, 1)
+    p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=8)
+    rows = wl.transitions(g, cap, w)
+    p.add(rows, np.full(cap, 1e-6, np.float32))
+    threshold = 32 * 2
+    seen = []
+    for rnd in range(8):
+        p.add(wl.transitions(g, 512, w), None)
+        _, want = p.sample(512, 0.4, check_rows=False)
+        p.update(want["idx"], (wl.td_errors(g, 512) * 1e-3).astype(np.float32))
+        p.check_tree()
+        seen.append(p.counters()["crowd"])
+    assert max(seen) >= threshold, seen       # the crowding was measured and seen
+    idx = np.arange(cap, dtype=np.int64)
+    p.update(idx, np.abs(wl.td_errors(g, cap)) + 0.5)   # a size-chosen rebuild: every slot near 1
+    p.check_tree()
+    for rnd in range(8):
+        p.add(wl.transitions(g, 512, w), (np.abs(wl.td_errors(g, 512)) + 0.5).astype(np.float32))
+        _, want = p.sample(512, 0.4, check_rows=False)
+        p.update(want["idx"], np.abs(wl.td_errors(g, 512)) + 0.5)
+        p.check_tree()
+        seen.append(p.counters()["crowd"])
+    assert seen[-1] < threshold, seen         # measured by the rebuild, then by the climb again
+    p.check_counters()
+    assert p.gpu.status_device() == 0
+    p.close()
+
+
 def test_equal_priorities_and_beta_zero():
     cap = 1 << 12
     w = _small("tiny", capacity=cap)
@@ -353,6 +390,33 @@ def test_rank_order_kept_between_samples(cap, fill, flags):
     p.check_counters()
     assert p.gpu.status_device() == 0
     p.close()
+
+
+def test_rank_refresh_then_sample():
+    """per_rank_refresh brings the order up to date on its own (merge after few writes, sort
+    after many); the sample that follows uses it as it is, and both match the oracle."""
+    cap = 40000
+    w = _small("rank", capacity=cap, state_dim=2, row_stride=4)
+    g = wl.rng(23, cap)
+    p = Pair(cap, 2, 4, 0.7, 1e-6, 1, seed=5)
+    prefill(p, w, g, count=cap, chunk=cap)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for rnd in range(6):
+        n_upd = 700 if rnd != 3 else cap // 4
+        idx = g.integers(0, cap, n_upd)
+        p.update(idx, wl.td_errors(g, n_upd))
+        assert capi.per_rank_refresh(p.gpu._h, st) == capi.PER_OK
+        torch.cuda.synchronize()
+        got = p.gpu.read_state(capi.PER_STATE_RANK_ORDER).astype(np.int64)
+        assert np.array_equal(got, p.orc.rank_order().astype(np.int64)), rnd
+        assert capi.per_rank_refresh(p.gpu._h, st) == capi.PER_OK   # nothing written since: no change
+        p.sample(1024, 0.5)
+        _assert_rank_order(p)
+    assert p.gpu.status_device() == 0
+    p.close()
+    q = capi.ReplayBuffer(64, 2)
+    assert capi.per_rank_refresh(q._h, st) == capi.PER_ERR_INVALID_ARG   # proportional mode
+    q.close()
 
 
 @pytest.mark.parametrize("seed", [3, 17, 31])
