@@ -521,7 +521,9 @@ def run_gpu(args, rank, world):
     cr.destroy([sa, sb])
     if buf.status_device() != 0:
         raise RuntimeError("device error flag raised during the steady-state steps")
+    crowd = int(buf.read_state(capi.PER_STATE_COUNTERS, 4, 1)[0])
     res["steady_state"] = {"value": round(aggregate_throughput(world, Ks, ss_s), 2), "unit": UNIT,
+                           "last_update_report": {"subtrees_log2": crowd >> 28, "most_entries": crowd & 0xFFFFF},
                            "ms_per_step": round(ss_s * 1e3 / Ks, 5), "steps": Ks, "after_steps": after,
                            "note": ("the same step, back to back between two events, once the ring has "
                                     "turned over (every slot rewritten since the prefill); `value` times "
@@ -667,7 +669,7 @@ def run_crowded(args):
         if buf.status_device() != 0:
             raise RuntimeError("device error flag raised during the crowded run")
         res[label] = {"value": round(K / secs, 2), "unit": UNIT, "us_per_step": round(secs * 1e6 / K, 3),
-                      "steps": K, "crowd_last": crowd}
+                      "steps": K, "last_report": {"subtrees_log2": crowd >> 28, "most_entries": crowd & 0xFFFFF}}
         buf.close()
         del staging, td, out
         torch.cuda.empty_cache()

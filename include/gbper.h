@@ -204,15 +204,16 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * entries instead mark each slot's last batch position in a winner word, write the winners and
  * rebuild every level of both trees (the post's level-synchronous rebuild, Measuring the
  * Trade Honestly: O(k + n) beats O(k log n) once k is a large share of n); the trees come out
- * the same.  Batches below that size rebuild as well while recent updates crowded one subtree:
- * the climb serves a subtree's entries 32 distinct leaves at a time, one group after the other,
- * so when one subtree (of the update's 2^P, about 8 entries each) received at least
- * 32 (2 + leaves / 2^20) entries, as when new rows entering at the running maximum keep most of
- * the mass, the next calls rebuild (measured on GB300 at 2^21 leaves, B = 512: up to 465 entries
- * in one subtree climbed in 68-104 us, rebuilt in 33 us), and return to the climb once the
- * counts the rebuild keeps fall below it.  The count reaches the host through mapped host
- * memory without a synchronisation, a few calls late; PER_STATE_COUNTERS[4] reads it.  A
- * rebuild_batch other than 0 turns this off.  Flat mode writes the leaves only (scatter path
+ * the same.  Smaller batches climb, each warp serving one subtree's entries 32 distinct leaves at
+ * a time, one group after the other, so crowding matters: the update kernels report the most
+ * entries one subtree received (with the split they used) through mapped host memory, without a
+ * synchronisation and a few calls late, and on each new report the next climbs split the tree
+ * twice as finely when a subtree held more than 32 entries (up to 2^10 subtrees) and once as
+ * coarsely again at 8 or fewer; when even the finest split leaves at least 32 (2 + leaves / 2^20)
+ * entries in a subtree, the next calls rebuild every level (measured on GB300 at 2^21 leaves,
+ * B = 512: up to 465 entries in one subtree climbed in 68-104 us, rebuilt in 33 us), until the
+ * counts the rebuild keeps fall below it.  PER_STATE_COUNTERS[4] reads the latest report.  A
+ * rebuild_batch other than 0 keeps the size rule alone.  Flat mode writes the leaves only (scatter path
  * always; the next sample sums them).  Rank mode stores raw.  Uniform mode has no
  * priorities: the call checks its arguments and changes nothing.  The running maximum
  * takes every raw priority of the batch.  Indices outside [0, size) are skipped and set
@@ -273,8 +274,10 @@ enum {
     PER_STATE_REWARDS = 8,  /* float [capacity] */
     PER_STATE_DONES = 9,    /* uint8 [capacity] */
     PER_STATE_COUNTERS = 10, /* uint64 [5]: sample calls, cursor, size, max raw (float bits), and
-                                (proportional mode) the most entries one update subtree received in
-                                the latest update that measured it (see per_update_priorities) */
+                                (proportional mode) the latest update's crowding report:
+                                bits 28-31 P, bits 20-27 a sequence number, bits 0-19 the
+                                most entries one of its 2^P subtrees received (see
+                                per_update_priorities) */
     PER_STATE_RANK_ORDER = 11, /* uint32 [size at the last sample]: slots by rank (rank mode) */
     PER_STATE_CUMULATIVE = 12  /* double [size on the device]: C[i] = leaves 0..i summed, as of the
                                   last sample, per_total or per_min (flat mode) */

@@ -959,7 +959,8 @@ __device__ __forceinline__ void rebuild_fold(const RebuildArgs &a)
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((threadIdx.x & 31) == 0 && m) atomicMax(&s_cmax, m);
         __syncthreads();
-        if (threadIdx.x == 0 && a.crowd.host) *(volatile unsigned *)a.crowd.host = s_cmax;
+        if (threadIdx.x == 0 && a.crowd.host)
+            *(volatile unsigned *)a.crowd.host = crowd_report(a.ctl, 31 - __clz(a.crowd.nsub), s_cmax);
     }
 }
 
@@ -1817,8 +1818,10 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     } else {
         top = last_to_arrive(&a.ctl->ticket_update);
     }
-    if (top && tid == 0 && a.crowd_host)   // every CTA's count is in: to the host, and reset
-        *(volatile unsigned *)a.crowd_host = atomicExch(&a.ctl->crowd_max, 0u);
+    if (top && tid == 0 && a.crowd_host) {   // every CTA's count is in: to the host, and reset
+        const unsigned m = atomicExch(&a.ctl->crowd_max, 0u);
+        *(volatile unsigned *)a.crowd_host = crowd_report(a.ctl, a.P, m);
+    }
     if (top) {
         if (a.proportional && a.P > 0 && a.P <= 8) {
             // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
@@ -2227,7 +2230,7 @@ int update_subtree_log(unsigned B, int D)
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
                           bool proportional, int num_sms, const DirtyRefs &dirty, const CrowdRefs &crowd,
-                          cudaStream_t st)
+                          int P_in, cudaStream_t st)
 {
     (void)num_sms;
     UpdArgs a;
@@ -2244,7 +2247,7 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.lp = make_leaf_pow_alpha(alpha);
     a.proportional = proportional ? 1 : 0;
     a.crowd_host = proportional && t.S ? crowd.host : nullptr;
-    const int P = update_subtree_log(B, t.D);
+    const int P = P_in >= 0 ? std::min(P_in, std::min(kMaxTopLog, std::max(t.D - 1, 0))) : update_subtree_log(B, t.D);
     a.P = P;
     const bool large = B >= kUpdLargeBatch;
     const int warps = large ? kUpdLargeWarps : kUpdSmallWarps;

@@ -53,6 +53,9 @@ struct per_buffer {
     // crowding of update batches (proportional mode): a host-mapped word the update kernels
     // write (crowd_host on the host, crowd_dev on the device) and the rebuild's subtree counts
     unsigned *crowd_host = nullptr, *crowd_dev = nullptr, *crowd_hist = nullptr;
+    unsigned crowd_seen = 0xffffffffu;   // the last report acted on
+    int upd_extra = 0;                   // the climb splits 2^upd_extra times as finely as by size
+    bool upd_rebuild = false;            // crowding chose the rebuild
     uint64_t order_size = 0, dirty_bound = 0;
     unsigned *dirty_words = nullptr;   // slot marks [dirty_nwords] + list, old keys [kMaxDirty each] + control [8]
     uint64_t dirty_nwords = 0;         // words of slot marks (one per slot)
@@ -139,23 +142,46 @@ uint64_t update_rebuild_batch(const per_buffer *h)
     return std::max<uint64_t>(h->n / 128, 1024);
 }
 
-// Crowding: the climb serves a subtree's entries 32 distinct leaves at a time, one group after
+// Crowding.  The climb serves a subtree's entries 32 distinct leaves at a time, one group after
 // the other, so a batch whose draws crowd a few subtrees (new rows entering at the running
-// maximum keep most of the mass, say) climbs for several times as long, while the level rebuild
-// does not care where the entries fall.  The most entries one subtree received in the latest
-// measured update reaches the host through a word in mapped host memory (no synchronisation: it
-// lags the enqueued calls by the few the GPU has not run yet).  From 32 (2 + leaves / 2^20)
-// entries -- measured on GB300 at 2^21 leaves and B = 512: 63 entries in a subtree climbed in
-// 22.6 us, as long as the rebuild's 22.5 us, and lasting crowding of up to 465 climbed in
-// 68-104 us against 33 us rebuilding -- the next updates below the size crossover rebuild too,
-// until the counts the rebuild keeps fall below it.  per_config.rebuild_batch other than 0 keeps
-// the choice by batch size alone.  A call captured in a CUDA graph keeps the choice made at
-// capture.
-bool update_crowded(const per_buffer *h)
+// maximum keep most of the mass, say) climbs for several times as long.  The update kernels report
+// the most entries one subtree received, with the split they used, through a word in mapped host
+// memory (no synchronisation: it lags the enqueued calls by the few the GPU has not run yet).
+// On each new report of the current split: above 32 entries, the next climbs split the tree twice
+// as finely (up to 2^10 subtrees), which spreads a crowded stretch of slots over more warps; at
+// most 8, once as coarsely again (down to the split for the batch size); and when even the finest
+// split leaves at least 32 (2 + leaves / 2^20) entries in a subtree, the next calls rebuild every
+// level (the rebuild does not care where the entries fall) until its own subtree counts fall below
+// that.  Measured on GB300 at 2^21 leaves, B = 512: 63 entries in one of 64 subtrees climbed in
+// 22.6 us, as long as a rebuild, and lasting crowding of up to 465 climbed in 68-104 us against
+// 33 us rebuilding.  per_config.rebuild_batch other than 0 keeps the size rule alone.  A call
+// captured in a CUDA graph keeps the plan made at capture.  Returns the subtree count's log2 for
+// the climb, or -1 for the rebuild.
+int update_plan(per_buffer *h, unsigned B)
 {
-    if (!h->crowd_host || h->rebuild_batch != 0) return false;
-    const unsigned last = *reinterpret_cast<volatile const unsigned *>(h->crowd_host);
-    return (uint64_t)last >= 32 * (2 + (h->n >> 20));
+    const int base = update_subtree_log(B, h->D);
+    const int pmax = std::min(kMaxUpdateLog, std::max(h->D - 1, 0));
+    if (!h->crowd_host || h->rebuild_batch != 0) return base;
+    const unsigned w = *reinterpret_cast<volatile const unsigned *>(h->crowd_host);
+    if (w != h->crowd_seen) {
+        h->crowd_seen = w;
+        const int pm = (int)(w >> 28);   // the report's split; bits 20..27 a sequence number
+        const uint64_t cnt = w & 0xfffffu;
+        const uint64_t rebuild_at = 32 * (2 + (h->n >> 20));
+        const int cur = h->upd_rebuild ? pmax : std::min(base + h->upd_extra, pmax);
+        if (w != 0 && pm == cur) {   // a report of the current plan
+            if (h->upd_rebuild) {
+                if (cnt < rebuild_at) h->upd_rebuild = false;
+            } else if (cnt > 32) {
+                if (cur < pmax) h->upd_extra = cur + 1 - base;
+                else if (cnt >= rebuild_at) h->upd_rebuild = true;
+            } else if (cnt <= 8 && h->upd_extra > 0) {
+                h->upd_extra -= 1;
+            }
+        }
+    }
+    if (h->upd_rebuild) return -1;
+    return std::min(base + std::max(h->upd_extra, 0), pmax);
 }
 
 // Proportional batches of fewer entries than this propagate entry by entry (per_config.element_batch,
@@ -555,18 +581,21 @@ per_status per_update_priorities(per_buffer *h, uint32_t B, const int64_t *d_idx
         // winners scattered, then (with a tree) every level rebuilt
         e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
                                   h->num_sms, h->rank.dirty, h->win, none, st);
-    } else if (update_crowded(h)) {
-        // the same, chosen because recent batches crowded a subtree; the crowding is measured
-        // on the way, so that the choice can return to the climb
-        const int P = update_subtree_log(B, h->D);
-        const CrowdRefs c{h->crowd_dev, h->crowd_hist, h->D - P, 1u << P};
-        e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
-                                  h->num_sms, h->rank.dirty, h->win, c, st);
     } else {
-        // the dirty-ancestor climb (measuring the crowding)
-        const CrowdRefs c{h->crowd_dev, nullptr, 0, 0};
-        e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
-                          h->rank.dirty, c, st);
+        const int P = h->mode == PER_MODE_PROPORTIONAL ? update_plan(h, B) : -1;
+        if (h->mode == PER_MODE_PROPORTIONAL && P < 0) {
+            // the rebuild, chosen because recent batches crowded even the finest split; the
+            // crowding is measured on the way (at that split), so the choice can return
+            const int pf = std::min(kMaxUpdateLog, std::max(h->D - 1, 0));
+            const CrowdRefs c{h->crowd_dev, h->crowd_hist, h->D - pf, 1u << pf};
+            e = launch_update_rebuild(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop,
+                                      h->num_sms, h->rank.dirty, h->win, c, st);
+        } else {
+            // the dirty-ancestor climb over 2^P subtrees (measuring the crowding)
+            const CrowdRefs c{h->crowd_dev, nullptr, 0, 0};
+            e = launch_update(tree_of(h), h->rank.raw, h->ctl, B, idx, d_td, h->alpha, h->eps, prop, h->num_sms,
+                              h->rank.dirty, c, P, st);
+        }
     }
     if (e != cudaSuccess) return cuda_fail(h, e, "per_update_priorities launch");
     if (h->mode == PER_MODE_RANK) h->dirty_bound += B;

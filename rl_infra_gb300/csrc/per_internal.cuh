@@ -31,11 +31,20 @@ struct Ctl {
     unsigned int add_max_bits;
     unsigned int max_leaf_bits;       // fl32(pow(running maximum, alpha)): the leaf of a new row
     unsigned int crowd_max;           // the update's most entries in one subtree (reset by the top CTA)
-    unsigned int pad;
+    unsigned int crowd_seq;           // crowding reports made
 };
 
+// A crowding report: (P << 28) | (sequence mod 256) << 20 | min(entries, 2^20 - 1).
+__device__ __forceinline__ unsigned crowd_report(Ctl *c, int P, unsigned entries)
+{
+    const unsigned seq = atomicAdd(&c->crowd_seq, 1u) & 0xffu;
+    return ((unsigned)P << 28) | (seq << 20) | min(entries, 0xfffffu);
+}
+
 // Crowding of update batches (proportional mode): the most entries one update subtree receives,
-// written to host-mapped memory for the host's choice between climbing and rebuilding (see
+// written with the subtree count's log2 P and a sequence number (crowd_report) to host-mapped
+// memory, for the
+// host's choice of the update's subtrees and between climbing and rebuilding (see
 // per_update_priorities).  The climb measures it while filing its batch; a rebuild chosen because
 // of crowding measures it with a histogram of 2^P subtrees (P the climb's subtree count for the
 // batch) so that the choice can return to the climb.
@@ -216,10 +225,13 @@ cudaError_t launch_update_rebuild(const TreeRefs &t, float *raw_store, Ctl *ctl,
                                   bool proportional, int num_sms, const DirtyRefs &dirty, unsigned *win,
                                   const CrowdRefs &crowd, cudaStream_t st);
 
+// P: log2 of the subtree count (-1: update_subtree_log(B, D)); at most 10 and D - 1.
 cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigned B,
                           const long long *idx, const float *td, double alpha, double eps,
                           bool proportional, int num_sms, const DirtyRefs &dirty, const CrowdRefs &crowd,
-                          cudaStream_t st);
+                          int P, cudaStream_t st);
+
+constexpr int kMaxUpdateLog = 10;   // the update kernel's subtree count is at most 2^10
 
 // log2 of the update kernel's subtree count for a batch of B entries on a tree of depth D
 int update_subtree_log(unsigned B, int D);

@@ -221,37 +221,42 @@ def test_climb_crowded_and_partly_filled(mode, size):
 
 
 def test_update_dispatch_follows_lasting_crowding():
-    """With the default dispatch, updates whose entries keep crowding one subtree switch to the
-    level rebuild, and the rebuild's own counts switch them back once the draws spread; the
-    trees match the oracle after every round on both paths.  Crowding: every slot prefilled at
-    priority 1e-6, each round inserts 512 rows at the running maximum (they hold nearly all the
-    mass), samples 512 and updates them with TD errors of order 1e-3.  Spread: one large update
-    gives every slot a priority of order 1, then rounds insert rows at such priorities."""
-    cap = 1 << 16                     # 2^16 leaves: crowding from 64 entries in one of 64 subtrees
+    """With the default dispatch, updates whose entries keep crowding a few slots first climb
+    over finer and finer subtree splits (2^6 up to 2^10 subtrees), then switch to the level
+    rebuild when even the finest split is crowded, and return to the climb (and to coarser
+    splits) once the draws spread; the trees match the oracle after every round, whatever the
+    path.  Crowding: every slot prefilled at priority 1e-6, each round inserts 64 rows at the
+    running maximum (they hold nearly all the mass), samples 512 and updates them with TD errors
+    of order 1e-3.  Spread: one large update gives every slot a priority of order 1, then rounds
+    insert rows at such priorities."""
+    cap = 1 << 16                     # 2^16 leaves: the finest split has 64-leaf subtrees
     w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
     g = wl.rng(31, 1)
     p = Pair(cap, 4, 4, 0.6, 1e-6, 0, seed=8)
     rows = wl.transitions(g, cap, w)
     p.add(rows, np.full(cap, 1e-6, np.float32))
-    threshold = 32 * 2
-    seen = []
-    for rnd in range(8):
-        p.add(wl.transitions(g, 512, w), None)
+    rebuild_at = 32 * 2
+    reports = []
+    for rnd in range(12):
+        p.add(wl.transitions(g, 64, w), None)
         _, want = p.sample(512, 0.4, check_rows=False)
         p.update(want["idx"], (wl.td_errors(g, 512) * 1e-3).astype(np.float32))
         p.check_tree()
-        seen.append(p.counters()["crowd"])
-    assert max(seen) >= threshold, seen       # the crowding was measured and seen
+        c = p.counters()["crowd"]
+        reports.append((c >> 28, c & 0xFFFFF))
+    assert any(P == 6 and n > 32 for P, n in reports), reports          # crowded at the size split
+    assert any(P == 10 and n >= rebuild_at for P, n in reports), reports  # still crowded at the finest
     idx = np.arange(cap, dtype=np.int64)
     p.update(idx, np.abs(wl.td_errors(g, cap)) + 0.5)   # a size-chosen rebuild: every slot near 1
     p.check_tree()
-    for rnd in range(8):
+    for rnd in range(12):
         p.add(wl.transitions(g, 512, w), (np.abs(wl.td_errors(g, 512)) + 0.5).astype(np.float32))
         _, want = p.sample(512, 0.4, check_rows=False)
         p.update(want["idx"], np.abs(wl.td_errors(g, 512)) + 0.5)
         p.check_tree()
-        seen.append(p.counters()["crowd"])
-    assert seen[-1] < threshold, seen         # measured by the rebuild, then by the climb again
+        c = p.counters()["crowd"]
+        reports.append((c >> 28, c & 0xFFFFF))
+    assert reports[-1][1] <= 32 and reports[-1][0] < 10, reports          # spread: climbing, coarser
     p.check_counters()
     assert p.gpu.status_device() == 0
     p.close()
