@@ -838,7 +838,10 @@ def run_other(args, name, resort=False, steps=None, warmup=None, op_steps=None):
     import torch
     from rl_infra_gb300 import capi
     from rl_infra_gb300 import workloads as wl
+    import dataclasses
     w = wl.WORKLOADS[name]
+    if getattr(args, "state_dim", None) is not None:   # the same tree and batch with other rows
+        w = dataclasses.replace(w, state_dim=args.state_dim, row_stride=max(args.state_dim, 0))
     torch.cuda.set_device(0)
     flags = (capi.PER_FLAG_RANK_RESORT if resort else 0) | (capi.PER_FLAG_DONES_F32 if w.mode == wl.UNIFORM else 0)
     buf = capi.ReplayBuffer(w.capacity, w.state_dim, w.alpha, w.eps, w.mode, w.row_stride, 0, flags=flags)
@@ -966,7 +969,9 @@ def run_other(args, name, resort=False, steps=None, warmup=None, op_steps=None):
         "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(total_s * 1e3 / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": OTHER[name], "l2": "flushed between steps" if flush_l2 else "not flushed",
+        "config": {"workload": OTHER[name] + (f" (rows of {w.state_dim} floats)" if getattr(args, "state_dim", None)
+                                              is not None else ""),
+                   "l2": "flushed between steps" if flush_l2 else "not flushed",
                    "wall_s_timed_loop": round(wall, 4)},
         "step_us_median": round(float(np.median(step_ms)) * 1e3, 3),
         "ops_median_us": {k: round(v[0] * 1e3, 3) for k, v in ops.items()},
@@ -1154,6 +1159,9 @@ def main():
     ap.add_argument("--workload", default="apex",
                     choices=["apex", "tiny", "dqn", "stress", "rank", "uniform", "crowded"],
                     help="apex is the headline workload; the others are measured with --workload")
+    ap.add_argument("--state-dim", type=int, default=None,
+                    help="with --workload other than apex: rows of this many floats (the same tree and "
+                         "batch; small rows keep a profiler capture of the tree kernels small)")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip timing the rounds captured as one CUDA graph")
     ap.add_argument("--l2", default="flush", choices=["flush", "warm"],

@@ -209,8 +209,8 @@ per_status per_sample(per_buffer *h, uint32_t B, float beta, int64_t *d_idx, flo
  * entries one subtree received (with the split they used) through mapped host memory, without a
  * synchronisation and a few calls late, and on each new report the next climbs split the tree
  * twice as finely when a subtree held more than 32 entries (up to 2^10 subtrees) and once as
- * coarsely again at 8 or fewer; when even the finest split leaves at least 32 (2 + leaves / 2^20)
- * entries in a subtree, the next calls rebuild every level (measured on GB300 at 2^21 leaves,
+ * coarsely again at 8 or fewer; when even the finest split leaves at least
+ * 32 max(2, 5/6 leaves / 2^20) entries in a subtree, the next calls rebuild every level (measured on GB300 at 2^21 leaves,
  * B = 512: up to 465 entries in one subtree climbed in 68-104 us, rebuilt in 33 us), until the
  * counts the rebuild keeps fall below it.  PER_STATE_COUNTERS[4] reads the latest report.  A
  * rebuild_batch other than 0 keeps the size rule alone.  Flat mode writes the leaves only (scatter path

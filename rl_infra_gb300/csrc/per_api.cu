@@ -150,9 +150,9 @@ uint64_t update_rebuild_batch(const per_buffer *h)
 // On each new report of the current split: above 32 entries, the next climbs split the tree twice
 // as finely (up to 2^10 subtrees), which spreads a crowded stretch of slots over more warps; at
 // most 8, once as coarsely again (down to the split for the batch size); and when even the finest
-// split leaves at least 32 (2 + leaves / 2^20) entries in a subtree, the next calls rebuild every
-// level (the rebuild does not care where the entries fall) until its own subtree counts fall below
-// that.  Measured on GB300 at 2^21 leaves, B = 512: 63 entries in one of 64 subtrees climbed in
+// split leaves at least 32 max(2, 5/6 leaves / 2^20) entries in a subtree (as many groups of 32
+// as a rebuild's time buys), the next calls rebuild every level (the rebuild does not care where
+// the entries fall) until its own subtree counts fall below that.  Measured on GB300 at 2^21 leaves, B = 512: 63 entries in one of 64 subtrees climbed in
 // 22.6 us, as long as a rebuild, and lasting crowding of up to 465 climbed in 68-104 us against
 // 33 us rebuilding.  per_config.rebuild_batch other than 0 keeps the size rule alone.  A call
 // captured in a CUDA graph keeps the plan made at capture.  Returns the subtree count's log2 for
@@ -167,7 +167,9 @@ int update_plan(per_buffer *h, unsigned B)
         h->crowd_seen = w;
         const int pm = (int)(w >> 28);   // the report's split; bits 20..27 a sequence number
         const uint64_t cnt = w & 0xfffffu;
-        const uint64_t rebuild_at = 32 * (2 + (h->n >> 20));
+        // a rebuild costs about 14 us + 4 ns a leaf, each further group of 32 leaves of a climb
+        // about 5 us (measured on GB300): rebuild once a subtree needs more groups than that
+        const uint64_t rebuild_at = 32 * std::max<uint64_t>(2, (h->n >> 20) * 5 / 6);
         const int cur = h->upd_rebuild ? pmax : std::min(base + h->upd_extra, pmax);
         if (w != 0 && pm == cur) {   // a report of the current plan
             if (h->upd_rebuild) {
