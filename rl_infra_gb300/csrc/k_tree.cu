@@ -1303,25 +1303,34 @@ __global__ void k_upd_finish(Ctl *c, double alpha)
 // Priority update: last-writer-wins scatter + dirty-ancestor upsweep, one launch.
 // The tree below depth P is cut into 2^P subtrees and each subtree belongs to one warp (a CTA
 // holds 4 or 16 of them), so nothing below depth P needs more than warp synchronisation:
-//   1. every CTA reads the whole batch, coalesced, and files each entry of its subtrees under
-//      the subtree's warp (while the ring fills, the subtrees split only the part that holds
-//      filled slots);
-//   2. each warp sorts its entries by (leaf, batch position), in registers up to 32 and in
-//      shared memory beyond, keeps the last position of every leaf and climbs its subtree 32
-//      distinct leaves at a time: one round of loads fetches every sibling a lane owns up to
-//      16 levels, the plan (which lane adds at which height, which takes a dirty sibling's
-//      value from another lane) comes from owner ballots while the loads are in flight, and a
-//      chain of binary64 adds carries nothing else;
-//   3. the last CTA to arrive (or CTA 0 after a cluster barrier) rebuilds the 2^P - 1 nodes
-//      above the subtree roots, and the spine above them while the ring fills, and folds the
-//      batch maximum into the running maximum.
+//   1. every CTA reads the whole batch, coalesced (the first entries of each thread in flight
+//      with the control words), and files each entry of its subtrees under the subtree's warp
+//      (while the ring fills, the subtrees split only the part that holds filled slots);
+//   2. each warp starts copying, for each of its entries, the siblings on the entry's path into
+//      shared memory (cp.async, up to 16 levels), computes the entries' leaf values meanwhile,
+//      sorts them by (leaf, batch position) -- in registers up to 32, in shared memory beyond --
+//      keeps the last position of every leaf, and climbs its subtree 32 distinct leaves at a
+//      time: joins of two paths are planned from one warp OR, and a chain of binary64 adds, one
+//      height per loop iteration, carries nothing else;
+//   3. the top: a grid of at most 16 CTAs runs as one cluster, and every warp writes its
+//      subtree's root (and every CTA its batch maximum and most entries per subtree) into CTA
+//      0's shared memory; after one cluster barrier CTA 0 builds the 2^P - 1 nodes above the
+//      roots from there.  A larger grid uses an arrival ticket, and the last CTA reads the
+//      roots back from L2.  The top CTA then rebuilds the spine above them while the ring
+//      fills, and folds the batch maximum into the running maximum.
 // A warp whose subtree receives more entries than its shared-memory list holds applies the
 // batch in position order 32 entries at a time (later chunks overwrite earlier ones, so the
 // last writer wins) and then rebuilds its whole subtree.
+//
+// Measured on GB300 (per-stage clock stamps, apex batch): the kernel is a chain of dependent
+// steps in few warps, where each instruction of straight-line code costs about twice its warm
+// time because it is fetched once per launch (a binary64 add alone takes 64 cycles); hence the
+// loops over heights and levels rather than unrolled code, and no memory round trip left between
+// the subtree climbs and the top (no fence, no reload of the roots).
 // ------------------------------------------------------------------------------------------
 // Two CTA shapes: 4 warps with lists of 512 entries (batches below 4096 entries), or 16 warps
 // with lists of 128 (larger batches: a quarter as many CTAs read the whole batch, each in one
-// round).  Both take the same shared memory.
+// round).  Both take the same list space; each warp has its own sibling prefetch area.
 constexpr int kUpdMaxWarps = 16;
 constexpr int kUpdMaxThreads = 32 * kUpdMaxWarps;
 constexpr int kUpdSmallWarps = 4, kUpdSmallCap = 512;
@@ -1377,7 +1386,7 @@ __device__ __forceinline__ WarpLists warp_lists(unsigned char *smem, int w, int 
 constexpr size_t kTopHeapBytes = (size_t)(2 << kMaxTopLog) * 12;  // the last CTA's top levels
 constexpr size_t kListsBytes = kListBytesPerEntry * (kUpdSmallWarps * kUpdSmallCap > kUpdLargeWarps * kUpdLargeCap
                                                          ? kUpdSmallWarps * kUpdSmallCap : kUpdLargeWarps * kUpdLargeCap);
-constexpr size_t kUpdSmemBytes = kListsBytes > kTopHeapBytes ? kListsBytes : kTopHeapBytes;
+constexpr int kClusterRoots = 256;   // subtrees of a one-cluster grid: at most 16 CTAs of 16 warps
 
 __device__ __forceinline__ void warp_bitonic_kv(unsigned long long *keys, unsigned *pay, int m2, int lane)
 {
@@ -1424,25 +1433,39 @@ __device__ __forceinline__ void warp_sort_n(unsigned long long &key, unsigned &p
     }
 }
 
+// The same for one 32-bit key per lane, without a payload (keys are distinct).
+template <int N>
+__device__ __forceinline__ void warp_sort_n32(unsigned &key, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const bool up = (lane & size) == 0;
+            const bool lower = (lane & stride) == 0;
+            const bool take = lower ? (up ? ok < key : ok > key) : (up ? ok > key : ok < key);
+            if (take) key = ok;
+        }
+    }
+}
+
 // Climb one warp's subtree when it has U <= 32 distinct leaves, one per lane, ascending: lane u
-// holds local leaf li (leaf - base, base = the subtree's first leaf) and its raw priority.
+// holds local leaf li (leaf - base, base = the subtree's first leaf) and its leaf value.
 //
 // Let J be the height at which a lane's path joins the previous lane's (the bit length of the
 // two local leaves' xor; lane 0 has none).  At height h the lane owns its node when h < J (or it
-// is lane 0), and the owners of one height are in leaf order, so the next owner after a lane is
-// the next set bit of the height's owner ballot.  The owner of a left child whose right sibling
-// is owned too (that owner has J = h + 1) adds the sibling owner's value, taken by a shuffle; the
-// owner of a right child whose left sibling is owned stops; every other owner adds its clean
-// sibling, loaded up front with all the others in one round.
+// is lane 0), and the owners of one height are in leaf order.  At a height where no lane has
+// J = h + 1 no two owned nodes are siblings, so every owner adds its clean sibling.  At a height
+// where some lane has J = h + 1 (a join), that lane's node is the right sibling of the node of the
+// previous owner of the height: the previous owner adds the joining lane's value, taken by a
+// shuffle, and the joining lane stops.  The joins are the set bits of one warp OR of 2^(J - 1), so
+// the ballots and shuffles run at those heights only (at most U - 1 of them).
 //
-// Everything but the values is known before the first add: the owner ballots of all heights,
-// which lanes add at each height and where a dirty sibling's value comes from.  So the chain of
-// binary64 adds carries nothing else: a lane that does not add at a height adds +0 (every value
-// is >= +0, and x + 0 = x), a shuffle and a select sit on it only at heights where two paths
-// join, and the nodes are stored after the chain.  (Binary64 addition is commutative, so one
-// operand order serves left and right children alike.)  Node indices inside the subtree are
-// 32-bit; no level needs shared memory or a warp barrier.
-constexpr int kMaxClimb = 16;  // levels whose siblings are loaded in the single prefetch round
+// The siblings were copied into the warp's prefetch area (prefetch_siblings) while the power and
+// the sort ran: the chain of binary64 adds reads them from shared memory and carries nothing else.
+// Each owner stores the node it computes; lane 0 ends with the subtree's root.
+constexpr int kMaxClimb = 16;  // levels whose siblings are copied in the single prefetch round
 
 struct ClimbLane {
     unsigned li;      // local leaf index
@@ -1485,100 +1508,131 @@ __device__ __forceinline__ void climb_level(const TreeRefs &t, unsigned long lon
     }
 }
 
-template <int W>
-__device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane, unsigned long long base,
-                                unsigned li, float raw, const LeafPowAlpha &alpha, const LeafPowTables &tb)
+// A warp's sibling prefetch area in shared memory: for each of 32 slots, the siblings of a leaf's
+// path at heights 1 .. kMaxClimb - 1 (S and M, height-major so that the 32 slots of one height are
+// consecutive) and its sibling leaf.
+struct SibArea {
+    double *S;   // [kMaxClimb][32]
+    float *M;    // [kMaxClimb][32]
+    float *L;    // [32]
+};
+constexpr size_t kSibBytesPerWarp = (size_t)kMaxClimb * 32 * 8 + (size_t)kMaxClimb * 32 * 4 + 32 * 4;
+
+// Dynamic shared memory of the update kernel: the entry lists (whose space the last CTA reuses for
+// the top levels), then one prefetch area per warp.
+static_assert(kTopHeapBytes <= kListsBytes, "top levels reuse the lists");
+constexpr size_t update_smem_bytes(int warps) { return kListsBytes + (size_t)warps * kSibBytesPerWarp; }
+
+__device__ __forceinline__ SibArea sib_area(unsigned char *base, int w)
 {
+    unsigned char *b = base + (size_t)w * kSibBytesPerWarp;
+    SibArea s;
+    s.S = reinterpret_cast<double *>(b);
+    s.M = reinterpret_cast<float *>(b + (size_t)kMaxClimb * 32 * 8);
+    s.L = s.M + kMaxClimb * 32;
+    return s;
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem)
+{
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async8(void *smem, const void *gmem)
+{
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// Waits for this thread's copies; the warp barrier then makes every lane's copies visible to the
+// whole warp.
+__device__ __forceinline__ void cp_async_wait_warp()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+}
+
+// Starts the copies (no wait) of the siblings on the path of leaf node v0 (= n + leaf) at
+// heights 0 .. hpre - 1 into slot `slot` of the area.
+__device__ __forceinline__ void prefetch_siblings(const TreeRefs &t, unsigned long long v0, int hpre,
+                                                  const SibArea &p, int slot)
+{
+    cp_async4(p.L + slot, t.L + ((v0 ^ 1ull) - t.n));
+#pragma unroll 1
+    for (int h = 1; h < hpre; ++h) {
+        const unsigned long long sib = (v0 >> h) ^ 1ull;
+        cp_async8(p.S + h * 32 + slot, t.S + sib);
+        cp_async4(p.M + h * 32 + slot, t.M + sib);
+    }
+}
+
+// The climb (see above).  Lane u < U: local leaf li, leaf value lv, siblings complete in slot
+// `slot` of the area.  Writes the leaves and every recomputed node; lane 0 returns the subtree's
+// root (height `shift`) in *rs / *rm.
+template <int W>
+__device__ void warp_climb(const TreeRefs &t, int U, int shift, int lane, unsigned long long base,
+                           unsigned li, float lv, const SibArea &p, int slot, double *rs, float *rm)
+{
+    constexpr unsigned kAll = 0xffffffffu;
     ClimbLane c;
     c.li = li;
     c.have = lane < U;
-    const unsigned prev = __shfl_up_sync(0xffffffffu, li, 1);
+    const unsigned prev = __shfl_up_sync(kAll, li, 1);
     c.J = (c.have && lane > 0) ? 32 - __clz(prev ^ li) : 64;
-    const unsigned long long top = t.n + base;   // node index of the subtree's first leaf
+    const unsigned long long v0 = t.n + base + li;
     const int hpre = min(shift, kMaxClimb);
-
-    // one round of loads: the sibling at every height this lane owns
-    double ps[kMaxClimb];
-    float pmn[kMaxClimb];
-    float sib_leaf = 0.0f;
-#pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h) {
-        ps[h] = 0.0;
-        pmn[h] = 0.0f;
-        if (c.have && h < hpre && (lane == 0 || c.J > h)) {
-            const unsigned long long sib = (top >> h) + ((li >> h) ^ 1u);
-            if (h == 0) {
-                sib_leaf = t.L[sib - t.n];
-            } else {
-                ps[h] = t.S[sib];
-                pmn[h] = t.M[sib];
-            }
-        }
-    }
     c.vs = 0.0;
     c.vm = 0.0f;
     if (c.have) {
-        const float lv = leaf_of(raw, alpha, tb);
         t.L[base + li] = lv;
         c.vs = (double)lv;
         c.vm = leaf_min_value(lv);
     }
-    // the plan, while the loads are in flight: owner ballots of every height, then per height
-    // whether this lane adds (add) and whether it takes a shuffled value (dty) from lane src
-    unsigned om[kMaxClimb + 1];
-#pragma unroll
-    for (int h = 0; h <= kMaxClimb; ++h) om[h] = __ballot_sync(0xffffffffu, c.have && (lane == 0 || c.J > h));
+    const unsigned joins = __reduce_or_sync(kAll, (c.have && lane > 0 && c.J <= hpre) ? 1u << (c.J - 1) : 0u);
     const unsigned above = ~((2u << lane) - 1u);
-    unsigned add = 0, dty = 0, join = 0;
-    int src[kMaxClimb];
-#pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h) {
-        const bool own = (om[h] >> lane) & 1u;
-        const bool odd = (li >> h) & 1u;
-        const int R = __ffs(om[h] & above) - 1;
-        const bool d = own && !odd && R >= 0 && !((om[h + 1] >> R) & 1u);
-        src[h] = d ? R : lane;
-        if (h < hpre && own && (!odd || ((om[h + 1] >> lane) & 1u))) add |= 1u << h;
-        if (h < hpre && d) dty |= 1u << h;
-        if (om[h] != om[h + 1] && (om[h] & ~om[h + 1] & ~1u)) join |= 1u << h;   // some lane has J = h + 1
-    }
-    // every prefetched sibling is complete here, in one wait after the power and the plan: the
-    // compiler may otherwise sink each load to its first use and pay one round trip per level
-#pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h) asm volatile("" ::"d"(ps[h]), "f"(pmn[h]));
-    asm volatile("" ::"f"(sib_leaf));
-    ps[0] = (double)sib_leaf;
-    pmn[0] = leaf_min_value(sib_leaf);
     const float kInf = __int_as_float(0x7f800000);
-    // the chain; ps[h] / pmn[h] then hold the parent's value at height h + 1 for the store
-#pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h) {
-        if (h < hpre) {
-            const bool a = (add >> h) & 1u;
-            double as = a ? ps[h] : 0.0;
-            float am = a ? pmn[h] : kInf;
-            if ((join >> h) & 1u) {
-                const double e = __shfl_sync(0xffffffffu, c.vs, src[h]);
-                const float em = __shfl_sync(0xffffffffu, c.vm, src[h]);
-                if ((dty >> h) & 1u) {
-                    as = e;
-                    am = em;
-                }
+    // The chain, one height per iteration: run once per launch, a loop's few instructions are
+    // fetched once where unrolled heights would each be fetched (measured on GB300: about half the
+    // time per height).  A lane that does not add at a height adds +0 and takes the minimum with
+    // +inf (every value is >= +0); the next height's sibling is read while this one is added.
+    float lsib = p.L[slot];
+    double ns = (double)lsib;
+    float nm = leaf_min_value(lsib);
+#pragma unroll 1
+    for (int h = 0; h < hpre; ++h) {
+        double as = ns;
+        float am = nm;
+        if (h + 1 < hpre) {
+            ns = p.S[(h + 1) * 32 + slot];
+            nm = p.M[(h + 1) * 32 + slot];
+        }
+        const bool own = c.have && (lane == 0 || c.J > h);
+        bool add = own;
+        if ((joins >> h) & 1u) {
+            const bool right = own && lane > 0 && c.J == h + 1;   // joins the previous owner at h + 1
+            const unsigned ob = __ballot_sync(kAll, own);
+            const unsigned rb = __ballot_sync(kAll, right);
+            const int R = __ffs(ob & above) - 1;                // next owner of height h
+            const int src = R < 0 ? lane : R;
+            const double e = __shfl_sync(kAll, c.vs, src);
+            const float em = __shfl_sync(kAll, c.vm, src);
+            if (own && R >= 0 && ((rb >> R) & 1u)) {
+                as = e;
+                am = em;
             }
-            c.vs = c.vs + as;
-            c.vm = fmin_tree(c.vm, am);
-            ps[h] = c.vs;
-            pmn[h] = c.vm;
+            add = own && !right;
+        }
+        c.vs = c.vs + (add ? as : 0.0);
+        c.vm = fmin_tree(c.vm, add ? am : kInf);
+        if (add) {
+            const unsigned long long node = v0 >> (h + 1);
+            t.S[node] = c.vs;
+            t.M[node] = c.vm;
         }
     }
-#pragma unroll
-    for (int h = 0; h < kMaxClimb; ++h)
-        if (h < hpre && ((add >> h) & 1u)) {
-            const unsigned long long node = (top >> (h + 1)) + ((li >> h) >> 1);
-            t.S[node] = ps[h];
-            t.M[node] = pmn[h];
-        }
     // heights beyond the prefetch round (subtrees deeper than kMaxClimb levels), W per round
+    const unsigned long long top = t.n + base;
     for (int h0 = hpre; h0 < shift; h0 += W) {
         double qs[W];
         float qm[W];
@@ -1596,30 +1650,38 @@ __device__ void warp_climb_regs(const TreeRefs &t, int U, int shift, int lane, u
 #pragma unroll
         for (int w = 0; w < W; ++w) {
             const int h = h0 + w;
-            const bool merge = __any_sync(0xffffffffu, c.have && lane > 0 && c.J == h + 1);
+            const bool merge = __any_sync(kAll, c.have && lane > 0 && c.J == h + 1);
             if (h < shift) climb_level(t, top, h, merge, lane, c, qs[w], qm[w]);
         }
     }
+    *rs = c.vs;
+    *rm = c.vm;
 }
 
 // Files the batch entries of this CTA's subtrees under their warp's list (slot order is the
-// order of arrival; the sort below restores batch order).  Returns this thread's largest raw
-// priority among the filed entries.
+// order of arrival; the sort below restores batch order).  Thread t takes entries t + u blockDim,
+// U at a time; the first U arrive preloaded.  Returns this thread's largest raw priority among the
+// filed entries.
+template <int U>
+__device__ __forceinline__ void load_entries(const UpdArgs &a, unsigned j0, long long (&iv)[U], float (&tv)[U])
+{
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const unsigned j = j0 + u * blockDim.x;
+        iv[u] = j < a.B ? __ldg(a.idx + j) : -2;
+        tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
+    }
+}
+
 template <int U>
 __device__ __forceinline__ unsigned file_batch(const UpdArgs &a, unsigned char *lists, int *s_cnt,
                                                unsigned long long first_sub, int shift,
-                                               unsigned long long size, float max_prev)
+                                               unsigned long long size, float max_prev,
+                                               long long (&iv)[U], float (&tv)[U])
 {
     unsigned mymax = 0;
     for (unsigned j0 = threadIdx.x; j0 < a.B; j0 += U * blockDim.x) {
-        long long iv[U];
-        float tv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const unsigned j = j0 + u * blockDim.x;
-            iv[u] = j < a.B ? __ldg(a.idx + j) : -2;
-            tv[u] = j < a.B ? __ldg(a.td + j) : 0.0f;
-        }
+        if (j0 != threadIdx.x) load_entries<U>(a, j0, iv, tv);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const unsigned j = j0 + u * blockDim.x;
@@ -1651,14 +1713,23 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     unsigned char *lists = smem_raw;
+    unsigned char *sibs = smem_raw + kListsBytes;   // the warps' sibling prefetch areas
     __shared__ int s_cnt[kUpdMaxWarps];
     __shared__ unsigned s_max;
     __shared__ LeafPowTables s_lp;
+    // one-cluster grids: CTA 0 receives every subtree's root and every CTA's batch maximum and
+    // most entries per subtree here (distributed shared memory), one slot per writer
+    __shared__ double s_rootS[2 * kClusterRoots];   // a heap: the roots at [2^P, 2^(P+1))
+    __shared__ float s_rootM[2 * kClusterRoots];
+    __shared__ unsigned s_cbmax[16], s_ccnt[16];
     {   // the power's tables (constant since the library loaded), staged while the batch is read
         const unsigned *src = reinterpret_cast<const unsigned *>(&g_leafpow);
         unsigned *dst = reinterpret_cast<unsigned *>(&s_lp);
         for (int i = threadIdx.x; i < (int)(sizeof(LeafPowTables) / 4); i += blockDim.x) dst[i] = src[i];
     }
+    // first half of a cluster barrier: the second half, before the first write into CTA 0's
+    // shared memory, ensures every CTA of the cluster has started
+    if (a.cluster) cluster_arrive_relaxed();
     pdl_wait();
     pdl_release();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1675,7 +1746,21 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     const int shift = D - a.P - skip;
     const unsigned long long nsub = 1ull << a.P;
     const unsigned long long first_sub = (unsigned long long)blockIdx.x * a.subs;
-    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    // the first U entries of this thread (indices and TD errors), in flight with the control words
+    const unsigned per_round = (a.B + blockDim.x - 1) / blockDim.x;
+    long long iv4[4], iv8[8], iv16[16];
+    float tv4[4], tv8[8], tv16[16];
+    if (per_round <= 4) load_entries<4>(a, tid, iv4, tv4);
+    else if (per_round <= 8) load_entries<8>(a, tid, iv8, tv8);
+    else load_entries<16>(a, tid, iv16, tv16);
+    const unsigned max_prev_bits = a.ctl->max_raw_bits;
+    const float max_prev = __uint_as_float(max_prev_bits);
+    // the crowding report's sequence number, taken now so that the top CTA does not wait for it
+    // (the top CTA's report, the maximum's fold and the resets run on a thread of warp 1, beside
+    // warp 0's rebuild of the top levels)
+    const int reporter = blockDim.x > 32 ? 32 : 0;
+    unsigned crowd_seq = 0;
+    if (a.cluster && a.crowd_host && blockIdx.x == 0 && tid == reporter) crowd_seq = atomicAdd(&a.ctl->crowd_seq, 1u);
     if (tid < kUpdMaxWarps) s_cnt[tid] = 0;
     if (tid == 0) s_max = 0;
     __syncthreads();
@@ -1683,15 +1768,14 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     // 1. file this CTA's entries under their subtree's warp (every CTA reads the whole batch:
     //    indices and TD errors together, 4, 8 or 16 per thread in flight as the batch grows)
     unsigned mymax = 0;
-    const unsigned per_round = (a.B + blockDim.x - 1) / blockDim.x;
-    if (per_round <= 4) mymax = file_batch<4>(a, lists, s_cnt, first_sub, shift, size, max_prev);
-    else if (per_round <= 8) mymax = file_batch<8>(a, lists, s_cnt, first_sub, shift, size, max_prev);
-    else mymax = file_batch<16>(a, lists, s_cnt, first_sub, shift, size, max_prev);
+    if (per_round <= 4) mymax = file_batch<4>(a, lists, s_cnt, first_sub, shift, size, max_prev, iv4, tv4);
+    else if (per_round <= 8) mymax = file_batch<8>(a, lists, s_cnt, first_sub, shift, size, max_prev, iv8, tv8);
+    else mymax = file_batch<16>(a, lists, s_cnt, first_sub, shift, size, max_prev, iv16, tv16);
     for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
     if (lane == 0 && mymax) atomicMax(&s_max, mymax);
     __syncthreads();
-    if (tid == 0 && s_max) atomicMax(&a.ctl->batch_max_bits, s_max);
-    if (tid == 0 && a.crowd_host) {   // crowding: the most entries one of this CTA's subtrees received
+    if (!a.cluster && tid == 0 && s_max) atomicMax(&a.ctl->batch_max_bits, s_max);
+    if (!a.cluster && tid == 0 && a.crowd_host) {   // crowding: the most entries one of this CTA's subtrees received
         int m = 0;
         for (int w = 0; w < a.subs; ++w) m = max(m, s_cnt[w]);
         if (m) atomicMax(&a.ctl->crowd_max, (unsigned)m);
@@ -1700,7 +1784,15 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     // 2. one warp per subtree
     const unsigned long long sub = first_sub + warp;
     const int m = s_cnt[warp];
-    if (warp < a.subs && sub < nsub && m > 0) {
+    const bool has_sub = warp < a.subs && sub < nsub;
+    const unsigned long long root = (n + (sub << shift)) >> shift;   // the subtree's root node
+    double root_s = 0.0;   // lane 0: the subtree root's value once this warp is done
+    float root_m = 0.0f;
+    if (a.cluster && a.proportional && has_sub && m == 0 && lane == 0) {   // untouched: as stored
+        root_s = a.t.S[root];
+        root_m = a.t.M[root];
+    }
+    if (has_sub && m > 0) {
         const WarpLists wl = warp_lists(lists, warp, a.cap);
         const unsigned long long base = sub << shift;
         if (m > a.cap) {
@@ -1733,27 +1825,65 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     }
                     __syncwarp();
                 }
+                if (lane == 0) {   // lane 0 computed the root last
+                    root_s = a.t.S[root];
+                    root_m = a.t.M[root];
+                }
             }
         } else if (m <= 32) {
-            // one entry per lane: sort in registers, keep the last position of each leaf, and
-            // move the u-th surviving leaf to lane u
-            unsigned long long key = lane < m ? wl.keys[lane] : ~0ull;
-            unsigned pay = lane < m ? wl.pay[lane] : 0u;
-            if (m <= 8) warp_sort_n<8>(key, pay, lane);
-            else if (m <= 16) warp_sort_n<16>(key, pay, lane);
-            else warp_sort_n<32>(key, pay, lane);
-            const unsigned long long nxt = __shfl_down_sync(0xffffffffu, key, 1);
-            const bool win = lane < m && (lane == m - 1 || (nxt >> a.pb) != (key >> a.pb));
-            const unsigned bal = __ballot_sync(0xffffffffu, win);
-            const int U = __popc(bal);
-            const float myraw = lane < m ? wl.rawv[pay] : 0.0f;
-            const int from = lane < U ? (int)__fns(bal, 0, lane + 1) : 0;
-            const unsigned long long k_from = __shfl_sync(0xffffffffu, key, from);
-            const float raw = __shfl_sync(0xffffffffu, myraw, from);
-            const unsigned li = (unsigned)(k_from >> a.pb);   // local leaf index
+            // one entry per lane (entry l of the list on lane l): the copies of its path's
+            // siblings start and its leaf value is computed, then the entries are sorted in
+            // registers, the last position of each leaf kept, and the u-th surviving leaf moved to
+            // lane u, which climbs with the siblings its entry's lane copied
+            const bool have = lane < m;
+            unsigned long long key = have ? wl.keys[lane] : ~0ull;
+            const float raw_e = have ? wl.rawv[lane] : 0.0f;   // pay[l] = l before the sort
+            const SibArea sp = sib_area(sibs, warp);
+            float lv_e = 0.0f;
+            if (a.proportional && have) {
+                prefetch_siblings(a.t, n + base + (key >> a.pb), min(shift, kMaxClimb), sp, lane);
+                lv_e = leaf_of(raw_e, a.lp, s_lp);
+            }
+            // the sort key (leaf, batch position) with the list position beside it: one 32-bit
+            // word when the three fit (then the position travels in the low 5 bits), else 64 bits
+            // with a payload
+            unsigned li, U;
+            int slot;
+            if (shift + a.pb + 5 <= 32) {
+                unsigned k32 = have ? ((unsigned)key << 5) | (unsigned)lane : ~0u;
+                if (m <= 8) warp_sort_n32<8>(k32, lane);
+                else if (m <= 16) warp_sort_n32<16>(k32, lane);
+                else warp_sort_n32<32>(k32, lane);
+                const unsigned sh = a.pb + 5;
+                const unsigned nxt = __shfl_down_sync(0xffffffffu, k32, 1);
+                const bool win = lane < m && (lane == m - 1 || (nxt >> sh) != (k32 >> sh));
+                const unsigned bal = __ballot_sync(0xffffffffu, win);
+                U = __popc(bal);
+                const int from = lane < (int)U ? (int)__fns(bal, 0, lane + 1) : 0;
+                const unsigned k_from = __shfl_sync(0xffffffffu, k32, from);
+                li = k_from >> sh;
+                slot = (int)(k_from & 31u);
+            } else {
+                unsigned pay = lane;
+                if (m <= 8) warp_sort_n<8>(key, pay, lane);
+                else if (m <= 16) warp_sort_n<16>(key, pay, lane);
+                else warp_sort_n<32>(key, pay, lane);
+                const unsigned long long nxt = __shfl_down_sync(0xffffffffu, key, 1);
+                const bool win = lane < m && (lane == m - 1 || (nxt >> a.pb) != (key >> a.pb));
+                const unsigned bal = __ballot_sync(0xffffffffu, win);
+                U = __popc(bal);
+                const int from = lane < (int)U ? (int)__fns(bal, 0, lane + 1) : 0;
+                const unsigned long long k_from = __shfl_sync(0xffffffffu, key, from);
+                slot = (int)__shfl_sync(0xffffffffu, pay, from);   // the entry's list position
+                li = (unsigned)(k_from >> a.pb);                    // local leaf index
+            }
+            const float raw = __shfl_sync(0xffffffffu, raw_e, slot);
+            const float lv = __shfl_sync(0xffffffffu, lv_e, slot);
             if (a.proportional) {
-                warp_climb_regs<W>(a.t, U, shift, lane, base, lane < U ? li : 0u, raw, a.lp, s_lp);
-            } else if (lane < U) {
+                cp_async_wait_warp();
+                warp_climb<W>(a.t, (int)U, shift, lane, base, lane < (int)U ? li : 0u, lv, sp,
+                              lane < (int)U ? slot : 0, &root_s, &root_m);
+            } else if (lane < (int)U) {
                 const float old = a.raw_store[base + li];
                 a.raw_store[base + li] = raw;
                 mark_dirty(a.dirty, base + li, old);
@@ -1796,12 +1926,18 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 // 32 distinct leaves at a time in ascending order, each group after the previous
                 // one has stored its nodes: a later group reads the earlier groups' nodes as its
                 // siblings and rewrites the ancestors they share
+                const SibArea sp = sib_area(sibs, warp);
                 for (int c0 = 0; c0 < U; c0 += 32) {
                     const int Uc = min(32, U - c0);
                     const bool have = lane < Uc;
                     const unsigned li = have ? wl.ulist[c0 + lane] - (unsigned)base : 0u;
-                    const float raw = have ? wl.uraw[c0 + lane] : 0.0f;
-                    warp_climb_regs<W>(a.t, Uc, shift, lane, base, li, raw, a.lp, s_lp);
+                    float lv = 0.0f;
+                    if (have) {
+                        prefetch_siblings(a.t, n + base + li, min(shift, kMaxClimb), sp, lane);
+                        lv = leaf_of(wl.uraw[c0 + lane], a.lp, s_lp);
+                    }
+                    cp_async_wait_warp();
+                    warp_climb<W>(a.t, Uc, shift, lane, base, li, lv, sp, lane, &root_s, &root_m);
                     __syncwarp();
                 }
             }
@@ -1812,18 +1948,67 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     //    is one cluster: CTA 0, after a cluster barrier, without the arrival ticket)
     bool top;
     if (a.cluster) {
-        __threadfence();
+        // every subtree's root and this CTA's maxima to CTA 0; the barrier's release and acquire
+        // order them (and every node stored above) before CTA 0's reads
+        cluster_wait_acquire();
+        if (a.proportional && has_sub && lane == 0) {
+            st_cluster_f64(cluster_smem_addr(&s_rootS[nsub + sub], 0), root_s);
+            st_cluster_f32(cluster_smem_addr(&s_rootM[nsub + sub], 0), root_m);
+        }
+        if (tid == 0) {
+            int mc = 0;
+            for (int w = 0; w < a.subs; ++w) mc = max(mc, s_cnt[w]);
+            st_cluster_u32(cluster_smem_addr(&s_cbmax[blockIdx.x], 0), s_max);
+            st_cluster_u32(cluster_smem_addr(&s_ccnt[blockIdx.x], 0), (unsigned)mc);
+        }
         cluster_sync_all();
-        top = cluster_cta_rank() == 0;
+        top = blockIdx.x == 0;
     } else {
         top = last_to_arrive(&a.ctl->ticket_update);
     }
-    if (top && tid == 0 && a.crowd_host) {   // every CTA's count is in: to the host, and reset
-        const unsigned m = atomicExch(&a.ctl->crowd_max, 0u);
-        *(volatile unsigned *)a.crowd_host = crowd_report(a.ctl, a.P, m);
+    if (top && tid == reporter && a.crowd_host) {   // every CTA's count is in: to the host, and reset
+        if (a.cluster) {
+            unsigned mc = 0;
+            for (unsigned c = 0; c < gridDim.x; ++c) mc = max(mc, s_ccnt[c]);
+            *(volatile unsigned *)a.crowd_host = crowd_word(a.P, crowd_seq, mc);
+        } else {
+            const unsigned m = atomicExch(&a.ctl->crowd_max, 0u);
+            *(volatile unsigned *)a.crowd_host = crowd_report(a.ctl, a.P, m);
+        }
+    }
+    if (top && tid == reporter) {
+        Ctl *cc = a.ctl;
+        if (a.cluster) {   // the CTAs' maxima gathered here; the running maximum read at the start
+            unsigned bm = 0;
+            for (unsigned c = 0; c < gridDim.x; ++c) bm = max(bm, s_cbmax[c]);
+            if (bm > max_prev_bits) fold_running_max(cc, bm, a.alpha);
+        } else {
+            fold_running_max(cc, __ldcg(&cc->batch_max_bits), a.alpha);
+            cc->batch_max_bits = 0;
+            cc->ticket_update = 0;
+        }
     }
     if (top) {
-        if (a.proportional && a.P > 0 && a.P <= 8) {
+        if (a.cluster && a.proportional) {
+            // warp 0: the levels above the roots in the shared-memory heap, one level per
+            // iteration (nodes of depth l + skip stored as they are made)
+            if (warp == 0) {
+#pragma unroll 1
+                for (int l = a.P - 1; l >= 0; --l) {
+                    const int lw = 1 << l;
+                    for (int i = lane; i < lw; i += 32) {
+                        const int node = lw + i;
+                        const double sum = s_rootS[2 * node] + s_rootS[2 * node + 1];
+                        const float mn = fmin_tree(s_rootM[2 * node], s_rootM[2 * node + 1]);
+                        s_rootS[node] = sum;
+                        s_rootM[node] = mn;
+                        a.t.S[((unsigned long long)lw << skip) + i] = sum;
+                        a.t.M[((unsigned long long)lw << skip) + i] = mn;
+                    }
+                    __syncwarp();
+                }
+            }
+        } else if (a.proportional && a.P > 0 && a.P <= 8) {
             // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
             // node of depth 5 in registers, or starts from depth-P node l (P < 5); every level
             // above is one shuffle and one add
@@ -2004,12 +2189,6 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                 }
             }
         }
-        if (tid == 0) {
-            Ctl *cc = a.ctl;
-            fold_running_max(cc, __ldcg(&cc->batch_max_bits), a.alpha);
-            cc->batch_max_bits = 0;
-            cc->ticket_update = 0;
-        }
     }
 }
 
@@ -2040,7 +2219,7 @@ cudaError_t init_tree_kernels(int carveout)
     cudaError_t e = cudaMemcpyToSymbol(g_leafpow, &tables, sizeof(tables));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kUpdSmemBytes);
+                                         (int)update_smem_bytes(kUpdMaxWarps));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_update<kUpdWindow>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess || carveout < 0) return e;
     // k_rebuild_tree keeps the driver's choice: its 25 KB of shared memory per CTA would hold it
@@ -2257,9 +2436,9 @@ cudaError_t launch_update(const TreeRefs &t, float *raw_store, Ctl *ctl, unsigne
     a.cluster = 0;
     if (grid > 1 && grid <= 16 && update_cluster_enabled()) {
         a.cluster = 1;
-        return launch_pdl_cluster(k_update<kUpdWindow>, grid, 32 * warps, kUpdSmemBytes, st, a);
+        return launch_pdl_cluster(k_update<kUpdWindow>, grid, 32 * warps, update_smem_bytes(warps), st, a);
     }
-    return launch_pdl(k_update<kUpdWindow>, grid, 32 * warps, kUpdSmemBytes, st, a);
+    return launch_pdl(k_update<kUpdWindow>, grid, 32 * warps, update_smem_bytes(warps), st, a);
 }
 
 }  // namespace gbper

@@ -35,10 +35,14 @@ struct Ctl {
 };
 
 // A crowding report: (P << 28) | (sequence mod 256) << 20 | min(entries, 2^20 - 1).
+__device__ __forceinline__ unsigned crowd_word(int P, unsigned seq, unsigned entries)
+{
+    return ((unsigned)P << 28) | ((seq & 0xffu) << 20) | min(entries, 0xfffffu);
+}
+
 __device__ __forceinline__ unsigned crowd_report(Ctl *c, int P, unsigned entries)
 {
-    const unsigned seq = atomicAdd(&c->crowd_seq, 1u) & 0xffu;
-    return ((unsigned)P << 28) | (seq << 20) | min(entries, 0xfffffu);
+    return crowd_word(P, atomicAdd(&c->crowd_seq, 1u), entries);
 }
 
 // Crowding of update batches (proportional mode): the most entries one update subtree receives,
@@ -388,6 +392,42 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned
 __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The two halves of a cluster barrier, for a barrier whose wait can come long after the arrival:
+// arrive (no memory ordering) ... wait (acquire).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The shared::cluster address of shared variable *p in the cluster's CTA `rank`.
+__device__ __forceinline__ unsigned cluster_smem_addr(const void *p, unsigned rank)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(p);
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(s), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f64(unsigned addr, double v)
+{
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(unsigned addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(unsigned addr, unsigned v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned cluster_cta_rank()
