@@ -168,6 +168,7 @@ __device__ __forceinline__ unsigned long long walk_decide(unsigned long long nod
 {
     int q = 0;
     const int kint = last ? k - 1 : k;
+#pragma unroll 1
     for (int lev = 1; lev <= kint; ++lev) {
         const int i = (1 << (lev - 1)) - 1 + q;
         const double left = __shfl_sync(kFull, pick_slot<S>(w.v, i / G), i & (G - 1), G);

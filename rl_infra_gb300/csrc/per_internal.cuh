@@ -123,9 +123,11 @@ __device__ __forceinline__ void mark_dirty(const DirtyRefs &d, unsigned long lon
 // ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) -----------------------------------
 // Round: (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0)) with
 // A = 0xD2511F53, B = 0xCD9E8D57; the key advances by (0x9E3779B9, 0xBB67AE85) per round.
+// (A loop rather than ten unrolled rounds: the kernels run it once or twice per thread, where
+// code fetched once per launch costs more than the loop's count and branch.)
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k)
 {
-#pragma unroll
+#pragma unroll 1
     for (int r = 0; r < 10; ++r) {
         const unsigned a_lo = 0xD2511F53u * c.x, a_hi = __umulhi(0xD2511F53u, c.x);
         const unsigned b_lo = 0xCD9E8D57u * c.z, b_hi = __umulhi(0xCD9E8D57u, c.z);
