@@ -417,6 +417,14 @@ __device__ __forceinline__ void copy_rows_flat(const AddArgs &a, const AddGeom &
 
 __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
 {
+    __shared__ LeafPowTables s_lp;
+    if (blockIdx.x < a.ntree && a.prio && a.proportional) {
+        // the power's tables (constant since the library loaded), staged before the wait
+        const unsigned *src = reinterpret_cast<const unsigned *>(&g_leafpow);
+        unsigned *dst = reinterpret_cast<unsigned *>(&s_lp);
+        for (int i = threadIdx.x; i < (int)(sizeof(LeafPowTables) / 4); i += blockDim.x) dst[i] = src[i];
+        __syncthreads();
+    }
     pdl_wait();
     pdl_release();
     const unsigned long long cursor = a.ctl->cursor;
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
                     const float raw = a.prio ? prio_to_raw(__ldg(a.prio + k), a.eps, max_prev) : max_prev;
                     mymax = __float_as_uint(raw);
                     if (a.proportional) {
-                        leaf = a.prio ? leaf_of(raw, a.lp) : max_leaf;
+                        leaf = a.prio ? leaf_of(raw, a.lp, s_lp) : max_leaf;
                         a.t.L[s] = leaf;
                     } else if (a.raw_store) {   // rank mode (uniform mode keeps no priorities)
                         const float old = a.raw_store[s];
@@ -1182,15 +1190,21 @@ constexpr unsigned kBlockBatch = (unsigned)(kBlockCtas * kBlockThreads * kBlockP
 __global__ void __launch_bounds__(kBlockThreads) k_upd_block(ScatterArgs a)
 {
     __shared__ unsigned s_w[kBlockThreads / 32];
-    __shared__ unsigned s_base;
+    // every CTA writes its count of new marks into every CTA's s_tot, and its batch maximum into
+    // CTA 0's s_bmax (distributed shared memory, before the second cluster barrier)
+    __shared__ unsigned s_tot[kBlockCtas], s_bmax[kBlockCtas];
     pdl_wait();
     pdl_release();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned gtid = cluster_cta_rank() * kBlockThreads + tid, gthreads = kBlockCtas * kBlockThreads;
+    const unsigned crank = cluster_cta_rank();
+    const unsigned gtid = crank * kBlockThreads + tid, gthreads = kBlockCtas * kBlockThreads;
     const unsigned long long size = a.ctl->size;
-    const float max_prev = __uint_as_float(a.ctl->max_raw_bits);
+    const unsigned max_prev_bits = a.ctl->max_raw_bits;
+    const float max_prev = __uint_as_float(max_prev_bits);
     const bool rank = !a.proportional;
     const unsigned epoch = rank && a.dirty.mark ? __ldcg(a.dirty.epoch) : 0u;
+    // the list's length before this call: nothing else appends during it
+    const unsigned count0 = rank && a.dirty.mark ? __ldcg(a.dirty.count) : 0u;
     constexpr unsigned kNone = 0xffffffffu;   // no entry, or an index outside the filled slots
     unsigned iv[kBlockPer];
     float tv[kBlockPer], oldv[kBlockPer];
@@ -1243,25 +1257,41 @@ __global__ void __launch_bounds__(kBlockThreads) k_upd_block(ScatterArgs a)
             }
         }
     }
+    // this CTA's count of new marks (exclusive prefix over its threads) and batch maximum, to the
+    // other CTAs; after the barrier each CTA places its marks after those of the CTAs before it
+    unsigned inc = 0, c = 0;
     if (rank && a.dirty.mark) {
-        // list positions for the new marks: a CTA-wide exclusive count, one counter increment
-        const unsigned c = __popc(newmark);
-        unsigned inc = c;
+        c = __popc(newmark);
+        inc = c;
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned x = __shfl_up_sync(0xffffffffu, inc, o);
             if (lane >= o) inc += x;
         }
         if (lane == 31) s_w[warp] = inc;
         __syncthreads();
-        unsigned before = 0, total = 0;
+    }
+    unsigned before = 0, total = 0;
+    if (rank && a.dirty.mark) {
         for (int w = 0; w < kBlockThreads / 32; ++w) {
             const unsigned x = s_w[w];
             if (w < warp) before += x;
             total += x;
         }
-        if (tid == 0) s_base = total ? atomicAdd(a.dirty.count, total) : 0u;
-        __syncthreads();
-        unsigned pos = s_base + before + inc - c;
+        __syncthreads();   // s_w is reused below
+    }
+    for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
+    if (lane == 0) s_w[warp] = mymax;
+    __syncthreads();
+    if (tid < kBlockCtas) st_cluster_u32(cluster_smem_addr(&s_tot[crank], (unsigned)tid), total);
+    if (tid == 32) {
+        unsigned bm = 0;
+        for (int w = 0; w < kBlockThreads / 32; ++w) bm = max(bm, s_w[w]);
+        st_cluster_u32(cluster_smem_addr(&s_bmax[crank], 0), bm);
+    }
+    cluster_sync_all();   // every CTA's count and maximum in
+    if (rank && a.dirty.mark) {
+        unsigned pos = count0 + before + inc - c;
+        for (unsigned q = 0; q < crank; ++q) pos += s_tot[q];
 #pragma unroll
         for (int u = 0; u < kBlockPer; ++u)
             if ((newmark >> u) & 1u) {
@@ -1271,21 +1301,16 @@ __global__ void __launch_bounds__(kBlockThreads) k_upd_block(ScatterArgs a)
                 }
                 ++pos;
             }
-        __syncthreads();   // s_w is reused below
+        if (crank == 0 && tid == 0) {
+            unsigned all = 0;
+            for (int q = 0; q < kBlockCtas; ++q) all += s_tot[q];
+            *a.dirty.count = count0 + all;
+        }
     }
-    for (int o = 16; o > 0; o >>= 1) mymax = max(mymax, __shfl_xor_sync(0xffffffffu, mymax, o));
-    if (lane == 0) s_w[warp] = mymax;
-    __syncthreads();
-    if (tid == 0) {
+    if (crank == 0 && tid == 32) {
         unsigned bm = 0;
-        for (int w = 0; w < kBlockThreads / 32; ++w) bm = max(bm, s_w[w]);
-        if (bm) atomicMax(&a.ctl->batch_max_bits, bm);
-    }
-    cluster_sync_all();   // every CTA's maximum in
-    if (cluster_cta_rank() == 0 && tid == 0) {
-        Ctl *c = a.ctl;
-        fold_running_max(c, __ldcg(&c->batch_max_bits), a.alpha);   // L2: this SM's L1 may hold the line
-        c->batch_max_bits = 0;
+        for (int q = 0; q < kBlockCtas; ++q) bm = max(bm, s_bmax[q]);
+        if (bm > max_prev_bits) fold_running_max(a.ctl, bm, a.alpha);
     }
 }
 
