@@ -385,24 +385,32 @@ __global__ void __launch_bounds__(1024) k_build_cdf(double *cdf, unsigned long l
     }
 }
 
-// guide[k] = the first r in [1, C] with cdf[r] > fl(k * delta) (C + 1 if none), k = 0 .. K, and
-// guide[K + 1] = C + 1.  The sampler forms fl(k * delta) with the same binary64 product.
-__global__ void k_build_guide(const double *cdf, unsigned long long C, unsigned *guide, unsigned K, double delta)
+// The first r in [1, C] with cdf[r] > thr (C + 1 if none).
+__device__ __forceinline__ unsigned long long cdf_first_above(const double *cdf, unsigned long long C, double thr)
 {
-    for (unsigned long long k = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; k <= (unsigned long long)K + 1;
+    unsigned long long lo = 1, hi = C + 1;
+    while (lo < hi) {
+        const unsigned long long mid = lo + (hi - lo) / 2;
+        if (cdf[mid] > thr) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+// guide[k], k = 0 .. K (see GuideEntry): r0 and r1 from the thresholds fl(k * delta) and
+// fl((k + 1) * delta), formed with the same binary64 products as the sampler's (r1 = C + 1 for
+// the last bucket).
+__global__ void k_build_guide(const double *cdf, unsigned long long C, GuideEntry *guide, unsigned K, double delta)
+{
+    for (unsigned long long k = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; k <= (unsigned long long)K;
          k += (unsigned long long)gridDim.x * blockDim.x) {
-        if (k == (unsigned long long)K + 1) {
-            guide[k] = (unsigned)(C + 1);
-            continue;
-        }
-        const double thr = __dmul_rn((double)k, delta);
-        unsigned long long lo = 1, hi = C + 1;
-        while (lo < hi) {
-            const unsigned long long mid = lo + (hi - lo) / 2;
-            if (cdf[mid] > thr) hi = mid;
-            else lo = mid + 1;
-        }
-        guide[k] = (unsigned)lo;
+        GuideEntry g;
+        const unsigned long long r0 = cdf_first_above(cdf, C, __dmul_rn((double)k, delta));
+        const unsigned long long r1 = k == K ? C + 1 : cdf_first_above(cdf, C, __dmul_rn((double)(k + 1), delta));
+        g.r0 = (unsigned)r0;
+        g.r1 = (unsigned)r1;
+        for (int i = 0; i < 3; ++i) g.c[i] = r0 + i < r1 && r0 + i <= C ? cdf[r0 + i] : 0.0;
+        guide[k] = g;
     }
 }
 
@@ -763,10 +771,10 @@ cudaError_t launch_rank_merge(RankWork &w, unsigned long long n_old, cudaStream_
                       w.vals[0], w.vals[1], n_old, w.dirty, w.merge_ctl, w.err);
 }
 
-cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, unsigned *guide, unsigned K,
+cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, GuideEntry *guide, unsigned K,
                                double delta, cudaStream_t st)
 {
-    const unsigned grid = (unsigned)std::min<unsigned long long>(((unsigned long long)K + 2 + 255) / 256, 4096);
+    const unsigned grid = (unsigned)std::min<unsigned long long>(((unsigned long long)K + 1 + 255) / 256, 4096);
     k_build_guide<<<grid, 256, 0, st>>>(cdf, capacity, guide, K, delta);
     return cudaGetLastError();
 }

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_flat(FlatSampleArgs a)
 // ------------------------------------------------------------------------------------------
 struct RankSampleArgs {
     const double *cdf;
-    const unsigned *guide;           // guide[0 .. guide_k + 1] (see RankWork), or null
+    const GuideEntry *guide;         // guide[0 .. guide_k] (see GuideEntry), or null
     unsigned guide_k;
     double guide_delta, guide_inv;
     const unsigned *sorted;          // the slot order, unless order_cur is set:
@@ -373,6 +373,7 @@ struct RankSampleArgs {
     RingRefs r;
     Ctl *ctl;
     unsigned B;
+    double inv_b;   // 1/B when B is a power of two (exact), else 0
     float ab;  // alpha * beta, the exponent of the closed-form weight
     unsigned long long seed;
     SampleOut o;
@@ -389,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
     const unsigned long long size = a.ctl->size;
     if (threadIdx.x == 0) {
         s_call = take_call_number(a.ctl);
-        s_seg = __ddiv_rn(a.cdf[size], (double)a.B);
+        const double total = a.cdf[size];
+        s_seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
     }
     __syncthreads();
     const unsigned long long call = s_call;
@@ -402,21 +404,32 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
         const double u = draw_uniform(a.seed, j, call, 1);
         const double m = __dmul_rn(__dadd_rn(exact_double(j, 0), u), seg);
         // first position p in [1, size] with cdf[p] > m; size + 1 when there is none.  The
-        // guide brackets it: with fl(k delta) <= m < fl((k+1) delta), the rank lies in
-        // [guide[k], guide[k+1]], so the search covers that stretch only (same comparisons)
-        unsigned long long lo = 1, hi = size + 1;
+        // guide brackets it: with fl(k delta) <= m < fl((k+1) delta), the rank lies in [r0, r1];
+        // when the bucket holds at most three candidates their CDF values come with it, else the
+        // search covers that stretch only (the same comparisons either way)
+        unsigned long long lo = 1, hi = size + 1, ans = 0;
+        bool found = false;
         if (a.guide) {
             long long k = (long long)__dmul_rn(m, a.guide_inv);
             if (k > (long long)a.guide_k) k = a.guide_k;
             if (k < 0) k = 0;
             while (k > 0 && __dmul_rn((double)k, a.guide_delta) > m) --k;
             while (k < (long long)a.guide_k && __dmul_rn((double)(k + 1), a.guide_delta) <= m) ++k;
-            const unsigned long long g0 = __ldg(a.guide + k), g1 = __ldg(a.guide + k + 1);
+            const ulonglong2 q0 = __ldg(reinterpret_cast<const ulonglong2 *>(a.guide + k));
+            const double2 q1 = __ldg(reinterpret_cast<const double2 *>(a.guide + k) + 1);
+            const unsigned long long g0 = (unsigned)q0.x, g1 = (unsigned)(q0.x >> 32);
+            if (g1 - g0 <= 3) {
+                const double c0 = __longlong_as_double((long long)q0.y);
+                const unsigned w = (unsigned)(g1 - g0);
+                ans = g0 + (w > 0 && !gt_nonneg(c0, m)) + (w > 1 && !gt_nonneg(q1.x, m)) + (w > 2 && !gt_nonneg(q1.y, m));
+                if (ans > hi) ans = hi;
+                found = true;
+            }
             if (g0 > lo) lo = g0;
             if (g1 < hi) hi = g1;
             if (lo > hi) lo = hi;
         }
-        const unsigned long long ans = first_above(a.cdf, lo, hi, m, lane);
+        if (!found) ans = first_above(a.cdf, lo, hi, m, lane);
         unsigned long long r = ans > size ? size : ans;
         const unsigned long long slot = sorted[r - 1];
         if (lane == 0) {
@@ -591,6 +604,7 @@ cudaError_t launch_sample_rank(const RankWork &w, const unsigned *sorted, const 
     a.r = r;
     a.ctl = ctl;
     a.B = B;
+    a.inv_b = (B & (B - 1)) == 0 ? 1.0 / (double)B : 0.0;
     a.ab = (float)(alpha * (double)beta);
     a.seed = seed;
     a.o = o;

@@ -412,16 +412,18 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
     if (h->rank.raw) h->rank.err = &h->ctl->err_flags;
     if (e == cudaSuccess && h->rank.cdf) e = launch_build_cdf(h->rank.cdf, capacity, h->alpha, 0);
     if (e == cudaSuccess && h->rank.cdf) {
-        // the CDF's guide: about 16 ranks per bucket of mass where ranks are sparsest in mass
-        // (the last, each of mass capacity^-alpha), at most two entries per slot
+        // the CDF's guide: buckets of mass at most two ranks' mass where ranks are sparsest in
+        // mass (the last, each of mass capacity^-alpha), so that each bucket holds at most three
+        // candidate ranks, with at most two buckets per slot (beyond that, the sparsest buckets
+        // hold more and the sampler searches them)
         double T = 0.0;
         e = cudaMemcpy(&T, h->rank.cdf + capacity, sizeof(double), cudaMemcpyDeviceToHost);
         uint64_t K = 1024, cap2 = 2;
         while (cap2 < capacity) cap2 <<= 1;
         cap2 *= 2;
-        const double est = T * std::pow((double)capacity, h->alpha) / 16.0;
+        const double est = T * std::pow((double)capacity, h->alpha) / 2.0;
         while ((double)K < est && K < cap2) K <<= 1;
-        if (e == cudaSuccess && !alloc(&h->rank.guide, K + 2)) {
+        if (e == cudaSuccess && !alloc(&h->rank.guide, K + 1)) {
             cudaGetLastError();
             free_all(h);
             delete h;

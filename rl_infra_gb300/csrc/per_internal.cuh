@@ -285,13 +285,22 @@ cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRef
                                float beta, unsigned long long seed, const SampleOut &o, int num_sms,
                                cudaStream_t st);
 
+// One bucket of the guide to the CDF: a mass m with fl(k delta) <= m < fl((k+1) delta) has its
+// rank (the first r with cdf[r] > m) in [r0, r1], r0 the first r with cdf[r] > fl(k delta) and r1
+// the first with cdf[r] > fl((k+1) delta) (capacity + 1 when none); c[i] = cdf[r0 + i] for
+// i < min(r1 - r0, 3), so a bucket with at most three candidates decides the rank from its own 32
+// bytes.
+struct GuideEntry {
+    unsigned r0, r1;
+    double c[3];
+};
+static_assert(sizeof(GuideEntry) == 32, "one sector per guide bucket");
+
 struct RankWork {
     float *raw;
     double *cdf;
-    // guide to the CDF: guide[k] = the first rank r with cdf[r] > fl(k * guide_delta), for
-    // k = 0 .. guide_k (guide_k + 1 past the end: capacity + 1), so a mass in
-    // [fl(k delta), fl((k+1) delta)) has its rank in [guide[k], guide[k+1]]
-    unsigned *guide;
+    // guide to the CDF: guide[k] for k = 0 .. guide_k (see GuideEntry)
+    GuideEntry *guide;
     unsigned guide_k;
     double guide_delta;
     unsigned *keys[2];
@@ -315,7 +324,7 @@ cudaError_t launch_build_cdf(double *cdf, unsigned long long capacity, double al
                              cudaStream_t st);
 
 // guide[0 .. K + 1] for a CDF of `capacity` ranks (K = guide_k, delta = guide_delta).
-cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, unsigned *guide, unsigned K,
+cudaError_t launch_build_guide(const double *cdf, unsigned long long capacity, GuideEntry *guide, unsigned K,
                                double delta, cudaStream_t st);
 
 // Sorts the `size` filled slots by raw priority descending, ties by slot ascending, leaving
