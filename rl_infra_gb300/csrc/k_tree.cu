@@ -1813,7 +1813,7 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     const unsigned long long root = (n + (sub << shift)) >> shift;   // the subtree's root node
     double root_s = 0.0;   // lane 0: the subtree root's value once this warp is done
     float root_m = 0.0f;
-    if (a.cluster && a.proportional && has_sub && m == 0 && lane == 0) {   // untouched: as stored
+    if (a.proportional && has_sub && m == 0 && lane == 0) {   // untouched: as stored
         root_s = a.t.S[root];
         root_m = a.t.M[root];
     }
@@ -1969,16 +1969,54 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
         }
     }
 
-    // 3. the last CTA rebuilds the top P levels and folds in the batch maximum (when the grid
-    //    is one cluster: CTA 0, after a cluster barrier, without the arrival ticket)
+    // 3. the levels above this CTA's 2^lg subtrees that no other CTA reaches, from the warps'
+    //    roots in shared memory (the CTA's group ends in one node of depth P + skip - lg); then
+    //    the last CTA rebuilds the top Pt = P - lg levels and folds in the batch maximum (when the
+    //    grid is one cluster: CTA 0, after a cluster barrier, without the arrival ticket)
+    int lg = 0;
+    while ((1 << (lg + 1)) <= a.subs && lg + 1 <= a.P) ++lg;
+    const int Pt = a.P - lg;
+    if (a.proportional && lg > 0) {
+        __shared__ double s_gS[kUpdMaxWarps];
+        __shared__ float s_gM[kUpdMaxWarps];
+        if (lane == 0 && warp < (1 << lg)) {
+            s_gS[warp] = root_s;
+            s_gM[warp] = root_m;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            double gs = 0.0;
+            float gm = 0.0f;
+#pragma unroll 1
+            for (int l = 1; l <= lg; ++l) {
+                const int cnt = 1 << (lg - l);
+                if (lane < cnt) {
+                    gs = s_gS[2 * lane] + s_gS[2 * lane + 1];
+                    gm = fmin_tree(s_gM[2 * lane], s_gM[2 * lane + 1]);
+                    const unsigned long long node = (1ull << (a.P + skip - l)) + (first_sub >> l) + lane;
+                    a.t.S[node] = gs;
+                    a.t.M[node] = gm;
+                }
+                __syncwarp();
+                if (lane < cnt) {
+                    s_gS[lane] = gs;
+                    s_gM[lane] = gm;
+                }
+                __syncwarp();
+            }
+            root_s = gs;   // lane 0: the group's node
+            root_m = gm;
+        }
+    }
     bool top;
     if (a.cluster) {
-        // every subtree's root and this CTA's maxima to CTA 0; the barrier's release and acquire
+        // every group's node and this CTA's maxima to CTA 0; the barrier's release and acquire
         // order them (and every node stored above) before CTA 0's reads
         cluster_wait_acquire();
-        if (a.proportional && has_sub && lane == 0) {
-            st_cluster_f64(cluster_smem_addr(&s_rootS[nsub + sub], 0), root_s);
-            st_cluster_f32(cluster_smem_addr(&s_rootM[nsub + sub], 0), root_m);
+        if (a.proportional && lane == 0 && (lg > 0 ? warp == 0 : has_sub)) {
+            const unsigned hi = (1u << Pt) + (unsigned)(lg > 0 ? blockIdx.x : sub);
+            st_cluster_f64(cluster_smem_addr(&s_rootS[hi], 0), root_s);
+            st_cluster_f32(cluster_smem_addr(&s_rootM[hi], 0), root_m);
         }
         if (tid == 0) {
             int mc = 0;
@@ -2015,11 +2053,11 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     }
     if (top) {
         if (a.cluster && a.proportional) {
-            // warp 0: the levels above the roots in the shared-memory heap, one level per
+            // warp 0: the levels above the groups' nodes in the shared-memory heap, one level per
             // iteration (nodes of depth l + skip stored as they are made)
             if (warp == 0) {
 #pragma unroll 1
-                for (int l = a.P - 1; l >= 0; --l) {
+                for (int l = Pt - 1; l >= 0; --l) {
                     const int lw = 1 << l;
                     for (int i = lane; i < lw; i += 32) {
                         const int node = lw + i;
@@ -2033,12 +2071,12 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     __syncwarp();
                 }
             }
-        } else if (a.proportional && a.P > 0 && a.P <= 8) {
+        } else if (a.proportional && Pt > 0 && Pt <= 8) {
             // warp 0: lane l first combines its g = 2^(P-5) depth-P nodes (P >= 5) down to one
             // node of depth 5 in registers, or starts from depth-P node l (P < 5); every level
             // above is one shuffle and one add
             if (warp == 0) {
-                const int P = a.P;
+                const int P = Pt;
                 double sv = 0.0;
                 float mv = __int_as_float(0x7f800000);
                 int w;   // nodes of the current depth, held by lanes 0, st, 2 st, ...
@@ -2092,13 +2130,13 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     }
                 }
             }
-        } else if (a.proportional && a.P >= 7 && a.P <= 10 && (blockDim.x >> 5) >= 4) {
+        } else if (a.proportional && Pt >= 7 && Pt <= 10 && (blockDim.x >> 5) >= 4) {
             // four warps: warp w rebuilds the subtree of node 4 + w from its 2^(P-2) depth-P
             // nodes (g = 2^(P-7) per lane combined in registers down to depth 7, then five
             // shuffle levels down to depth 2); warp 0 then adds nodes 4..7 up to the root
             __shared__ double s_q[4];
             __shared__ float s_qm[4];
-            const int P = a.P;
+            const int P = Pt;
             const int g = 1 << (P - 7);
             if (warp < 4) {
             double gs[8];
@@ -2162,10 +2200,10 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
                     }
                 }
             }
-        } else if (a.proportional && a.P > 0) {
+        } else if (a.proportional && Pt > 0) {
             double *heapS = reinterpret_cast<double *>(smem_raw);
             float *heapM = reinterpret_cast<float *>(heapS + (2 << kMaxTopLog));
-            const int P = a.P;
+            const int P = Pt;
             const int width = 1 << P;
             for (int i = tid; i < width; i += blockDim.x) {
                 heapS[width + i] = ld_sum_cg(a.t, ((unsigned long long)width << skip) + i);
