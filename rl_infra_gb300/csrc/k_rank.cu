@@ -675,11 +675,12 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
             dpre[warp * 32 + lane] = inc - c;   // within the warp's 32 words, fixed up below
             if (lane == 31) s_wd[warp] = inc;
         }
-        c_old = 0;
-        c_new = 0;
-        for (int w = 0; w < kMThreads / 32; ++w) {
-            c_old += s_wo[w];
-            c_new += s_wn[w];
+        // the CTA's counts: lane l takes warp l's partial counts, then a warp sum
+        c_old = lane < kMThreads / 32 ? s_wo[lane] : 0u;
+        c_new = lane < kMThreads / 32 ? s_wn[lane] : 0u;
+        for (int o = 16; o > 0; o >>= 1) {
+            c_old += __shfl_xor_sync(kFull, c_old, o);
+            c_new += __shfl_xor_sync(kFull, c_new, o);
         }
         __syncthreads();   // the warps' bitmap totals
         if (warp < kMWords / 32) {

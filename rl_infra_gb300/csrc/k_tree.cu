@@ -1865,8 +1865,12 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
             const float raw_e = have ? wl.rawv[lane] : 0.0f;   // pay[l] = l before the sort
             const SibArea sp = sib_area(sibs, warp);
             float lv_e = 0.0f;
+            // entries of the same leaf share one copy of its path's siblings: the lowest lane of
+            // each such group copies them into its slot
+            const unsigned same = __match_any_sync(0xffffffffu, have ? (unsigned)(key >> a.pb) : 0xffffffffu);
+            const int copier = __ffs(same) - 1;
             if (a.proportional && have) {
-                prefetch_siblings(a.t, n + base + (key >> a.pb), min(shift, kMaxClimb), sp, lane);
+                if (copier == lane) prefetch_siblings(a.t, n + base + (key >> a.pb), min(shift, kMaxClimb), sp, lane);
                 lv_e = leaf_of(raw_e, a.lp, s_lp);
             }
             // the sort key (leaf, batch position) with the list position beside it: one 32-bit
@@ -1904,10 +1908,11 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
             }
             const float raw = __shfl_sync(0xffffffffu, raw_e, slot);
             const float lv = __shfl_sync(0xffffffffu, lv_e, slot);
+            const int cslot = __shfl_sync(0xffffffffu, copier, slot);   // where the leaf's siblings are
             if (a.proportional) {
                 cp_async_wait_warp();
                 warp_climb<W>(a.t, (int)U, shift, lane, base, lane < (int)U ? li : 0u, lv, sp,
-                              lane < (int)U ? slot : 0, &root_s, &root_m);
+                              lane < (int)U ? cslot : 0, &root_s, &root_m);
             } else if (lane < (int)U) {
                 const float old = a.raw_store[base + li];
                 a.raw_store[base + li] = raw;
