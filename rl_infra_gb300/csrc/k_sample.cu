@@ -410,11 +410,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
         unsigned long long lo = 1, hi = size + 1, ans = 0;
         bool found = false;
         if (a.guide) {
+            // delta is a power of two: m / delta is exact and its truncation is the bucket
             long long k = (long long)__dmul_rn(m, a.guide_inv);
             if (k > (long long)a.guide_k) k = a.guide_k;
             if (k < 0) k = 0;
-            while (k > 0 && __dmul_rn((double)k, a.guide_delta) > m) --k;
-            while (k < (long long)a.guide_k && __dmul_rn((double)(k + 1), a.guide_delta) <= m) ++k;
             const ulonglong2 q0 = __ldg(reinterpret_cast<const ulonglong2 *>(a.guide + k));
             const double2 q1 = __ldg(reinterpret_cast<const double2 *>(a.guide + k) + 1);
             const unsigned long long g0 = (unsigned)q0.x, g1 = (unsigned)(q0.x >> 32);

@@ -415,14 +415,19 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
         // the CDF's guide: buckets of mass at most two ranks' mass where ranks are sparsest in
         // mass (the last, each of mass capacity^-alpha), so that each bucket holds at most three
         // candidate ranks, with at most two buckets per slot (beyond that, the sparsest buckets
-        // hold more and the sampler searches them)
+        // hold more and the sampler searches them).  The bucket width delta is a power of two, so
+        // k delta is exact and a mass's bucket is the truncation of one exact product.
         double T = 0.0;
         e = cudaMemcpy(&T, h->rank.cdf + capacity, sizeof(double), cudaMemcpyDeviceToHost);
-        uint64_t K = 1024, cap2 = 2;
+        uint64_t cap2 = 2;
         while (cap2 < capacity) cap2 <<= 1;
         cap2 *= 2;
-        const double est = T * std::pow((double)capacity, h->alpha) / 2.0;
-        while ((double)K < est && K < cap2) K <<= 1;
+        const double dmax = 2.0 / std::pow((double)capacity, h->alpha);   // at most two ranks' mass
+        double delta = std::ldexp(1.0, (int)std::floor(std::log2(dmax)));   // the largest power of two <= dmax
+        while (delta * 2.0 <= dmax) delta *= 2.0;
+        while (delta > dmax) delta *= 0.5;
+        while (std::ceil(T / delta) > (double)cap2) delta *= 2.0;
+        const uint64_t K = std::max<uint64_t>((uint64_t)std::ceil(T / delta), 1);
         if (e == cudaSuccess && !alloc(&h->rank.guide, K + 1)) {
             cudaGetLastError();
             free_all(h);
@@ -430,7 +435,7 @@ per_status per_create(uint64_t capacity, uint32_t state_dim, const per_config *c
             return fail(nullptr, PER_ERR_OOM, "per_create: device allocation failed");
         }
         h->rank.guide_k = (unsigned)K;
-        h->rank.guide_delta = T / (double)K;
+        h->rank.guide_delta = delta;
         if (e == cudaSuccess) e = launch_build_guide(h->rank.cdf, capacity, h->rank.guide, (unsigned)K,
                                                      h->rank.guide_delta, 0);
     }
