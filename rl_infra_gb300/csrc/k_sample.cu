@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_sample_rank(RankSampleArgs a)
     const unsigned long long size = a.ctl->size;
     if (threadIdx.x == 0) {
         s_call = take_call_number(a.ctl);
-        const double total = a.cdf[size];
+        const double total = __longlong_as_double((long long)a.ctl->rank_total_bits);   // cdf[size]
         s_seg = a.inv_b != 0.0 ? __dmul_rn(total, a.inv_b) : __ddiv_rn(total, (double)a.B);
     }
     __syncthreads();

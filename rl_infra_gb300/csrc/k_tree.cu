@@ -278,6 +278,7 @@ struct AddArgs {
     unsigned ntree;    // tree CTAs (upper bound over cursor positions)
     unsigned ncopy;    // row-copy CTAs
     int vec4;          // rows copy as float4
+    const double *rank_cdf;   // rank mode: the rank CDF, whose value at the new size the last CTA keeps
 };
 
 struct AddGeom {
@@ -559,8 +560,9 @@ __global__ void __launch_bounds__(kThreads) k_add(AddArgs a)
             fold_running_max(c, call_max, a.alpha);
             c->add_max_bits = 0;
             c->cursor = (cursor + a.count) % C;
-            const unsigned long long sz = size0 + a.count;
-            c->size = sz < C ? sz : C;
+            const unsigned long long sz = size0 + a.count < C ? size0 + a.count : C;
+            c->size = sz;
+            if (a.rank_cdf && sz != size0) c->rank_total_bits = (unsigned long long)__double_as_longlong(a.rank_cdf[sz]);
             c->ticket_add = 0;
         }
     }
@@ -1005,14 +1007,16 @@ __global__ void __launch_bounds__(kThreads) k_rebuild_tree(RebuildArgs a)
     }
 }
 
-__global__ void k_add_finish(Ctl *c, unsigned long long count, unsigned long long C, double alpha)
+__global__ void k_add_finish(Ctl *c, unsigned long long count, unsigned long long C, double alpha,
+                             const double *rank_cdf)
 {
     if (threadIdx.x == 0 && blockIdx.x == 0) {
         fold_running_max(c, c->add_max_bits, alpha);
         c->add_max_bits = 0;
         c->cursor = (c->cursor + count) % C;
-        const unsigned long long sz = c->size + count;
-        c->size = sz < C ? sz : C;
+        const unsigned long long sz = c->size + count < C ? c->size + count : C;
+        c->size = sz;
+        if (rank_cdf) c->rank_total_bits = (unsigned long long)__double_as_longlong(rank_cdf[sz]);
     }
 }
 
@@ -2350,7 +2354,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
                        const unsigned *actions, const float *rewards, const unsigned char *dones,
                        const float *prio, double alpha, double eps, bool proportional,
                        unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
-                       bool *marked, cudaStream_t st)
+                       const double *rank_cdf, bool *marked, cudaStream_t st)
 {
     (void)host_cursor;
     AddArgs a;
@@ -2375,6 +2379,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
     a.bl = std::min(kAddBlockLog, t.D);
     const unsigned long long bsz = 1ull << a.bl;
     a.vec4 = (r.d % 4 == 0) && ((reinterpret_cast<uintptr_t>(states) | reinterpret_cast<uintptr_t>(next)) % 16 == 0);
+    a.rank_cdf = rank_cdf;
     if (r.d == 0) a.vec4 = 0;
 
     // rows: about `per` elements of each array per copy thread, at most 4 CTAs per SM.  8 (16
@@ -2402,7 +2407,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
         e = launch_rebuild_tree(rebuild_args(t, ctl), st);
         if (e != cudaSuccess) return e;
     }
-    k_add_finish<<<1, 32, 0, st>>>(ctl, count, C, alpha);
+    k_add_finish<<<1, 32, 0, st>>>(ctl, count, C, alpha, rank_cdf);
     return cudaGetLastError();
 }
 

@@ -488,7 +488,8 @@ per_status per_add(per_buffer *h, uint64_t count, const float *d_states, const f
                                      d_actions, d_rewards, d_dones, d_raw_prio, h->alpha, h->eps,
                                      h->mode == PER_MODE_PROPORTIONAL || h->mode == PER_MODE_FLAT,
                                      h->host_cursor, h->num_sms,
-                                     h->rank.dirty, &marked, as_stream(stream));
+                                     h->rank.dirty, h->mode == PER_MODE_RANK ? h->rank.cdf : nullptr, &marked,
+                                     as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "per_add launch");
     if (h->mode == PER_MODE_RANK) {
         if (marked) h->dirty_bound += count;

@@ -32,6 +32,7 @@ struct Ctl {
     unsigned int max_leaf_bits;       // fl32(pow(running maximum, alpha)): the leaf of a new row
     unsigned int crowd_max;           // the update's most entries in one subtree (reset by the top CTA)
     unsigned int crowd_seq;           // crowding reports made
+    unsigned long long rank_total_bits;   // rank mode: cdf[size] (binary64 bits), kept with size
 };
 
 // A crowding report: (P << 28) | (sequence mod 256) << 20 | min(entries, 2^20 - 1).
@@ -216,7 +217,7 @@ cudaError_t launch_add(const TreeRefs &t, const RingRefs &r, float *raw_store, C
                        const unsigned *actions, const float *rewards, const unsigned char *dones,
                        const float *prio, double alpha, double eps, bool proportional,
                        unsigned long long host_cursor, int num_sms, const DirtyRefs &dirty,
-                       bool *marked, cudaStream_t st);
+                       const double *rank_cdf, bool *marked, cudaStream_t st);
 
 // A few entries (proportional mode, with a tree): one warp propagates them one after another,
 // each from its leaf to the root.  Same result as launch_update.
