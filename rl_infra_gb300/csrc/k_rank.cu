@@ -568,26 +568,18 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
     pdl_wait();
     pdl_release();
     const unsigned tile = blockIdx.x;
-    // thread 0 reads the control words for the CTA; the last CTA to have read them opens a new
-    // mark epoch (which unmarks every slot), empties the list and flips the buffer pair (the
-    // kernels after this one see them once every CTA's output is complete)
+    // thread 0 reads the control words for the CTA and then arrives on a ticket (the values are
+    // in hand before the arrival is issued); the last CTA to have read them opens a new mark epoch
+    // (which unmarks every slot), empties the list and flips the buffer pair at its end, which the
+    // kernels after this one see once every CTA's output is complete
     __shared__ unsigned s_ctl[2];
     if (tid == 0) {
-        const unsigned c0 = *(volatile unsigned *)dirty.count, c1 = *(volatile unsigned *)&mctl[4] & 1u;
-        s_ctl[0] = c0;
-        s_ctl[1] = c1;
-        __threadfence();   // both read before the arrival
-        if (atomicAdd(&mctl[2], 1u) == gridDim.x - 1) {
-            if (c0 <= kMaxDirty) {
-                *dirty.count = 0u;
-                mctl[1] += 1u;
-                mctl[4] = c1 ^ 1u;   // the merged order is in the other pair
-            }
-            mctl[2] = 0u;
-        }
+        s_ctl[0] = *(volatile unsigned *)dirty.count;
+        s_ctl[1] = *(volatile unsigned *)&mctl[4] & 1u;
     }
     __syncthreads();
     const unsigned cnt = s_ctl[0], cur = s_ctl[1];
+    const unsigned arrival = tid == 0 ? atomicAdd(&mctl[2], 1u) : 0u;   // awaited only at the end
     const unsigned *keys_in = cur ? keys1 : keys0, *vals_in = cur ? vals1 : vals0;
     unsigned *keys_out = cur ? keys0 : keys1, *vals_out = cur ? vals0 : vals1;
     const bool over = cnt > kMaxDirty;   // more slots than listed: the order cannot be merged
@@ -722,6 +714,14 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
         }
     } else if (tid == 0 && tile == 0) {
         atomicOr(err, kFlagRankStale);
+    }
+    if (tid == 0 && arrival == gridDim.x - 1) {
+        if (cnt <= kMaxDirty) {
+            *dirty.count = 0u;
+            mctl[1] += 1u;
+            mctl[4] = cur ^ 1u;   // the merged order is in the other pair
+        }
+        mctl[2] = 0u;
     }
 }
 
