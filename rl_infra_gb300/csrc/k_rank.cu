@@ -509,7 +509,8 @@ __device__ __forceinline__ void sort_small(unsigned long long *a, unsigned *p, u
         if (warp == w) {
             unsigned long long x = (unsigned)lane < n ? a[lane] : ~0ull;
             unsigned px = (unsigned)lane < n ? p[lane] : 0u;
-            for (unsigned kk = 2; kk <= 32; kk <<= 1)
+            const unsigned lim = n <= 8 ? 8u : (n <= 16 ? 16u : 32u);   // lanes past n hold the largest key
+            for (unsigned kk = 2; kk <= lim; kk <<= 1)
                 for (unsigned j = kk >> 1; j > 0; j >>= 1) {
                     const unsigned long long y = __shfl_xor_sync(kFull, x, j);
                     const unsigned py = __shfl_xor_sync(kFull, px, j);
