@@ -364,6 +364,27 @@ def _assert_rank_order(p):
     assert np.array_equal(got, want), f"rank order differs at {np.flatnonzero(got != want)[:8]}"
 
 
+@pytest.mark.parametrize("alpha", [0.0, 1.0, 1.5])
+def test_rank_guide_across_alphas(alpha):
+    """The rank sampler's guide buckets at other exponents: at alpha 0 every bucket spans two
+    ranks' mass; at 1.5 the bucket count is capped, so the sparse end's buckets hold more than
+    three candidate ranks and the sampler searches them.  Draws, weights and rows match the
+    oracle, partly filled and full."""
+    cap = 50000
+    w = _small("rank", capacity=cap, state_dim=4, row_stride=4)
+    g = wl.rng(31, int(alpha * 10))
+    p = Pair(cap, 4, 4, alpha, 1e-6, 1, seed=13)
+    prefill(p, w, g, count=30000, chunk=30000)
+    for rnd in range(4):
+        if rnd == 2:
+            prefill(p, w, g, count=cap - 30000, chunk=cap - 30000)
+        _, want = p.sample(1024, 0.5)
+        p.update(want["idx"], wl.td_errors(g, 1024))
+        p.check_tree()
+    p.check_counters()
+    p.close()
+
+
 @pytest.mark.parametrize("cap,fill,flags", [(50000, 50000, 0), (30000, 20000, 0),
                                             (30000, 20000, capi.PER_FLAG_RANK_RESORT)])
 def test_rank_order_kept_between_samples(cap, fill, flags):
