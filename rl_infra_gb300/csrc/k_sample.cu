@@ -233,7 +233,7 @@ __device__ __forceinline__ unsigned long long walk_decide(unsigned long long nod
 // one warp instruction every 19 cycles per SM, so large batches share each instruction among 2
 // or 4 draws; the deepest round also reads 17 sectors of nodes and leaves instead of 33.
 template <int G, int S>
-__global__ void __launch_bounds__(kThreads, 4) k_sample_prop(SampleArgs a)
+__global__ void __launch_bounds__(kThreads, 2) k_sample_prop(SampleArgs a)
 {
     constexpr int K = G * S >= 127 ? 7 : (G * S >= 63 ? 6 : 5);   // levels per round
     constexpr int GV = G >= 16 ? 128 / G : 8;                      // float4 per lane per gather chunk
