@@ -2038,24 +2038,27 @@ __global__ void __launch_bounds__(kUpdMaxThreads) k_update(UpdArgs a)
     } else {
         top = last_to_arrive(&a.ctl->ticket_update);
     }
-    if (top && tid == reporter && a.crowd_host) {   // every CTA's count is in: to the host, and reset
-        if (a.cluster) {
-            unsigned mc = 0;
-            for (unsigned c = 0; c < gridDim.x; ++c) mc = max(mc, s_ccnt[c]);
-            *(volatile unsigned *)a.crowd_host = crowd_word(a.P, crowd_seq, mc);
-        } else {
-            const unsigned m = atomicExch(&a.ctl->crowd_max, 0u);
-            *(volatile unsigned *)a.crowd_host = crowd_report(a.ctl, a.P, m);
-        }
-    }
     if (top && tid == reporter) {
         Ctl *cc = a.ctl;
-        if (a.cluster) {   // the CTAs' maxima gathered here; the running maximum read at the start
+        if (a.cluster) {
+            // the CTAs' counts and maxima gathered here; the running maximum and the report's
+            // sequence number read at the start
+            if (a.crowd_host) {   // every CTA's count is in: to the host
+                unsigned mc = 0;
+                for (unsigned c = 0; c < gridDim.x; ++c) mc = max(mc, s_ccnt[c]);
+                *(volatile unsigned *)a.crowd_host = crowd_word(a.P, crowd_seq, mc);
+            }
             unsigned bm = 0;
             for (unsigned c = 0; c < gridDim.x; ++c) bm = max(bm, s_cbmax[c]);
             if (bm > max_prev_bits) fold_running_max(cc, bm, a.alpha);
         } else {
-            fold_running_max(cc, __ldcg(&cc->batch_max_bits), a.alpha);
+            // the count, the sequence number and the batch maximum requested together (one
+            // round trip), then the report, the fold and the resets
+            const unsigned mc = a.crowd_host ? atomicExch(&cc->crowd_max, 0u) : 0u;
+            const unsigned seq = a.crowd_host ? atomicAdd(&cc->crowd_seq, 1u) : 0u;
+            const unsigned bm = __ldcg(&cc->batch_max_bits);
+            if (a.crowd_host) *(volatile unsigned *)a.crowd_host = crowd_word(a.P, seq, mc);
+            if (bm > max_prev_bits) fold_running_max(cc, bm, a.alpha);
             cc->batch_max_bits = 0;
             cc->ticket_update = 0;
         }
