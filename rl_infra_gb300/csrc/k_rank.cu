@@ -448,7 +448,8 @@ static_assert(kMTile % 4 == 0, "the tile's slot array must start 16 bytes after 
 constexpr size_t kMergeSmem = (size_t)kMTile * 2 * sizeof(unsigned)             // the tile: keys, slots
                               + (size_t)kMaxDirty * sizeof(unsigned long long)  // own new entries
                               + (size_t)kMaxDirty * sizeof(unsigned)            // their places in the tile
-                              + (size_t)2 * (kMWords + 1) * sizeof(unsigned);   // dropped bitmap, prefix counts
+                              + (size_t)2 * (kMWords + 1) * sizeof(unsigned)    // dropped bitmap, prefix counts
+                              + (size_t)(kMWords + 2) * sizeof(unsigned);       // own entries before each word
 
 __device__ __forceinline__ unsigned long long pack_key_slot(unsigned key, unsigned slot)
 {
@@ -486,18 +487,6 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-// entries of a[0, n) (ascending) that are <= x
-__device__ __forceinline__ unsigned count_at_most(const unsigned *a, unsigned n, unsigned x)
-{
-    unsigned lo = 0, hi = n;
-    while (lo < hi) {
-        const unsigned mid = (lo + hi) >> 1;
-        if (a[mid] <= x) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
 }
 
 // Sorts a[0, n) ascending, carrying p[0, n) along, n <= kMaxDirty: one warp's shuffles up to 32
@@ -561,11 +550,13 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
     unsigned *nins = reinterpret_cast<unsigned *>(nl + kMaxDirty);   // [kMaxDirty] tile entries below each
     unsigned *dbits = nins + kMaxDirty;                   // [kMWords + 1] dropped tile entries
     unsigned *dpre = dbits + kMWords + 1;                 // [kMWords + 1] dropped entries in earlier words
+    unsigned *ipre = dpre + kMWords + 1;                  // [kMWords + 2] own entries placed in each word, then before it
     __shared__ unsigned s_nn;
     __shared__ unsigned s_wo[kMThreads / 32], s_wn[kMThreads / 32], s_wd[kMWords / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) s_nn = 0;
     for (int i = tid; i <= kMWords; i += kMThreads) dbits[i] = 0u;
+    for (int i = tid; i <= kMWords + 1; i += kMThreads) ipre[i] = 0u;
     pdl_wait();
     pdl_release();
     const unsigned tile = blockIdx.x;
@@ -645,7 +636,9 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
             } else if (lastt || xn <= x_last) {   // own: with the count of tile entries below it
                 const unsigned j = atomicAdd(&s_nn, 1u);
                 nl[j] = xn;
-                nins[j] = tile_below(tk, tv, (unsigned)nt, xn);
+                const unsigned ij = tile_below(tk, tv, (unsigned)nt, xn);
+                nins[j] = ij;
+                atomicAdd(&ipre[ij >> 5], 1u);
             }
         }
         for (int o = 16; o > 0; o >>= 1) {
@@ -683,24 +676,45 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
             if (warp == kMWords / 32 - 1 && lane == 31) dpre[kMWords] = before + s_wd[warp];
         }
         sort_small(nl, nins, nn, kMWords / 32);   // a warp that does not build the prefix, when short
-        __syncthreads();   // dpre, own entries sorted with their places
+        if (warp == kMWords / 32 + 1) {   // another: own entries placed before each word (9 words a lane)
+            constexpr int kPer = (kMWords + 1 + 31) / 32;
+            unsigned v[kPer], s = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int wi = lane * kPer + k;
+                v[k] = wi <= kMWords ? ipre[wi] : 0u;
+                s += v[k];
+            }
+            unsigned inc = s;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned x = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += x;
+            }
+            unsigned run = inc - s;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int wi = lane * kPer + k;
+                if (wi <= kMWords) ipre[wi] = run;
+                run += v[k];
+            }
+            if (lane == 31) ipre[kMWords + 1] = inc;
+        }
+        __syncthreads();   // dpre, ipre, own entries sorted with their places
         // 3. the tile's output from base = t0 - c_old + c_new
         const unsigned long long base = t0 - c_old + c_new;
-        // this thread's entries rise with q, so the own entries at or below each are counted by one
-        // pointer that only moves forward (found for the first entry by binary search)
-        unsigned sn = count_at_most(nins, nn, (unsigned)tid);
-        unsigned nxt = sn < nn ? nins[sn] : 0xffffffffu;
+        // own entries at or below tile entry e: those placed in earlier words, and those of e's word
+        // (a contiguous stretch of the sorted places, rarely more than one) compared one by one
 #pragma unroll
         for (int q = 0; q < kMItems; ++q) {
             const unsigned e = tid + q * kMThreads;
             if ((int)e >= nt) break;
-            while (nxt <= e) {
-                ++sn;
-                nxt = sn < nn ? nins[sn] : 0xffffffffu;
-            }
-            const unsigned wd = dbits[e >> 5], bit = 1u << (e & 31);
+            const unsigned wi = e >> 5;
+            const unsigned wd = dbits[wi], bit = 1u << (e & 31);
             if (wd & bit) continue;   // dropped
-            const unsigned sd = dpre[e >> 5] + __popc(wd & (bit - 1u));
+            const unsigned i0 = ipre[wi], i1 = ipre[wi + 1];
+            unsigned sn = i0;
+            for (unsigned j = i0; j < i1; ++j) sn += nins[j] <= e ? 1u : 0u;
+            const unsigned sd = dpre[wi] + __popc(wd & (bit - 1u));
             const unsigned long long o = base + e - sd + sn;
             keys_out[o] = tk[e];
             vals_out[o] = tv[e];
