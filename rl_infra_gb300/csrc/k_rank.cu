@@ -449,7 +449,8 @@ constexpr size_t kMergeSmem = (size_t)kMTile * 2 * sizeof(unsigned)             
                               + (size_t)kMaxDirty * sizeof(unsigned long long)  // own new entries
                               + (size_t)kMaxDirty * sizeof(unsigned)            // their places in the tile
                               + (size_t)2 * (kMWords + 1) * sizeof(unsigned)    // dropped bitmap, prefix counts
-                              + (size_t)(kMWords + 2) * sizeof(unsigned);       // own entries before each word
+                              + (size_t)(kMWords + 2) * sizeof(unsigned)        // own entries before each word
+                              + (size_t)(kMWords + 1) * sizeof(uint4);          // the three per word, packed
 
 __device__ __forceinline__ unsigned long long pack_key_slot(unsigned key, unsigned slot)
 {
@@ -551,6 +552,7 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
     unsigned *dbits = nins + kMaxDirty;                   // [kMWords + 1] dropped tile entries
     unsigned *dpre = dbits + kMWords + 1;                 // [kMWords + 1] dropped entries in earlier words
     unsigned *ipre = dpre + kMWords + 1;                  // [kMWords + 2] own entries placed in each word, then before it
+    uint4 *winfo = reinterpret_cast<uint4 *>(ipre + kMWords + 2);   // [kMWords + 1] dbits, dpre, ipre, next ipre
     __shared__ unsigned s_nn;
     __shared__ unsigned s_wo[kMThreads / 32], s_wn[kMThreads / 32], s_wd[kMWords / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -700,6 +702,9 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
             if (lane == 31) ipre[kMWords + 1] = inc;
         }
         __syncthreads();   // dpre, ipre, own entries sorted with their places
+        for (int wi = tid; wi <= kMWords; wi += kMThreads)   // one 16-byte read a word in the copy below
+            winfo[wi] = make_uint4(dbits[wi], dpre[wi], ipre[wi], ipre[wi + 1]);
+        __syncthreads();
         // 3. the tile's output from base = t0 - c_old + c_new
         const unsigned long long base = t0 - c_old + c_new;
         // own entries at or below tile entry e: those placed in earlier words, and those of e's word
@@ -708,13 +713,12 @@ __global__ void __launch_bounds__(kMThreads) k_rank_merge(const float *raw, unsi
         for (int q = 0; q < kMItems; ++q) {
             const unsigned e = tid + q * kMThreads;
             if ((int)e >= nt) break;
-            const unsigned wi = e >> 5;
-            const unsigned wd = dbits[wi], bit = 1u << (e & 31);
+            const uint4 wf = winfo[e >> 5];   // the same word for the whole warp
+            const unsigned wd = wf.x, bit = 1u << (e & 31);
             if (wd & bit) continue;   // dropped
-            const unsigned i0 = ipre[wi], i1 = ipre[wi + 1];
-            unsigned sn = i0;
-            for (unsigned j = i0; j < i1; ++j) sn += nins[j] <= e ? 1u : 0u;
-            const unsigned sd = dpre[wi] + __popc(wd & (bit - 1u));
+            unsigned sn = wf.z;
+            for (unsigned j = wf.z; j < wf.w; ++j) sn += nins[j] <= e ? 1u : 0u;
+            const unsigned sd = wf.y + __popc(wd & (bit - 1u));
             const unsigned long long o = base + e - sd + sn;
             keys_out[o] = tk[e];
             vals_out[o] = tv[e];
