@@ -714,8 +714,11 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
     # G-step groups over 2G device arenas each way: group g+1's inputs go up on one copy stream
     # while group g computes, and group g-1's batches come down on another.  The compute stream
     # waits on the copy streams once per group, so the kernels of a group keep their
-    # programmatic overlap; every step still has its own H2D copy and its own D2H copy.
-    G = 4
+    # programmatic overlap; every step still has its own H2D copy and its own D2H copy.  A short
+    # run is set by the pipeline's fill (the first step starts after its group's copies), a long
+    # one by the group boundaries: measured on GB300, groups of one step for 20 steps (35.0-35.3K
+    # steps/s against 33.6K with groups of 4), of 4 for 20,000 (36.3K against 34.5K for 1).
+    G = 1 if K <= 64 else 4
     NA = 2 * G
     dev_in = [torch.empty(arena, dtype=torch.uint8, device="cuda") for _ in range(NA)]
     dev_out = [torch.empty(out_bytes, dtype=torch.uint8, device="cuda") for _ in range(NA)]
@@ -810,7 +813,7 @@ def run_e2e(torch, buf, w, staging, g, K, dist):
             "h2d_bytes_per_step": int(sum(n for _, n in sizes)),
             "d2h_bytes_per_step": int(sum(n for _, n in osz)), "steps": K,
             "note": ("pinned host rows + TD errors in, sampled batch out, one copy each way for every step, "
-                     "inside the timing; the copies run on two copy streams in groups of 4 steps over 8 "
+                     f"inside the timing; the copies run on two copy streams in groups of {G} step(s) over {2 * G} "
                      "device arenas each way, overlapping the neighbouring groups' kernels")}
 
 
