@@ -41,6 +41,7 @@ struct SampleArgs {
     unsigned long long seed;
     SampleOut o;
     int vec4;  // rows move as float4
+    int top;   // levels walked from the copy of the tree's top in shared memory (0: none)
 };
 
 // The sampled row, copied by the G lanes that served the draw: every load of a chunk of G V
@@ -227,30 +228,135 @@ __device__ __forceinline__ unsigned long long walk_decide(unsigned long long nod
     return (node << k) + q;
 }
 
+// The last round under the shared-memory top reads its leaves only (walk_leaves, up to 4 leaves a
+// lane): one line a draw instead of a line for each level of left children.  Deeper rounds of
+// internal nodes rebuilt the same way from their bottom rows cut the stress sampler's DRAM reads
+// further (8.6 against 11.3 MB a launch with rows of 4 floats) but their pairwise sums cost 10
+// more binary64 instructions a warp, about 2 us a stress step on GB300; they stay on left
+// children.
+constexpr bool kLeafRounds = true;
+
+// The last round of a walk from the 2^k leaves under `node` alone: every stored node is the
+// binary64 sum of its two children (the leaves taken as binary64), so the pairwise sums below
+// are the k - 1 levels of nodes above the leaves bit for bit.  Lane l of the G holds leaves
+// [l R, l R + R), R = 2^LR = 2^k / G: it adds them pairwise in registers, the G lanes add their
+// sums pairwise by shuffles, and each of the k decisions takes its left child from the lane
+// that holds it.  Returns the leaf's heap index; *lv receives its value.
+template <int G, int LR>
+__device__ __forceinline__ unsigned long long walk_leaves(const TreeRefs &t, unsigned long long node, double &m,
+                                                          int lane, float *lv)
+{
+    constexpr int LG = G == 32 ? 5 : (G == 16 ? 4 : 3);   // log2(G)
+    constexpr int R = 1 << LR;
+    const unsigned long long first = node << (LG + LR);   // heap index of the first leaf
+    const float *src = t.L + (first - t.n) + (unsigned long long)lane * R;
+    float f[R];
+    if constexpr (R == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(src);
+        f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    } else if constexpr (R == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(src);
+        f[0] = x.x; f[1] = x.y;
+    } else {
+        f[0] = src[0];
+    }
+    // h: the lane's leaves at [0, R), then its pairwise sums level by level (level j at
+    // [2R - 2R/2^j, 2R - R/2^j)); the lane's sum at 2R - 2
+    double h[2 * R - 1];
+#pragma unroll
+    for (int r = 0; r < R; ++r) h[r] = (double)f[r];
+#pragma unroll
+    for (int j = 1; j <= LR; ++j) {
+        const int in = 2 * R - (2 * R >> (j - 1)), out = 2 * R - (2 * R >> j);
+#pragma unroll
+        for (int i = 0; i < (R >> j); ++i) h[out + i] = __dadd_rn(h[in + 2 * i], h[in + 2 * i + 1]);
+    }
+    // the sums of the lane's blocks of 1, 2, 4, ... lanes: bf[j] covers 2^j lanes
+    double bf[LG];
+    bf[0] = h[2 * R - 2];
+#pragma unroll
+    for (int j = 0; j + 1 < LG; ++j) bf[j + 1] = __dadd_rn(bf[j], __shfl_xor_sync(kFull, bf[j], 1 << j, G));
+    // levels 1 .. LG choose the lane: the left half of the block of lanes [L, L + 2 half)
+    int L = 0;
+#pragma unroll
+    for (int i = 1; i <= LG; ++i) {
+        const double left = __shfl_sync(kFull, bf[LG - i], L, G);
+        if (!gt_nonneg(left, m)) {
+            m = __dsub_rn(m, left);
+            L += G >> i;
+        }
+    }
+    // levels LG + 1 .. k inside lane L: the left child is the first entry of the level just below
+    // the current block, and each decision keeps the half of every lower level (and of the
+    // leaves) that it took -- selects at fixed positions, so the rows stay in registers
+    int q = 0;
+#pragma unroll
+    for (int i = 1; i <= LR; ++i) {
+        const int lvl = LR - i;
+        const double left = __shfl_sync(kFull, h[2 * R - (2 * R >> lvl)], L, G);
+        const bool right = !gt_nonneg(left, m);
+        if (right) {
+            m = __dsub_rn(m, left);
+            q += R >> i;
+        }
+#pragma unroll
+        for (int j = 0; j < lvl; ++j) {
+            const int b = 2 * R - (2 * R >> j), cnt = R >> (j + i);
+#pragma unroll
+            for (int e = 0; e < cnt; ++e) h[b + e] = right ? h[b + cnt + e] : h[b + e];
+        }
+#pragma unroll
+        for (int e = 0; e < (R >> i); ++e) f[e] = right ? f[(R >> i) + e] : f[e];
+    }
+    *lv = __shfl_sync(kFull, f[0], L, G);
+    return first + (unsigned long long)L * R + q;
+}
+
 // G lanes serve one draw (32 / G draws per warp at once), each lane holding S nodes of a round:
 // rounds of K = log2(G S + 1) levels (7 for 32 x 4; 6 for 16 x 4 and 8 x 8).  Every level of the
 // walk is one binary64 subtraction per warp instruction, and GB300's binary64 pipe retires about
 // one warp instruction every 19 cycles per SM, so large batches share each instruction among 2
 // or 4 draws; the deepest round also reads 17 sectors of nodes and leaves instead of 33.
-template <int G, int S>
+// With TOP > 0 (large batches, where every draw walks its own path below the top few levels)
+// each CTA copies the nodes of depths 0 .. TOP into shared memory and the first a.top levels of
+// every draw are walked there, one node a level; the levels below follow in as few rounds as K
+// allows, the shallower rounds taking the extra level (a round of k levels reads about 2^k
+// nodes, and below the top every draw reads its own), and the last round reads its leaves alone
+// (walk_leaves).  DRAM moves 128-byte lines here: below the levels the draws share, each level
+// of left children costs a draw a line, and a round of leaves one line for all its levels.
+template <int G, int S, int TOP>
 __global__ void __launch_bounds__(kThreads, 2) k_sample_prop(SampleArgs a)
 {
     constexpr int K = G * S >= 127 ? 7 : (G * S >= 63 ? 6 : 5);   // levels per round
     constexpr int GV = G >= 16 ? 128 / G : 8;                      // float4 per lane per gather chunk
     constexpr int per_warp = 32 / G;
+    constexpr int LG = G == 32 ? 5 : (G == 16 ? 4 : 3);           // log2(G)
     __shared__ unsigned long long s_call;
+    __shared__ __align__(16) double s_top[TOP > 0 ? 2 << TOP : 2];
     pdl_wait();
     pdl_release();
     const unsigned long long n = a.t.n;
     const int D = a.t.D;
     if (threadIdx.x == 0) s_call = take_call_number(a.ctl);
+    const int top = TOP > 0 ? a.top : 0;   // the host passes 0 or TOP, and TOP < D
+    if (TOP > 0 && top > 0) {
+        // 16-byte loads, all issued before the first store (the tree's arrays are 256-byte aligned)
+        const double2 *src = reinterpret_cast<const double2 *>(a.t.S);
+        double2 *dst = reinterpret_cast<double2 *>(s_top);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < (1 << TOP); i += blockDim.x) dst[i] = src[i];
+    }
     // while the call number is on its way: the total, the minimum, the size and the first
     // round's nodes (the same for every draw)
     const double total = D == 0 ? (double)a.t.L[0] : a.t.S[1];
     const float pmin = D == 0 ? leaf_min_value(a.t.L[0]) : a.t.M[1];
     const unsigned long long size = a.ctl->size;
-    const int rounds = (D + K - 1) / K;             // K levels per round; the first takes the rest
-    const int first = D - K * (rounds - 1);
+    // rounds below the top: without a top, K levels each and the first takes the rest; with one,
+    // kb or kb + 1 levels each, the first kx rounds taking kb + 1
+    const int dk = D - top;
+    const int rounds = (dk + K - 1) / K;
+    const int kb = top > 0 ? dk / rounds : K, kx = top > 0 ? dk % rounds : 0;
+    const int first = top > 0 ? kb + (kx != 0) : dk - K * (rounds - 1);
     const int lane = threadIdx.x & (G - 1);
     const unsigned sub = (threadIdx.x & 31) / G;
     // the first round's nodes are preloaded (before the call number arrives) when they fit the
@@ -280,12 +386,34 @@ __global__ void __launch_bounds__(kThreads, 2) k_sample_prop(SampleArgs a)
             leaf = 0;
             lv = a.t.L[0];
         } else {
-            if (!kPre) walk_load<G, S>(a.t, 1, first, rounds == 1, lane, w0);
-            unsigned long long node = walk_decide<G, S>(1, first, rounds == 1, m, lane, w0, &lv);
+            unsigned long long node = 1;
+            if (TOP > 0 && top > 0) {
+#pragma unroll 1
+                for (int lev = 0; lev < top; ++lev) {
+                    const double left = s_top[2 * node];
+                    if (gt_nonneg(left, m)) {
+                        node = 2 * node;
+                    } else {
+                        m = __dsub_rn(m, left);
+                        node = 2 * node + 1;
+                    }
+                }
+            }
+            if (!kPre) walk_load<G, S>(a.t, node, first, rounds == 1, lane, w0);
+            node = walk_decide<G, S>(node, first, rounds == 1, m, lane, w0, &lv);
             for (int rd = 1; rd < rounds; ++rd) {
-                WalkRegs<S> w;
-                walk_load<G, S>(a.t, node, K, rd == rounds - 1, lane, w);
-                node = walk_decide<G, S>(node, K, rd == rounds - 1, m, lane, w, &lv);
+                const int k = top > 0 ? kb + (rd < kx) : K;
+                const bool lst = rd == rounds - 1;
+                // the last round from its leaves alone
+                if (TOP > 0 && kLeafRounds && top > 0 && lst && k >= LG && k <= LG + 2) {
+                    if (k == LG) node = walk_leaves<G, 0>(a.t, node, m, lane, &lv);
+                    else if (k == LG + 1) node = walk_leaves<G, 1>(a.t, node, m, lane, &lv);
+                    else node = walk_leaves<G, 2>(a.t, node, m, lane, &lv);
+                } else {
+                    WalkRegs<S> w;
+                    walk_load<G, S>(a.t, node, k, lst, lane, w);
+                    node = walk_decide<G, S>(node, k, lst, m, lane, w, &lv);
+                }
             }
             leaf = node - n;
         }
@@ -531,6 +659,10 @@ int warps_per_cta(unsigned B) { return (B <= 512 || B >= 4096) ? 2 : 8; }
 constexpr unsigned kHalfWarpBatch = 4096;
 constexpr unsigned kQuarterWarpBatch = 8192;
 
+// Levels of the tree's top that the half- and quarter-warp samplers walk in shared memory (a
+// copy of 2^(kTopLevels + 1) nodes a CTA), on trees deeper than kTopMinDepth.
+constexpr int kTopLevels = 8, kTopMinDepth = 12;
+
 bool rows_vec4(const RingRefs &r, const SampleOut &o)
 {
     if (r.d % 4 != 0 || o.dp % 4 != 0) return false;
@@ -545,8 +677,8 @@ cudaError_t init_sample_kernels(int carveout)
 {
     if (carveout < 0) return cudaSuccess;
     cudaError_t e;
-    const void *fns[] = {(const void *)k_sample_prop<32, 4>, (const void *)k_sample_prop<16, 4>,
-                         (const void *)k_sample_prop<8, 8>, (const void *)k_sample_rank,
+    const void *fns[] = {(const void *)k_sample_prop<32, 4, 0>, (const void *)k_sample_prop<16, 4, kTopLevels>,
+                         (const void *)k_sample_prop<8, 8, kTopLevels>, (const void *)k_sample_rank,
                          (const void *)k_sample_uniform, (const void *)k_sample_flat};
     for (const void *f : fns) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
@@ -575,9 +707,10 @@ cudaError_t launch_sample_prop(const TreeRefs &t, const RingRefs &r, Ctl *ctl, u
     const int per_warp = (B >= kQuarterWarpBatch && r6 == r7) ? 4 : (B >= kHalfWarpBatch && r6 == r7) ? 2 : 1;
     const unsigned long long ctas = (B + wpb * per_warp - 1) / (wpb * per_warp);
     const unsigned grid = (unsigned)std::min<unsigned long long>(ctas, (unsigned long long)num_sms * sampler_ctas_per_sm());
-    if (per_warp == 4) return launch_pdl(k_sample_prop<8, 8>, grid, wpb * 32, 0, st, a);
-    if (per_warp == 2) return launch_pdl(k_sample_prop<16, 4>, grid, wpb * 32, 0, st, a);
-    return launch_pdl(k_sample_prop<32, 4>, grid, wpb * 32, 0, st, a);
+    a.top = per_warp > 1 && t.D > kTopMinDepth ? kTopLevels : 0;
+    if (per_warp == 4) return launch_pdl(k_sample_prop<8, 8, kTopLevels>, grid, wpb * 32, 0, st, a);
+    if (per_warp == 2) return launch_pdl(k_sample_prop<16, 4, kTopLevels>, grid, wpb * 32, 0, st, a);
+    return launch_pdl(k_sample_prop<32, 4, 0>, grid, wpb * 32, 0, st, a);
 }
 
 cudaError_t launch_sample_flat(const float *L, const FlatWork &fw, const RingRefs &r, Ctl *ctl, unsigned B,

@@ -293,16 +293,38 @@ def test_many_sizes_of_batch_and_tree(rb):
         p.close()
 
 
-@pytest.mark.parametrize("D,cap", [(0, 1), (3, 5), (6, 64), (10, 1000), (12, 1 << 12), (16, 40000),
-                                   (18, 1 << 18)])
+@pytest.mark.parametrize("D,cap", [(0, 1), (3, 5), (6, 64), (10, 1000), (12, 1 << 12), (13, 5000),
+                                   (16, 40000), (18, 1 << 18)])
 def test_large_batches_two_draws_per_warp(D, cap):
-    """Batches of 4096 draws or more walk on 16-lane halves of a warp in rounds of up to 6 levels
-    (for trees whose round count that keeps); odd batch sizes leave one half without a draw."""
+    """Batches of 4096 draws or more walk on 16-lane halves (8-lane quarters from 8192) of a warp
+    in rounds of up to 6 levels (for trees whose round count that keeps), below a top of 8 levels
+    walked in shared memory on trees deeper than 12; odd batch sizes leave sub-warps without a
+    draw."""
     w = _small("tiny", capacity=cap, state_dim=64, row_stride=64)
     g = wl.rng(17, D)
     p = Pair(cap, 64, 64, 0.7, 1e-6, 0, seed=D)
     prefill(p, w, g)
     for B in (4096, 5001, 8192, 8195):
+        _, want = p.sample(B, 0.5)
+        idx = wl.duplicate_positions(g, want["idx"], 0.25)
+        p.update(idx, wl.td_errors(g, B))
+    p.check_tree()
+    p.check_counters()
+    p.close()
+
+
+@pytest.mark.parametrize("D,cap", [(22, 1 << 22), (23, (1 << 22) + 5)])
+def test_large_batches_top_levels_in_shared_memory(D, cap):
+    """Batches of 4096 draws or more (16-lane halves or 8-lane quarters of a warp) on trees of
+    2^22 leaves and up: the top 8 levels are walked from a copy in shared memory, the middle
+    rounds from left children and the last round from its leaves alone, the nodes above them
+    rebuilt by pairwise sums; the second tree is barely half filled, so its right half holds
+    empty subtrees."""
+    w = _small("tiny", capacity=cap, state_dim=4, row_stride=4)
+    g = wl.rng(19, D)
+    p = Pair(cap, 4, 4, 0.7, 1e-6, 0, seed=D)
+    prefill(p, w, g, chunk=1 << 18)
+    for B in (8192, 6000, 8195, 12000):
         _, want = p.sample(B, 0.5)
         idx = wl.duplicate_positions(g, want["idx"], 0.25)
         p.update(idx, wl.td_errors(g, B))
