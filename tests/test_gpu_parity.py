@@ -294,7 +294,7 @@ def test_many_sizes_of_batch_and_tree(rb):
 
 
 @pytest.mark.parametrize("D,cap", [(0, 1), (3, 5), (6, 64), (10, 1000), (12, 1 << 12), (13, 5000),
-                                   (16, 40000), (18, 1 << 18)])
+                                   (15, 20000), (16, 40000), (18, 1 << 18)])
 def test_large_batches_two_draws_per_warp(D, cap):
     """Batches of 4096 draws or more walk on 16-lane halves (8-lane quarters from 8192) of a warp
     in rounds of up to 6 levels (for trees whose round count that keeps), below a top of 8 levels
