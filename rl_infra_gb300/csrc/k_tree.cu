@@ -61,20 +61,25 @@ __device__ __forceinline__ float ld_min(const TreeRefs &t, unsigned long long no
     return node >= t.n ? leaf_min_value(t.L[node - t.n]) : t.M[node];
 }
 
-// Arrival ticket: returns true in every thread of the last CTA to arrive.  No CTA waits.
+// Arrival ticket: returns true in every thread of the last CTA to arrive.  No CTA waits.  The
+// CTA barrier orders every thread's earlier accesses before thread 0's release fence and ticket
+// (a fence is cumulative over what happens before it), and the last CTA's thread 0 fences again
+// (acquire) before the barrier that lets its other threads read: one fence a CTA instead of one
+// a thread (measured on GB300: the dqn step 27.7 against 28.7 us, the apex step 38.9K against
+// 38.6K steps/s).
 __device__ __forceinline__ bool last_to_arrive(unsigned *ticket)
 {
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         const unsigned t = atomicAdd(ticket, 1u);
-        s_last = (t == gridDim.x - 1);
+        const int l = t == gridDim.x - 1;
+        if (l) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        s_last = l;
     }
     __syncthreads();
-    const bool last = s_last;
-    if (last) __threadfence();
-    return last;
+    return s_last;
 }
 
 __device__ __forceinline__ unsigned block_max_u32(unsigned v)
